@@ -1,0 +1,79 @@
+"""Strength of the oracle's pins: plant a plausible mistake in a copy of the
+oracle source (on the CPU), rebuild it, and check that at least one pin from
+``test_oracle_pins`` fails against the broken copy, while all of them pass
+against the real one."""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "gqa_oracle.c")
+
+PIN_BATTERY = [
+    pins.test_head_map_worked_example,
+    pins.test_mha_special_case_matches_library_attention,
+    pins.test_mqa_special_case_matches_shared_kv_einsum,
+    lambda: pins.test_general_gqa_matches_library_attention(8, 2),
+    pins.test_identical_keys_give_plain_mean,
+    pins.test_zero_scale_gives_plain_mean,
+    pins.test_length_one_returns_first_value_row,
+    pins.test_dominant_logit_selects_its_value,
+    pins.test_softmax_weights_sum_to_one,
+    pins.test_poisoned_tail_is_never_read,
+    pins.test_empty_and_overlong_lengths,
+    pins.test_brute_force_high_precision,
+    pins.test_kv_append_oracle_places_rows_and_increments,
+    pins.test_append_then_attend_includes_new_token,
+    pins.test_meanpool_identity_when_groups_equal_heads,
+    pins.test_meanpool_single_group_is_mean_of_all_heads,
+    pins.test_meanpool_is_the_group_mean_of_projections,
+]
+
+# (name, text in the oracle source, replacement)
+MUTANTS = [
+    ("interleaved head->group map",
+     "off[(size_t)b * H + (size_t)g * n_rep + r]", "off[(size_t)b * H + (size_t)r * G + g]"),
+    ("no max subtraction", "w[n] = exp(w[n] - m);", "w[n] = exp(w[n]);"),
+    ("scale dropped", "w[n] = dot * scale;", "w[n] = dot;"),
+    ("reads one position past L", "int b = (int)(bh / H);\n        int L = clamp_len(seq_lens[b], Nmax);",
+     "int b = (int)(bh / H);\n        int L = clamp_len(seq_lens[b] + 1, Nmax);"),
+    ("softmax not normalised", "for (int n = 0; n < L; ++n) w[n] /= z;", "(void)z;"),
+    ("K used in place of V", "o[i] += w[n] * load_value(v,", "o[i] += w[n] * load_value(k,"),
+    ("q read reversed", "load_value(q, q_off + i, dtype)", "load_value(q, q_off + (d - 1 - i), dtype)"),
+    ("wrong sign of logits", "w[n] = dot * scale;", "w[n] = -dot * scale;"),
+    ("meanpool sums instead of averaging", "w_out[(size_t)g * per_head + e] = s / n_rep;",
+     "w_out[(size_t)g * per_head + e] = s;"),
+    ("append does not advance the length", "seq_lens[b] = L + 1;", "seq_lens[b] = L;"),
+    ("append writes the wrong row", "* Nmax + (size_t)L) * row;", "* Nmax + (size_t)L + 1) * row;"),
+]
+
+
+def _failures():
+    failed = []
+    for pin in PIN_BATTERY:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            failed.append(getattr(pin, "__name__", "lambda"))
+    return failed
+
+
+def test_every_pin_passes_on_the_real_oracle():
+    assert _failures() == []
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not found once: {old!r}"
+    mutant = tmp_path / "mutant.c"
+    mutant.write_text(src.replace(old, new))
+    so = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+                           "-o", str(so), str(mutant), "-lm"])
+    with oracle.use_library(str(so)):
+        failed = _failures()
+    assert failed, f"no pin caught the planted mistake: {name}"
