@@ -1,0 +1,239 @@
+"""Grouped-query decode attention over a KV cache on NVIDIA B300 (sm_103a).
+
+Thin Python binding of ``libgqa.so`` (C ABI in ``include/gqa.h``).  Every
+function here only marshals arguments -- torch tensors become device pointers
+and the current CUDA stream -- and calls the library entry point of the same
+name; all arithmetic runs in the library's CUDA kernels.  There is no CPU
+fallback: without the built library, or without a CUDA device, every call
+raises.
+
+Entry points (see ``include/gqa.h`` for the full contract):
+  gqa_decode_attention(q, k_cache, v_cache, seq_lens, scale, out)
+  gqa_decode_attention_ws(..., workspace)        caller-provided workspace
+  gqa_decode_attention_ex(..., split_tokens, workspace)
+  gqa_decode_workspace_bytes(B, H, G, d, Nmax, dtype)
+  kv_append(k_new, v_new, k_cache, v_cache, seq_lens)
+  mha_to_gqa_meanpool(w, w_out)
+  gqa_get_device_error()
+  gqa_status_string(status)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import cost  # noqa: F401  (host-side byte/flop accounting)
+
+__all__ = [
+    "GQAError", "GQA_F32", "GQA_BF16", "library_path", "load_library",
+    "gqa_decode_attention", "gqa_decode_attention_ws", "gqa_decode_attention_ex",
+    "gqa_decode_workspace_bytes", "gqa_decode_workspace_bytes_ex", "kv_append",
+    "mha_to_gqa_meanpool", "gqa_get_device_error", "gqa_status_string",
+    "DEVERR_ATTN_LEN", "DEVERR_APPEND_LEN", "DEVERR_TIMEOUT", "EXPORTED_SYMBOLS",
+]
+
+GQA_F32, GQA_BF16 = 0, 1
+DEVERR_ATTN_LEN, DEVERR_APPEND_LEN, DEVERR_TIMEOUT = 1, 2, 4
+
+EXPORTED_SYMBOLS = (
+    "gqa_decode_attention", "gqa_decode_workspace_bytes", "gqa_decode_attention_ws",
+    "gqa_decode_workspace_bytes_ex", "gqa_decode_attention_ex", "kv_append",
+    "mha_to_gqa_meanpool", "gqa_get_device_error", "gqa_status_string",
+)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libgqa.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class GQAError(RuntimeError):
+    def __init__(self, fn: str, status: int, text: str):
+        super().__init__(f"{fn} failed: {text} (status {status})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Loads libgqa.so (built by ``__graft_entry__.build()``); raises when it
+    is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libgqa.so is not built ({_LIB_PATH}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, ci, cf, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        attn = [vp, vp, vp, vp, cf, vp, ci, ci, ci, ci, ci, ci]
+        lib.gqa_decode_attention.argtypes = attn + [vp]
+        lib.gqa_decode_attention_ws.argtypes = attn + [vp, sz, vp]
+        lib.gqa_decode_attention_ex.argtypes = attn + [ci, vp, sz, vp]
+        for f in ("gqa_decode_attention", "gqa_decode_attention_ws", "gqa_decode_attention_ex"):
+            getattr(lib, f).restype = ci
+        lib.gqa_decode_workspace_bytes.argtypes = [ci] * 6
+        lib.gqa_decode_workspace_bytes.restype = sz
+        lib.gqa_decode_workspace_bytes_ex.argtypes = [ci] * 7
+        lib.gqa_decode_workspace_bytes_ex.restype = sz
+        lib.kv_append.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, vp]
+        lib.kv_append.restype = ci
+        lib.mha_to_gqa_meanpool.argtypes = [vp, vp, ci, ci, ci, ci, ci, vp]
+        lib.mha_to_gqa_meanpool.restype = ci
+        lib.gqa_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
+        lib.gqa_get_device_error.restype = ci
+        lib.gqa_status_string.argtypes = [ci]
+        lib.gqa_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def gqa_status_string(status: int) -> str:
+    return load_library().gqa_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise GQAError(fn, status, gqa_status_string(status))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return GQA_BF16
+    if t.dtype == torch.float32:
+        return GQA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: bf16 or fp32")
+
+
+def _dev(t: torch.Tensor, name: str) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(t: torch.Tensor, stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(t.device)
+    return s.cuda_stream
+
+
+def _attn_shapes(q, k_cache, v_cache, seq_lens, out):
+    B, H, d = q.shape
+    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache must both be [B, G, Nmax, d]")
+    Bk, G, Nmax, dk = k_cache.shape
+    if Bk != B or dk != d:
+        raise ValueError("q [B,H,d] and the caches [B,G,Nmax,d] disagree")
+    if tuple(out.shape) != (B, H, d):
+        raise ValueError("out must be [B, H, d]")
+    if seq_lens.dtype != torch.int32 or tuple(seq_lens.shape) != (B,):
+        raise ValueError("seq_lens must be int32 [B]")
+    if not (q.dtype == k_cache.dtype == v_cache.dtype == out.dtype):
+        raise ValueError("q, k_cache, v_cache and out must share one dtype")
+    return B, H, G, d, Nmax
+
+
+def _attn_args(q, k_cache, v_cache, seq_lens, scale, out):
+    B, H, G, d, Nmax = _attn_shapes(q, k_cache, v_cache, seq_lens, out)
+    return [_dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _dev(seq_lens, "seq_lens"),
+            float(scale), _dev(out, "out"), B, H, G, d, Nmax, _dtype_code(q)]
+
+
+def gqa_decode_attention(q, k_cache, v_cache, seq_lens, scale, out, stream=None):
+    """out[b,h,:] = softmax(scale * q[b,h] . K[b,g]^T) V[b,g] over the first
+    seq_lens[b] cached positions, g = h // (H // G).  Workspace from the
+    stream-ordered allocator."""
+    lib = load_library()
+    _check("gqa_decode_attention",
+           lib.gqa_decode_attention(*_attn_args(q, k_cache, v_cache, seq_lens, scale, out), _stream(q, stream)))
+    return out
+
+
+def gqa_decode_workspace_bytes(B, H, G, d, Nmax, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else (GQA_BF16 if dtype == torch.bfloat16 else GQA_F32)
+    return int(load_library().gqa_decode_workspace_bytes(B, H, G, d, Nmax, code))
+
+
+def gqa_decode_workspace_bytes_ex(B, H, G, d, Nmax, dtype, split_tokens) -> int:
+    code = dtype if isinstance(dtype, int) else (GQA_BF16 if dtype == torch.bfloat16 else GQA_F32)
+    return int(load_library().gqa_decode_workspace_bytes_ex(B, H, G, d, Nmax, code, int(split_tokens)))
+
+
+def _ws(workspace: Optional[torch.Tensor]):
+    if workspace is None or workspace.numel() == 0:
+        return None, 0
+    return _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+
+
+def gqa_decode_attention_ws(q, k_cache, v_cache, seq_lens, scale, out, workspace, stream=None):
+    """As gqa_decode_attention with a caller-owned device workspace (a byte
+    tensor of at least gqa_decode_workspace_bytes(...) bytes)."""
+    lib = load_library()
+    wp, wn = _ws(workspace)
+    _check("gqa_decode_attention_ws",
+           lib.gqa_decode_attention_ws(*_attn_args(q, k_cache, v_cache, seq_lens, scale, out), wp, wn,
+                                       _stream(q, stream)))
+    return out
+
+
+def gqa_decode_attention_ex(q, k_cache, v_cache, seq_lens, scale, out, split_tokens, workspace, stream=None):
+    """As gqa_decode_attention_ws with the positions per split forced
+    (0 = automatic)."""
+    lib = load_library()
+    wp, wn = _ws(workspace)
+    _check("gqa_decode_attention_ex",
+           lib.gqa_decode_attention_ex(*_attn_args(q, k_cache, v_cache, seq_lens, scale, out), int(split_tokens),
+                                       wp, wn, _stream(q, stream)))
+    return out
+
+
+def kv_append(k_new, v_new, k_cache, v_cache, seq_lens, stream=None):
+    """Writes k_new/v_new [B,G,d] into row seq_lens[b] of the caches and
+    increments seq_lens (in place, on the device)."""
+    lib = load_library()
+    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache must both be [B, G, Nmax, d]")
+    B, G, Nmax, d = k_cache.shape
+    if tuple(k_new.shape) != (B, G, d) or tuple(v_new.shape) != (B, G, d):
+        raise ValueError("k_new and v_new must be [B, G, d]")
+    if seq_lens.dtype != torch.int32 or tuple(seq_lens.shape) != (B,):
+        raise ValueError("seq_lens must be int32 [B]")
+    if not (k_new.dtype == v_new.dtype == k_cache.dtype == v_cache.dtype):
+        raise ValueError("k_new, v_new and the caches must share one dtype")
+    _check("kv_append", lib.kv_append(_dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(k_cache, "k_cache"),
+                                      _dev(v_cache, "v_cache"), _dev(seq_lens, "seq_lens"), B, G, d, Nmax,
+                                      _dtype_code(k_cache), _stream(k_cache, stream)))
+
+
+def mha_to_gqa_meanpool(w, w_out, stream=None):
+    """w [H, d, D] -> w_out [G, d, D]: each KV head's projection is the mean of
+    its group's H/G per-head projections."""
+    lib = load_library()
+    if w.dim() < 2 or w_out.dim() != w.dim() or tuple(w.shape[1:]) != tuple(w_out.shape[1:]):
+        raise ValueError("w [H, ...] and w_out [G, ...] must agree past the head axis")
+    if w.dtype != w_out.dtype:
+        raise ValueError("w and w_out must share one dtype")
+    H, G = w.shape[0], w_out.shape[0]
+    d = w.shape[1]
+    D = int(w[0].numel() // d) if d else 0
+    _check("mha_to_gqa_meanpool", lib.mha_to_gqa_meanpool(_dev(w, "w"), _dev(w_out, "w_out"), H, G, d, D,
+                                                          _dtype_code(w), _stream(w, stream)))
+    return w_out
+
+
+def gqa_get_device_error(stream=None, device=None) -> int:
+    """Reads and clears the current device's error word (synchronises)."""
+    lib = load_library()
+    v = ctypes.c_int32(0)
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    _check("gqa_get_device_error", lib.gqa_get_device_error(ctypes.byref(v), s.cuda_stream))
+    return int(v.value)

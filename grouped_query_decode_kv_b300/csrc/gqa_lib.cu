@@ -1,0 +1,387 @@
+// libgqa.so: host side of the C ABI declared in include/gqa.h — argument
+// checks, the split plan, TMA descriptors and the kernel launches.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+
+#include "gqa.h"
+#include "gqa_device.cuh"
+#include "gqa_params.cuh"
+#include "gqa_small_kernels.cuh"
+#include "gqa_split_mma.cuh"
+#include "gqa_split_simt.cuh"
+
+namespace gqa {
+namespace {
+
+// ----------------------------------------------------------- kernel configs
+// Stages of ~32 KB (K + V tiles); three stages per CTA, two CTAs per SM.
+using MmaD128x1 = MmaCfg<128, 1, 1, 64, 3>;   // n_rep 3..16
+using MmaD128x2 = MmaCfg<128, 2, 1, 64, 3>;   // n_rep 17..32
+using MmaD128x4 = MmaCfg<128, 2, 2, 64, 3>;   // n_rep >= 33 (64 heads per CTA)
+using MmaD64x1 = MmaCfg<64, 1, 1, 128, 3>;
+using MmaD64x2 = MmaCfg<64, 2, 1, 128, 3>;
+using MmaD64x4 = MmaCfg<64, 2, 2, 128, 3>;
+
+template <typename T, int D, int NH>
+using SimtFor = SimtCfg<T, D, NH, (32768 / (2 * D * (int)sizeof(T))), 3>;
+
+struct KernelChoice {
+  const void *func;
+  int threads;
+  int smem;
+  int block_n;
+  int heads;
+  int box_elems;
+  void (*launch)(dim3, const CUtensorMap &, const CUtensorMap &, const SplitParams &, cudaStream_t);
+};
+
+template <class C, bool MMA>
+void launch_split(dim3 grid, const CUtensorMap &k, const CUtensorMap &v, const SplitParams &p, cudaStream_t st) {
+  if constexpr (MMA)
+    gqa_split_mma_kernel<C><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(k, v, p);
+  else
+    gqa_split_simt_kernel<C><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(k, v, p);
+}
+
+template <class C, bool MMA>
+KernelChoice make_choice() {
+  KernelChoice c;
+  if constexpr (MMA)
+    c.func = reinterpret_cast<const void *>(&gqa_split_mma_kernel<C>);
+  else
+    c.func = reinterpret_cast<const void *>(&gqa_split_simt_kernel<C>);
+  c.threads = C::THREADS;
+  c.smem = C::SMEM_BYTES;
+  c.block_n = C::BLOCK_N;
+  c.heads = C::HEADS;
+  if constexpr (MMA)
+    c.box_elems = 64;
+  else
+    c.box_elems = C::BOX_ELEMS;
+  c.launch = &launch_split<C, MMA>;
+  return c;
+}
+
+KernelChoice choose_kernel(gqa_dtype_t dt, int d, int n_rep) {
+  if (dt == GQA_BF16) {
+    if (d == 128) {
+      if (n_rep == 1) return make_choice<SimtFor<__nv_bfloat16, 128, 1>, false>();
+      if (n_rep == 2) return make_choice<SimtFor<__nv_bfloat16, 128, 2>, false>();
+      if (n_rep <= 16) return make_choice<MmaD128x1, true>();
+      if (n_rep <= 32) return make_choice<MmaD128x2, true>();
+      return make_choice<MmaD128x4, true>();
+    }
+    if (n_rep == 1) return make_choice<SimtFor<__nv_bfloat16, 64, 1>, false>();
+    if (n_rep == 2) return make_choice<SimtFor<__nv_bfloat16, 64, 2>, false>();
+    if (n_rep <= 16) return make_choice<MmaD64x1, true>();
+    if (n_rep <= 32) return make_choice<MmaD64x2, true>();
+    return make_choice<MmaD64x4, true>();
+  }
+  if (d == 128) {
+    if (n_rep == 1) return make_choice<SimtFor<float, 128, 1>, false>();
+    if (n_rep == 2) return make_choice<SimtFor<float, 128, 2>, false>();
+    return make_choice<SimtFor<float, 128, 4>, false>();
+  }
+  if (n_rep == 1) return make_choice<SimtFor<float, 64, 1>, false>();
+  if (n_rep == 2) return make_choice<SimtFor<float, 64, 2>, false>();
+  return make_choice<SimtFor<float, 64, 4>, false>();
+}
+
+// ----------------------------------------------------------- split plan
+struct Plan {
+  KernelChoice k;
+  int head_chunks;
+  int chunk;
+  int S_max;
+};
+
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+int device_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 148;
+  return sms;
+}
+
+// Positions per split.  Aim at about four CTAs per resident slot (two CTAs
+// per SM) so that the block scheduler balances the tail, but never fewer
+// than four tiles per split; Nmax stands in for the (device-resident)
+// lengths.
+Plan make_plan(int B, int H, int G, int d, int Nmax, gqa_dtype_t dt, int split_tokens) {
+  Plan pl;
+  const int n_rep = H / G;
+  pl.k = choose_kernel(dt, d, n_rep);
+  pl.head_chunks = ceil_div(n_rep, pl.k.heads);
+  const int bn = pl.k.block_n;
+  const int tiles = ceil_div(Nmax, bn);
+  int tps;
+  if (split_tokens > 0) {
+    tps = std::max(1, ceil_div(split_tokens, bn));
+  } else {
+    const long long units = (long long)B * G * pl.head_chunks;
+    const long long want = 4LL * 2 * device_sm_count();
+    const int S = (int)std::max<long long>(1, (want + units - 1) / units);
+    tps = std::max(std::min(4, tiles), ceil_div(tiles, S));
+  }
+  tps = std::min(tps, tiles);
+  pl.chunk = tps * bn;
+  pl.S_max = ceil_div(Nmax, pl.chunk);
+  return pl;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Grid limits: y = G * head_chunks and z = B must stay within 65535.
+bool plan_fits(const Plan &pl, int B, int G) { return B <= 65535 && (long long)G * pl.head_chunks <= 65535; }
+
+size_t workspace_for(const Plan &pl, int B, int H, int d) {
+  if (pl.S_max <= 1) return 0;
+  const size_t parts = (size_t)B * H * pl.S_max;
+  return align256(parts * d * sizeof(float)) + align256(parts * 2 * sizeof(float));
+}
+
+// ----------------------------------------------------------- TMA descriptors
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// The cache [B*G, Nmax, d] as a 3-D tensor; a box is 128 bytes of one row
+// (box_elems elements) by block_n positions, 128-byte swizzled.
+bool encode_cache_map(CUtensorMap *map, const void *base, gqa_dtype_t dt, int d, int Nmax, int BG, int block_n,
+                      int box_elems) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const size_t elt = dt == GQA_BF16 ? 2 : 4;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Nmax, (cuuint64_t)BG};
+  cuuint64_t strides[2] = {(cuuint64_t)(d * elt), (cuuint64_t)((size_t)Nmax * d * elt)};
+  cuuint32_t box[3] = {(cuuint32_t)box_elems, (cuuint32_t)block_n, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, dt == GQA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                  const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_attention_args(const void *q, const void *k, const void *v, const int32_t *sl, const void *out, int B,
+                         int H, int G, int d, int Nmax, gqa_dtype_t dt) {
+  if (!q || !k || !v || !sl || !out) return GQA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || G <= 0 || d <= 0 || Nmax <= 0) return GQA_ERR_INVALID_ARG;
+  if (H % G != 0) return GQA_ERR_INVALID_ARG;
+  if (dt != GQA_F32 && dt != GQA_BF16) return GQA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
+  if (B > 65535) return GQA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return GQA_ERR_INVALID_ARG;
+  return GQA_OK;
+}
+
+int ensure_smem_attr(const KernelChoice &kc) {
+  // Idempotent and cheap; set on every call so that each device gets it.
+  if (cudaFuncSetAttribute(kc.func, cudaFuncAttributeMaxDynamicSharedMemorySize, kc.smem) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  return GQA_OK;
+}
+
+int run_attention(const void *q, const void *k, const void *v, const int32_t *sl, float scale, void *out, int B,
+                  int H, int G, int d, int Nmax, gqa_dtype_t dt, const Plan &pl, void *ws, cudaStream_t st) {
+  CUtensorMap mk, mv;
+  if (!encode_cache_map(&mk, k, dt, d, Nmax, B * G, pl.k.block_n, pl.k.box_elems) ||
+      !encode_cache_map(&mv, v, dt, d, Nmax, B * G, pl.k.block_n, pl.k.box_elems))
+    return GQA_ERR_CUDA;
+  if (int rc = ensure_smem_attr(pl.k)) return rc;
+  SplitParams p;
+  p.q = q;
+  p.seq_lens = sl;
+  p.out = out;
+  const size_t parts = (size_t)B * H * pl.S_max;
+  p.o_part = pl.S_max > 1 ? reinterpret_cast<float *>(ws) : nullptr;
+  p.ml_part = pl.S_max > 1 ? reinterpret_cast<float *>(reinterpret_cast<char *>(ws) +
+                                                       align256(parts * d * sizeof(float)))
+                           : nullptr;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.B = B;
+  p.H = H;
+  p.G = G;
+  p.Nmax = Nmax;
+  p.n_rep = H / G;
+  p.chunk = pl.chunk;
+  p.S_max = pl.S_max;
+  p.heads_per_cta = pl.k.heads;
+  p.head_chunks = pl.head_chunks;
+  dim3 grid(pl.S_max, G * pl.head_chunks, B);
+  pl.k.launch(grid, mk, mv, p, st);
+  if (cudaPeekAtLastError() != cudaSuccess) {
+    cudaGetLastError();
+    return GQA_ERR_CUDA;
+  }
+  if (pl.S_max > 1) {
+    CombineParams c;
+    c.seq_lens = sl;
+    c.o_part = p.o_part;
+    c.ml_part = p.ml_part;
+    c.out = out;
+    c.B = B;
+    c.H = H;
+    c.Nmax = Nmax;
+    c.chunk = pl.chunk;
+    c.S_max = pl.S_max;
+    const int blocks = ceil_div((long long)B * H, 4);
+    if (dt == GQA_BF16) {
+      if (d == 128)
+        gqa_combine_kernel<__nv_bfloat16, 128><<<blocks, 128, 0, st>>>(c);
+      else
+        gqa_combine_kernel<__nv_bfloat16, 64><<<blocks, 128, 0, st>>>(c);
+    } else {
+      if (d == 128)
+        gqa_combine_kernel<float, 128><<<blocks, 128, 0, st>>>(c);
+      else
+        gqa_combine_kernel<float, 64><<<blocks, 128, 0, st>>>(c);
+    }
+    if (cudaPeekAtLastError() != cudaSuccess) {
+      cudaGetLastError();
+      return GQA_ERR_CUDA;
+    }
+  }
+  return GQA_OK;
+}
+
+}  // namespace
+}  // namespace gqa
+
+using namespace gqa;
+
+extern "C" {
+
+size_t gqa_decode_workspace_bytes_ex(int B, int H, int G, int d, int Nmax, gqa_dtype_t dtype, int split_tokens) {
+  if (B <= 0 || H <= 0 || G <= 0 || Nmax <= 0 || H % G != 0 || (d != 64 && d != 128)) return 0;
+  if (dtype != GQA_F32 && dtype != GQA_BF16) return 0;
+  return workspace_for(make_plan(B, H, G, d, Nmax, dtype, split_tokens), B, H, d);
+}
+
+size_t gqa_decode_workspace_bytes(int B, int H, int G, int d, int Nmax, gqa_dtype_t dtype) {
+  return gqa_decode_workspace_bytes_ex(B, H, G, d, Nmax, dtype, 0);
+}
+
+int gqa_decode_attention_ex(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
+                            float scale, void *out, int B, int H, int G, int d, int Nmax, gqa_dtype_t dtype,
+                            int split_tokens, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (int rc = check_attention_args(q, k_cache, v_cache, seq_lens, out, B, H, G, d, Nmax, dtype)) return rc;
+  if (split_tokens < 0) return GQA_ERR_INVALID_ARG;
+  const Plan pl = make_plan(B, H, G, d, Nmax, dtype, split_tokens);
+  if (!plan_fits(pl, B, G)) return GQA_ERR_UNSUPPORTED;
+  const size_t need = workspace_for(pl, B, H, d);
+  if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+    return GQA_ERR_INVALID_ARG;
+  return run_attention(q, k_cache, v_cache, seq_lens, scale, out, B, H, G, d, Nmax, dtype, pl, workspace, stream);
+}
+
+int gqa_decode_attention_ws(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
+                            float scale, void *out, int B, int H, int G, int d, int Nmax, gqa_dtype_t dtype,
+                            void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return gqa_decode_attention_ex(q, k_cache, v_cache, seq_lens, scale, out, B, H, G, d, Nmax, dtype, 0, workspace,
+                                 workspace_bytes, stream);
+}
+
+int gqa_decode_attention(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
+                         float scale, void *out, int B, int H, int G, int d, int Nmax, gqa_dtype_t dtype,
+                         cudaStream_t stream) {
+  if (int rc = check_attention_args(q, k_cache, v_cache, seq_lens, out, B, H, G, d, Nmax, dtype)) return rc;
+  const Plan pl = make_plan(B, H, G, d, Nmax, dtype, 0);
+  if (!plan_fits(pl, B, G)) return GQA_ERR_UNSUPPORTED;
+  const size_t need = workspace_for(pl, B, H, d);
+  void *ws = nullptr;
+  if (need > 0) {
+    if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return GQA_ERR_NO_MEMORY;
+    }
+  }
+  int rc = run_attention(q, k_cache, v_cache, seq_lens, scale, out, B, H, G, d, Nmax, dtype, pl, ws, stream);
+  if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && rc == GQA_OK) rc = GQA_ERR_CUDA;
+  return rc;
+}
+
+int kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache, int32_t *seq_lens, int B, int G,
+              int d, int Nmax, gqa_dtype_t dtype, cudaStream_t stream) {
+  if (!k_new || !v_new || !k_cache || !v_cache || !seq_lens) return GQA_ERR_INVALID_ARG;
+  if (B <= 0 || G <= 0 || d <= 0 || Nmax <= 0) return GQA_ERR_INVALID_ARG;
+  if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
+  if (B > 2147483647) return GQA_ERR_UNSUPPORTED;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return GQA_ERR_INVALID_ARG;
+  const int chunks = d * (dtype == GQA_BF16 ? 2 : 4) / 16;
+  gqa_kv_append_kernel<<<B, 256, 0, stream>>>(
+      reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new),
+      reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache), seq_lens, G, Nmax, chunks);
+  if (cudaPeekAtLastError() != cudaSuccess) {
+    cudaGetLastError();
+    return GQA_ERR_CUDA;
+  }
+  return GQA_OK;
+}
+
+int mha_to_gqa_meanpool(const void *w, void *w_out, int H, int G, int d, int D, gqa_dtype_t dtype,
+                        cudaStream_t stream) {
+  if (!w || !w_out) return GQA_ERR_INVALID_ARG;
+  if (H <= 0 || G <= 0 || d <= 0 || D <= 0 || H % G != 0) return GQA_ERR_INVALID_ARG;
+  if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
+  const long long per_head = (long long)d * D;
+  const long long total = per_head * G;
+  const int blocks = (int)std::min<long long>((total + 255) / 256, 148LL * 16);
+  if (dtype == GQA_BF16)
+    gqa_meanpool_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16 *>(w), reinterpret_cast<__nv_bfloat16 *>(w_out), G, H / G, per_head);
+  else
+    gqa_meanpool_kernel<float><<<blocks, 256, 0, stream>>>(reinterpret_cast<const float *>(w),
+                                                           reinterpret_cast<float *>(w_out), G, H / G, per_head);
+  if (cudaPeekAtLastError() != cudaSuccess) {
+    cudaGetLastError();
+    return GQA_ERR_CUDA;
+  }
+  return GQA_OK;
+}
+
+int gqa_get_device_error(int32_t *host_err, cudaStream_t stream) {
+  if (!host_err) return GQA_ERR_INVALID_ARG;
+  int v = 0;
+  if (cudaMemcpyFromSymbolAsync(&v, g_device_error, sizeof(int), 0, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return GQA_ERR_CUDA;
+  *host_err = v;
+  return GQA_OK;
+}
+
+const char *gqa_status_string(int status) {
+  switch (status) {
+    case GQA_OK: return "ok";
+    case GQA_ERR_INVALID_ARG: return "invalid argument";
+    case GQA_ERR_UNSUPPORTED: return "unsupported shape";
+    case GQA_ERR_CUDA: return "CUDA error";
+    case GQA_ERR_NO_MEMORY: return "out of device memory";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,302 @@
+// Split-KV GQA decode kernel on CUDA cores (fp32 FMA), for groups of one or
+// two query heads in bf16 (MHA-like shapes, where a K/V row is used by too few
+// heads to fill an MMA tile) and for every shape in fp32.
+//
+// Same TMA pipeline as the MMA kernel.  Inside a warp, 8 lanes share one
+// cached position: lane j holds the 16-byte chunk j of every 128-byte box of
+// the row (so a quarter-warp reads one full 128-byte line of the swizzled
+// tile, free of bank conflicts), the q.k partial sums are reduced over the 8
+// lanes with shuffles, and each 8-lane group keeps its own online-softmax
+// state (running max, sum, output slice) over the positions it visits.
+// The four groups of a warp and the four consumer warps are merged by
+// log-sum-exp at the end.
+#pragma once
+
+#include "gqa_params.cuh"
+#include "gqa_pipeline.cuh"
+
+namespace gqa {
+
+template <typename T, int D_, int NH_, int BLOCK_N_, int STAGES_>
+struct SimtCfg {
+  using Elem = T;
+  static constexpr int D = D_;
+  static constexpr int NH = NH_;  // query heads per CTA
+  static constexpr int ELT = sizeof(T);
+  static constexpr int NBOX = D * ELT / 128;
+  static constexpr int BOX_ELEMS = 128 / ELT;
+  static constexpr int EPC = 16 / ELT;      // elements per 16-byte chunk
+  static constexpr int EPL = NBOX * EPC;    // elements of a row held by one lane
+  static constexpr int CONSUMER_WARPS = 4;
+  static constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;
+  static constexpr int HEADS = NH;
+  using Pipe = KVPipe<NBOX, BLOCK_N_, STAGES_, CONSUMER_WARPS>;
+  static constexpr int BLOCK_N = BLOCK_N_;
+  static constexpr int ROWS_PER_WARP = BLOCK_N / 4;
+  static constexpr int SLOT_WORDS = NH * (EPL + 2) * 8;
+  static constexpr int EPI_BYTES = 3 * SLOT_WORDS * 4;
+  static constexpr int BODY_BYTES = Pipe::PIPE_BYTES > EPI_BYTES ? Pipe::PIPE_BYTES : EPI_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + BODY_BYTES + 2 * Pipe::STAGES * 8;
+  static_assert(ROWS_PER_WARP % 4 == 0, "four 8-lane groups per warp");
+  static_assert(NBOX >= 1, "a row spans at least one 128-byte box");
+};
+
+// Widen the EPC elements of one 16-byte chunk to fp32.
+template <typename T>
+__device__ __forceinline__ void widen_chunk(const uint4 &c, float *f);
+
+template <>
+__device__ __forceinline__ void widen_chunk<__nv_bfloat16>(const uint4 &c, float *f) {
+  f[0] = bf16_lo(c.x); f[1] = bf16_hi(c.x);
+  f[2] = bf16_lo(c.y); f[3] = bf16_hi(c.y);
+  f[4] = bf16_lo(c.z); f[5] = bf16_hi(c.z);
+  f[6] = bf16_lo(c.w); f[7] = bf16_hi(c.w);
+}
+
+template <>
+__device__ __forceinline__ void widen_chunk<float>(const uint4 &c, float *f) {
+  f[0] = __uint_as_float(c.x); f[1] = __uint_as_float(c.y);
+  f[2] = __uint_as_float(c.z); f[3] = __uint_as_float(c.w);
+}
+
+// Round EPC fp32 values to T and store them as one 16-byte chunk.
+template <typename T>
+__device__ __forceinline__ void store_chunk(T *dst, const float *f);
+
+template <>
+__device__ __forceinline__ void store_chunk<__nv_bfloat16>(__nv_bfloat16 *dst, const float *f) {
+  uint4 c;
+  c.x = pack_bf16x2(f[0], f[1]);
+  c.y = pack_bf16x2(f[2], f[3]);
+  c.z = pack_bf16x2(f[4], f[5]);
+  c.w = pack_bf16x2(f[6], f[7]);
+  *reinterpret_cast<uint4 *>(dst) = c;
+}
+
+template <>
+__device__ __forceinline__ void store_chunk<float>(float *dst, const float *f) {
+  *reinterpret_cast<float4 *>(dst) = make_float4(f[0], f[1], f[2], f[3]);
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS)
+    gqa_split_simt_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                          const SplitParams p) {
+  using T = typename C::Elem;
+  using Pipe = typename C::Pipe;
+  constexpr int D = C::D, NH = C::NH, EPC = C::EPC, EPL = C::EPL, NBOX = C::NBOX;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+
+  const int s = blockIdx.x, b = blockIdx.z;
+  const int g = blockIdx.y / p.head_chunks, hc = blockIdx.y % p.head_chunks;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h_first = g * p.n_rep + hc * NH;
+  const int nh = min(NH, p.n_rep - hc * NH);
+
+  int L = p.seq_lens[b];
+  if ((L <= 0 || L > p.Nmax) && s == 0 && hc == 0 && threadIdx.x == 0) flag_error(GQA_DEVERR_ATTN_LEN);
+  L = max(0, min(L, p.Nmax));
+  if (L == 0) {
+    if (s == 0) {
+      T *o = reinterpret_cast<T *>(p.out) + ((size_t)b * p.H + h_first) * D;
+      for (int i = threadIdx.x; i < nh * D; i += C::THREADS) o[i] = T(0.f);
+    }
+    return;
+  }
+  const int start = s * p.chunk;
+  if (start >= L) return;
+  const int end = min(start + p.chunk, L);
+  const int ntiles = (end - start + C::BLOCK_N - 1) / C::BLOCK_N;
+  const bool direct = (L + p.chunk - 1) / p.chunk == 1;
+
+  Pipe pipe;
+  pipe.base = smem_u32(smem);
+  pipe.full0 = pipe.base + C::BODY_BYTES;
+  pipe.empty0 = pipe.full0 + 8 * Pipe::STAGES;
+  if (threadIdx.x == 0) pipe.init();
+  __syncthreads();
+
+  if (warp == C::CONSUMER_WARPS) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      pipe.produce(&tmK, &tmV, C::BOX_ELEMS, b * p.G + g, start, ntiles);
+    }
+    return;
+  }
+
+  const int tg = lane >> 3, j = lane & 7;
+
+  // this lane's slice of q: element e of box bx is d = bx*BOX_ELEMS + j*EPC + e
+  float qf[NH][EPL];
+#pragma unroll
+  for (int h = 0; h < NH; ++h) {
+    const int hh = h_first + (h < nh ? h : 0);
+    const T *qrow = reinterpret_cast<const T *>(p.q) + ((size_t)b * p.H + hh) * D;
+#pragma unroll
+    for (int bx = 0; bx < NBOX; ++bx) {
+      const uint4 c = __ldg(reinterpret_cast<const uint4 *>(qrow + bx * C::BOX_ELEMS + j * EPC));
+      widen_chunk<T>(c, &qf[h][bx * EPC]);
+    }
+  }
+
+  float acc[NH][EPL], m_run[NH], l_run[NH];
+#pragma unroll
+  for (int h = 0; h < NH; ++h) {
+    m_run[h] = -INFINITY;
+    l_run[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[h][e] = 0.f;
+  }
+
+  for (int t = 0; t < ntiles; ++t) {
+    const int st = t % Pipe::STAGES;
+    if (!mbar_wait(pipe.full(st), (t / Pipe::STAGES) & 1)) break;
+    const uint32_t kt = pipe.k_tile(st), vt = pipe.v_tile(st);
+    const int n0 = start + t * C::BLOCK_N;
+#pragma unroll 2
+    for (int i = tg; i < C::ROWS_PER_WARP; i += 4) {
+      const int row = warp * C::ROWS_PER_WARP + i;
+      const int tok = n0 + row;
+      if (n0 + warp * C::ROWS_PER_WARP + (i - tg) >= end) break;  // warp-uniform: no position of this step left
+      const bool valid = tok < end;
+      float kf[EPL];
+#pragma unroll
+      for (int bx = 0; bx < NBOX; ++bx) widen_chunk<T>(lds128(swz128(kt + bx * Pipe::BOX_BYTES, row, j)), &kf[bx * EPC]);
+      float x[NH];
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) dot = fmaf(qf[h][e], kf[e], dot);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+        x[h] = dot * p.scale_log2;
+      }
+      if (valid) {
+        float vf[EPL];
+#pragma unroll
+        for (int bx = 0; bx < NBOX; ++bx) widen_chunk<T>(lds128(swz128(vt + bx * Pipe::BOX_BYTES, row, j)), &vf[bx * EPC]);
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          if (x[h] > m_run[h]) {
+            const float corr = merge_weight(m_run[h], x[h]);
+            m_run[h] = x[h];
+            l_run[h] *= corr;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[h][e] *= corr;
+          }
+          const float pw = exp2f(x[h] - m_run[h]);
+          l_run[h] += pw;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) acc[h][e] = fmaf(pw, vf[e], acc[h][e]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(pipe.empty(st));
+  }
+
+  // ---- merge the four 8-lane groups of the warp (xor 8, xor 16)
+#pragma unroll
+  for (int off = 8; off <= 16; off <<= 1) {
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      const float mo = __shfl_xor_sync(0xffffffffu, m_run[h], off);
+      const float lo = __shfl_xor_sync(0xffffffffu, l_run[h], off);
+      const float M = fmaxf(m_run[h], mo);
+      const float ws = merge_weight(m_run[h], M), wo = merge_weight(mo, M);
+      l_run[h] = l_run[h] * ws + lo * wo;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        const float ao = __shfl_xor_sync(0xffffffffu, acc[h][e], off);
+        acc[h][e] = acc[h][e] * ws + ao * wo;
+      }
+      m_run[h] = M;
+    }
+  }
+
+  // ---- merge the four warps through shared memory (lanes 0..7 hold the state)
+  consumer_bar_sync(C::CONSUMER_WARPS * 32);
+  float *scratch = reinterpret_cast<float *>(smem);
+  if (warp > 0 && lane < 8) {
+    float *slot = scratch + (warp - 1) * C::SLOT_WORDS + lane;
+    int i = 0;
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) slot[8 * i++] = acc[h][e];
+      slot[8 * i++] = m_run[h];
+      slot[8 * i++] = l_run[h];
+    }
+  }
+  consumer_bar_sync(C::CONSUMER_WARPS * 32);
+  if (warp != 0 || lane >= 8) return;
+
+#pragma unroll
+  for (int h = 0; h < NH; ++h) {
+    const int base = h * (EPL + 2);
+    float mk[3], lk[3], wk[3];
+    float M = m_run[h];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const float *slot = scratch + k * C::SLOT_WORDS + lane;
+      mk[k] = slot[8 * (base + EPL)];
+      lk[k] = slot[8 * (base + EPL + 1)];
+      M = fmaxf(M, mk[k]);
+    }
+    const float ws = merge_weight(m_run[h], M);
+    float l = l_run[h] * ws;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      wk[k] = merge_weight(mk[k], M);
+      l += lk[k] * wk[k];
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      float v = acc[h][e] * ws;
+#pragma unroll
+      for (int k = 0; k < 3; ++k) v += scratch[k * C::SLOT_WORDS + lane + 8 * (base + e)] * wk[k];
+      acc[h][e] = v;
+    }
+    m_run[h] = M;
+    l_run[h] = l;
+  }
+
+#pragma unroll
+  for (int h = 0; h < NH; ++h) {
+    if (h >= nh) break;
+    const size_t bh = (size_t)b * p.H + h_first + h;
+    if (direct) {
+      const float inv = 1.f / l_run[h];
+      T *orow = reinterpret_cast<T *>(p.out) + bh * D;
+#pragma unroll
+      for (int bx = 0; bx < NBOX; ++bx) {
+        float f[EPC];
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) f[e] = acc[h][bx * EPC + e] * inv;
+        store_chunk<T>(orow + bx * C::BOX_ELEMS + j * EPC, f);
+      }
+    } else {
+      float *prow = p.o_part + (bh * p.S_max + s) * D;
+#pragma unroll
+      for (int bx = 0; bx < NBOX; ++bx)
+#pragma unroll
+        for (int e = 0; e < EPC; e += 4)
+          *reinterpret_cast<float4 *>(prow + bx * C::BOX_ELEMS + j * EPC + e) =
+              make_float4(acc[h][bx * EPC + e], acc[h][bx * EPC + e + 1], acc[h][bx * EPC + e + 2],
+                          acc[h][bx * EPC + e + 3]);
+      if (j == 0) reinterpret_cast<float2 *>(p.ml_part)[bh * p.S_max + s] = make_float2(m_run[h], l_run[h]);
+    }
+  }
+}
+
+}  // namespace gqa

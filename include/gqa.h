@@ -1,0 +1,170 @@
+/*
+ * gqa.h — C ABI of libgqa.so: grouped-query decode attention over a KV cache
+ * on one NVIDIA B300 (sm_103a).
+ *
+ * The operation (GQA paper, Ainslie et al., section 2.2; 2kiu.com MHA/MQA/GQA
+ * explainer, section 3): H query heads are split into G contiguous groups of
+ * n_rep = H / G heads; every head of group g attends to the one K head and the
+ * one V head of that group.  G = H is multi-head attention, G = 1 multi-query
+ * attention.  One autoregressive decode step (fogdragon's CSDN blog on
+ * MQA/GQA, section "KV Cache") first appends the new token's k and v to the
+ * cache and then, per head, takes softmax(q.K^T * scale) over the cached
+ * positions and the weighted sum of V.
+ *
+ * Conventions shared by every call:
+ *  - Ownership: the caller owns every buffer.  All tensor pointers are DEVICE
+ *    pointers to contiguous row-major data in the layouts stated per call;
+ *    the library keeps no pointer after a call returns.
+ *  - Element types: q, k_cache, v_cache, out (and k_new, v_new) share one
+ *    gqa_dtype_t.  Lengths are int32.
+ *  - Asynchrony: every call only enqueues work on `stream` and returns a host
+ *    status without synchronising (except gqa_get_device_error).
+ *  - Host-checked errors: bad arguments are rejected before any launch and
+ *    return a negative gqa_status_t; nothing is enqueued then.
+ *  - Device-detected errors: lengths outside their valid range are clamped
+ *    (see each call), never trap, and set a bit in a per-device error word
+ *    that gqa_get_device_error reads.  The kernels contain no unbounded wait:
+ *    a pipeline wait that exceeds about one second sets GQA_DEVERR_TIMEOUT and
+ *    the block returns.
+ *  - No C++ exception crosses this interface.
+ */
+#ifndef GQA_DECODE_H_
+#define GQA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GQA_F32 = 0,  /* IEEE binary32 */
+    GQA_BF16 = 1  /* bfloat16, fp32 accumulation inside the kernels */
+} gqa_dtype_t;
+
+typedef enum {
+    GQA_OK = 0,
+    GQA_ERR_INVALID_ARG = -1, /* null pointer, non-positive size, H % G != 0, bad dtype,
+                                 misaligned pointer, workspace too small */
+    GQA_ERR_UNSUPPORTED = -2, /* head dimension d not in {64, 128} */
+    GQA_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed */
+    GQA_ERR_NO_MEMORY = -4    /* stream-ordered workspace allocation failed */
+} gqa_status_t;
+
+/* Bits of the device error word. */
+#define GQA_DEVERR_ATTN_LEN 1   /* attention saw seq_lens[b] <= 0 or > Nmax */
+#define GQA_DEVERR_APPEND_LEN 2 /* kv_append saw seq_lens[b] < 0 or >= Nmax */
+#define GQA_DEVERR_TIMEOUT 4    /* a pipeline wait gave up after its time limit */
+
+/*
+ * gqa_decode_attention — attention of one decode token per sequence.
+ *
+ *   out[b,h,:] = sum_{n < L_b} softmax_n( scale * <q[b,h,:], K[b,g,n,:]> ) * V[b,g,n,:]
+ *   with g = h / (H/G) and L_b = seq_lens[b].
+ *
+ * Source: fogdragon's CSDN blog on MQA/GQA, section "KV Cache" (logits =
+ * einsum("bhd,bhnd->bhn"), softmax(logits / sqrt(d)), einsum("bhn,bhnd->bhd"))
+ * with the KV head shared by a group as in the GQA paper, section 2.2.
+ *
+ *   q        [B, H, d]        query of the current token
+ *   k_cache  [B, G, Nmax, d]  keys;   rows n >= L_b are never read
+ *   v_cache  [B, G, Nmax, d]  values; rows n >= L_b are never read
+ *   seq_lens [B] int32, DEVICE memory: cached length of each sequence
+ *   scale    logit scale (1/sqrt(d) for the standard step)
+ *   out      [B, H, d]        result, rounded to nearest even in `dtype`
+ *   d in {64, 128}; H % G == 0; pointers 16-byte aligned.
+ *
+ * A length L_b > Nmax is treated as Nmax and L_b <= 0 gives out[b] = 0; both
+ * set GQA_DEVERR_ATTN_LEN.  Long sequences are split across thread blocks
+ * whose partial results are merged by log-sum-exp in a second kernel; the
+ * partials live in a workspace taken from the stream-ordered allocator
+ * (cudaMallocAsync / cudaFreeAsync on `stream`).
+ */
+int gqa_decode_attention(const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *seq_lens, float scale, void *out,
+                         int B, int H, int G, int d, int Nmax, gqa_dtype_t dtype,
+                         cudaStream_t stream);
+
+/*
+ * Bytes of workspace gqa_decode_attention_ws needs for this shape on the
+ * current device (0 when no split is ever needed).  Host-only; enqueues
+ * nothing.  Returns 0 for invalid shapes as well.
+ */
+size_t gqa_decode_workspace_bytes(int B, int H, int G, int d, int Nmax, gqa_dtype_t dtype);
+
+/*
+ * gqa_decode_attention_ws — as gqa_decode_attention, with the split partials
+ * in a caller-provided device workspace of at least
+ * gqa_decode_workspace_bytes(...) bytes (256-byte aligned).  Allocates
+ * nothing, so it can be captured in a CUDA graph.  Calls that share one
+ * workspace must not overlap on the device.
+ */
+int gqa_decode_attention_ws(const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *seq_lens, float scale, void *out,
+                            int B, int H, int G, int d, int Nmax, gqa_dtype_t dtype,
+                            void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * gqa_decode_attention_ex — as gqa_decode_attention_ws, with the number of
+ * positions per split forced to `split_tokens` (rounded up to the kernel's
+ * tile of 32..128 positions; 0 = the automatic choice).  For tests of the
+ * split/combine path and for tuning.  split_tokens < 0 is rejected.
+ * gqa_decode_workspace_bytes_ex gives the workspace that choice needs.
+ */
+size_t gqa_decode_workspace_bytes_ex(int B, int H, int G, int d, int Nmax, gqa_dtype_t dtype,
+                                     int split_tokens);
+int gqa_decode_attention_ex(const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *seq_lens, float scale, void *out,
+                            int B, int H, int G, int d, int Nmax, gqa_dtype_t dtype,
+                            int split_tokens, void *workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
+
+/*
+ * kv_append — the cache concatenation of one decode step (fogdragon's CSDN
+ * blog, section "KV Cache": K = cat([K_prev, k]), V = cat([V_prev, v])).
+ *
+ *   k_cache[b,g,L_b,:] = k_new[b,g,:];  v_cache[b,g,L_b,:] = v_new[b,g,:];  seq_lens[b] = L_b + 1
+ *
+ *   k_new, v_new [B, G, d]; k_cache, v_cache [B, G, Nmax, d];
+ *   seq_lens [B] int32 DEVICE memory, read and updated in place.
+ * Rows are copied bit-exactly.  A batch with L_b < 0 or L_b >= Nmax is left
+ * untouched (no write, no increment) and sets GQA_DEVERR_APPEND_LEN.
+ * Calling kv_append and then gqa_decode_attention with the same seq_lens on
+ * the same stream is one decode step; the new token takes part in it.
+ */
+int kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+              int32_t *seq_lens, int B, int G, int d, int Nmax, gqa_dtype_t dtype,
+              cudaStream_t stream);
+
+/*
+ * mha_to_gqa_meanpool — checkpoint conversion of the GQA paper, section 2.1
+ * and 2.2 (2kiu.com explainer, section 4.3): the key (or value) projection of
+ * KV head g is the mean of the projections of the n_rep = H/G heads of
+ * group g.
+ *
+ *   w_out[g, :, :] = (1/n_rep) * sum_{j < n_rep} w[g*n_rep + j, :, :]
+ *
+ *   w [H, d, D] (heads leading; d = head dim, D = model width), w_out [G, d, D].
+ * Any layout with the head axis leading works: only d*D, the element count
+ * per head, matters.  A bias [H, d] is pooled the same way with D = 1.
+ * Accumulates in fp32; the result is rounded to `dtype`.
+ */
+int mha_to_gqa_meanpool(const void *w, void *w_out, int H, int G, int d, int D,
+                        gqa_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * Reads the current device's error word into *host_err and clears it.  This
+ * call synchronises `stream` (it copies the word to the host on it).
+ */
+int gqa_get_device_error(int32_t *host_err, cudaStream_t stream);
+
+/* Static, human-readable text of a gqa_status_t value. */
+const char *gqa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_DECODE_H_ */

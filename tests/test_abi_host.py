@@ -1,0 +1,127 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function include/gqa.h declares, and rejects bad arguments before any
+CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import grouped_query_decode_kv_b300 as gqa
+
+HEADER_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(HEADER_DIR)):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(HEADER_DIR, fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^(?:const\s+)?(?:int|size_t|char|void)\s*\**\s*(\w+)\s*\(", text, flags=re.M):
+            names.append(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(gqa.library_path()):
+        import __graft_entry__
+        __graft_entry__.build()
+    return gqa.load_library()
+
+
+def test_header_declares_the_abi():
+    names = _declared_functions()
+    for required in ("gqa_decode_attention", "gqa_decode_attention_ws", "gqa_decode_workspace_bytes",
+                     "kv_append", "mha_to_gqa_meanpool", "gqa_get_device_error", "gqa_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_function(lib):
+    names = _declared_functions()
+    assert names
+    for n in names:
+        assert hasattr(lib, n), f"libgqa.so does not export {n}"
+    assert set(gqa.EXPORTED_SYMBOLS) <= set(names)
+
+
+def test_status_strings(lib):
+    assert gqa.gqa_status_string(0) == "ok"
+    assert "invalid" in gqa.gqa_status_string(-1)
+    assert "unsupported" in gqa.gqa_status_string(-2)
+    assert gqa.gqa_status_string(12345) == "unknown status"
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every case below is rejected on the host
+
+
+def _attn(lib, q=FAKE, k=FAKE, v=FAKE, sl=FAKE, out=FAKE, B=2, H=8, G=2, d=128, N=64, dt=1):
+    return lib.gqa_decode_attention(q, k, v, sl, 0.1, out, B, H, G, d, N, dt, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=0), -1), (dict(k=0), -1), (dict(v=0), -1), (dict(sl=0), -1), (dict(out=0), -1),
+    (dict(B=0), -1), (dict(H=0), -1), (dict(G=0), -1), (dict(N=0), -1), (dict(d=-1), -1),
+    (dict(H=8, G=3), -1), (dict(dt=7), -1), (dict(d=96), -2), (dict(d=256), -2),
+    (dict(q=FAKE + 4), -1), (dict(k=FAKE + 8), -1), (dict(B=70000), -2),
+])
+def test_attention_rejects_bad_arguments(lib, kw, status):
+    assert _attn(lib, **kw) == status
+
+
+def test_ws_variant_rejects_missing_workspace(lib):
+    need = lib.gqa_decode_workspace_bytes_ex(2, 8, 2, 128, 4096, 1, 256)
+    assert need > 0
+    rc = lib.gqa_decode_attention_ex(FAKE, FAKE, FAKE, FAKE, 0.1, FAKE, 2, 8, 2, 128, 4096, 1, 256, None, 0, None)
+    assert rc == -1
+    rc = lib.gqa_decode_attention_ex(FAKE, FAKE, FAKE, FAKE, 0.1, FAKE, 2, 8, 2, 128, 4096, 1, 256, FAKE, need - 1,
+                                     None)
+    assert rc == -1
+    rc = lib.gqa_decode_attention_ex(FAKE, FAKE, FAKE, FAKE, 0.1, FAKE, 2, 8, 2, 128, 4096, 1, -5, FAKE, need, None)
+    assert rc == -1
+
+
+def test_workspace_bytes(lib):
+    # a single split needs no workspace; forced splits need the partials
+    assert lib.gqa_decode_workspace_bytes_ex(1, 8, 2, 64, 128, 0, 128) == 0
+    need = lib.gqa_decode_workspace_bytes_ex(2, 8, 2, 128, 1024, 1, 256)
+    parts = 2 * 8 * 4
+    assert need >= parts * 128 * 4 + parts * 2 * 4
+    assert lib.gqa_decode_workspace_bytes(2, 8, 3, 128, 1024, 1) == 0      # invalid shape
+    assert lib.gqa_decode_workspace_bytes(2, 8, 2, 96, 1024, 1) == 0       # unsupported d
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, FAKE, FAKE, FAKE, FAKE, 2, 2, 128, 64, 1), -1),
+    ((FAKE, FAKE, FAKE, FAKE, 0, 2, 2, 128, 64, 1), -1),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 0, 2, 128, 64, 1), -1),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 100, 64, 1), -2),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 128, 64, 9), -1),
+    ((FAKE + 2, FAKE, FAKE, FAKE, FAKE, 2, 2, 128, 64, 1), -1),
+])
+def test_kv_append_rejects_bad_arguments(lib, args, status):
+    assert lib.kv_append(*args, None) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, FAKE, 8, 2, 128, 64, 1), -1),
+    ((FAKE, FAKE, 8, 3, 128, 64, 1), -1),
+    ((FAKE, FAKE, 8, 2, 0, 64, 1), -1),
+    ((FAKE, FAKE, 8, 2, 128, 64, 5), -1),
+])
+def test_meanpool_rejects_bad_arguments(lib, args, status):
+    assert lib.mha_to_gqa_meanpool(*args, None) == status
+
+
+def test_device_error_needs_output_pointer(lib):
+    assert lib.gqa_get_device_error(None, None) == -1
+
+
+def test_binding_raises_without_cuda_tensors():
+    import torch
+    q = torch.zeros(1, 8, 64)
+    k = torch.zeros(1, 2, 16, 64)
+    with pytest.raises((ValueError, RuntimeError)):
+        gqa.gqa_decode_attention(q, k, k, torch.zeros(1, dtype=torch.int32), 0.1, q.clone())

@@ -1,0 +1,238 @@
+"""Parity of the CUDA path (called through the C ABI) with the fp64 CPU oracle
+on the same seeded inputs.
+
+Tolerance for attention outputs: |gpu - oracle| <= 1e-2 + 1e-2 * |oracle|
+elementwise (bf16 or fp32 inputs, fp32 accumulation).  kv_append is compared
+byte for byte, including every cache byte it must not touch.
+"""
+import numpy as np
+import pytest
+import torch
+
+import grouped_query_decode_kv_b300 as gqa
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 1e-2
+RTOL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    torch.cuda.set_device(0)
+    gqa.load_library()
+    gqa.gqa_get_device_error()  # start from a clear error word
+    yield
+
+
+def assert_parity(got: np.ndarray, ref: np.ndarray, what: str = ""):
+    assert got.shape == ref.shape
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} elements out of tolerance; worst at {i}: "
+                             f"gpu {got[i]:.6g} oracle {ref[i]:.6g}")
+
+
+def gpu_attention(x, scale, split_tokens=None, stream=None):
+    dev = torch.device("cuda")
+    q, k, v = x["q"].to(dev), x["k_cache"].to(dev), x["v_cache"].to(dev)
+    sl = x["seq_lens"].to(dev)
+    out = torch.full_like(q, float("nan"))
+    if split_tokens is None:
+        gqa.gqa_decode_attention(q, k, v, sl, scale, out, stream=stream)
+    else:
+        B, H, d = q.shape
+        G, N = k.shape[1], k.shape[2]
+        need = gqa.gqa_decode_workspace_bytes_ex(B, H, G, d, N, q.dtype, split_tokens)
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        gqa.gqa_decode_attention_ex(q, k, v, sl, scale, out, split_tokens, ws, stream=stream)
+    torch.cuda.synchronize()
+    return out.double().cpu().numpy()
+
+
+def check_case(w, seq_lens=None, split_tokens=None):
+    x = workloads.make_inputs(w, seq_lens=seq_lens)
+    ref = oracle.decode_attention(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], w.scale)
+    got = gpu_attention(x, w.scale, split_tokens)
+    assert_parity(got, ref, f"{w.name} split={split_tokens}")
+    assert gqa.gqa_get_device_error() == 0
+
+
+# ------------------------------------------------------------ small shapes
+def _small(H, G, d, N, dtype, lens, index):
+    return workloads.Workload(f"small_h{H}_g{G}_d{d}_{dtype}", len(lens), H, G, d, N, dtype,
+                              ("fixed", N), index)
+
+
+SMALL_SHAPES = [
+    # (H, G): n_rep = 1, 2, 3, 4, 5, 8, 12, 16, 24, 32, 48, 64, 128
+    (8, 8), (8, 4), (6, 2), (8, 2), (10, 2), (16, 2), (24, 2), (32, 2), (48, 2), (64, 2), (96, 2),
+    (64, 1), (128, 1),
+]
+
+
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("H,G", SMALL_SHAPES)
+def test_small_bf16_shapes(H, G, d):
+    N = 700
+    lens = torch.tensor([700, 1, 129, 64, 383], dtype=torch.int32)
+    w = _small(H, G, d, N, "bf16", lens.tolist(), 3000 + H + G + d)
+    check_case(w, lens)
+
+
+@pytest.mark.parametrize("split_tokens", [32, 64, 128, 256, 1000])
+@pytest.mark.parametrize("H,G", [(8, 8), (8, 4), (16, 2), (64, 2), (64, 1)])
+def test_forced_splits_exercise_the_combine(H, G, split_tokens):
+    N = 900
+    lens = torch.tensor([900, 2, 511, 513, 64], dtype=torch.int32)
+    w = _small(H, G, 128, N, "bf16", lens.tolist(), 4000 + H + G)
+    check_case(w, lens, split_tokens)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("H,G", [(8, 8), (8, 4), (8, 2), (12, 2), (16, 2), (8, 1)])
+@pytest.mark.parametrize("split_tokens", [None, 64])
+def test_small_fp32_shapes(H, G, d, split_tokens):
+    N = 300
+    lens = torch.tensor([300, 1, 77, 32], dtype=torch.int32)
+    w = _small(H, G, d, N, "f32", lens.tolist(), 5000 + H + G + d)
+    check_case(w, lens, split_tokens)
+
+
+def test_tiny_config():
+    check_case(workloads.workload("tiny"))
+
+
+def test_nonfinite_tail_never_leaks():
+    """Rows at and past L hold NaN (the input recipe); also put +inf there."""
+    w = _small(16, 2, 128, 256, "bf16", [1, 2, 3], 6001)
+    x = workloads.make_inputs(w, seq_lens=torch.tensor([100, 17, 255], dtype=torch.int32))
+    x["k_cache"][0, :, 100:] = float("inf")
+    x["v_cache"][0, :, 100:] = float("inf")
+    ref = oracle.decode_attention(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], w.scale)
+    for split in (None, 64):
+        assert_parity(gpu_attention(x, w.scale, split), ref, f"poisoned split={split}")
+
+
+def test_workspace_variant_matches_default_bitwise():
+    w = workloads.workload("gqa8").replace(B=4, Nmax=2048, index=6002)
+    x = workloads.make_inputs(w)
+    a = gpu_attention(x, w.scale)
+    dev = torch.device("cuda")
+    q, k, v, sl = x["q"].to(dev), x["k_cache"].to(dev), x["v_cache"].to(dev), x["seq_lens"].to(dev)
+    out = torch.empty_like(q)
+    ws = torch.empty(max(gqa.gqa_decode_workspace_bytes(4, 64, 8, 128, 2048, torch.bfloat16), 1),
+                     dtype=torch.uint8, device=dev)
+    gqa.gqa_decode_attention_ws(q, k, v, sl, w.scale, out, ws)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out.double().cpu().numpy(), a)
+
+
+def test_repeated_calls_are_deterministic_and_stream_safe():
+    w = workloads.workload("mqa").replace(B=8, index=6003)
+    x = workloads.make_inputs(w)
+    a = gpu_attention(x, w.scale)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        b = gpu_attention(x, w.scale, stream=s)
+    np.testing.assert_array_equal(a, b)
+
+
+# ------------------------------------------------------------ device errors
+def test_empty_and_overlong_lengths_are_clamped_and_flagged():
+    w = _small(8, 2, 128, 128, "bf16", [0, 0, 0], 6004)
+    sl = torch.tensor([0, 500, 40], dtype=torch.int32)
+    x = workloads.make_inputs(w, seq_lens=torch.tensor([128, 128, 40], dtype=torch.int32), poison=False)
+    x["seq_lens"] = sl
+    ref = oracle.decode_attention(x["q"], x["k_cache"], x["v_cache"], sl, w.scale)
+    got = gpu_attention(x, w.scale)
+    assert np.all(got[0] == 0)
+    assert_parity(got, ref, "clamped lengths")
+    err = gqa.gqa_get_device_error()
+    assert err & gqa.DEVERR_ATTN_LEN
+    assert gqa.gqa_get_device_error() == 0  # read clears it
+
+
+# ------------------------------------------------------------ kv_append
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_kv_append_is_bit_exact(dtype, d):
+    B, G, N = 5, 3, 40
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    gen = torch.Generator().manual_seed(6100 + d)
+    # canary-filled caches: random bytes everywhere
+    elt = 2 if dtype == "bf16" else 4
+    k = torch.randint(0, 256, (B, G, N, d * elt), generator=gen, dtype=torch.uint8).view(dt)
+    v = torch.randint(0, 256, (B, G, N, d * elt), generator=gen, dtype=torch.uint8).view(dt)
+    assert k.shape == (B, G, N, d)
+    kn = torch.randn(B, G, d, generator=gen).to(dt)
+    vn = torch.randn(B, G, d, generator=gen).to(dt)
+    sl = torch.tensor([0, 17, N - 1, N, -1], dtype=torch.int32)
+    k_ref, v_ref, sl_ref, skipped = oracle.kv_append(kn, vn, k, v, sl)
+    assert skipped == 2
+    dev = torch.device("cuda")
+    kd, vd, sld = k.to(dev), v.to(dev), sl.to(dev)
+    gqa.kv_append(kn.to(dev), vn.to(dev), kd, vd, sld)
+    torch.cuda.synchronize()
+    assert torch.equal(kd.cpu().view(torch.uint8), k_ref.view(torch.uint8))
+    assert torch.equal(vd.cpu().view(torch.uint8), v_ref.view(torch.uint8))
+    assert torch.equal(sld.cpu(), sl_ref)
+    assert gqa.gqa_get_device_error() & gqa.DEVERR_APPEND_LEN
+
+
+@pytest.mark.parametrize("name", ["tiny", "mha", "gqa8", "mqa"])
+def test_decode_step_append_then_attend(name):
+    """One full decode step: kv_append, then attention with the same lengths."""
+    w = workloads.workload(name)
+    if w.B * w.G * w.Nmax * w.d > 2 ** 28:
+        w = w.replace(B=2)
+    sl0 = workloads.make_seq_lens(w) - 1        # room for the new token
+    sl0 = torch.clamp(sl0, min=0)
+    x = workloads.make_inputs(w, seq_lens=sl0)
+    k_ref, v_ref, sl_ref, skipped = oracle.kv_append(x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], sl0)
+    assert skipped == 0
+    ref = oracle.decode_attention(x["q"], k_ref, v_ref, sl_ref, w.scale)
+    dev = torch.device("cuda")
+    q, k, v, sl = x["q"].to(dev), x["k_cache"].to(dev), x["v_cache"].to(dev), sl0.to(dev)
+    out = torch.empty_like(q)
+    gqa.kv_append(x["k_new"].to(dev), x["v_new"].to(dev), k, v, sl)
+    gqa.gqa_decode_attention(q, k, v, sl, w.scale, out)
+    torch.cuda.synchronize()
+    assert torch.equal(sl.cpu(), sl_ref)
+    assert_parity(out.double().cpu().numpy(), ref, f"step {name}")
+    assert gqa.gqa_get_device_error() == 0
+
+
+# ------------------------------------------------------------ meanpool
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("H,G", [(32, 8), (64, 8), (8, 1), (8, 8), (12, 4)])
+def test_meanpool_matches_oracle(H, G, dtype):
+    d, D = 128, 96
+    w = workloads.make_projection(H, d, D, 6200 + H + G, dtype)
+    ref = oracle.meanpool(w, G)
+    dev = torch.device("cuda")
+    wo = torch.empty(G, d, D, dtype=dtype, device=dev)
+    gqa.mha_to_gqa_meanpool(w.to(dev), wo)
+    torch.cuda.synchronize()
+    got = wo.double().cpu().numpy()
+    # fp32 sum of H/G terms, then one rounding to the output type
+    eps = 2.0 ** -8 if dtype == torch.bfloat16 else 2.0 ** -22
+    scale = np.abs(w.double().numpy()).reshape(G, H // G, d, D).max(axis=1)
+    assert np.all(np.abs(got - ref) <= eps * np.abs(ref) + (H // G) * 2.0 ** -23 * scale + 1e-30)
+
+
+# ------------------------------------------------------------ full-size configs
+FULL = ["tiny", "mha", "gqa8", "mqa", "long"] + workloads.sweep_names()
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_config_matches_oracle(name):
+    check_case(workloads.workload(name))
