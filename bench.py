@@ -1,0 +1,597 @@
+#!/usr/bin/env python
+"""Benchmark of one grouped-query decode step on B300.
+
+A step is one pass of the whole decode path over one batch: ``kv_append``
+(the new token's K/V written into the cache) followed by
+``gqa_decode_attention`` (split-KV kernel + log-sum-exp combine), both
+through the C ABI of ``libgqa.so``.  Inputs are seeded synthetic N(0, 1)
+tensors resident in HBM.  Every step gets its own copy of the lengths
+``seq_lens = L - 1``, so that each step appends at row L-1 and attends over
+exactly the workload's L_b positions; the caches rotate through enough
+copies that the bytes read between two uses of one copy exceed three L2
+sizes.
+
+Default workload: MHA decode, B=8, H=G=32, d=128, N=4096, bf16.  ``value`` is
+the algorithmic HBM bytes of all steps on all ranks (K/V rows read once, q
+read, out written, new K/V rows read and written) over the slowest rank's
+time, in GB/s.  The line also carries the roofline of the attention call,
+the end-to-end figure through host buffers, a CPU baseline (the fp64
+oracle on a bounded sample) and a per-workload table (µs per call, GB/s)
+covering the other decode workloads and the group-count sweep.
+
+Usage:
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference] [--no-table]
+  torchrun --nproc-per-node N bench.py --gpus N ...   (N > 1: one replica per GPU)
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+from grouped_query_decode_kv_b300 import cost  # noqa: E402
+
+METRIC = "GQA decode attention µs/step and achieved HBM GB/s (fraction of B300 peak) vs G"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6400.0
+TABLE_WORKLOADS = ["tiny", "mha", "gqa8", "mqa", "long"] + workloads.sweep_names()
+CSRC = os.path.join(ROOT, "grouped_query_decode_kv_b300", "csrc")
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+# ----------------------------------------------------------------- helpers
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+def hbm_peak():
+    pk = measured_peaks()
+    if "hbm_gbs" in pk:
+        return float(pk["hbm_gbs"]), "measured (copy, MEASURED_PEAKS.json)"
+    return FALLBACK_HBM_GBS, "fallback 6.4 TB/s"
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources; an ncu traffic figure is only reported while
+    it was taken on the same sources."""
+    h = hashlib.sha256()
+    for fn in sorted(os.listdir(CSRC)):
+        if fn.endswith((".cu", ".cuh")):
+            with open(os.path.join(CSRC, fn), "rb") as f:
+                h.update(fn.encode() + f.read())
+    with open(os.path.join(ROOT, "include", "gqa.h"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_name: str):
+    """DRAM bytes per launch of the split kernel from the committed ncu
+    summary of this workload, if it was taken on the current sources."""
+    path = os.path.join(PROFILES, f"gqa_split_{workload_name}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            line = line.strip().strip("`- ")
+            if ":" in line:
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return int(float(vals["traffic_bytes_per_call"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of this GPU's SM clock and throttle
+    reasons while the benchmark runs; read-only."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", uuid, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        """Median SM clock and the active throttle reasons of the samples
+        taken within [t0 - 0.25 s, t1 + 0.25 s] (wall clock)."""
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                    rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+                except (ValueError, IndexError):
+                    continue
+        try:
+            os.unlink(self.path)
+        except OSError:
+            pass
+        sel = [r for r in rows if t0 - 0.25 <= r[0] <= t1 + 0.25]
+        if not sel and rows:
+            sel = [min(rows, key=lambda r: abs(r[0] - 0.5 * (t0 + t1)))]
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in sel for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": max(r[2] for r in sel),
+                "reasons": reasons, "samples": len(sel)}
+
+
+# ----------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a host scalar over all ranks (the slowest rank's time)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def aggregate(per_rank_bytes: int, seconds_max: float, world: int) -> float:
+    """Whole-job GB/s: the bytes every replica processed over the slowest
+    replica's time (weak scaling: each rank runs the full workload)."""
+    return per_rank_bytes * world / seconds_max / 1e9
+
+
+# ----------------------------------------------------------------- GPU state
+class DecodeState:
+    """Device tensors of one workload: `copies` rotating cache sets, one
+    lengths row per step, and the step's q / k_new / v_new / out."""
+
+    def __init__(self, w: workloads.Workload, steps_total: int, device, copies: int, seed: int = 0):
+        dt = w.torch_dtype
+        self.w = w
+        self.lens = workloads.make_seq_lens(w).to(torch.int64)
+        g = torch.Generator(device=device).manual_seed(1000 + w.index + seed)
+        self.k = [torch.randn(w.B, w.G, w.Nmax, w.d, generator=g, device=device).to(dt) for _ in range(copies)]
+        self.v = [torch.randn(w.B, w.G, w.Nmax, w.d, generator=g, device=device).to(dt) for _ in range(copies)]
+        self.q = [torch.randn(w.B, w.H, w.d, generator=g, device=device).to(dt) for _ in range(copies)]
+        self.kn = [torch.randn(w.B, w.G, w.d, generator=g, device=device).to(dt) for _ in range(copies)]
+        self.vn = [torch.randn(w.B, w.G, w.d, generator=g, device=device).to(dt) for _ in range(copies)]
+        self.out = [torch.empty(w.B, w.H, w.d, dtype=dt, device=device) for _ in range(copies)]
+        pre = torch.clamp(self.lens - 1, min=0).to(torch.int32)
+        self.sl = pre.unsqueeze(0).repeat(steps_total, 1).to(device).contiguous()
+        self.copies = copies
+        self.lens_after = torch.clamp(self.lens - 1, min=0) + 1
+        from grouped_query_decode_kv_b300 import gqa_decode_workspace_bytes
+        self.ws_bytes = gqa_decode_workspace_bytes(w.B, w.H, w.G, w.d, w.Nmax, dt)
+
+    def reset_lengths(self):
+        pre = torch.clamp(self.lens - 1, min=0).to(torch.int32)
+        self.sl.copy_(pre.unsqueeze(0).expand_as(self.sl))
+
+    @property
+    def attention_bytes(self) -> int:
+        return cost.decode_attention_bytes(self.lens_after.tolist(), self.w.H, self.w.G, self.w.d, self.w.elt)
+
+    @property
+    def append_bytes(self) -> int:
+        return cost.kv_append_bytes(self.w.B, self.w.G, self.w.d, self.w.elt)
+
+    @property
+    def launches_per_step(self) -> int:
+        return 2 + (1 if self.ws_bytes > 0 else 0)
+
+
+def copies_for(w: workloads.Workload, l2_bytes: int, mem_budget: int) -> int:
+    cache = cost.kv_cache_bytes(w.B, w.G, w.Nmax, w.d, w.elt)
+    c = max(2, math.ceil(3 * l2_bytes / max(cache, 1)))
+    return max(1, min(c, mem_budget // max(cache, 1), 64))
+
+
+def run_steps(st: DecodeState, first: int, count: int, ev=None):
+    """`count` decode steps; step i uses cache copy i % copies and lengths row
+    i.  With `ev` (a list of event pairs) the attention call of every step is
+    bracketed by CUDA events on the current stream."""
+    import grouped_query_decode_kv_b300 as gqa
+    w = st.w
+    for i in range(first, first + count):
+        c = i % st.copies
+        sl = st.sl[i]
+        gqa.kv_append(st.kn[c], st.vn[c], st.k[c], st.v[c], sl)
+        if ev is not None:
+            ev[i - first][0].record()
+        gqa.gqa_decode_attention(st.q[c], st.k[c], st.v[c], sl, w.scale, st.out[c])
+        if ev is not None:
+            ev[i - first][1].record()
+
+
+def time_attention_only(w: workloads.Workload, device, iters: int, warm: int, l2_bytes: int, mem_budget: int):
+    """Per-workload table row: the attention call alone and kv_append alone,
+    CUDA events around each call, lengths fixed at L_b."""
+    import grouped_query_decode_kv_b300 as gqa
+    copies = copies_for(w, l2_bytes, mem_budget)
+    st = DecodeState(w, 1, device, copies, seed=17)
+    full = st.lens.to(torch.int32).to(device)
+    ws = torch.empty(max(st.ws_bytes, 1), dtype=torch.uint8, device=device)
+    for i in range(warm):
+        c = i % copies
+        gqa.gqa_decode_attention_ws(st.q[c], st.k[c], st.v[c], full, w.scale, st.out[c], ws)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    torch.cuda.synchronize()
+    for i in range(iters):
+        c = i % copies
+        evs[i][0].record()
+        gqa.gqa_decode_attention_ws(st.q[c], st.k[c], st.v[c], full, w.scale, st.out[c], ws)
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    ts = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+    # kv_append alone (lengths reset below L so that every append lands)
+    sl = torch.clamp(st.lens - 1, min=0).to(torch.int32).to(device)
+    sl_rows = sl.unsqueeze(0).repeat(iters, 1).contiguous()
+    aev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for i in range(iters):
+        c = i % copies
+        aev[i][0].record()
+        gqa.kv_append(st.kn[c], st.vn[c], st.k[c], st.v[c], sl_rows[i])
+        aev[i][1].record()
+    torch.cuda.synchronize()
+    ta = sorted(a.elapsed_time(b) * 1e3 for a, b in aev)
+    err = gqa.gqa_get_device_error()
+    lens_full = st.lens.tolist()
+    abytes = cost.decode_attention_bytes(lens_full, w.H, w.G, w.d, w.elt)
+    med = statistics.median(ts)
+    peak, _ = hbm_peak()
+    row = {
+        "B": w.B, "H": w.H, "G": w.G, "d": w.d, "Nmax": w.Nmax, "dtype": w.dtype, "sum_L": int(sum(lens_full)),
+        "us_median": round(med, 2), "us_p10": round(ts[len(ts) // 10], 2), "us_p90": round(ts[(9 * len(ts)) // 10], 2),
+        "bytes": abytes, "gbs": round(abytes / med / 1e3, 1),
+        "frac_measured": round(abytes / med / 1e3 / peak, 3),
+        "frac_8tbs": round(abytes / med / 1e3 / NOMINAL_HBM_GBS, 3),
+        "tflops": round(cost.decode_attention_flops(lens_full, w.H, w.d) / med / 1e6, 1),
+        "kv_append_us": round(statistics.median(ta), 2), "copies": copies, "device_error": err,
+    }
+    del st, ws
+    torch.cuda.empty_cache()
+    return row
+
+
+def read_ceiling(device) -> float:
+    """Read-only streaming ceiling (library reduction over 4 GiB), GB/s."""
+    x = torch.ones(2 ** 31, dtype=torch.bfloat16, device=device)
+    for _ in range(3):
+        x.sum()
+    ts = []
+    for _ in range(10):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        x.sum()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) * 1e-3)
+    del x
+    torch.cuda.empty_cache()
+    return 2 ** 32 / min(ts) / 1e9
+
+
+# ----------------------------------------------------------------- CPU oracle
+def oracle_sample(w: workloads.Workload, budget_s: float, max_units: int = 1 << 30, _cache={}):
+    """Times the fp64 CPU oracle on a bounded sample of the workload: whole
+    (batch, KV group) units, batch rows in order, as many as fit in about
+    `budget_s` seconds (at least one).  Returns (GB/s of algorithmic bytes,
+    units done, seconds, threads)."""
+    import oracle
+    threads = len(os.sched_getaffinity(0))
+    lens = workloads.make_seq_lens(w).tolist()
+    key = w.name
+    if key not in _cache:
+        # one batch row of inputs, reused for every sampled row (timing only)
+        small = w.replace(B=1, Nmax=max(lens))
+        _cache[key] = workloads.make_inputs(small, seq_lens=torch.tensor([max(lens)], dtype=torch.int32),
+                                            poison=False)
+    x = _cache[key]
+    done_bytes, done_units, spent = 0, 0, 0.0
+    b = 0
+    per_row = None
+    while (done_units == 0 or spent < budget_s) and done_units < max_units:
+        L = int(lens[b % w.B])
+        groups = w.G
+        if per_row is not None and spent + per_row > budget_s * 1.2:
+            # a whole row would overrun the budget: take a slice of its groups
+            groups = max(1, int(w.G * (budget_s - spent) / per_row))
+        groups = min(groups, max_units - done_units)
+        q = x["q"][:, : groups * w.n_rep].contiguous()
+        k = x["k_cache"][:, :groups, :L].contiguous()
+        v = x["v_cache"][:, :groups, :L].contiguous()
+        sl = torch.tensor([L], dtype=torch.int32)
+        t0 = time.perf_counter()
+        oracle.decode_attention(q, k, v, sl, w.scale, nthreads=threads)
+        dt = time.perf_counter() - t0
+        spent += dt
+        if groups == w.G:
+            per_row = dt
+        done_units += groups
+        done_bytes += cost.decode_attention_bytes([L], groups * w.n_rep, groups, w.d, w.elt)
+        b += 1
+    return done_bytes / spent / 1e9, done_units, spent, threads
+
+
+# ----------------------------------------------------------------- arms
+def run_reference(args, world, rank):
+    """The reference arm: the fp64 CPU oracle, as it stands, timed on this
+    host's cores over a bounded sample of the workload per step."""
+    if rank != 0:
+        return 0
+    w = workloads.workload(args.workload)
+    steps, warm = args.steps, args.warmup
+    # size each step so that the whole run stays within about two minutes
+    _, units1, t1, threads = oracle_sample(w, 0.0, max_units=1)
+    per_unit = max(t1, 1e-6)
+    per_step_budget = min(5.0, 120.0 / max(steps + warm, 1))
+    units = max(1, min(w.B * w.G, int(per_step_budget / per_unit)))
+    for _ in range(warm):
+        oracle_sample(w, 0.0, max_units=units)
+    tot_bytes, tot_s = 0.0, 0.0
+    for _ in range(steps):
+        gbs, u, s, _ = oracle_sample(w, 1e9, max_units=units)
+        tot_bytes += gbs * s * 1e9
+        tot_s += s
+    value = tot_bytes / tot_s / 1e9
+    sample = f"{units} of {w.B * w.G} (batch, KV-group) units of the {w.name} workload per step, fp64 oracle"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": steps, "warmup": warm, "ms_per_step": round(tot_s / steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.description, "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, world, rank, local):
+    import grouped_query_decode_kv_b300 as gqa
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    gqa.load_library()
+    gqa.gqa_get_device_error()
+
+    w = workloads.workload(args.workload)
+    props = torch.cuda.get_device_properties(device)
+    l2 = props.L2_cache_size
+    mem_budget = int(props.total_memory * 0.5)
+    copies = copies_for(w, l2, mem_budget)
+    steps, warm = args.steps, args.warmup
+    st = DecodeState(w, warm + steps, device, copies)
+    stream = torch.cuda.current_stream(device)
+
+    # ---- device-resident timed region
+    run_steps(st, 0, warm)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(device.index)
+    time.sleep(0.4)
+    barrier(world, device)
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t_begin.record(stream)
+    run_steps(st, warm, steps, ev)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world, device)
+    wall1 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(wall0, wall1)
+    secs = t_begin.elapsed_time(t_end) * 1e-3
+    secs_max = reduce_max(secs, world, device)
+    attn_us = [a.elapsed_time(b) * 1e3 for a, b in ev]
+    dev_err = gqa.gqa_get_device_error()
+
+    step_bytes = st.attention_bytes + st.append_bytes
+    value = aggregate(step_bytes * steps, secs_max, world)
+    peak, peak_src = hbm_peak()
+    attn_mean = statistics.mean(attn_us)
+    achieved = st.attention_bytes / attn_mean / 1e3
+
+    # ---- end to end through host buffers: q, k_new, v_new in, out back
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    hq = [pin(t) for t in st.q]
+    hk = [pin(t) for t in st.kn]
+    hv = [pin(t) for t in st.vn]
+    ho = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in st.out]
+    st.reset_lengths()
+    e_steps = steps
+
+    def e2e_step(i):
+        c = i % copies
+        st.q[c].copy_(hq[c], non_blocking=True)
+        st.kn[c].copy_(hk[c], non_blocking=True)
+        st.vn[c].copy_(hv[c], non_blocking=True)
+        sl = st.sl[i]
+        gqa.kv_append(st.kn[c], st.vn[c], st.k[c], st.v[c], sl)
+        gqa.gqa_decode_attention(st.q[c], st.k[c], st.v[c], sl, w.scale, st.out[c])
+        ho[c].copy_(st.out[c], non_blocking=True)
+
+    for i in range(warm):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    st.reset_lengths()
+    barrier(world, device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e_steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world, device)
+    e_secs = reduce_max(e0.elapsed_time(e1) * 1e-3, world, device)
+    e2e_value = aggregate(step_bytes * e_steps, e_secs, world)
+    h2d = sum(t[0].numel() * t[0].element_size() for t in (hq, hk, hv))
+    d2h = ho[0].numel() * ho[0].element_size()
+    dev_err |= gqa.gqa_get_device_error()
+
+    # ---- per-workload table and the read-only ceiling (rank 0 only)
+    table = None
+    ceiling = None
+    del st
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_table:
+        ceiling = round(read_ceiling(device), 1)
+        table = {}
+        for name in TABLE_WORKLOADS:
+            table[name] = time_attention_only(workloads.workload(name), device, args.table_iters, 5, l2, mem_budget)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        gbs, units, spent, threads = oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{units} of {w.B * w.G} (batch, KV-group) units of the {w.name} workload "
+                         f"({spent:.1f} s of fp64 CPU work)"}
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+
+    traffic = profiled_traffic(w.name)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": warm,
+        "ms_per_step": round(secs_max / steps * 1e3, 5),
+        "us_per_step": round(secs_max / steps * 1e6, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {
+            "workload": w.description, "B": w.B, "H": w.H, "G": w.G, "d": w.d, "Nmax": w.Nmax,
+            "seq_lens": "fixed" if w.lens[0] == "fixed" else f"uniform[{w.lens[1]},{w.lens[2]}]",
+            "parallelism": f"replicas x{world}",
+            "l2": f"rotating {copies} cache copies ({copies * cost.kv_cache_bytes(w.B, w.G, w.Nmax, w.d, w.elt) / 2**20:.0f} MiB"
+                  f" >= 3 x L2 {l2 / 2**20:.0f} MiB)",
+            "step": "kv_append + gqa_decode_attention (split-KV + combine)",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "gqa_decode_attention call (split-KV kernel + LSE combine)",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_source": peak_src,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+            "bytes_per_call": st_bytes(w),
+            "us_per_call": round(attn_mean, 2),
+            "traffic": traffic,
+        },
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "us_per_step": round(e_secs / e_steps * 1e6, 2)},
+        "gpu_launches": (2 + (1 if gqa.gqa_decode_workspace_bytes(w.B, w.H, w.G, w.d, w.Nmax, w.torch_dtype) else 0))
+        * steps,
+        "clocks": clocks,
+        "device_error": dev_err,
+        "read_ceiling_gbs": ceiling,
+        "table": table,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def st_bytes(w: workloads.Workload) -> int:
+    lens = workloads.make_seq_lens(w).tolist()
+    return cost.decode_attention_bytes(lens, w.H, w.G, w.d, w.elt)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="mha", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-table", action="store_true", help="skip the per-workload table")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--table-iters", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
