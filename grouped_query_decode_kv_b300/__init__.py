@@ -12,6 +12,7 @@ Entry points (see ``include/gqa.h`` for the full contract):
   gqa_decode_attention_ws(..., workspace)        caller-provided workspace
   gqa_decode_attention_ex(..., split_tokens, workspace)
   gqa_decode_workspace_bytes(B, H, G, d, Nmax, dtype)
+  gqa_decode_attention_noalloc(...)              no allocation: fixed in-library scratch
   kv_append(k_new, v_new, k_cache, v_cache, seq_lens)
   mha_to_gqa_meanpool(w, w_out)
   gqa_get_device_error()
@@ -33,16 +34,20 @@ __all__ = [
     "gqa_decode_attention", "gqa_decode_attention_ws", "gqa_decode_attention_ex",
     "gqa_decode_workspace_bytes", "gqa_decode_workspace_bytes_ex", "kv_append",
     "mha_to_gqa_meanpool", "gqa_get_device_error", "gqa_status_string",
+    "gqa_decode_attention_noalloc", "NOALLOC_SCRATCH_BYTES", "ERR_SCRATCH_LIMIT",
     "DEVERR_ATTN_LEN", "DEVERR_APPEND_LEN", "DEVERR_TIMEOUT", "EXPORTED_SYMBOLS",
 ]
 
 GQA_F32, GQA_BF16 = 0, 1
 DEVERR_ATTN_LEN, DEVERR_APPEND_LEN, DEVERR_TIMEOUT = 1, 2, 4
+ERR_SCRATCH_LIMIT = -5
+NOALLOC_SCRATCH_BYTES = 32 << 20  # GQA_NOALLOC_SCRATCH_BYTES in include/gqa.h
 
 EXPORTED_SYMBOLS = (
     "gqa_decode_attention", "gqa_decode_workspace_bytes", "gqa_decode_attention_ws",
     "gqa_decode_workspace_bytes_ex", "gqa_decode_attention_ex", "kv_append",
     "mha_to_gqa_meanpool", "gqa_get_device_error", "gqa_status_string",
+    "gqa_decode_attention_noalloc",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -76,7 +81,9 @@ def load_library():
         lib.gqa_decode_attention.argtypes = attn + [vp]
         lib.gqa_decode_attention_ws.argtypes = attn + [vp, sz, vp]
         lib.gqa_decode_attention_ex.argtypes = attn + [ci, vp, sz, vp]
-        for f in ("gqa_decode_attention", "gqa_decode_attention_ws", "gqa_decode_attention_ex"):
+        lib.gqa_decode_attention_noalloc.argtypes = attn + [vp]
+        for f in ("gqa_decode_attention", "gqa_decode_attention_ws", "gqa_decode_attention_ex",
+                  "gqa_decode_attention_noalloc"):
             getattr(lib, f).restype = ci
         lib.gqa_decode_workspace_bytes.argtypes = [ci] * 6
         lib.gqa_decode_workspace_bytes.restype = sz
@@ -193,6 +200,21 @@ def gqa_decode_attention_ex(q, k_cache, v_cache, seq_lens, scale, out, split_tok
     _check("gqa_decode_attention_ex",
            lib.gqa_decode_attention_ex(*_attn_args(q, k_cache, v_cache, seq_lens, scale, out), int(split_tokens),
                                        wp, wn, _stream(q, stream)))
+    return out
+
+
+def gqa_decode_attention_noalloc(q, k_cache, v_cache, seq_lens, scale, out, stream=None):
+    """As gqa_decode_attention, for callers that cannot allocate device memory
+    during the call (an engine whose KV-cache pool already holds all free
+    HBM, a plugin whose framework owns the allocator, a decode loop that
+    cannot pay for an allocator call per step).  The split partials live in
+    a fixed in-library buffer of NOALLOC_SCRATCH_BYTES per device; larger
+    shapes raise GQAError with status ERR_SCRATCH_LIMIT.  Calls that overlap
+    on the GPU share that buffer and race: keep them on one stream."""
+    lib = load_library()
+    _check("gqa_decode_attention_noalloc",
+           lib.gqa_decode_attention_noalloc(*_attn_args(q, k_cache, v_cache, seq_lens, scale, out),
+                                            _stream(q, stream)))
     return out
 
 

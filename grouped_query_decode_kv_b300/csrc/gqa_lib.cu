@@ -266,6 +266,44 @@ int run_attention(const void *q, const void *k, const void *v, const int32_t *sl
 }  // namespace
 }  // namespace gqa
 
+// Fixed split scratch of gqa_decode_attention_noalloc: partial outputs and
+// softmax states of one call.  A static device array, so every device that
+// loads the library holds it until the process exits; calls on one device
+// share it (see gqa.h).
+static __device__ __align__(256) unsigned char g_noalloc_scratch[GQA_NOALLOC_SCRATCH_BYTES];
+
+namespace gqa {
+namespace {
+
+// Device address of g_noalloc_scratch for the current device.  In host code
+// the array's name is only a host-side stand-in, so the real address is
+// looked up once per device (with that device current) and cached.
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+int noalloc_scratch(void **ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return GQA_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return GQA_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return GQA_OK;
+}
+
+}  // namespace
+}  // namespace gqa
+
 using namespace gqa;
 
 extern "C" {
@@ -317,6 +355,21 @@ int gqa_decode_attention(const void *q, const void *k_cache, const void *v_cache
   int rc = run_attention(q, k_cache, v_cache, seq_lens, scale, out, B, H, G, d, Nmax, dtype, pl, ws, stream);
   if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && rc == GQA_OK) rc = GQA_ERR_CUDA;
   return rc;
+}
+
+int gqa_decode_attention_noalloc(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
+                                 float scale, void *out, int B, int H, int G, int d, int Nmax, gqa_dtype_t dtype,
+                                 cudaStream_t stream) {
+  if (int rc = check_attention_args(q, k_cache, v_cache, seq_lens, out, B, H, G, d, Nmax, dtype)) return rc;
+  const Plan pl = make_plan(B, H, G, d, Nmax, dtype, 0);
+  if (!plan_fits(pl, B, G)) return GQA_ERR_UNSUPPORTED;
+  const size_t need = workspace_for(pl, B, H, d);
+  if (need > GQA_NOALLOC_SCRATCH_BYTES) return GQA_ERR_SCRATCH_LIMIT;
+  void *ws = nullptr;
+  if (need > 0) {
+    if (int rc = noalloc_scratch(&ws)) return rc;
+  }
+  return run_attention(q, k_cache, v_cache, seq_lens, scale, out, B, H, G, d, Nmax, dtype, pl, ws, stream);
 }
 
 int kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache, int32_t *seq_lens, int B, int G,
@@ -380,6 +433,7 @@ const char *gqa_status_string(int status) {
     case GQA_ERR_UNSUPPORTED: return "unsupported shape";
     case GQA_ERR_CUDA: return "CUDA error";
     case GQA_ERR_NO_MEMORY: return "out of device memory";
+    case GQA_ERR_SCRATCH_LIMIT: return "shape needs more split scratch than the fixed no-allocation buffer holds";
     default: return "unknown status";
   }
 }

@@ -50,7 +50,9 @@ typedef enum {
                                  misaligned pointer, workspace too small */
     GQA_ERR_UNSUPPORTED = -2, /* head dimension d not in {64, 128} */
     GQA_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed */
-    GQA_ERR_NO_MEMORY = -4    /* stream-ordered workspace allocation failed */
+    GQA_ERR_NO_MEMORY = -4,   /* stream-ordered workspace allocation failed */
+    GQA_ERR_SCRATCH_LIMIT = -5 /* gqa_decode_attention_noalloc: the shape needs more split
+                                  scratch than GQA_NOALLOC_SCRATCH_BYTES */
 } gqa_status_t;
 
 /* Bits of the device error word. */
@@ -120,6 +122,40 @@ int gqa_decode_attention_ex(const void *q, const void *k_cache, const void *v_ca
                             int B, int H, int G, int d, int Nmax, gqa_dtype_t dtype,
                             int split_tokens, void *workspace, size_t workspace_bytes,
                             cudaStream_t stream);
+
+/*
+ * gqa_decode_attention_noalloc — gqa_decode_attention for callers that must
+ * not allocate device memory during the call.  The paper has no counterpart:
+ * this is an integration entry point, not part of the method.
+ *
+ * Who needs it: a serving engine that has already handed all free HBM to its
+ * KV-cache pool (any further cudaMalloc would fail), a plugin whose host
+ * framework owns the device allocator and forbids side allocations, or a
+ * decode loop that cannot afford an allocator call on every step.
+ *
+ * Same arguments, result and error behaviour as gqa_decode_attention.  The
+ * split partials go to one fixed buffer inside the library instead of a
+ * per-call workspace: a static device array of GQA_NOALLOC_SCRATCH_BYTES that
+ * every device which loads the library holds until the process exits.  The
+ * call itself allocates nothing: no cudaMalloc/cudaMallocAsync/cudaFree and
+ * no allocating library routine.
+ *  - A shape whose partials need more than GQA_NOALLOC_SCRATCH_BYTES is
+ *    rejected with GQA_ERR_SCRATCH_LIMIT before anything is enqueued
+ *    (gqa_decode_workspace_bytes gives the need).
+ *  - The first call on a device looks up that device's address of the
+ *    buffer (cudaGetSymbolAddress, once per device, with the device
+ *    current).  Make that first call before any stream capture begins.
+ *  - Every call on a device shares the one buffer, which keeps the previous
+ *    call's contents.  Nothing in it needs to start at zero: each call
+ *    writes every partial it later reads.  Calls whose kernels overlap on
+ *    the GPU (other streams, other host threads) race on the buffer:
+ *    order them, e.g. on one stream.
+ */
+#define GQA_NOALLOC_SCRATCH_BYTES (32u << 20) /* 32 MiB per device */
+int gqa_decode_attention_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                 const int32_t *seq_lens, float scale, void *out,
+                                 int B, int H, int G, int d, int Nmax, gqa_dtype_t dtype,
+                                 cudaStream_t stream);
 
 /*
  * kv_append — the cache concatenation of one decode step (fogdragon's CSDN
