@@ -262,50 +262,75 @@ def run_steps(st: DecodeState, first: int, count: int, ev=None):
             ev[i - first][1].record()
 
 
+def _graph_time(fn_seq, reset=None, reps: int = 3) -> float:
+    """Device time per call (µs) of a sequence of library calls captured into
+    one CUDA graph: the graph is replayed `reps` times, each replay bracketed
+    by CUDA events, and the best replay is divided by the number of calls.
+    `reset` (outside the timed replay) restores state between replays."""
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn_seq()  # warm the calls once outside capture (module load, attributes)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    if reset:
+        reset()
+    with torch.cuda.graph(g):
+        n = fn_seq()
+    best = float("inf")
+    for _ in range(reps + 1):
+        if reset:
+            reset()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        best = min(best, a.elapsed_time(b) * 1e3 / n)
+    del g
+    return best
+
+
 def time_attention_only(w: workloads.Workload, device, iters: int, warm: int, l2_bytes: int, mem_budget: int):
-    """Per-workload table row: the attention call alone and kv_append alone,
-    CUDA events around each call, lengths fixed at L_b."""
+    """Per-workload table row: device time per attention call and per
+    kv_append call, from CUDA-graph replays of `iters` back-to-back calls
+    (the caches rotate over enough copies to defeat L2; lengths fixed at L_b)."""
     import grouped_query_decode_kv_b300 as gqa
     copies = copies_for(w, l2_bytes, mem_budget)
-    st = DecodeState(w, 1, device, copies, seed=17)
+    st = DecodeState(w, iters, device, copies, seed=17)
     full = st.lens.to(torch.int32).to(device)
     ws = torch.empty(max(st.ws_bytes, 1), dtype=torch.uint8, device=device)
+
+    def attn_seq():
+        for i in range(iters):
+            c = i % copies
+            gqa.gqa_decode_attention_ws(st.q[c], st.k[c], st.v[c], full, w.scale, st.out[c], ws)
+        return iters
+
+    def append_seq():
+        for i in range(iters):
+            c = i % copies
+            gqa.kv_append(st.kn[c], st.vn[c], st.k[c], st.v[c], st.sl[i])
+        return iters
+
     for i in range(warm):
         c = i % copies
         gqa.gqa_decode_attention_ws(st.q[c], st.k[c], st.v[c], full, w.scale, st.out[c], ws)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
-    torch.cuda.synchronize()
-    for i in range(iters):
-        c = i % copies
-        evs[i][0].record()
-        gqa.gqa_decode_attention_ws(st.q[c], st.k[c], st.v[c], full, w.scale, st.out[c], ws)
-        evs[i][1].record()
-    torch.cuda.synchronize()
-    ts = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
-    # kv_append alone (lengths reset below L so that every append lands)
-    sl = torch.clamp(st.lens - 1, min=0).to(torch.int32).to(device)
-    sl_rows = sl.unsqueeze(0).repeat(iters, 1).contiguous()
-    aev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
-    for i in range(iters):
-        c = i % copies
-        aev[i][0].record()
-        gqa.kv_append(st.kn[c], st.vn[c], st.k[c], st.v[c], sl_rows[i])
-        aev[i][1].record()
-    torch.cuda.synchronize()
-    ta = sorted(a.elapsed_time(b) * 1e3 for a, b in aev)
+    us = _graph_time(attn_seq)
+    us_append = _graph_time(append_seq, reset=st.reset_lengths)
     err = gqa.gqa_get_device_error()
     lens_full = st.lens.tolist()
     abytes = cost.decode_attention_bytes(lens_full, w.H, w.G, w.d, w.elt)
-    med = statistics.median(ts)
     peak, _ = hbm_peak()
     row = {
         "B": w.B, "H": w.H, "G": w.G, "d": w.d, "Nmax": w.Nmax, "dtype": w.dtype, "sum_L": int(sum(lens_full)),
-        "us_median": round(med, 2), "us_p10": round(ts[len(ts) // 10], 2), "us_p90": round(ts[(9 * len(ts)) // 10], 2),
-        "bytes": abytes, "gbs": round(abytes / med / 1e3, 1),
-        "frac_measured": round(abytes / med / 1e3 / peak, 3),
-        "frac_8tbs": round(abytes / med / 1e3 / NOMINAL_HBM_GBS, 3),
-        "tflops": round(cost.decode_attention_flops(lens_full, w.H, w.d) / med / 1e6, 1),
-        "kv_append_us": round(statistics.median(ta), 2), "copies": copies, "device_error": err,
+        "us": round(us, 2), "bytes": abytes, "gbs": round(abytes / us / 1e3, 1),
+        "frac_measured": round(abytes / us / 1e3 / peak, 3),
+        "frac_8tbs": round(abytes / us / 1e3 / NOMINAL_HBM_GBS, 3),
+        "tflops": round(cost.decode_attention_flops(lens_full, w.H, w.d) / us / 1e6, 1),
+        "kv_append_us": round(us_append, 2), "copies": copies, "device_error": err,
     }
     del st, ws
     torch.cuda.empty_cache()
@@ -428,24 +453,45 @@ def run_ours(args, world, rank, local):
     st = DecodeState(w, warm + steps, device, copies)
     stream = torch.cuda.current_stream(device)
 
-    # ---- device-resident timed region
+    # ---- pre-warm: about a second of the same step so that clocks settle
+    # before the W warm-up steps (untimed; lengths are reset afterwards).
+    # The clock sampler starts first, and nothing idles the GPU between the
+    # pre-warm and the timed region.
+    sampler = ClockSampler(device.index)
+    pre = 0
+    t_pre = time.time()
+    while time.time() - t_pre < args.prewarm:
+        run_steps(st, 0, min(warm + steps, 200))
+        torch.cuda.synchronize()
+        st.reset_lengths()
+        pre += 1
+
+    # ---- device-resident timed region: K steps, nothing else in the stream
     run_steps(st, 0, warm)
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(device.index)
-    time.sleep(0.4)
     barrier(world, device)
     torch.cuda.synchronize()
     wall0 = time.time()
     t_begin.record(stream)
-    run_steps(st, warm, steps, ev)
+    run_steps(st, warm, steps)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world, device)
     wall1 = time.time()
+
+    # ---- the same K steps again with CUDA events around every attention
+    # call, for the per-call duration of the roofline (events between the
+    # kernels cost a few µs of overlap, so they stay out of the region above)
+    st.reset_lengths()
+    run_steps(st, 0, warm)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    run_steps(st, warm, steps, ev)
+    torch.cuda.synchronize()
+    wall2 = time.time()
     sampler.stop()
-    clocks = sampler.summary(wall0, wall1)
+    clocks = sampler.summary(wall0, wall2)
     secs = t_begin.elapsed_time(t_end) * 1e-3
     secs_max = reduce_max(secs, world, device)
     attn_us = [a.elapsed_time(b) * 1e3 for a, b in ev]
@@ -540,6 +586,9 @@ def run_ours(args, world, rank, local):
             "l2": f"rotating {copies} cache copies ({copies * cost.kv_cache_bytes(w.B, w.G, w.Nmax, w.d, w.elt) / 2**20:.0f} MiB"
                   f" >= 3 x L2 {l2 / 2**20:.0f} MiB)",
             "step": "kv_append + gqa_decode_attention (split-KV + combine)",
+            "timing": f"{args.prewarm:.1f} s untimed pre-warm, W warm-up steps, then K steps bracketed by "
+                      "CUDA events with nothing else in the stream; the roofline's per-call time comes from "
+                      "a second pass of K steps with events around each attention call",
         },
         "roofline": {
             "bound": "hbm",
@@ -552,6 +601,8 @@ def run_ours(args, world, rank, local):
             "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
             "bytes_per_call": st_bytes(w),
             "us_per_call": round(attn_mean, 2),
+            "us_per_call_p10_p90": [round(sorted(attn_us)[len(attn_us) // 10], 2),
+                                    round(sorted(attn_us)[(9 * len(attn_us)) // 10], 2)],
             "traffic": traffic,
         },
         "cpu_baseline": cpu,
@@ -584,6 +635,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--table-iters", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--prewarm", type=float, default=1.0, help="seconds of untimed steps before the warm-up")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -151,3 +151,15 @@ __device__ __forceinline__ float merge_weight(float m, float M) {
 }
 
 }  // namespace gqa
+
+namespace gqa {
+
+// Programmatic dependent launch: wait until the kernels this grid depends on
+// have finished and their writes are visible (a no-op without a dependency),
+// and let the next kernel in the stream start its launch early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+}  // namespace gqa

@@ -5,8 +5,10 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <mutex>
+#include <utility>
 
 #include "gqa.h"
 #include "gqa_device.cuh"
@@ -19,13 +21,14 @@ namespace gqa {
 namespace {
 
 // ----------------------------------------------------------- kernel configs
-// Stages of ~32 KB (K + V tiles); three stages per CTA, two CTAs per SM.
-using MmaD128x1 = MmaCfg<128, 1, 1, 64, 3>;   // n_rep 3..16
-using MmaD128x2 = MmaCfg<128, 2, 1, 64, 3>;   // n_rep 17..32
-using MmaD128x4 = MmaCfg<128, 2, 2, 64, 3>;   // n_rep >= 33 (64 heads per CTA)
-using MmaD64x1 = MmaCfg<64, 1, 1, 128, 3>;
-using MmaD64x2 = MmaCfg<64, 2, 1, 128, 3>;
-using MmaD64x4 = MmaCfg<64, 2, 2, 128, 3>;
+// Stages of ~32 KB (K + V tiles).  Ring and per-unit merge scratch are sized
+// so that two CTAs fit on one SM where registers allow.
+using MmaD128x1 = MmaCfg<128, 1, 1, 64, 3, 2>;  // n_rep 3..16
+using MmaD128x2 = MmaCfg<128, 2, 1, 64, 2>;   // n_rep 17..32
+using MmaD128x4 = MmaCfg<128, 2, 2, 64, 2>;   // n_rep >= 33 (64 heads per CTA)
+using MmaD64x1 = MmaCfg<64, 1, 1, 128, 3, 2>;
+using MmaD64x2 = MmaCfg<64, 2, 1, 128, 2>;
+using MmaD64x4 = MmaCfg<64, 2, 2, 128, 2>;
 
 template <typename T, int D, int NH>
 using SimtFor = SimtCfg<T, D, NH, (32768 / (2 * D * (int)sizeof(T))), 3>;
@@ -37,15 +40,35 @@ struct KernelChoice {
   int block_n;
   int heads;
   int box_elems;
-  void (*launch)(dim3, const CUtensorMap &, const CUtensorMap &, const SplitParams &, cudaStream_t);
+  cudaError_t (*launch)(dim3, const CUtensorMap &, const CUtensorMap &, const SplitParams &, cudaStream_t);
 };
 
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous kernel in the stream finishes; it calls griddepcontrol.wait
+// before reading anything that kernel writes.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <class C, bool MMA>
-void launch_split(dim3 grid, const CUtensorMap &k, const CUtensorMap &v, const SplitParams &p, cudaStream_t st) {
+cudaError_t launch_split(dim3 grid, const CUtensorMap &k, const CUtensorMap &v, const SplitParams &p,
+                         cudaStream_t st) {
   if constexpr (MMA)
-    gqa_split_mma_kernel<C><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(k, v, p);
+    return launch_pdl(gqa_split_mma_kernel<C>, grid, dim3(C::THREADS), C::SMEM_BYTES, st, k, v, p);
   else
-    gqa_split_simt_kernel<C><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(k, v, p);
+    return launch_pdl(gqa_split_simt_kernel<C>, grid, dim3(C::THREADS), C::SMEM_BYTES, st, k, v, p);
 }
 
 template <class C, bool MMA>
@@ -95,55 +118,103 @@ KernelChoice choose_kernel(gqa_dtype_t dt, int d, int n_rep) {
 // ----------------------------------------------------------- split plan
 struct Plan {
   KernelChoice k;
-  int head_chunks;
-  int chunk;
-  int S_max;
+  int head_chunks;  // HC
+  int P;            // CTAs of the split kernel
+  long long units;  // B * G * HC
 };
 
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
+constexpr int kMaxDevices = 64;
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return -1;
+  }
+  return dev;
+}
+
+// SM count of the current device, read once per device (148 without one).
 int device_sm_count() {
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 148;
+  static std::atomic<int> cache[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return 148;
+  int sms = cache[dev].load(std::memory_order_relaxed);
+  if (sms > 0) return sms;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    cudaGetLastError();
+    return 148;
+  }
+  cache[dev].store(sms, std::memory_order_relaxed);
   return sms;
 }
 
-// Positions per split.  Aim at about four CTAs per resident slot (two CTAs
-// per SM) so that the block scheduler balances the tail, but never fewer
-// than four tiles per split; Nmax stands in for the (device-resident)
-// lengths.
+// Resident CTAs of a split kernel per SM (queried once per kernel; without
+// a device, estimated from its shared memory).
+int ctas_per_sm(const KernelChoice &kc) {
+  static std::mutex mu;
+  static const void *funcs[32];
+  static int counts[32];
+  static int n = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n; ++i)
+    if (funcs[i] == kc.func) return counts[i];
+  int c = 0;
+  if (cudaFuncSetAttribute(kc.func, cudaFuncAttributeMaxDynamicSharedMemorySize, kc.smem) != cudaSuccess ||
+      cudaFuncSetAttribute(kc.func, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, kc.func, kc.threads, kc.smem) != cudaSuccess || c <= 0) {
+    cudaGetLastError();
+    return std::max(1, std::min(2, (228 * 1024) / (kc.smem + 1024)));
+  }
+  if (n < 32) {
+    funcs[n] = kc.func;
+    counts[n] = c;
+    ++n;
+  }
+  return c;
+}
+
+// The split kernel is a persistent grid of one wave (SMs x resident CTAs per
+// SM); the stream-K split gives every CTA the same number of tiles whatever
+// the lengths.  split_tokens > 0 instead asks for about that many positions
+// per CTA when every sequence is full (for tests of the combine and for
+// tuning).
 Plan make_plan(int B, int H, int G, int d, int Nmax, gqa_dtype_t dt, int split_tokens) {
   Plan pl;
   const int n_rep = H / G;
   pl.k = choose_kernel(dt, d, n_rep);
   pl.head_chunks = ceil_div(n_rep, pl.k.heads);
-  const int bn = pl.k.block_n;
-  const int tiles = ceil_div(Nmax, bn);
-  int tps;
+  pl.units = (long long)B * G * pl.head_chunks;
+  const long long tiles_full = pl.units * ceil_div(Nmax, pl.k.block_n);
+  long long P;
   if (split_tokens > 0) {
-    tps = std::max(1, ceil_div(split_tokens, bn));
+    const long long per_cta = std::max(1, ceil_div(split_tokens, pl.k.block_n));
+    P = (tiles_full + per_cta - 1) / per_cta;
   } else {
-    const long long units = (long long)B * G * pl.head_chunks;
-    const long long want = 4LL * 2 * device_sm_count();
-    const int S = (int)std::max<long long>(1, (want + units - 1) / units);
-    tps = std::max(std::min(4, tiles), ceil_div(tiles, S));
+    P = (long long)device_sm_count() * ctas_per_sm(pl.k);
   }
-  tps = std::min(tps, tiles);
-  pl.chunk = tps * bn;
-  pl.S_max = ceil_div(Nmax, pl.chunk);
+  P = std::max<long long>(1, std::min<long long>(P, std::min<long long>(tiles_full, 1 << 20)));
+  pl.P = (int)P;
   return pl;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Grid limits: y = G * head_chunks and z = B must stay within 65535.
-bool plan_fits(const Plan &pl, int B, int G) { return B <= 65535 && (long long)G * pl.head_chunks <= 65535; }
+bool plan_fits(const Plan &pl, int B, int G) { return B <= 65535 && pl.units < (1LL << 31); }
+
+// Workspace: partial outputs and (m, l) of two slots per CTA, and the
+// per-unit record of split units.  A single CTA never splits a unit.
+size_t ws_opart_bytes(const Plan &pl, int d) { return align256((size_t)2 * pl.P * pl.k.heads * d * sizeof(float)); }
+size_t ws_ml_bytes(const Plan &pl) { return align256((size_t)2 * pl.P * pl.k.heads * 2 * sizeof(float)); }
 
 size_t workspace_for(const Plan &pl, int B, int H, int d) {
-  if (pl.S_max <= 1) return 0;
-  const size_t parts = (size_t)B * H * pl.S_max;
-  return align256(parts * d * sizeof(float)) + align256(parts * 2 * sizeof(float));
+  (void)B;
+  (void)H;
+  if (pl.P <= 1) return 0;
+  return ws_opart_bytes(pl, d) + ws_ml_bytes(pl) + align256((size_t)pl.units * sizeof(int2));
 }
 
 // ----------------------------------------------------------- TMA descriptors
@@ -193,10 +264,27 @@ int check_attention_args(const void *q, const void *k, const void *v, const int3
   return GQA_OK;
 }
 
+// Opts a split kernel in to its dynamic shared memory, once per device.
 int ensure_smem_attr(const KernelChoice &kc) {
-  // Idempotent and cheap; set on every call so that each device gets it.
-  if (cudaFuncSetAttribute(kc.func, cudaFuncAttributeMaxDynamicSharedMemorySize, kc.smem) != cudaSuccess)
+  static std::mutex mu;
+  static const void *done_func[256];
+  static int done_dev[256];
+  static int n = 0;
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n; ++i)
+    if (done_func[i] == kc.func && done_dev[i] == dev) return GQA_OK;
+  if (cudaFuncSetAttribute(kc.func, cudaFuncAttributeMaxDynamicSharedMemorySize, kc.smem) != cudaSuccess ||
+      cudaFuncSetAttribute(kc.func, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+          cudaSuccess) {
+    cudaGetLastError();
     return GQA_ERR_CUDA;
+  }
+  if (n < 256 && dev >= 0) {
+    done_func[n] = kc.func;
+    done_dev[n] = dev;
+    ++n;
+  }
   return GQA_OK;
 }
 
@@ -211,51 +299,46 @@ int run_attention(const void *q, const void *k, const void *v, const int32_t *sl
   p.q = q;
   p.seq_lens = sl;
   p.out = out;
-  const size_t parts = (size_t)B * H * pl.S_max;
-  p.o_part = pl.S_max > 1 ? reinterpret_cast<float *>(ws) : nullptr;
-  p.ml_part = pl.S_max > 1 ? reinterpret_cast<float *>(reinterpret_cast<char *>(ws) +
-                                                       align256(parts * d * sizeof(float)))
-                           : nullptr;
+  const bool split = pl.P > 1;
+  char *w = reinterpret_cast<char *>(ws);
+  p.o_part = split ? reinterpret_cast<float *>(w) : nullptr;
+  p.ml_part = split ? reinterpret_cast<float *>(w + ws_opart_bytes(pl, d)) : nullptr;
+  p.unit_info = split ? reinterpret_cast<int2 *>(w + ws_opart_bytes(pl, d) + ws_ml_bytes(pl)) : nullptr;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.B = B;
   p.H = H;
   p.G = G;
   p.Nmax = Nmax;
   p.n_rep = H / G;
-  p.chunk = pl.chunk;
-  p.S_max = pl.S_max;
   p.heads_per_cta = pl.k.heads;
   p.head_chunks = pl.head_chunks;
-  dim3 grid(pl.S_max, G * pl.head_chunks, B);
-  pl.k.launch(grid, mk, mv, p, st);
-  if (cudaPeekAtLastError() != cudaSuccess) {
+  if (pl.k.launch(dim3(pl.P), mk, mv, p, st) != cudaSuccess) {
     cudaGetLastError();
     return GQA_ERR_CUDA;
   }
-  if (pl.S_max > 1) {
+  if (split) {
     CombineParams c;
     c.seq_lens = sl;
     c.o_part = p.o_part;
     c.ml_part = p.ml_part;
+    c.unit_info = p.unit_info;
     c.out = out;
     c.B = B;
     c.H = H;
+    c.G = G;
     c.Nmax = Nmax;
-    c.chunk = pl.chunk;
-    c.S_max = pl.S_max;
-    const int blocks = ceil_div((long long)B * H, 4);
-    if (dt == GQA_BF16) {
-      if (d == 128)
-        gqa_combine_kernel<__nv_bfloat16, 128><<<blocks, 128, 0, st>>>(c);
-      else
-        gqa_combine_kernel<__nv_bfloat16, 64><<<blocks, 128, 0, st>>>(c);
-    } else {
-      if (d == 128)
-        gqa_combine_kernel<float, 128><<<blocks, 128, 0, st>>>(c);
-      else
-        gqa_combine_kernel<float, 64><<<blocks, 128, 0, st>>>(c);
-    }
-    if (cudaPeekAtLastError() != cudaSuccess) {
+    c.n_rep = p.n_rep;
+    c.heads_per_cta = p.heads_per_cta;
+    c.head_chunks = p.head_chunks;
+    const dim3 blocks(ceil_div((long long)B * H, 4));
+    cudaError_t e;
+    if (dt == GQA_BF16)
+      e = d == 128 ? launch_pdl(gqa_combine_kernel<__nv_bfloat16, 128>, blocks, dim3(128), 0, st, c)
+                   : launch_pdl(gqa_combine_kernel<__nv_bfloat16, 64>, blocks, dim3(128), 0, st, c);
+    else
+      e = d == 128 ? launch_pdl(gqa_combine_kernel<float, 128>, blocks, dim3(128), 0, st, c)
+                   : launch_pdl(gqa_combine_kernel<float, 64>, blocks, dim3(128), 0, st, c);
+    if (e != cudaSuccess) {
       cudaGetLastError();
       return GQA_ERR_CUDA;
     }
@@ -278,7 +361,6 @@ namespace {
 // Device address of g_noalloc_scratch for the current device.  In host code
 // the array's name is only a host-side stand-in, so the real address is
 // looked up once per device (with that device current) and cached.
-constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;
 void *g_noalloc_ptr[kMaxDevices] = {};
 
@@ -382,10 +464,9 @@ int kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
     return GQA_ERR_INVALID_ARG;
   const int chunks = d * (dtype == GQA_BF16 ? 2 : 4) / 16;
-  gqa_kv_append_kernel<<<B, 256, 0, stream>>>(
-      reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new),
-      reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache), seq_lens, G, Nmax, chunks);
-  if (cudaPeekAtLastError() != cudaSuccess) {
+  if (launch_pdl(gqa_kv_append_kernel, dim3(B), dim3(256), 0, stream, reinterpret_cast<const uint4 *>(k_new),
+                 reinterpret_cast<const uint4 *>(v_new), reinterpret_cast<uint4 *>(k_cache),
+                 reinterpret_cast<uint4 *>(v_cache), seq_lens, G, Nmax, chunks) != cudaSuccess) {
     cudaGetLastError();
     return GQA_ERR_CUDA;
   }

@@ -5,30 +5,32 @@
 
 namespace gqa {
 
-// One CTA of a split kernel owns (batch b, KV head g, head chunk hc,
-// sequence split s): the positions [s*chunk, min((s+1)*chunk, L_b)) of K/V
-// head g and the query heads [g*n_rep + hc*heads_per_cta, ...) of its group.
+// The split kernels run a persistent grid; CTA c walks its stream-K range of
+// tiles (see gqa_schedule.cuh) unit by unit.  A unit is (batch b, KV head g,
+// head chunk hc): the query heads [g*n_rep + hc*heads_per_cta, ...) of
+// group g against K/V head g.
 struct SplitParams {
   const void *q;            // [B, H, D]
   const int32_t *seq_lens;  // [B]
-  void *out;                // [B, H, D]      written when a batch needs one split
-  float *o_part;            // [B, H, S_max, D] unnormalised partial outputs
-  float *ml_part;           // [B, H, S_max, 2] (running max in log2 units, sum)
+  void *out;                // [B, H, D]       whole units are written here directly
+  float *o_part;            // [2P, heads_per_cta, D] unnormalised partial outputs
+  float *ml_part;           // [2P, heads_per_cta, 2] (running max in log2 units, sum)
+  int2 *unit_info;          // [B*G*HC]        (first slot, last CTA) of split units
   float scale_log2;         // scale * log2(e): softmax is evaluated with exp2
   int B, H, G, Nmax;
   int n_rep;                // H / G
-  int chunk;                // positions per split, a multiple of the tile
-  int S_max;                // ceil(Nmax / chunk)
   int heads_per_cta;
-  int head_chunks;          // ceil(n_rep / heads_per_cta)
+  int head_chunks;          // HC = ceil(n_rep / heads_per_cta)
 };
 
 struct CombineParams {
   const int32_t *seq_lens;
   const float *o_part;
   const float *ml_part;
+  const int2 *unit_info;
   void *out;
-  int B, H, Nmax, chunk, S_max;
+  int B, H, G, Nmax;
+  int n_rep, heads_per_cta, head_chunks;
 };
 
 }  // namespace gqa

@@ -4,11 +4,14 @@
 // boxes of `block_n` positions) into a ring of STAGES shared-memory stages;
 // the consumer warps wait on a per-stage "full" mbarrier (completed by the
 // copies' transaction bytes) and release the stage through an "empty"
-// mbarrier that counts one arrival per consumer warp.  Every wait is bounded
-// (see mbar_wait).  Each K/V byte of the split is read from HBM once.
+// mbarrier that counts one arrival per consumer warp.  The ring runs on
+// across the units a persistent CTA visits, so the next unit's tiles stream
+// in while the consumers finish the previous one.  Every wait is bounded
+// (see mbar_wait).  Each K/V byte of the CTA's range is read from HBM once.
 #pragma once
 
 #include "gqa_device.cuh"
+#include "gqa_schedule.cuh"
 
 namespace gqa {
 
@@ -41,33 +44,85 @@ struct KVPipe {
     fence_barrier_init();
   }
 
-  // Producer (one thread): copies tiles [0, ntiles) of K/V head `bg`
-  // starting at position n_start.  Returns after the last copy it issued has
-  // landed (bounded), so that no copy is in flight when the block exits.
-  __device__ __forceinline__ void produce(const CUtensorMap *tmK, const CUtensorMap *tmV, int box_elems,
-                                          int bg, int n_start, int ntiles) const {
-    const uint64_t pol = l2_policy_evict_first();
-    int issued = 0;
-    for (int t = 0; t < ntiles; ++t) {
-      const int st = t % STAGES;
-      if (t >= STAGES && !mbar_wait(empty(st), ((t / STAGES) - 1) & 1)) break;
-      mbar_arrive_expect_tx(full(st), STAGE_BYTES);
-      const int n0 = n_start + t * BLOCK_N;
-#pragma unroll
-      for (int bx = 0; bx < NBOX; ++bx) {
-        tma_load_3d(k_tile(st) + bx * BOX_BYTES, tmK, bx * box_elems, n0, bg, full(st), pol);
-        tma_load_3d(v_tile(st) + bx * BOX_BYTES, tmV, bx * box_elems, n0, bg, full(st), pol);
-      }
-      issued = t + 1;
-    }
-    // drain: the last min(issued, STAGES) copies
-    for (int t = (issued > STAGES ? issued - STAGES : 0); t < issued; ++t)
-      if (!mbar_wait(full(t % STAGES), (t / STAGES) & 1)) break;
+  // Producer side (one thread).  Ring slot r (counted across the whole
+  // CTA) lives in stage r % STAGES; before refilling a stage the producer
+  // waits until every consumer warp released its previous use.  Returns
+  // false when that wait timed out.
+  __device__ __forceinline__ bool acquire(int r) const {
+    return r < STAGES || mbar_wait(empty(r % STAGES), ((r / STAGES) - 1) & 1);
   }
+
+  // Copies the K and V rows [n0, n0 + BLOCK_N) of K/V head `bg` into ring
+  // slot r; the stage's full barrier completes when all bytes landed.
+  // Rows past the tensor's end arrive as zeros.
+  __device__ __forceinline__ void load(int r, const CUtensorMap *tmK, const CUtensorMap *tmV, int box_elems,
+                                       int bg, int n0, uint64_t pol) const {
+    const int st = r % STAGES;
+    mbar_arrive_expect_tx(full(st), STAGE_BYTES);
+#pragma unroll
+    for (int bx = 0; bx < NBOX; ++bx) {
+      tma_load_3d(k_tile(st) + bx * BOX_BYTES, tmK, bx * box_elems, n0, bg, full(st), pol);
+      tma_load_3d(v_tile(st) + bx * BOX_BYTES, tmV, bx * box_elems, n0, bg, full(st), pol);
+    }
+  }
+
+  // Waits (bounded) for the last min(issued, STAGES) copies to land, so that
+  // no copy is in flight when the block exits.
+  __device__ __forceinline__ void drain(int issued) const {
+    for (int r = (issued > STAGES ? issued - STAGES : 0); r < issued; ++r)
+      if (!mbar_wait(full(r % STAGES), (r / STAGES) & 1)) break;
+  }
+
+  // Consumer side: wait until ring slot r holds its tile / release it.
+  __device__ __forceinline__ bool wait_full(int r) const { return mbar_wait(full(r % STAGES), (r / STAGES) & 1); }
+  __device__ __forceinline__ void release(int r) const { mbar_arrive(empty(r % STAGES)); }
 };
+
+// The producer thread's whole job: stream the K/V tiles of every segment of
+// this CTA's range, in order, through the ring.  Unit u = (b, g*HC + hc)
+// reads K/V head b*G + g.
+template <class Pipe>
+__device__ __forceinline__ void produce_range(const Pipe &pipe, const SchedParams &s, const CtaRange &range,
+                                              const CUtensorMap *tmK, const CUtensorMap *tmV, int box_elems, int G,
+                                              int HC) {
+  const uint64_t pol = l2_policy_evict_first();
+  SegmentCursor cur;
+  cur.init(s, range);
+  Segment seg;
+  int r = 0;
+  bool ok = true;
+  while (ok && cur.next(s, seg)) {
+    const int bg = seg.b * G + seg.uib / HC;
+    for (int t = seg.t0; t < seg.t1; ++t) {
+      if (!pipe.acquire(r)) {
+        ok = false;
+        break;
+      }
+      pipe.load(r, tmK, tmV, box_elems, bg, t * Pipe::BLOCK_N, pol);
+      ++r;
+    }
+  }
+  pipe.drain(r);
+}
 
 __device__ __forceinline__ void consumer_bar_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// Named barrier 1 over the consumer threads that also ANDs `ok` across
+// them, so that every consumer warp takes the same decision after a timed
+// out wait (and they keep meeting at the same barriers).
+__device__ __forceinline__ bool consumer_bar_and(int nthreads, bool ok) {
+  uint32_t res;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(res)
+      : "r"((uint32_t)ok), "r"(nthreads)
+      : "memory");
+  return res != 0;
 }
 
 // Rounds the dynamic shared-memory base up to 1024 bytes.

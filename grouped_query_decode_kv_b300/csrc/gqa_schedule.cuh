@@ -1,0 +1,178 @@
+// Stream-K work split of one decode-attention call over a persistent grid.
+//
+// Work units are u = (b*G + g)*HC + hc (batch row b, KV head g, head chunk
+// hc), in this order.  Every unit of batch row b holds tiles_b =
+// ceil(L_b / BLOCK_N) tiles of BLOCK_N cached positions, so the call has
+// T = sum_b G*HC*tiles_b tiles in one flat index space.  CTA c of a grid of
+// P CTAs takes the contiguous range [start(c), start(c+1)):
+//   start(c) = floor(c*T/P)   when T >= P (every range non-empty),
+//   start(c) = min(c, T)      when T <  P (one tile each, the rest idle).
+// So every CTA streams the same number of K/V bytes (to within one tile),
+// whatever the lengths, and a range cuts a unit only at its two ends.
+//
+// A range is walked as segments: the part of one unit that lies in the
+// range.  A segment that is a whole unit is finished in place (out written
+// directly).  Otherwise it leaves a partial softmax state in a workspace
+// slot: slot 2c for CTA c's first segment, 2c+1 for its last.  The CTA that
+// holds a split unit's first tile records (its slot, last CTA of the unit)
+// in unit_info[u]; the combine kernel merges the unit's partials from that
+// slot and slots 2c of the CTAs after it.
+//
+// The lengths live in device memory, so each CTA derives T and its own
+// starting row from seq_lens with a warp scan (O(B/32) steps per CTA).
+#pragma once
+
+#include "gqa_device.cuh"
+
+namespace gqa {
+
+struct SchedParams {
+  const int32_t *seq_lens;
+  int B;
+  int Nmax;
+  int units_per_b;  // G * HC
+  int block_n;      // positions per tile
+};
+
+__device__ __forceinline__ int clamp_len(int L, int Nmax) { return max(0, min(L, Nmax)); }
+
+__device__ __forceinline__ int row_tiles(const SchedParams &s, int b) {
+  const int L = clamp_len(__ldg(s.seq_lens + b), s.Nmax);
+  return (L + s.block_n - 1) / s.block_n;
+}
+
+__device__ __forceinline__ long long cta_start(long long c, long long T, long long P) {
+  return T >= P ? (c * T) / P : (c < T ? c : T);
+}
+
+// The CTA whose range holds global tile t (0 <= t < T).
+__device__ __forceinline__ int cta_of_tile(long long t, long long T, long long P) {
+  if (T < P) return (int)t;
+  return (int)(((t + 1) * P + T - 1) / T - 1);
+}
+
+__device__ __forceinline__ long long warp_incl_scan(long long v, int lane) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const long long o = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += o;
+  }
+  return v;
+}
+
+// This CTA's place in the flat tile space, computed by one warp.
+struct CtaRange {
+  long long T;      // total tiles of the call
+  long long begin;  // first tile of this CTA
+  long long end;    // one past its last tile
+  long long pre_b;  // global index of the first tile of row b
+  int b;            // row holding `begin` (valid when begin < end)
+};
+
+// All 32 lanes of one warp call this.  Also flags out-of-range lengths and
+// zero-fills the output rows of empty sequences (L_b = 0) that this CTA owns
+// (row b is owned by CTA b % P), writing `row_bytes` bytes per row of `out`.
+__device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int lane, void *out, size_t row_bytes) {
+  const int P = gridDim.x, c = blockIdx.x;
+  long long T = 0;
+  for (int base = 0; base < s.B; base += 32) {
+    const int b = base + lane;
+    long long t = 0;
+    bool zero_mine = false;
+    if (b < s.B) {
+      const int Lraw = __ldg(s.seq_lens + b);
+      const int L = clamp_len(Lraw, s.Nmax);
+      t = (long long)((L + s.block_n - 1) / s.block_n) * s.units_per_b;
+      const bool mine = (b % P) == c;
+      if (mine && (Lraw <= 0 || Lraw > s.Nmax)) flag_error(GQA_DEVERR_ATTN_LEN);
+      zero_mine = mine && L == 0;
+    }
+    unsigned zero_rows = __ballot_sync(0xffffffffu, zero_mine);
+    while (zero_rows) {  // warp-uniform loop over this chunk's empty rows
+      const int src = __ffs(zero_rows) - 1;
+      zero_rows &= zero_rows - 1;
+      uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(out) + (size_t)(base + src) * row_bytes);
+      for (size_t i = lane; i < row_bytes / 16; i += 32) o[i] = make_uint4(0, 0, 0, 0);
+    }
+    const long long incl = warp_incl_scan(t, lane);
+    T += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  CtaRange r;
+  r.T = T;
+  r.begin = cta_start(c, T, P);
+  r.end = cta_start(c + 1, T, P);
+  r.b = 0;
+  r.pre_b = 0;
+  if (r.begin >= r.end) return r;
+  long long acc = 0;
+  for (int base = 0; base < s.B; base += 32) {
+    const int b = base + lane;
+    const long long t = b < s.B ? (long long)row_tiles(s, b) * s.units_per_b : 0;
+    const long long incl = warp_incl_scan(t, lane);
+    const long long lo = acc + incl - t, hi = acc + incl;
+    const unsigned hit = __ballot_sync(0xffffffffu, b < s.B && lo <= r.begin && r.begin < hi);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      r.b = base + src;
+      r.pre_b = __shfl_sync(0xffffffffu, lo, src);
+      break;
+    }
+    acc += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return r;
+}
+
+// One segment: tiles [t0, t1) of unit (b, uib) where uib = g*HC + hc.
+struct Segment {
+  int b, uib;
+  int t0, t1;
+  int tiles;             // tiles of every unit of row b
+  long long unit_first;  // global index of the unit's first tile
+};
+
+// Walks the segments of a range; every thread that calls next() with the
+// same cursor sees the same sequence.
+struct SegmentCursor {
+  long long pos, end, pre_b;
+  int b, tiles_b;
+
+  __device__ __forceinline__ void init(const SchedParams &s, const CtaRange &r) {
+    pos = r.begin;
+    end = r.end;
+    pre_b = r.pre_b;
+    b = r.b;
+    tiles_b = pos < end ? row_tiles(s, b) : 0;
+  }
+
+  __device__ __forceinline__ bool next(const SchedParams &s, Segment &seg) {
+    if (pos >= end) return false;
+    while (pos >= pre_b + (long long)tiles_b * s.units_per_b) {
+      pre_b += (long long)tiles_b * s.units_per_b;
+      ++b;
+      tiles_b = row_tiles(s, b);
+    }
+    const long long off = pos - pre_b;
+    seg.b = b;
+    seg.uib = (int)(off / tiles_b);
+    seg.t0 = (int)(off % tiles_b);
+    const long long left = end - pos;
+    seg.t1 = (int)(left < (long long)(tiles_b - seg.t0) ? seg.t0 + left : tiles_b);
+    seg.tiles = tiles_b;
+    seg.unit_first = pre_b + (long long)seg.uib * tiles_b;
+    pos += seg.t1 - seg.t0;
+    return true;
+  }
+};
+
+// Bookkeeping of a finished segment that is not a whole unit: the slot its
+// partial goes to, and (for the unit's first CTA) the unit_info record.
+__device__ __forceinline__ int partial_slot(int seg_index) {
+  return 2 * (int)blockIdx.x + (seg_index == 0 ? 0 : 1);
+}
+
+__device__ __forceinline__ int2 unit_record(const Segment &seg, int slot, long long T) {
+  const long long last_tile = seg.unit_first + seg.tiles - 1;
+  return make_int2(slot, cta_of_tile(last_tile, T, gridDim.x));
+}
+
+}  // namespace gqa

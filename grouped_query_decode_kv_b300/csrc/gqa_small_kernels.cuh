@@ -22,38 +22,52 @@ __device__ __forceinline__ float to_float<__nv_bfloat16>(__nv_bfloat16 x) { retu
 template <>
 __device__ __forceinline__ float to_float<float>(float x) { return x; }
 
-// One warp per (b, h): out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over
-// the S_b = ceil(L_b / chunk) splits of the sequence.  Batches with a single
-// split were written directly by the split kernel and are skipped.
+// One warp per (b, h): merge the partial softmax states of the unit that
+// holds head h when the stream-K split cut that unit between CTAs:
+//   out = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k,  M = max_k m_k,
+// over the unit's partials (slot info.x of its first CTA, then slot 2c of
+// every later CTA c up to info.y).  Units finished inside one CTA
+// (info.y < 0) and empty sequences were written by the split kernel.
+// Launched as a programmatic dependent of the split kernel: it waits for
+// that grid to finish before reading the workspace.
 template <typename T, int D>
 __global__ void __launch_bounds__(128) gqa_combine_kernel(const CombineParams p) {
   constexpr int PER_LANE = D / 32;
+  griddep_wait();
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x * 4 + warp;
-  if (bh >= p.B * p.H) return;
-  const int b = bh / p.H;
+  const long long bh = (long long)blockIdx.x * 4 + warp;
+  if (bh >= (long long)p.B * p.H) return;
+  const int b = (int)(bh / p.H), h = (int)(bh % p.H);
   const int L = max(0, min(p.seq_lens[b], p.Nmax));
-  const int S_b = (L + p.chunk - 1) / p.chunk;
-  if (S_b <= 1) return;
-  const float2 *ml = reinterpret_cast<const float2 *>(p.ml_part) + (size_t)bh * p.S_max;
+  if (L == 0) return;
+  const int g = h / p.n_rep, rr = h % p.n_rep;
+  const int hc = rr / p.heads_per_cta, hl = rr % p.heads_per_cta;
+  const int2 info = p.unit_info[((size_t)b * p.G + g) * p.head_chunks + hc];
+  if (info.y < 0) return;
+  const int c_lo = info.x >> 1;
+  const int n = info.y - c_lo + 1;  // number of partials
+  const float2 *ml = reinterpret_cast<const float2 *>(p.ml_part);
+  auto slot_of = [&](int k) { return k == 0 ? info.x : 2 * (c_lo + k); };
   float M = -INFINITY;
-  for (int s = lane; s < S_b; s += 32) M = fmaxf(M, ml[s].x);
+  for (int k = lane; k < n; k += 32) M = fmaxf(M, ml[(size_t)slot_of(k) * p.heads_per_cta + hl].x);
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float acc[PER_LANE];
 #pragma unroll
   for (int e = 0; e < PER_LANE; ++e) acc[e] = 0.f;
   float l = 0.f;
-  const float *op = p.o_part + (size_t)bh * p.S_max * D + lane * PER_LANE;
-  for (int s = 0; s < S_b; ++s) {
-    const float2 mls = ml[s];
+  for (int k = 0; k < n; ++k) {
+    const size_t ps = (size_t)slot_of(k) * p.heads_per_cta + hl;
+    const float2 mls = ml[ps];
     const float w = merge_weight(mls.x, M);
     l += w * mls.y;
+    const float *op = p.o_part + ps * D + lane * PER_LANE;
     if constexpr (PER_LANE == 4) {
-      const float4 v = *reinterpret_cast<const float4 *>(op + (size_t)s * D);
+      const float4 v = *reinterpret_cast<const float4 *>(op);
       acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
     } else {
-      const float2 v = *reinterpret_cast<const float2 *>(op + (size_t)s * D);
+      const float2 v = *reinterpret_cast<const float2 *>(op);
       acc[0] += w * v.x; acc[1] += w * v.y;
     }
   }
@@ -70,6 +84,8 @@ __global__ void __launch_bounds__(256) gqa_kv_append_kernel(const uint4 *__restr
                                                             uint4 *__restrict__ k_cache,
                                                             uint4 *__restrict__ v_cache, int32_t *seq_lens,
                                                             int G, int Nmax, int chunks_per_row) {
+  griddep_wait();  // launched as a programmatic dependent: earlier kernels' writes are visible
+  griddep_launch_dependents();
   const int b = blockIdx.x;
   const int L = seq_lens[b];
   __syncthreads();  // every thread has read L before thread 0 may update it

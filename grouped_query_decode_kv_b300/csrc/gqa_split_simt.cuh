@@ -2,14 +2,17 @@
 // two query heads in bf16 (MHA-like shapes, where a K/V row is used by too few
 // heads to fill an MMA tile) and for every shape in fp32.
 //
-// Same TMA pipeline as the MMA kernel.  Inside a warp, 8 lanes share one
+// Persistent grid: each CTA walks its stream-K range of tiles (see
+// gqa_schedule.cuh) unit by unit, with the same TMA pipeline as the MMA
+// kernel running on across units.  Inside a warp, 8 lanes share one
 // cached position: lane j holds the 16-byte chunk j of every 128-byte box of
 // the row (so a quarter-warp reads one full 128-byte line of the swizzled
 // tile, free of bank conflicts), the q.k partial sums are reduced over the 8
 // lanes with shuffles, and each 8-lane group keeps its own online-softmax
 // state (running max, sum, output slice) over the positions it visits.
 // The four groups of a warp and the four consumer warps are merged by
-// log-sum-exp at the end.
+// log-sum-exp at the end of every unit, in a scratch area of its own so that
+// the ring keeps filling meanwhile.
 #pragma once
 
 #include "gqa_params.cuh"
@@ -35,8 +38,10 @@ struct SimtCfg {
   static constexpr int ROWS_PER_WARP = BLOCK_N / 4;
   static constexpr int SLOT_WORDS = NH * (EPL + 2) * 8;
   static constexpr int EPI_BYTES = 3 * SLOT_WORDS * 4;
-  static constexpr int BODY_BYTES = Pipe::PIPE_BYTES > EPI_BYTES ? Pipe::PIPE_BYTES : EPI_BYTES;
-  static constexpr int SMEM_BYTES = 1024 + BODY_BYTES + 2 * Pipe::STAGES * 8;
+  static constexpr int EPI_OFF = Pipe::PIPE_BYTES;            // merge scratch
+  static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;         // full[], empty[] mbarriers
+  static constexpr int RANGE_OFF = BAR_OFF + 2 * Pipe::STAGES * 8;
+  static constexpr int SMEM_BYTES = 1024 + RANGE_OFF + (int)sizeof(CtaRange);
   static_assert(ROWS_PER_WARP % 4 == 0, "four 8-lane groups per warp");
   static_assert(NBOX >= 1, "a row spans at least one 128-byte box");
 };
@@ -93,209 +98,230 @@ __global__ void __launch_bounds__(C::THREADS)
   constexpr int D = C::D, NH = C::NH, EPC = C::EPC, EPL = C::EPL, NBOX = C::NBOX;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-
-  const int s = blockIdx.x, b = blockIdx.z;
-  const int g = blockIdx.y / p.head_chunks, hc = blockIdx.y % p.head_chunks;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h_first = g * p.n_rep + hc * NH;
-  const int nh = min(NH, p.n_rep - hc * NH);
-
-  int L = p.seq_lens[b];
-  if ((L <= 0 || L > p.Nmax) && s == 0 && hc == 0 && threadIdx.x == 0) flag_error(GQA_DEVERR_ATTN_LEN);
-  L = max(0, min(L, p.Nmax));
-  if (L == 0) {
-    if (s == 0) {
-      T *o = reinterpret_cast<T *>(p.out) + ((size_t)b * p.H + h_first) * D;
-      for (int i = threadIdx.x; i < nh * D; i += C::THREADS) o[i] = T(0.f);
-    }
-    return;
-  }
-  const int start = s * p.chunk;
-  if (start >= L) return;
-  const int end = min(start + p.chunk, L);
-  const int ntiles = (end - start + C::BLOCK_N - 1) / C::BLOCK_N;
-  const bool direct = (L + p.chunk - 1) / p.chunk == 1;
 
   Pipe pipe;
   pipe.base = smem_u32(smem);
-  pipe.full0 = pipe.base + C::BODY_BYTES;
+  pipe.full0 = pipe.base + C::BAR_OFF;
   pipe.empty0 = pipe.full0 + 8 * Pipe::STAGES;
+  CtaRange *range_smem = reinterpret_cast<CtaRange *>(smem + C::RANGE_OFF);
+  SchedParams sp;
+  sp.seq_lens = p.seq_lens;
+  sp.B = p.B;
+  sp.Nmax = p.Nmax;
+  sp.units_per_b = p.G * p.head_chunks;
+  sp.block_n = C::BLOCK_N;
+
   if (threadIdx.x == 0) pipe.init();
+  griddep_wait();  // lengths and cache rows written by earlier kernels are visible
+  if (warp == 0) {
+    const CtaRange r = warp_plan_range(sp, lane, p.out, (size_t)p.H * D * sizeof(T));
+    if (lane == 0) *range_smem = r;
+  }
   __syncthreads();
+  griddep_launch_dependents();
+  const CtaRange range = *range_smem;
+  if (range.begin >= range.end) return;
 
   if (warp == C::CONSUMER_WARPS) {
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      pipe.produce(&tmK, &tmV, C::BOX_ELEMS, b * p.G + g, start, ntiles);
+      produce_range(pipe, sp, range, &tmK, &tmV, C::BOX_ELEMS, p.G, p.head_chunks);
     }
     return;
   }
 
   const int tg = lane >> 3, j = lane & 7;
+  float *scratch = reinterpret_cast<float *>(smem + C::EPI_OFF);
+  SegmentCursor cur;
+  cur.init(sp, range);
+  Segment seg;
+  int r = 0;  // ring slot of the next tile
+  bool alive = true;
+  for (int seg_index = 0; alive && cur.next(sp, seg); ++seg_index) {
+    const int g = seg.uib / p.head_chunks, hc = seg.uib % p.head_chunks;
+    const int b = seg.b;
+    const int h_first = g * p.n_rep + hc * NH;
+    const int nh = min(NH, p.n_rep - hc * NH);
+    const int L = clamp_len(__ldg(p.seq_lens + b), p.Nmax);
 
-  // this lane's slice of q: element e of box bx is d = bx*BOX_ELEMS + j*EPC + e
-  float qf[NH][EPL];
-#pragma unroll
-  for (int h = 0; h < NH; ++h) {
-    const int hh = h_first + (h < nh ? h : 0);
-    const T *qrow = reinterpret_cast<const T *>(p.q) + ((size_t)b * p.H + hh) * D;
-#pragma unroll
-    for (int bx = 0; bx < NBOX; ++bx) {
-      const uint4 c = __ldg(reinterpret_cast<const uint4 *>(qrow + bx * C::BOX_ELEMS + j * EPC));
-      widen_chunk<T>(c, &qf[h][bx * EPC]);
-    }
-  }
-
-  float acc[NH][EPL], m_run[NH], l_run[NH];
-#pragma unroll
-  for (int h = 0; h < NH; ++h) {
-    m_run[h] = -INFINITY;
-    l_run[h] = 0.f;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[h][e] = 0.f;
-  }
-
-  for (int t = 0; t < ntiles; ++t) {
-    const int st = t % Pipe::STAGES;
-    if (!mbar_wait(pipe.full(st), (t / Pipe::STAGES) & 1)) break;
-    const uint32_t kt = pipe.k_tile(st), vt = pipe.v_tile(st);
-    const int n0 = start + t * C::BLOCK_N;
-#pragma unroll 2
-    for (int i = tg; i < C::ROWS_PER_WARP; i += 4) {
-      const int row = warp * C::ROWS_PER_WARP + i;
-      const int tok = n0 + row;
-      if (n0 + warp * C::ROWS_PER_WARP + (i - tg) >= end) break;  // warp-uniform: no position of this step left
-      const bool valid = tok < end;
-      float kf[EPL];
-#pragma unroll
-      for (int bx = 0; bx < NBOX; ++bx) widen_chunk<T>(lds128(swz128(kt + bx * Pipe::BOX_BYTES, row, j)), &kf[bx * EPC]);
-      float x[NH];
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        float dot = 0.f;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) dot = fmaf(qf[h][e], kf[e], dot);
-        dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-        dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-        dot += __shfl_xor_sync(0xffffffffu, dot, 4);
-        x[h] = dot * p.scale_log2;
-      }
-      if (valid) {
-        float vf[EPL];
-#pragma unroll
-        for (int bx = 0; bx < NBOX; ++bx) widen_chunk<T>(lds128(swz128(vt + bx * Pipe::BOX_BYTES, row, j)), &vf[bx * EPC]);
-#pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          if (x[h] > m_run[h]) {
-            const float corr = merge_weight(m_run[h], x[h]);
-            m_run[h] = x[h];
-            l_run[h] *= corr;
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) acc[h][e] *= corr;
-          }
-          const float pw = exp2f(x[h] - m_run[h]);
-          l_run[h] += pw;
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) acc[h][e] = fmaf(pw, vf[e], acc[h][e]);
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(pipe.empty(st));
-  }
-
-  // ---- merge the four 8-lane groups of the warp (xor 8, xor 16)
-#pragma unroll
-  for (int off = 8; off <= 16; off <<= 1) {
+    // this lane's slice of q: element e of box bx is d = bx*BOX_ELEMS + j*EPC + e
+    float qf[NH][EPL];
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
-      const float mo = __shfl_xor_sync(0xffffffffu, m_run[h], off);
-      const float lo = __shfl_xor_sync(0xffffffffu, l_run[h], off);
-      const float M = fmaxf(m_run[h], mo);
-      const float ws = merge_weight(m_run[h], M), wo = merge_weight(mo, M);
-      l_run[h] = l_run[h] * ws + lo * wo;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        const float ao = __shfl_xor_sync(0xffffffffu, acc[h][e], off);
-        acc[h][e] = acc[h][e] * ws + ao * wo;
-      }
-      m_run[h] = M;
-    }
-  }
-
-  // ---- merge the four warps through shared memory (lanes 0..7 hold the state)
-  consumer_bar_sync(C::CONSUMER_WARPS * 32);
-  float *scratch = reinterpret_cast<float *>(smem);
-  if (warp > 0 && lane < 8) {
-    float *slot = scratch + (warp - 1) * C::SLOT_WORDS + lane;
-    int i = 0;
-#pragma unroll
-    for (int h = 0; h < NH; ++h) {
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) slot[8 * i++] = acc[h][e];
-      slot[8 * i++] = m_run[h];
-      slot[8 * i++] = l_run[h];
-    }
-  }
-  consumer_bar_sync(C::CONSUMER_WARPS * 32);
-  if (warp != 0 || lane >= 8) return;
-
-#pragma unroll
-  for (int h = 0; h < NH; ++h) {
-    const int base = h * (EPL + 2);
-    float mk[3], lk[3], wk[3];
-    float M = m_run[h];
-#pragma unroll
-    for (int k = 0; k < 3; ++k) {
-      const float *slot = scratch + k * C::SLOT_WORDS + lane;
-      mk[k] = slot[8 * (base + EPL)];
-      lk[k] = slot[8 * (base + EPL + 1)];
-      M = fmaxf(M, mk[k]);
-    }
-    const float ws = merge_weight(m_run[h], M);
-    float l = l_run[h] * ws;
-#pragma unroll
-    for (int k = 0; k < 3; ++k) {
-      wk[k] = merge_weight(mk[k], M);
-      l += lk[k] * wk[k];
-    }
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      float v = acc[h][e] * ws;
-#pragma unroll
-      for (int k = 0; k < 3; ++k) v += scratch[k * C::SLOT_WORDS + lane + 8 * (base + e)] * wk[k];
-      acc[h][e] = v;
-    }
-    m_run[h] = M;
-    l_run[h] = l;
-  }
-
-#pragma unroll
-  for (int h = 0; h < NH; ++h) {
-    if (h >= nh) break;
-    const size_t bh = (size_t)b * p.H + h_first + h;
-    if (direct) {
-      const float inv = 1.f / l_run[h];
-      T *orow = reinterpret_cast<T *>(p.out) + bh * D;
+      const int hh = h_first + (h < nh ? h : 0);
+      const T *qrow = reinterpret_cast<const T *>(p.q) + ((size_t)b * p.H + hh) * D;
 #pragma unroll
       for (int bx = 0; bx < NBOX; ++bx) {
-        float f[EPC];
-#pragma unroll
-        for (int e = 0; e < EPC; ++e) f[e] = acc[h][bx * EPC + e] * inv;
-        store_chunk<T>(orow + bx * C::BOX_ELEMS + j * EPC, f);
+        const uint4 c = __ldg(reinterpret_cast<const uint4 *>(qrow + bx * C::BOX_ELEMS + j * EPC));
+        widen_chunk<T>(c, &qf[h][bx * EPC]);
       }
-    } else {
-      float *prow = p.o_part + (bh * p.S_max + s) * D;
-#pragma unroll
-      for (int bx = 0; bx < NBOX; ++bx)
-#pragma unroll
-        for (int e = 0; e < EPC; e += 4)
-          *reinterpret_cast<float4 *>(prow + bx * C::BOX_ELEMS + j * EPC + e) =
-              make_float4(acc[h][bx * EPC + e], acc[h][bx * EPC + e + 1], acc[h][bx * EPC + e + 2],
-                          acc[h][bx * EPC + e + 3]);
-      if (j == 0) reinterpret_cast<float2 *>(p.ml_part)[bh * p.S_max + s] = make_float2(m_run[h], l_run[h]);
     }
+
+    float acc[NH][EPL], m_run[NH], l_run[NH];
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      m_run[h] = -INFINITY;
+      l_run[h] = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[h][e] = 0.f;
+    }
+
+    for (int t = seg.t0; t < seg.t1; ++t, ++r) {
+      if (!pipe.wait_full(r)) {
+        alive = false;
+        break;
+      }
+      const int st = r % Pipe::STAGES;
+      const uint32_t kt = pipe.k_tile(st), vt = pipe.v_tile(st);
+      const int n0 = t * C::BLOCK_N;
+      const int end = min(n0 + C::BLOCK_N, L);
+#pragma unroll 2
+      for (int i = tg; i < C::ROWS_PER_WARP; i += 4) {
+        const int row = warp * C::ROWS_PER_WARP + i;
+        const int tok = n0 + row;
+        if (n0 + warp * C::ROWS_PER_WARP + (i - tg) >= end) break;  // warp-uniform: no position of this step left
+        const bool valid = tok < end;
+        float kf[EPL];
+#pragma unroll
+        for (int bx = 0; bx < NBOX; ++bx)
+          widen_chunk<T>(lds128(swz128(kt + bx * Pipe::BOX_BYTES, row, j)), &kf[bx * EPC]);
+        float x[NH];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          float dot = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) dot = fmaf(qf[h][e], kf[e], dot);
+          dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+          dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+          dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+          x[h] = dot * p.scale_log2;
+        }
+        if (valid) {
+          float vf[EPL];
+#pragma unroll
+          for (int bx = 0; bx < NBOX; ++bx)
+            widen_chunk<T>(lds128(swz128(vt + bx * Pipe::BOX_BYTES, row, j)), &vf[bx * EPC]);
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            if (x[h] > m_run[h]) {
+              const float corr = merge_weight(m_run[h], x[h]);
+              m_run[h] = x[h];
+              l_run[h] *= corr;
+#pragma unroll
+              for (int e = 0; e < EPL; ++e) acc[h][e] *= corr;
+            }
+            const float pw = exp2f(x[h] - m_run[h]);
+            l_run[h] += pw;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[h][e] = fmaf(pw, vf[e], acc[h][e]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) pipe.release(r);
+    }
+
+    // ---- merge the four 8-lane groups of the warp (xor 8, xor 16)
+#pragma unroll
+    for (int off = 8; off <= 16; off <<= 1) {
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m_run[h], off);
+        const float lo = __shfl_xor_sync(0xffffffffu, l_run[h], off);
+        const float M = fmaxf(m_run[h], mo);
+        const float ws = merge_weight(m_run[h], M), wo = merge_weight(mo, M);
+        l_run[h] = l_run[h] * ws + lo * wo;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          const float ao = __shfl_xor_sync(0xffffffffu, acc[h][e], off);
+          acc[h][e] = acc[h][e] * ws + ao * wo;
+        }
+        m_run[h] = M;
+      }
+    }
+
+    // ---- merge the four warps through the scratch (lanes 0..7 hold the state)
+    alive = consumer_bar_and(C::CONSUMER_WARPS * 32, alive);
+    if (warp > 0 && lane < 8) {
+      float *slot = scratch + (warp - 1) * C::SLOT_WORDS + lane;
+      int i = 0;
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) slot[8 * i++] = acc[h][e];
+        slot[8 * i++] = m_run[h];
+        slot[8 * i++] = l_run[h];
+      }
+    }
+    consumer_bar_sync(C::CONSUMER_WARPS * 32);
+    if (warp == 0 && lane < 8) {
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const int base = h * (EPL + 2);
+        float mk[3], lk[3], wk[3];
+        float M = m_run[h];
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          const float *slot = scratch + k * C::SLOT_WORDS + lane;
+          mk[k] = slot[8 * (base + EPL)];
+          lk[k] = slot[8 * (base + EPL + 1)];
+          M = fmaxf(M, mk[k]);
+        }
+        const float ws = merge_weight(m_run[h], M);
+        float l = l_run[h] * ws;
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          wk[k] = merge_weight(mk[k], M);
+          l += lk[k] * wk[k];
+        }
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          float v = acc[h][e] * ws;
+#pragma unroll
+          for (int k = 0; k < 3; ++k) v += scratch[k * C::SLOT_WORDS + lane + 8 * (base + e)] * wk[k];
+          acc[h][e] = v;
+        }
+        m_run[h] = M;
+        l_run[h] = l;
+      }
+
+      const bool whole = seg.t0 == 0 && seg.t1 == seg.tiles;
+      const int slot = partial_slot(seg_index);
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        if (h >= nh) break;
+        const size_t bh = (size_t)b * p.H + h_first + h;
+        if (whole) {
+          const float inv = 1.f / l_run[h];
+          T *orow = reinterpret_cast<T *>(p.out) + bh * D;
+#pragma unroll
+          for (int bx = 0; bx < NBOX; ++bx) {
+            float f[EPC];
+#pragma unroll
+            for (int e = 0; e < EPC; ++e) f[e] = acc[h][bx * EPC + e] * inv;
+            store_chunk<T>(orow + bx * C::BOX_ELEMS + j * EPC, f);
+          }
+        } else {
+          const size_t ps = (size_t)slot * p.heads_per_cta + h;
+          float *prow = p.o_part + ps * D;
+#pragma unroll
+          for (int bx = 0; bx < NBOX; ++bx)
+#pragma unroll
+            for (int e = 0; e < EPC; e += 4)
+              *reinterpret_cast<float4 *>(prow + bx * C::BOX_ELEMS + j * EPC + e) =
+                  make_float4(acc[h][bx * EPC + e], acc[h][bx * EPC + e + 1], acc[h][bx * EPC + e + 2],
+                              acc[h][bx * EPC + e + 3]);
+          if (j == 0) reinterpret_cast<float2 *>(p.ml_part)[ps] = make_float2(m_run[h], l_run[h]);
+        }
+      }
+      if (lane == 0 && seg.t0 == 0 && p.unit_info) {
+        const size_t u = (size_t)b * sp.units_per_b + seg.uib;
+        p.unit_info[u] = whole ? make_int2(-1, -1) : unit_record(seg, slot, range.T);
+      }
+    }
+    consumer_bar_sync(C::CONSUMER_WARPS * 32);  // scratch free for the next unit
   }
 }
 

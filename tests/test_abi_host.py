@@ -84,11 +84,13 @@ def test_ws_variant_rejects_missing_workspace(lib):
 
 
 def test_workspace_bytes(lib):
-    # a single split needs no workspace; forced splits need the partials
-    assert lib.gqa_decode_workspace_bytes_ex(1, 8, 2, 64, 128, 0, 128) == 0
+    # one CTA for the whole call (split_tokens covers every tile) needs no
+    # workspace; forced splits need two partial slots per CTA and the unit
+    # records
+    assert lib.gqa_decode_workspace_bytes_ex(1, 8, 2, 64, 128, 0, 256) == 0
     need = lib.gqa_decode_workspace_bytes_ex(2, 8, 2, 128, 1024, 1, 256)
-    parts = 2 * 8 * 4
-    assert need >= parts * 128 * 4 + parts * 2 * 4
+    ctas = (2 * 2 * 1024 // 64) // (256 // 64)     # 4 units x 16 tiles, 4 tiles per CTA
+    assert need >= 2 * ctas * 16 * 128 * 4 + 2 * ctas * 16 * 8 + 4 * 8
     assert lib.gqa_decode_workspace_bytes(2, 8, 3, 128, 1024, 1) == 0      # invalid shape
     assert lib.gqa_decode_workspace_bytes(2, 8, 2, 96, 1024, 1) == 0       # unsupported d
 

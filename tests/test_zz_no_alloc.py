@@ -37,11 +37,12 @@ def _c_args(x, w, out):
 
 def test_oversized_shape_is_rejected_before_any_launch():
     lib = gqa.load_library()
-    # B=512, H=64, G=1, N=4096 needs about 50 MB of partials, above the 32 MiB buffer
-    need = lib.gqa_decode_workspace_bytes(512, 64, 1, 128, 4096, gqa.GQA_BF16)
+    # 65535 sequences x 64 KV heads: the per-unit split records alone take
+    # about 34 MB, above the 32 MiB buffer
+    need = lib.gqa_decode_workspace_bytes(65535, 64, 64, 128, 4096, gqa.GQA_BF16)
     assert need > gqa.NOALLOC_SCRATCH_BYTES
     rc = lib.gqa_decode_attention_noalloc(FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.1), FAKE,
-                                          512, 64, 1, 128, 4096, gqa.GQA_BF16, None)
+                                          65535, 64, 64, 128, 4096, gqa.GQA_BF16, None)
     assert rc == gqa.ERR_SCRATCH_LIMIT
     assert "scratch" in gqa.gqa_status_string(rc)
 
