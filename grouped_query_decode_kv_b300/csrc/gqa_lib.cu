@@ -16,6 +16,7 @@
 #include "gqa_small_kernels.cuh"
 #include "gqa_split_mma.cuh"
 #include "gqa_split_simt.cuh"
+#include "gqa_split_tc.cuh"
 
 namespace gqa {
 namespace {
@@ -35,6 +36,7 @@ using SimtFor = SimtCfg<T, D, NH, (32768 / (2 * D * (int)sizeof(T))), 3>;
 
 struct KernelChoice {
   const void *func;
+  int family;
   int threads;
   int smem;
   int block_n;
@@ -62,62 +64,83 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-template <class C, bool MMA>
-cudaError_t launch_split(dim3 grid, const CUtensorMap &k, const CUtensorMap &v, const SplitParams &p,
-                         cudaStream_t st) {
-  if constexpr (MMA)
-    return launch_pdl(gqa_split_mma_kernel<C>, grid, dim3(C::THREADS), C::SMEM_BYTES, st, k, v, p);
+enum Family { kSimt = 0, kMma = 1, kTc = 2 };
+
+template <class C, int F>
+auto split_kernel_ptr() {
+  if constexpr (F == kMma)
+    return &gqa_split_mma_kernel<C>;
+  else if constexpr (F == kTc)
+    return &gqa_split_tc_kernel<C>;
   else
-    return launch_pdl(gqa_split_simt_kernel<C>, grid, dim3(C::THREADS), C::SMEM_BYTES, st, k, v, p);
+    return &gqa_split_simt_kernel<C>;
 }
 
-template <class C, bool MMA>
+template <class C, int F>
+cudaError_t launch_split(dim3 grid, const CUtensorMap &k, const CUtensorMap &v, const SplitParams &p,
+                         cudaStream_t st) {
+  return launch_pdl(split_kernel_ptr<C, F>(), grid, dim3(C::THREADS), C::SMEM_BYTES, st, k, v, p);
+}
+
+template <class C, int F>
 KernelChoice make_choice() {
   KernelChoice c;
-  if constexpr (MMA)
-    c.func = reinterpret_cast<const void *>(&gqa_split_mma_kernel<C>);
-  else
-    c.func = reinterpret_cast<const void *>(&gqa_split_simt_kernel<C>);
+  c.func = reinterpret_cast<const void *>(split_kernel_ptr<C, F>());
+  c.family = F;
   c.threads = C::THREADS;
   c.smem = C::SMEM_BYTES;
   c.block_n = C::BLOCK_N;
   c.heads = C::HEADS;
-  if constexpr (MMA)
-    c.box_elems = 64;
-  else
+  if constexpr (F == kSimt)
     c.box_elems = C::BOX_ELEMS;
-  c.launch = &launch_split<C, MMA>;
+  else
+    c.box_elems = 64;
+  c.launch = &launch_split<C, F>;
   return c;
 }
+
+// Query heads per KV head from which bf16 d=128 groups go to the tcgen05
+// kernel (tensor-core MMAs with TMEM accumulators); smaller groups use the
+// warp-level MMA kernel, groups of one or two the CUDA-core kernel.
+constexpr int kTcMinNrep = 8;
+using TcD128x16 = TcCfg<16, 3>;
+using TcD128x32 = TcCfg<32, 3>;
+using TcD128x64 = TcCfg<64, 3>;
 
 KernelChoice choose_kernel(gqa_dtype_t dt, int d, int n_rep) {
   if (dt == GQA_BF16) {
     if (d == 128) {
-      if (n_rep == 1) return make_choice<SimtFor<__nv_bfloat16, 128, 1>, false>();
-      if (n_rep == 2) return make_choice<SimtFor<__nv_bfloat16, 128, 2>, false>();
-      if (n_rep <= 16) return make_choice<MmaD128x1, true>();
-      if (n_rep <= 32) return make_choice<MmaD128x2, true>();
-      return make_choice<MmaD128x4, true>();
+      if (n_rep == 1) return make_choice<SimtFor<__nv_bfloat16, 128, 1>, kSimt>();
+      if (n_rep == 2) return make_choice<SimtFor<__nv_bfloat16, 128, 2>, kSimt>();
+      if (n_rep >= kTcMinNrep) {
+        if (n_rep <= 16) return make_choice<TcD128x16, kTc>();
+        if (n_rep <= 32) return make_choice<TcD128x32, kTc>();
+        return make_choice<TcD128x64, kTc>();
+      }
+      if (n_rep <= 16) return make_choice<MmaD128x1, kMma>();
+      if (n_rep <= 32) return make_choice<MmaD128x2, kMma>();
+      return make_choice<MmaD128x4, kMma>();
     }
-    if (n_rep == 1) return make_choice<SimtFor<__nv_bfloat16, 64, 1>, false>();
-    if (n_rep == 2) return make_choice<SimtFor<__nv_bfloat16, 64, 2>, false>();
-    if (n_rep <= 16) return make_choice<MmaD64x1, true>();
-    if (n_rep <= 32) return make_choice<MmaD64x2, true>();
-    return make_choice<MmaD64x4, true>();
+    if (n_rep == 1) return make_choice<SimtFor<__nv_bfloat16, 64, 1>, kSimt>();
+    if (n_rep == 2) return make_choice<SimtFor<__nv_bfloat16, 64, 2>, kSimt>();
+    if (n_rep <= 16) return make_choice<MmaD64x1, kMma>();
+    if (n_rep <= 32) return make_choice<MmaD64x2, kMma>();
+    return make_choice<MmaD64x4, kMma>();
   }
   if (d == 128) {
-    if (n_rep == 1) return make_choice<SimtFor<float, 128, 1>, false>();
-    if (n_rep == 2) return make_choice<SimtFor<float, 128, 2>, false>();
-    return make_choice<SimtFor<float, 128, 4>, false>();
+    if (n_rep == 1) return make_choice<SimtFor<float, 128, 1>, kSimt>();
+    if (n_rep == 2) return make_choice<SimtFor<float, 128, 2>, kSimt>();
+    return make_choice<SimtFor<float, 128, 4>, kSimt>();
   }
-  if (n_rep == 1) return make_choice<SimtFor<float, 64, 1>, false>();
-  if (n_rep == 2) return make_choice<SimtFor<float, 64, 2>, false>();
-  return make_choice<SimtFor<float, 64, 4>, false>();
+  if (n_rep == 1) return make_choice<SimtFor<float, 64, 1>, kSimt>();
+  if (n_rep == 2) return make_choice<SimtFor<float, 64, 2>, kSimt>();
+  return make_choice<SimtFor<float, 64, 4>, kSimt>();
 }
 
 // ----------------------------------------------------------- split plan
 struct Plan {
   KernelChoice k;
+  int heads;        // query heads per unit (per CTA segment)
   int head_chunks;  // HC
   int P;            // CTAs of the split kernel
   long long units;  // B * G * HC
@@ -186,7 +209,10 @@ Plan make_plan(int B, int H, int G, int d, int Nmax, gqa_dtype_t dt, int split_t
   Plan pl;
   const int n_rep = H / G;
   pl.k = choose_kernel(dt, d, n_rep);
-  pl.head_chunks = ceil_div(n_rep, pl.k.heads);
+  // the tcgen05 kernel takes a group of up to 64 heads per unit (its MMA N);
+  // the others have a fixed number of heads per CTA
+  pl.heads = pl.k.family == kTc ? std::min(n_rep, pl.k.heads) : pl.k.heads;
+  pl.head_chunks = ceil_div(n_rep, pl.heads);
   pl.units = (long long)B * G * pl.head_chunks;
   const long long tiles_full = pl.units * ceil_div(Nmax, pl.k.block_n);
   long long P;
@@ -207,8 +233,8 @@ bool plan_fits(const Plan &pl, int B, int G) { return B <= 65535 && pl.units < (
 
 // Workspace: partial outputs and (m, l) of two slots per CTA, and the
 // per-unit record of split units.  A single CTA never splits a unit.
-size_t ws_opart_bytes(const Plan &pl, int d) { return align256((size_t)2 * pl.P * pl.k.heads * d * sizeof(float)); }
-size_t ws_ml_bytes(const Plan &pl) { return align256((size_t)2 * pl.P * pl.k.heads * 2 * sizeof(float)); }
+size_t ws_opart_bytes(const Plan &pl, int d) { return align256((size_t)2 * pl.P * pl.heads * d * sizeof(float)); }
+size_t ws_ml_bytes(const Plan &pl) { return align256((size_t)2 * pl.P * pl.heads * 2 * sizeof(float)); }
 
 size_t workspace_for(const Plan &pl, int B, int H, int d) {
   (void)B;
@@ -310,7 +336,7 @@ int run_attention(const void *q, const void *k, const void *v, const int32_t *sl
   p.G = G;
   p.Nmax = Nmax;
   p.n_rep = H / G;
-  p.heads_per_cta = pl.k.heads;
+  p.heads_per_cta = pl.heads;
   p.head_chunks = pl.head_chunks;
   if (pl.k.launch(dim3(pl.P), mk, mv, p, st) != cudaSuccess) {
     cudaGetLastError();

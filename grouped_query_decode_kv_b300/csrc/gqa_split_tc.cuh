@@ -1,0 +1,551 @@
+// Split-KV GQA decode kernel on the 5th-generation tensor cores (tcgen05,
+// accumulators in tensor memory), bf16, head dimension 128, for groups of
+// n_rep >= 8 query heads per KV head (GQA-8 and coarser, MQA).
+//
+// Per tile of 128 cached positions of one unit (batch b, KV head g), with
+// the group's query heads (up to 64 per unit, padded to N = 64) as N:
+//   S^T  = K_tile . Q^T     M = 128 positions, N = 64 heads, K = d = 128
+//                           A = K tile as TMA landed it (K-major, 128-byte
+//                           swizzle), B = Q (K-major, swizzled by the kernel)
+//   O^T += V_tile^T . P^T   M = d = 128, N = 64 heads, K = 128 positions
+//                           A = V tile as TMA landed it (MN-major: d runs
+//                           along the 128-byte rows), B = P^T written by the
+//                           softmax threads (MN-major: heads along the rows)
+// Each K/V byte read from HBM serves every query head of the group (the
+// point of GQA: GQA paper, section 2.2), and the MMA work per tile is the
+// same 4.2 MFLOP whatever n_rep, well under the tensor pipe's rate.
+//
+// Softmax: thread R of the four softmax warps owns TMEM lane R, which is
+// cached position R of the tile in S^T and output dimension R in O^T.  For
+// each head h it keeps the running max m[h] (replicated in every thread,
+// base-2 units) and its own partial sum l_R[h].  A tile first votes whether
+// any logit exceeds m[h] + 8; only then (always on a unit's first tile) the
+// tile's per-head maxima are reduced across the 128 threads and m moves,
+// with O^T rescaled in TMEM.  P = 2^(S - m) is written to shared memory as
+// bf16; the l_R[h] are summed across threads once per unit.
+//
+// Warp roles (192 threads, one CTA per SM):
+//   warp 0     TMA producer of the CTA's stream-K range (gqa_pipeline.cuh)
+//   warp 1     MMA issuer (one thread) and TMEM owner
+//   warps 2..5 softmax, Q loads, output
+// S^T is double-buffered in TMEM so that S of tile t+1 overlaps the softmax
+// of tile t; O^T is double-buffered across units.  Every mbarrier wait is
+// bounded (about one second), after which the CTA winds down and flags
+// GQA_DEVERR_TIMEOUT.
+#pragma once
+
+#include "gqa_params.cuh"
+#include "gqa_pipeline.cuh"
+#include "gqa_tcgen05.cuh"
+
+namespace gqa {
+
+template <int NR_, int STAGES_>
+struct TcCfg {
+  static constexpr int D = 128;
+  static constexpr int BLOCK_N = 128;  // positions per tile: M of S^T, K of P.V
+  static constexpr int STAGES = STAGES_;
+  static constexpr int NQ = 64;        // N of both MMAs: heads per unit, zero-padded
+  static constexpr int NR = NR_;       // heads a softmax thread processes (>= heads per unit)
+  static constexpr int HEADS = NR;
+  static_assert(NR == 16 || NR == 32 || NR == 64, "per-thread head count");
+  using Pipe = KVPipe<2, BLOCK_N, STAGES, 1>;  // one "empty" arrival per tile: the MMA commit
+  static constexpr int THREADS = 6 * 32;
+  static constexpr int SOFT = 128;             // softmax threads
+  // TMEM columns: S^T buffers [0, 2*NQ), O^T buffers [2*NQ, 4*NQ)
+  static constexpr int TM_S = 0;
+  static constexpr int TM_O = 2 * NQ;
+  static constexpr int TM_COLS = 4 * NQ;  // 256: a power of two
+  // shared memory
+  static constexpr int Q_OFF = Pipe::PIPE_BYTES;  // Q: two 128-byte-wide boxes of NQ rows
+  static constexpr int Q_BOX = NQ * 128;
+  static constexpr int P_OFF = Q_OFF + 2 * Q_BOX;  // P^T: BLOCK_N rows of NQ bf16 (128 B)
+  static constexpr int RED_OFF = P_OFF + BLOCK_N * 128;  // [4][NQ] cross-warp reduction
+  static constexpr int FIN_OFF = RED_OFF + 4 * NQ * 4;   // [NQ] reduced value
+  static constexpr int M_OFF = FIN_OFF + NQ * 4;         // [NQ] running max of the unit
+  static constexpr int CORR_OFF = M_OFF + NQ * 4;        // [NQ] rescale factor of a tile
+  static constexpr int BAR_OFF = CORR_OFF + NQ * 4;
+  // pipe full[STAGES], empty[STAGES]; then s_full[2], s_free[2], p_full,
+  // pv_done, o_free[2], q_full, mma_done
+  static constexpr int NBAR = 2 * STAGES + 10;
+  static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int RANGE_OFF = TMEM_SLOT_OFF + 16;
+  static constexpr int SMEM_BYTES = 1024 + RANGE_OFF + (int)sizeof(CtaRange);
+  // more than half of an SM's shared memory: one CTA per SM, so the TMEM
+  // allocation never waits for another CTA
+  static_assert(SMEM_BYTES > 116 * 1024 && SMEM_BYTES <= 227 * 1024, "one resident CTA per SM");
+};
+
+struct TcBars {
+  uint32_t b0;
+  __device__ __forceinline__ uint32_t s_full(int i) const { return b0 + 8 * i; }
+  __device__ __forceinline__ uint32_t s_free(int i) const { return b0 + 16 + 8 * i; }
+  __device__ __forceinline__ uint32_t p_full() const { return b0 + 32; }
+  __device__ __forceinline__ uint32_t pv_done() const { return b0 + 40; }
+  __device__ __forceinline__ uint32_t o_free(int i) const { return b0 + 48 + 8 * i; }
+  __device__ __forceinline__ uint32_t q_full() const { return b0 + 64; }
+  __device__ __forceinline__ uint32_t mma_done() const { return b0 + 72; }
+};
+
+// All lanes of a warp wait; a wait that timed out in any lane counts as
+// timed out in all of them, so that the warp stays converged for the
+// warp-collective tcgen05 loads and stores.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+}
+
+// Named barrier 2 over the 128 softmax threads; the second form ORs a flag.
+__device__ __forceinline__ void soft_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+__device__ __forceinline__ bool soft_bar_or(bool v) {
+  uint32_t res;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 2, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(res)
+      : "r"((uint32_t)v)
+      : "memory");
+  return res != 0;
+}
+
+// Reduces v[h] (h < NR) across the 32 lanes of a warp (a butterfly that
+// halves the values kept per lane at each step while more than one is left,
+// then combines single values).  Afterwards lane L holds the result for head
+// j + K*(L >> SHIFT) in v[j], j < K = max(1, NR/32).
+template <int NR>
+struct TransposeReduce {
+  static constexpr int K = NR > 32 ? NR / 32 : 1;
+  static constexpr int HALVINGS = NR >= 32 ? 5 : (NR == 16 ? 4 : 3);
+  static constexpr int SHIFT = 5 - HALVINGS;
+};
+
+template <int NR, bool MAX>
+__device__ __forceinline__ void warp_transpose_reduce(float (&v)[NR], int lane) {
+#pragma unroll
+  for (int s = 0; s < 5; ++s) {
+    const int o = 16 >> s, n = NR >> s;
+    if (n > TransposeReduce<NR>::K) {
+      const bool upper = (lane & o) != 0;
+#pragma unroll
+      for (int j = 0; j < n / 2; ++j) {
+        const float give = upper ? v[j] : v[j + n / 2];
+        const float keep = upper ? v[j + n / 2] : v[j];
+        const float got = __shfl_xor_sync(0xffffffffu, give, o);
+        v[j] = MAX ? fmaxf(keep, got) : keep + got;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < TransposeReduce<NR>::K; ++j) {
+        const float got = __shfl_xor_sync(0xffffffffu, v[j], o);
+        v[j] = MAX ? fmaxf(v[j], got) : v[j] + got;
+      }
+    }
+  }
+}
+
+// Per-head reduction of v over the 128 softmax threads (v is clobbered);
+// afterwards every softmax thread can read the result of head h from fin[h].
+template <class C, bool MAX>
+__device__ __forceinline__ void soft_reduce(float (&v)[C::NR], int sub, int lane, float *red, float *fin, int R) {
+  using TR = TransposeReduce<C::NR>;
+  warp_transpose_reduce<C::NR, MAX>(v, lane);
+#pragma unroll
+  for (int j = 0; j < TR::K; ++j) red[sub * C::NQ + j + TR::K * (lane >> TR::SHIFT)] = v[j];
+  soft_bar();
+  if (R < C::NR) {
+    const float a = red[R], b2 = red[C::NQ + R], c = red[2 * C::NQ + R], d = red[3 * C::NQ + R];
+    fin[R] = MAX ? fmaxf(fmaxf(a, b2), fmaxf(c, d)) : (a + b2) + (c + d);
+  }
+  soft_bar();
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+    gqa_split_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const SplitParams p) {
+  using Pipe = typename C::Pipe;
+  constexpr int D = C::D, BN = C::BLOCK_N, ST = C::STAGES, NQ = C::NQ, NR = C::NR;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  Pipe pipe;
+  pipe.base = smem_u32(smem);
+  pipe.full0 = pipe.base + C::BAR_OFF;
+  pipe.empty0 = pipe.full0 + 8 * ST;
+  TcBars bars{pipe.empty0 + 8 * ST};
+  const uint32_t qbase = pipe.base + C::Q_OFF;
+  const uint32_t pbase = pipe.base + C::P_OFF;
+  float *red = reinterpret_cast<float *>(smem + C::RED_OFF);
+  float *fin = reinterpret_cast<float *>(smem + C::FIN_OFF);
+  float *m_s = reinterpret_cast<float *>(smem + C::M_OFF);
+  float *corr_s = reinterpret_cast<float *>(smem + C::CORR_OFF);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::TMEM_SLOT_OFF);
+  CtaRange *range_smem = reinterpret_cast<CtaRange *>(smem + C::RANGE_OFF);
+  SchedParams sp;
+  sp.seq_lens = p.seq_lens;
+  sp.B = p.B;
+  sp.Nmax = p.Nmax;
+  sp.units_per_b = p.G * p.head_chunks;
+  sp.block_n = BN;
+
+  if (threadIdx.x == 0) {
+    pipe.init();
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bars.s_full(i), 1);
+      mbar_init(bars.s_free(i), 4);
+      mbar_init(bars.o_free(i), 4);
+    }
+    mbar_init(bars.p_full(), 4);
+    mbar_init(bars.pv_done(), 1);
+    mbar_init(bars.q_full(), 4);
+    mbar_init(bars.mma_done(), 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
+    tc::tmem_relinquish();
+  }
+  griddep_wait();  // lengths, q and cache rows written by earlier kernels are visible
+  if (warp == 0) {
+    const CtaRange r = warp_plan_range(sp, lane, p.out, (size_t)p.H * D * sizeof(__nv_bfloat16));
+    if (lane == 0) *range_smem = r;
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  griddep_launch_dependents();
+  const CtaRange range = *range_smem;
+  const uint32_t tmem = *tmem_slot;
+
+  if (range.begin < range.end) {
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        produce_range(pipe, sp, range, &tmK, &tmV, 64, p.G, p.head_chunks);
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(BN, NQ, false, false);
+        constexpr uint32_t IDESC_PV = tc::idesc_bf16_f32(D, NQ, true, true);
+        // Two walks over the CTA's tiles: S^T of tile ts may start once its K
+        // tile landed, its S buffer is free and (first tile of a unit) the
+        // unit's Q is in place; P.V of tile tp once its P is written and
+        // (first tile of a unit) its O buffer is free.  The thread issues
+        // whichever is ready, so that a stage is released as soon as its P.V
+        // is done rather than after the next tile's load.
+        struct Walk {
+          SegmentCursor cur;
+          Segment seg;
+          bool has;
+          int unit, i, tg;
+          __device__ __forceinline__ void start(const SchedParams &s, const CtaRange &r) {
+            cur.init(s, r);
+            has = cur.next(s, seg);
+            unit = i = tg = 0;
+          }
+          __device__ __forceinline__ void advance(const SchedParams &s) {
+            ++tg;
+            if (++i == seg.t1 - seg.t0) {
+              i = 0;
+              ++unit;
+              has = cur.next(s, seg);
+            }
+          }
+        };
+        Walk ws, wp;
+        ws.start(sp, range);
+        wp.start(sp, range);
+        unsigned long long idle_since = 0;
+        while (wp.has) {
+          bool progressed = false;
+          if (ws.has && ws.tg < wp.tg + 2) {
+            const int tg = ws.tg, st = tg % ST;
+            if ((ws.i != 0 || mbar_test(bars.q_full(), ws.unit & 1)) && mbar_test(pipe.full(st), (tg / ST) & 1) &&
+                (tg < 2 || mbar_test(bars.s_free(tg & 1), ((tg >> 1) - 1) & 1))) {
+              tc::fence_after();
+              const uint32_t kt = pipe.k_tile(st);
+#pragma unroll
+              for (int ks = 0; ks < D / 16; ++ks) {
+                const uint64_t a = tc::smem_desc_sw128(kt + (ks >> 2) * Pipe::BOX_BYTES + (ks & 3) * 32, 16, 1024);
+                const uint64_t b = tc::smem_desc_sw128(qbase + (ks >> 2) * C::Q_BOX + (ks & 3) * 32, 16, 1024);
+                tc::mma_ss(tmem + C::TM_S + (tg & 1) * NQ, a, b, IDESC_S, ks > 0);
+              }
+              tc::commit(bars.s_full(tg & 1));
+              ws.advance(sp);
+              progressed = true;
+            }
+          }
+          if (wp.tg < ws.tg) {
+            const int tg = wp.tg, ob = wp.unit & 1;
+            if (mbar_test(bars.p_full(), tg & 1) &&
+                (wp.i != 0 || wp.unit < 2 || mbar_test(bars.o_free(ob), ((wp.unit >> 1) - 1) & 1))) {
+              tc::fence_after();
+              const uint32_t vt = pipe.v_tile(tg % ST);
+#pragma unroll
+              for (int ks = 0; ks < BN / 16; ++ks) {
+                const uint64_t a = tc::smem_desc_sw128(vt + ks * 2048, Pipe::BOX_BYTES, 1024);
+                const uint64_t b = tc::smem_desc_sw128(pbase + ks * 2048, 8192, 1024);
+                tc::mma_ss(tmem + C::TM_O + ob * NQ, a, b, IDESC_PV, wp.i > 0 || ks > 0);
+              }
+              tc::commit(pipe.empty(tg % ST));
+              tc::commit(bars.pv_done());
+              wp.advance(sp);
+              progressed = true;
+            }
+          }
+          if (progressed) {
+            idle_since = 0;
+          } else {
+            __nanosleep(32);  // leave the issue slots to the softmax warp on this SM sub-partition
+            const unsigned long long now = global_timer_ns();
+            if (idle_since == 0) {
+              idle_since = now;
+            } else if (now - idle_since > kWaitLimitNs) {
+              flag_error(GQA_DEVERR_TIMEOUT);
+              break;
+            }
+          }
+        }
+        // nothing of this thread's may still run when TMEM is freed
+        tc::commit(bars.mma_done());
+        mbar_wait(bars.mma_done(), 0);
+      }
+      __syncwarp();
+    } else {
+      // ------------------------------------------------------------ softmax
+      const int sub = warp & 3;       // TMEM lane quarter of this warp
+      const int R = 32 * sub + lane;  // TMEM lane: tile position (S^T) / output dim (O^T)
+      const uint32_t trow = tmem + ((uint32_t)(32 * sub) << 16);
+      SegmentCursor cur;
+      cur.init(sp, range);
+      Segment seg;
+      bool have = cur.next(sp, seg);
+      auto unit_heads = [&](const Segment &s, int &h_first, int &nh) {
+        const int g = s.uib / p.head_chunks, hc = s.uib % p.head_chunks;
+        h_first = g * p.n_rep + hc * p.heads_per_cta;
+        nh = min(p.heads_per_cta, p.n_rep - hc * p.heads_per_cta);
+      };
+      // Q rows of a unit: thread R writes the 128-byte half R & 1 of row R >> 1
+      auto load_q = [&](const Segment &s) {
+        int h_first, nh;
+        unit_heads(s, h_first, nh);
+        const int row = R >> 1, half = R & 1;
+        const bool real = row < nh;
+        const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(p.q) +
+                                                           ((size_t)s.b * p.H + h_first + min(row, nh - 1)) * D +
+                                                           half * 64);
+        const uint32_t dst = qbase + half * C::Q_BOX + row * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = real ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst + ((c ^ (row & 7)) << 4)), "r"(v.x),
+                       "r"(v.y), "r"(v.z), "r"(v.w)
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.q_full());
+      };
+      if (have) load_q(seg);
+      // After a wait that timed out the thread is "dead": its later waits
+      // return at once, but it keeps the same control flow, so the four
+      // softmax warps still meet at every named barrier and finish (the
+      // error word already holds GQA_DEVERR_TIMEOUT).
+      bool dead = false;
+      auto wait = [&](uint32_t bar, uint32_t parity) {
+        if (!dead && !warp_wait(bar, parity)) dead = true;
+      };
+      int t = 0;
+      for (int unit = 0; have; ++unit) {
+        int h_first, nh;
+        unit_heads(seg, h_first, nh);
+        const int b = seg.b;
+        const int L = clamp_len(__ldg(p.seq_lens + b), p.Nmax);
+        const int ob = unit & 1;
+        const int ntl = seg.t1 - seg.t0;
+        float lp[NR];
+#pragma unroll
+        for (int h = 0; h < NR; ++h) lp[h] = 0.f;
+        if (R < NQ) m_s[R] = -INFINITY;
+        soft_bar();
+        for (int i = 0; i < ntl; ++i) {
+          const int tg = t + i, sb = tg & 1, st = tg % ST;
+          const bool valid = (seg.t0 + i) * BN + R < L;
+          wait(bars.s_full(sb), (tg >> 1) & 1);
+          tc::fence_after();
+          // this position's logits (log2 units), -inf past L and for padding heads
+          float x[NR];
+          auto load_s = [&]() {
+#pragma unroll
+            for (int c0 = 0; c0 < NR; c0 += (NR < 32 ? NR : 32)) {
+              uint32_t r[32];
+              if constexpr (NR >= 32) {
+                tc::ld_32x32b_x32(trow + C::TM_S + sb * NQ + c0, r);
+              } else {
+                tc::ld_32x32b_x16(trow + C::TM_S + sb * NQ + c0, r);
+              }
+              tc::wait_ld();
+#pragma unroll
+              for (int c = 0; c < (NR < 32 ? NR : 32); ++c) {
+                const int h = c0 + c;
+                x[h] = (valid && h < nh) ? __uint_as_float(r[c]) * p.scale_log2 : -INFINITY;
+              }
+            }
+          };
+          load_s();
+          bool need = false;
+#pragma unroll
+          for (int h = 0; h < NR; ++h) need |= x[h] > m_s[h] + 8.f;
+          if (soft_bar_or(need)) {
+            // move the running maxima to this tile's maxima where they grew by
+            // more than 8 (always on a unit's first tile); x is reduced in
+            // place and read again from TMEM afterwards
+            soft_reduce<C, true>(x, sub, lane, red, fin, R);
+            bool moved_mine = false;
+            if (R < NR) {
+              const float tmax = fin[R], mo = m_s[R];
+              float corr = 1.f;
+              if (tmax > mo + 8.f) {
+                corr = merge_weight(mo, tmax);
+                m_s[R] = tmax;
+                moved_mine = true;
+              }
+              corr_s[R] = corr;
+            }
+            const bool moved = soft_bar_or(moved_mine);
+#pragma unroll
+            for (int h = 0; h < NR; ++h) lp[h] *= corr_s[h];
+            if (i > 0 && moved) {
+              // O^T holds P.V of the unit's tiles so far: rescale it once the
+              // last of them landed (the same decision in every thread)
+              wait(bars.pv_done(), (tg - 1) & 1);
+              tc::fence_after();
+#pragma unroll
+              for (int c0 = 0; c0 < NR; c0 += (NR < 32 ? NR : 32)) {
+                uint32_t r[32];
+                if constexpr (NR >= 32) {
+                  tc::ld_32x32b_x32(trow + C::TM_O + ob * NQ + c0, r);
+                } else {
+                  tc::ld_32x32b_x16(trow + C::TM_O + ob * NQ + c0, r);
+                }
+                tc::wait_ld();
+#pragma unroll
+                for (int c = 0; c < (NR < 32 ? NR : 32); ++c)
+                  r[c] = __float_as_uint(__uint_as_float(r[c]) * corr_s[c0 + c]);
+                if constexpr (NR >= 32) {
+                  tc::st_32x32b_x32(trow + C::TM_O + ob * NQ + c0, r);
+                } else {
+                  tc::st_32x32b_x16(trow + C::TM_O + ob * NQ + c0, r);
+                }
+              }
+              tc::wait_st();
+            }
+            load_s();
+          }
+          // P^T row R: 2^(x - m) as bf16, heads along the 128-byte row (zero
+          // for padding heads)
+          uint32_t pk[NQ / 2];
+#pragma unroll
+          for (int h = 0; h < NQ; h += 2) {
+            if (h < NR) {
+              const float p0 = h < nh ? tc::ex2(x[h] - m_s[h]) : 0.f;
+              const float p1 = h + 1 < nh ? tc::ex2(x[h + 1] - m_s[h + 1]) : 0.f;
+              lp[h] += p0;
+              lp[h + 1] += p1;
+              pk[h / 2] = pack_bf16x2(p0, p1);
+            } else {
+              pk[h / 2] = 0u;
+            }
+          }
+          // the P buffer was last read by the P.V of tile tg-1
+          if (tg >= 1) wait(bars.pv_done(), (tg - 1) & 1);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(pbase + R * 128 + ((c ^ (R & 7)) << 4)),
+                         "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
+                         : "memory");
+          if (!valid && !dead && mbar_wait(pipe.full(st), (tg / ST) & 1)) {
+            // position past L: its V row may hold anything (NaN included) and
+            // 0 * NaN = NaN inside the MMA, so clear it (after it landed)
+            const uint32_t a = pipe.v_tile(st) + R * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(a + 16 * c), "r"(0u) : "memory");
+              asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(a + Pipe::BOX_BYTES + 16 * c), "r"(0u)
+                           : "memory");
+            }
+          }
+          fence_proxy_async_smem();
+          tc::fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(bars.s_free(sb));
+            mbar_arrive(bars.p_full());
+          }
+        }
+        t += ntl;
+        // the S^T of every tile of this unit is done, so Q may take the next unit
+        Segment nseg;
+        const bool next = cur.next(sp, nseg);
+        if (next) load_q(nseg);
+        // ---- epilogue: l[h] summed over the 128 positions' partials
+        const float mR = R < NQ ? m_s[R] : 0.f;
+        soft_reduce<C, false>(lp, sub, lane, red, fin, R);
+        // O^T of this unit is final once the P.V of its last tile landed
+        wait(bars.pv_done(), (t - 1) & 1);
+        tc::fence_after();
+        const bool whole = seg.t0 == 0 && seg.t1 == seg.tiles;
+        const int slot = partial_slot(unit);
+        const size_t bh0 = (size_t)b * p.H + h_first;
+#pragma unroll
+        for (int c0 = 0; c0 < NR; c0 += (NR < 32 ? NR : 32)) {
+          uint32_t r[32];
+          if constexpr (NR >= 32) {
+            tc::ld_32x32b_x32(trow + C::TM_O + ob * NQ + c0, r);
+          } else {
+            tc::ld_32x32b_x16(trow + C::TM_O + ob * NQ + c0, r);
+          }
+          tc::wait_ld();
+#pragma unroll
+          for (int c = 0; c < (NR < 32 ? NR : 32); ++c) {
+            const int h = c0 + c;
+            if (h < nh) {
+              const float o = __uint_as_float(r[c]);
+              if (whole)
+                reinterpret_cast<__nv_bfloat16 *>(p.out)[(bh0 + h) * D + R] = __float2bfloat16_rn(o / fin[h]);
+              else
+                p.o_part[((size_t)slot * p.heads_per_cta + h) * D + R] = o;
+            }
+          }
+        }
+        if (!whole && R < nh)
+          reinterpret_cast<float2 *>(p.ml_part)[(size_t)slot * p.heads_per_cta + R] = make_float2(mR, fin[R]);
+        if (R == 0 && seg.t0 == 0 && p.unit_info) {
+          const size_t u = (size_t)b * sp.units_per_b + seg.uib;
+          p.unit_info[u] = whole ? make_int2(-1, -1) : unit_record(seg, slot, range.T);
+        }
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.o_free(ob));
+        soft_bar();  // fin[] is reused by the next unit's reductions
+        seg = nseg;
+        have = next;
+      }
+    }
+  }
+  // ---- teardown: every tcgen05 operation has completed (the MMA thread
+  // waited for its last commit); free the tensor memory
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after();
+    tc::tmem_dealloc(tmem, C::TM_COLS);
+  }
+}
+
+}  // namespace gqa
