@@ -203,7 +203,7 @@ int ctas_per_sm(const KernelChoice &kc) {
 // The split kernel is a persistent grid of one wave (SMs x resident CTAs per
 // SM); the stream-K split gives every CTA the same number of tiles whatever
 // the lengths.  split_tokens > 0 instead asks for about that many positions
-// per CTA when every sequence is full (for tests of the combine and for
+// per CTA when every sequence is full (for tests of the merge and for
 // tuning).
 Plan make_plan(int B, int H, int G, int d, int Nmax, gqa_dtype_t dt, int split_tokens) {
   Plan pl;
@@ -231,16 +231,25 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 bool plan_fits(const Plan &pl, int B, int G) { return B <= 65535 && pl.units < (1LL << 31); }
 
-// Workspace: partial outputs and (m, l) of two slots per CTA, and the
-// per-unit record of split units.  A single CTA never splits a unit.
+// Workspace: partial outputs and (m, l) of two slots per CTA, and 8 bytes
+// of merge bookkeeping per unit.  A single CTA never splits a unit.
 size_t ws_opart_bytes(const Plan &pl, int d) { return align256((size_t)2 * pl.P * pl.heads * d * sizeof(float)); }
 size_t ws_ml_bytes(const Plan &pl) { return align256((size_t)2 * pl.P * pl.heads * 2 * sizeof(float)); }
+
+// A call's epoch tells its counter words from those other calls left in a
+// reused workspace; never zero (zero-filled memory reads as a stale word).
+unsigned next_epoch() {
+  static std::atomic<unsigned> epoch{0};
+  unsigned e = epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+  if (e == 0) e = epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+  return e;
+}
 
 size_t workspace_for(const Plan &pl, int B, int H, int d) {
   (void)B;
   (void)H;
   if (pl.P <= 1) return 0;
-  return ws_opart_bytes(pl, d) + ws_ml_bytes(pl) + align256((size_t)pl.units * sizeof(int2));
+  return ws_opart_bytes(pl, d) + ws_ml_bytes(pl) + align256((size_t)pl.units * sizeof(unsigned long long));
 }
 
 // ----------------------------------------------------------- TMA descriptors
@@ -329,7 +338,13 @@ int run_attention(const void *q, const void *k, const void *v, const int32_t *sl
   char *w = reinterpret_cast<char *>(ws);
   p.o_part = split ? reinterpret_cast<float *>(w) : nullptr;
   p.ml_part = split ? reinterpret_cast<float *>(w + ws_opart_bytes(pl, d)) : nullptr;
-  p.unit_info = split ? reinterpret_cast<int2 *>(w + ws_opart_bytes(pl, d) + ws_ml_bytes(pl)) : nullptr;
+  // units of one or two heads merge inside the split kernel; larger ones in
+  // the merge kernel, which spreads the (bigger) partials over every SM
+  void *book = split ? w + ws_opart_bytes(pl, d) + ws_ml_bytes(pl) : nullptr;
+  const bool merge_in_kernel = pl.k.family == kSimt;
+  p.unit_cnt = merge_in_kernel ? reinterpret_cast<unsigned long long *>(book) : nullptr;
+  p.unit_info = merge_in_kernel ? nullptr : reinterpret_cast<int2 *>(book);
+  p.epoch = next_epoch();
   p.scale_log2 = scale * 1.4426950408889634f;
   p.B = B;
   p.H = H;
@@ -342,28 +357,15 @@ int run_attention(const void *q, const void *k, const void *v, const int32_t *sl
     cudaGetLastError();
     return GQA_ERR_CUDA;
   }
-  if (split) {
-    CombineParams c;
-    c.seq_lens = sl;
-    c.o_part = p.o_part;
-    c.ml_part = p.ml_part;
-    c.unit_info = p.unit_info;
-    c.out = out;
-    c.B = B;
-    c.H = H;
-    c.G = G;
-    c.Nmax = Nmax;
-    c.n_rep = p.n_rep;
-    c.heads_per_cta = p.heads_per_cta;
-    c.head_chunks = p.head_chunks;
+  if (split && !merge_in_kernel) {
     const dim3 blocks(ceil_div((long long)B * H, 4));
     cudaError_t e;
     if (dt == GQA_BF16)
-      e = d == 128 ? launch_pdl(gqa_combine_kernel<__nv_bfloat16, 128>, blocks, dim3(128), 0, st, c)
-                   : launch_pdl(gqa_combine_kernel<__nv_bfloat16, 64>, blocks, dim3(128), 0, st, c);
+      e = d == 128 ? launch_pdl(gqa_combine_kernel<__nv_bfloat16, 128>, blocks, dim3(128), 0, st, p)
+                   : launch_pdl(gqa_combine_kernel<__nv_bfloat16, 64>, blocks, dim3(128), 0, st, p);
     else
-      e = d == 128 ? launch_pdl(gqa_combine_kernel<float, 128>, blocks, dim3(128), 0, st, c)
-                   : launch_pdl(gqa_combine_kernel<float, 64>, blocks, dim3(128), 0, st, c);
+      e = d == 128 ? launch_pdl(gqa_combine_kernel<float, 128>, blocks, dim3(128), 0, st, p)
+                   : launch_pdl(gqa_combine_kernel<float, 64>, blocks, dim3(128), 0, st, p);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return GQA_ERR_CUDA;

@@ -1,0 +1,168 @@
+// Log-sum-exp merge of the partial softmax states of a unit that the
+// stream-K split cut between CTAs:
+//   out = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k,   M = max_k m_k
+// over the unit's partials, always read in the same slot order, so the
+// result does not depend on timing.  Two ways, chosen per kernel by the host:
+//
+//  * In the split kernel, by whichever of the unit's CTAs finishes last (no
+//    second launch; for units of one or two heads, whose partials are
+//    small).  Each unit has a 64-bit counter word in the workspace holding
+//    (call epoch << 32) | finished CTAs.  A word left by another call (another
+//    epoch) counts as zero, so the workspace needs no clearing; the merging
+//    CTA puts the count back to zero, so a call captured in a graph can be
+//    replayed.
+//  * In a second kernel, one warp per (batch row, query head), launched as a
+//    programmatic dependent of the split kernel (for units of many heads,
+//    whose merge is spread over the whole GPU this way).  The unit's first
+//    CTA records (its slot, the unit's last CTA) in unit_info.
+#pragma once
+
+#include "gqa_params.cuh"
+#include "gqa_schedule.cuh"
+
+namespace gqa {
+
+struct UnitMerge {
+  int last;   // this CTA merges the unit
+  int slot0;  // partial slot of the unit's first CTA
+  int c_lo;   // the unit's first CTA
+  int n;      // number of CTAs (partials) of the unit
+};
+
+// Counts one more finished CTA of the unit and returns the new count.  The
+// compare-and-swap loop retries only while another CTA of the same unit
+// updates the word, at most once per such CTA.
+__device__ __forceinline__ unsigned arrive_unit(unsigned long long *cnt, unsigned epoch) {
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(cnt), assumed, nv;
+  do {
+    assumed = old;
+    const unsigned c = (unsigned)(assumed >> 32) == epoch ? (unsigned)assumed : 0u;
+    nv = ((unsigned long long)epoch << 32) | (unsigned long long)(c + 1);
+    old = atomicCAS(cnt, assumed, nv);
+  } while (old != assumed);
+  return (unsigned)nv;
+}
+
+// Called by the `nthr` threads (tid 0..nthr-1) of the group that wrote this
+// CTA's partial of a split unit (heads [h_first, h_first + nh) of batch row
+// b), after those writes; `bar` synchronises the group.  When this CTA is the
+// unit's last, the group merges all its partials into out.
+template <typename T, int D, class Bar>
+__device__ __forceinline__ void finish_split_unit(const SplitParams &p, const Segment &seg, long long T_total, int b,
+                                                  int h_first, int nh, int tid, int nthr, UnitMerge *um, Bar bar) {
+  __threadfence();
+  bar();
+  if (tid == 0) {
+    const int P = gridDim.x;
+    const int c_lo = cta_of_tile(seg.unit_first, T_total, P);
+    const int c_hi = cta_of_tile(seg.unit_first + seg.tiles - 1, T_total, P);
+    const size_t u = (size_t)b * p.G * p.head_chunks + seg.uib;
+    const int n = c_hi - c_lo + 1;
+    const bool last = arrive_unit(p.unit_cnt + u, p.epoch) == (unsigned)n;
+    if (last) {
+      __threadfence();
+      atomicExch(p.unit_cnt + u, (unsigned long long)p.epoch << 32);
+    }
+    um->last = last;
+    um->c_lo = c_lo;
+    um->n = n;
+    um->slot0 = cta_start(c_lo, T_total, P) == seg.unit_first ? 2 * c_lo : 2 * c_lo + 1;
+  }
+  bar();
+  if (!um->last) return;
+  const int c_lo = um->c_lo, n = um->n, slot0 = um->slot0, hpc = p.heads_per_cta;
+  const float2 *ml = reinterpret_cast<const float2 *>(p.ml_part);
+  for (int e = tid; e < nh * (D / 4); e += nthr) {
+    const int h = e / (D / 4), d0 = (e % (D / 4)) * 4;
+    float M = -INFINITY;
+    for (int k = 0; k < n; ++k) {
+      const int slot = k == 0 ? slot0 : 2 * (c_lo + k);
+      M = fmaxf(M, __ldcg(ml + (size_t)slot * hpc + h).x);
+    }
+    float L = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    for (int k = 0; k < n; ++k) {
+      const size_t ps = (size_t)(k == 0 ? slot0 : 2 * (c_lo + k)) * hpc + h;
+      const float2 mk = __ldcg(ml + ps);
+      const float w = merge_weight(mk.x, M);
+      const float4 o = __ldcg(reinterpret_cast<const float4 *>(p.o_part + ps * D + d0));
+      L += w * mk.y;
+      a0 += w * o.x;
+      a1 += w * o.y;
+      a2 += w * o.z;
+      a3 += w * o.w;
+    }
+    const float inv = 1.f / L;
+    T *dst = reinterpret_cast<T *>(p.out) + ((size_t)b * p.H + h_first + h) * D + d0;
+    dst[0] = from_float<T>(a0 * inv);
+    dst[1] = from_float<T>(a1 * inv);
+    dst[2] = from_float<T>(a2 * inv);
+    dst[3] = from_float<T>(a3 * inv);
+  }
+}
+
+// Combine-mode bookkeeping of a finished segment (one thread): the unit's
+// first CTA records where its partials are, or that it was finished whole.
+__device__ __forceinline__ void record_unit(const SplitParams &p, const Segment &seg, bool whole, int slot,
+                                            long long T_total, int b) {
+  if (!p.unit_info || seg.t0 != 0) return;
+  const size_t u = (size_t)b * p.G * p.head_chunks + seg.uib;
+  p.unit_info[u] = whole ? make_int2(-1, -1)
+                         : make_int2(slot, cta_of_tile(seg.unit_first + seg.tiles - 1, T_total, gridDim.x));
+}
+
+// One warp per (b, h): the merge of the unit that holds head h when the
+// split cut it (info.y >= 0).  Whole units and empty sequences were written
+// by the split kernel.  It waits for the split grid to finish before it
+// reads the workspace.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) gqa_combine_kernel(const SplitParams p) {
+  constexpr int PER_LANE = D / 32;
+  griddep_wait();
+  griddep_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long bh = (long long)blockIdx.x * 4 + warp;
+  if (bh >= (long long)p.B * p.H) return;
+  const int b = (int)(bh / p.H), h = (int)(bh % p.H);
+  const int L = max(0, min(p.seq_lens[b], p.Nmax));
+  if (L == 0) return;
+  const int g = h / p.n_rep, rr = h % p.n_rep;
+  const int hc = rr / p.heads_per_cta, hl = rr % p.heads_per_cta;
+  const int2 info = p.unit_info[((size_t)b * p.G + g) * p.head_chunks + hc];
+  if (info.y < 0) return;
+  const int c_lo = info.x >> 1;
+  const int n = info.y - c_lo + 1;  // number of partials
+  const float2 *ml = reinterpret_cast<const float2 *>(p.ml_part);
+  auto slot_of = [&](int k) { return k == 0 ? info.x : 2 * (c_lo + k); };
+  float M = -INFINITY;
+  for (int k = lane; k < n; k += 32) M = fmaxf(M, ml[(size_t)slot_of(k) * p.heads_per_cta + hl].x);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float acc[PER_LANE];
+#pragma unroll
+  for (int e = 0; e < PER_LANE; ++e) acc[e] = 0.f;
+  float l = 0.f;
+  for (int k = 0; k < n; ++k) {
+    const size_t ps = (size_t)slot_of(k) * p.heads_per_cta + hl;
+    const float2 mls = ml[ps];
+    const float w = merge_weight(mls.x, M);
+    l += w * mls.y;
+    const float *op = p.o_part + ps * D + lane * PER_LANE;
+    if constexpr (PER_LANE == 4) {
+      const float4 v = *reinterpret_cast<const float4 *>(op);
+      acc[0] += w * v.x;
+      acc[1] += w * v.y;
+      acc[2] += w * v.z;
+      acc[3] += w * v.w;
+    } else {
+      const float2 v = *reinterpret_cast<const float2 *>(op);
+      acc[0] += w * v.x;
+      acc[1] += w * v.y;
+    }
+  }
+  const float inv = 1.f / l;
+  T *o = reinterpret_cast<T *>(p.out) + (size_t)bh * D + lane * PER_LANE;
+#pragma unroll
+  for (int e = 0; e < PER_LANE; ++e) o[e] = from_float<T>(acc[e] * inv);
+}
+
+}  // namespace gqa

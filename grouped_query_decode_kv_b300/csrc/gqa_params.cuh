@@ -1,4 +1,4 @@
-// Launch parameters shared by the split-KV decode kernels and the combine.
+// Launch parameters of the split-KV decode kernels.
 #pragma once
 
 #include <stdint.h>
@@ -15,22 +15,15 @@ struct SplitParams {
   void *out;                // [B, H, D]       whole units are written here directly
   float *o_part;            // [2P, heads_per_cta, D] unnormalised partial outputs
   float *ml_part;           // [2P, heads_per_cta, 2] (running max in log2 units, sum)
-  int2 *unit_info;          // [B*G*HC]        (first slot, last CTA) of split units
+  // Per-unit merge bookkeeping, one of the two (the other null):
+  unsigned long long *unit_cnt;  // [B*G*HC] in-kernel merge: (call epoch << 32) | CTAs of the unit done
+  int2 *unit_info;          // [B*G*HC] merge kernel: (first slot, last CTA) of a split unit, or -1
+  unsigned epoch;           // nonzero, different for every call
   float scale_log2;         // scale * log2(e): softmax is evaluated with exp2
   int B, H, G, Nmax;
   int n_rep;                // H / G
   int heads_per_cta;
   int head_chunks;          // HC = ceil(n_rep / heads_per_cta)
-};
-
-struct CombineParams {
-  const int32_t *seq_lens;
-  const float *o_part;
-  const float *ml_part;
-  const int2 *unit_info;
-  void *out;
-  int B, H, G, Nmax;
-  int n_rep, heads_per_cta, head_chunks;
 };
 
 }  // namespace gqa

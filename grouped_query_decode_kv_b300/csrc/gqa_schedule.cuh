@@ -13,13 +13,15 @@
 // A range is walked as segments: the part of one unit that lies in the
 // range.  A segment that is a whole unit is finished in place (out written
 // directly).  Otherwise it leaves a partial softmax state in a workspace
-// slot: slot 2c for CTA c's first segment, 2c+1 for its last.  The CTA that
-// holds a split unit's first tile records (its slot, last CTA of the unit)
-// in unit_info[u]; the combine kernel merges the unit's partials from that
-// slot and slots 2c of the CTAs after it.
+// slot: slot 2c for CTA c's first segment, 2c+1 for its last; the unit's CTAs
+// are c_lo..c_hi (cta_of_tile of its first and last tile), its partials slot
+// 2*c_lo or 2*c_lo+1 (the latter when the unit is not c_lo's first segment)
+// and 2c for every later c, and the last of them to finish merges them
+// (gqa_merge.cuh).
 //
 // The lengths live in device memory, so each CTA derives T and its own
-// starting row from seq_lens with a warp scan (O(B/32) steps per CTA).
+// starting row from seq_lens with a warp scan (O(B/32) steps per CTA; the
+// first 64 rows are read once).
 #pragma once
 
 #include "gqa_device.cuh"
@@ -75,6 +77,7 @@ struct CtaRange {
 __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int lane, void *out, size_t row_bytes) {
   const int P = gridDim.x, c = blockIdx.x;
   long long T = 0;
+  long long keep0 = 0, keep1 = 0;  // this lane's tile counts of rows lane and 32 + lane
   for (int base = 0; base < s.B; base += 32) {
     const int b = base + lane;
     long long t = 0;
@@ -94,6 +97,8 @@ __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int la
       uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(out) + (size_t)(base + src) * row_bytes);
       for (size_t i = lane; i < row_bytes / 16; i += 32) o[i] = make_uint4(0, 0, 0, 0);
     }
+    if (base == 0) keep0 = t;
+    if (base == 32) keep1 = t;
     const long long incl = warp_incl_scan(t, lane);
     T += __shfl_sync(0xffffffffu, incl, 31);
   }
@@ -107,7 +112,9 @@ __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int la
   long long acc = 0;
   for (int base = 0; base < s.B; base += 32) {
     const int b = base + lane;
-    const long long t = b < s.B ? (long long)row_tiles(s, b) * s.units_per_b : 0;
+    const long long t = base == 0    ? keep0
+                        : base == 32 ? keep1
+                        : (b < s.B ? (long long)row_tiles(s, b) * s.units_per_b : 0);
     const long long incl = warp_incl_scan(t, lane);
     const long long lo = acc + incl - t, hi = acc + incl;
     const unsigned hit = __ballot_sync(0xffffffffu, b < s.B && lo <= r.begin && r.begin < hi);
@@ -164,15 +171,10 @@ struct SegmentCursor {
   }
 };
 
-// Bookkeeping of a finished segment that is not a whole unit: the slot its
-// partial goes to, and (for the unit's first CTA) the unit_info record.
+// Workspace slot of the partial of this CTA's segment number seg_index
+// (only its first and last segments can be partial).
 __device__ __forceinline__ int partial_slot(int seg_index) {
   return 2 * (int)blockIdx.x + (seg_index == 0 ? 0 : 1);
-}
-
-__device__ __forceinline__ int2 unit_record(const Segment &seg, int slot, long long T) {
-  const long long last_tile = seg.unit_first + seg.tiles - 1;
-  return make_int2(slot, cta_of_tile(last_tile, T, gridDim.x));
 }
 
 }  // namespace gqa

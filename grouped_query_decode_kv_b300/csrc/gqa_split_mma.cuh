@@ -23,6 +23,7 @@
 // max was used.
 #pragma once
 
+#include "gqa_merge.cuh"
 #include "gqa_params.cuh"
 #include "gqa_pipeline.cuh"
 
@@ -51,7 +52,8 @@ struct MmaCfg {
   static constexpr int FIN_OFF = ML_OFF + 4 * HEADS * 8;
   static constexpr int BAR_OFF = FIN_OFF + HEADS * 8;
   static constexpr int RANGE_OFF = BAR_OFF + 2 * Pipe::STAGES * 8;
-  static constexpr int SMEM_BYTES = 1024 + RANGE_OFF + (int)sizeof(CtaRange);
+  static constexpr int MERGE_OFF = RANGE_OFF + 64;
+  static constexpr int SMEM_BYTES = 1024 + MERGE_OFF + (int)sizeof(UnitMerge);
   static_assert(ROWS_PER_WARP % 16 == 0, "each warp takes whole 16-position sub-tiles");
   static_assert(D == 64 || D == 128, "head dimension");
 };
@@ -72,6 +74,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   pipe.full0 = pipe.base + C::BAR_OFF;
   pipe.empty0 = pipe.full0 + 8 * Pipe::STAGES;
   CtaRange *range_smem = reinterpret_cast<CtaRange *>(smem + C::RANGE_OFF);
+  UnitMerge *um = reinterpret_cast<UnitMerge *>(smem + C::MERGE_OFF);
   float *osum = reinterpret_cast<float *>(smem + C::OSUM_OFF);    // [HEADS][OSUM_LD]
   float2 *ml_s = reinterpret_cast<float2 *>(smem + C::ML_OFF);    // [4][HEADS]
   float2 *fin_s = reinterpret_cast<float2 *>(smem + C::FIN_OFF);  // [HEADS]
@@ -367,10 +370,10 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
     if (!whole)
       for (int hl = threadIdx.x; hl < nh; hl += NCONS)
         reinterpret_cast<float2 *>(p.ml_part)[(size_t)slot * p.heads_per_cta + hl] = fin_s[hl];
-    if (threadIdx.x == 0 && seg.t0 == 0 && p.unit_info) {
-      const size_t u = (size_t)b * sp.units_per_b + seg.uib;
-      p.unit_info[u] = whole ? make_int2(-1, -1) : unit_record(seg, slot, range.T);
-    }
+    if (threadIdx.x == 0) record_unit(p, seg, whole, slot, range.T, b);
+    if (!whole && p.unit_cnt)
+      finish_split_unit<__nv_bfloat16, D>(p, seg, range.T, b, h_first, nh, threadIdx.x, NCONS, um,
+                                          [] { consumer_bar_sync(NCONS); });
     consumer_bar_sync(NCONS);  // scratch free for the next unit
   }
 }

@@ -15,6 +15,7 @@
 // the ring keeps filling meanwhile.
 #pragma once
 
+#include "gqa_merge.cuh"
 #include "gqa_params.cuh"
 #include "gqa_pipeline.cuh"
 
@@ -41,7 +42,8 @@ struct SimtCfg {
   static constexpr int EPI_OFF = Pipe::PIPE_BYTES;            // merge scratch
   static constexpr int BAR_OFF = EPI_OFF + EPI_BYTES;         // full[], empty[] mbarriers
   static constexpr int RANGE_OFF = BAR_OFF + 2 * Pipe::STAGES * 8;
-  static constexpr int SMEM_BYTES = 1024 + RANGE_OFF + (int)sizeof(CtaRange);
+  static constexpr int MERGE_OFF = RANGE_OFF + 64;
+  static constexpr int SMEM_BYTES = 1024 + MERGE_OFF + (int)sizeof(UnitMerge);
   static_assert(ROWS_PER_WARP % 4 == 0, "four 8-lane groups per warp");
   static_assert(NBOX >= 1, "a row spans at least one 128-byte box");
 };
@@ -105,6 +107,7 @@ __global__ void __launch_bounds__(C::THREADS)
   pipe.full0 = pipe.base + C::BAR_OFF;
   pipe.empty0 = pipe.full0 + 8 * Pipe::STAGES;
   CtaRange *range_smem = reinterpret_cast<CtaRange *>(smem + C::RANGE_OFF);
+  UnitMerge *um = reinterpret_cast<UnitMerge *>(smem + C::MERGE_OFF);
   SchedParams sp;
   sp.seq_lens = p.seq_lens;
   sp.B = p.B;
@@ -316,11 +319,12 @@ __global__ void __launch_bounds__(C::THREADS)
           if (j == 0) reinterpret_cast<float2 *>(p.ml_part)[ps] = make_float2(m_run[h], l_run[h]);
         }
       }
-      if (lane == 0 && seg.t0 == 0 && p.unit_info) {
-        const size_t u = (size_t)b * sp.units_per_b + seg.uib;
-        p.unit_info[u] = whole ? make_int2(-1, -1) : unit_record(seg, slot, range.T);
-      }
     }
+    const bool whole = seg.t0 == 0 && seg.t1 == seg.tiles;
+    if (threadIdx.x == 0) record_unit(p, seg, whole, partial_slot(seg_index), range.T, b);
+    if (!whole && p.unit_cnt)
+      finish_split_unit<T, D>(p, seg, range.T, b, h_first, nh, threadIdx.x, C::CONSUMER_WARPS * 32, um,
+                              [] { consumer_bar_sync(C::CONSUMER_WARPS * 32); });
     consumer_bar_sync(C::CONSUMER_WARPS * 32);  // scratch free for the next unit
   }
 }

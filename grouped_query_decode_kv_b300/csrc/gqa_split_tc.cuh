@@ -34,6 +34,7 @@
 // GQA_DEVERR_TIMEOUT.
 #pragma once
 
+#include "gqa_merge.cuh"
 #include "gqa_params.cuh"
 #include "gqa_pipeline.cuh"
 #include "gqa_tcgen05.cuh"
@@ -70,7 +71,8 @@ struct TcCfg {
   static constexpr int NBAR = 2 * STAGES + 10;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBAR * 8;
   static constexpr int RANGE_OFF = TMEM_SLOT_OFF + 16;
-  static constexpr int SMEM_BYTES = 1024 + RANGE_OFF + (int)sizeof(CtaRange);
+  static constexpr int MERGE_OFF = RANGE_OFF + 64;
+  static constexpr int SMEM_BYTES = 1024 + MERGE_OFF + (int)sizeof(UnitMerge);
   // more than half of an SM's shared memory: one CTA per SM, so the TMEM
   // allocation never waits for another CTA
   static_assert(SMEM_BYTES > 116 * 1024 && SMEM_BYTES <= 227 * 1024, "one resident CTA per SM");
@@ -183,6 +185,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   float *corr_s = reinterpret_cast<float *>(smem + C::CORR_OFF);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::TMEM_SLOT_OFF);
   CtaRange *range_smem = reinterpret_cast<CtaRange *>(smem + C::RANGE_OFF);
+  UnitMerge *um = reinterpret_cast<UnitMerge *>(smem + C::MERGE_OFF);
   SchedParams sp;
   sp.seq_lens = p.seq_lens;
   sp.B = p.B;
@@ -525,10 +528,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         if (!whole && R < nh)
           reinterpret_cast<float2 *>(p.ml_part)[(size_t)slot * p.heads_per_cta + R] = make_float2(mR, fin[R]);
-        if (R == 0 && seg.t0 == 0 && p.unit_info) {
-          const size_t u = (size_t)b * sp.units_per_b + seg.uib;
-          p.unit_info[u] = whole ? make_int2(-1, -1) : unit_record(seg, slot, range.T);
-        }
+        if (R == 0) record_unit(p, seg, whole, slot, range.T, b);
+        if (!whole && p.unit_cnt)
+          finish_split_unit<__nv_bfloat16, D>(p, seg, range.T, b, h_first, nh, R, C::SOFT, um, [] { soft_bar(); });
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.o_free(ob));

@@ -79,10 +79,13 @@ typedef enum {
  *   d in {64, 128}; H % G == 0; pointers 16-byte aligned.
  *
  * A length L_b > Nmax is treated as Nmax and L_b <= 0 gives out[b] = 0; both
- * set GQA_DEVERR_ATTN_LEN.  Long sequences are split across thread blocks
- * whose partial results are merged by log-sum-exp in a second kernel; the
- * partials live in a workspace taken from the stream-ordered allocator
- * (cudaMallocAsync / cudaFreeAsync on `stream`).
+ * set GQA_DEVERR_ATTN_LEN.  The cached positions of all sequences are divided
+ * evenly among a persistent grid of thread blocks (one or two per SM); a
+ * sequence's KV head that falls on several blocks leaves partial softmax
+ * states that the last of those blocks to finish merges by log-sum-exp.  The
+ * partials and a counter per (sequence, KV head) live in a workspace taken
+ * from the stream-ordered allocator (cudaMallocAsync / cudaFreeAsync on
+ * `stream`).  Results are deterministic: the merge order is fixed.
  */
 int gqa_decode_attention(const void *q, const void *k_cache, const void *v_cache,
                          const int32_t *seq_lens, float scale, void *out,
@@ -99,9 +102,9 @@ size_t gqa_decode_workspace_bytes(int B, int H, int G, int d, int Nmax, gqa_dtyp
 /*
  * gqa_decode_attention_ws — as gqa_decode_attention, with the split partials
  * in a caller-provided device workspace of at least
- * gqa_decode_workspace_bytes(...) bytes (256-byte aligned).  Allocates
- * nothing, so it can be captured in a CUDA graph.  Calls that share one
- * workspace must not overlap on the device.
+ * gqa_decode_workspace_bytes(...) bytes (256-byte aligned; its contents need
+ * no initialisation).  Allocates nothing, so it can be captured in a CUDA
+ * graph.  Calls that share one workspace must not overlap on the device.
  */
 int gqa_decode_attention_ws(const void *q, const void *k_cache, const void *v_cache,
                             const int32_t *seq_lens, float scale, void *out,
@@ -109,10 +112,11 @@ int gqa_decode_attention_ws(const void *q, const void *k_cache, const void *v_ca
                             void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
- * gqa_decode_attention_ex — as gqa_decode_attention_ws, with the number of
- * positions per split forced to `split_tokens` (rounded up to the kernel's
- * tile of 32..128 positions; 0 = the automatic choice).  For tests of the
- * split/combine path and for tuning.  split_tokens < 0 is rejected.
+ * gqa_decode_attention_ex — as gqa_decode_attention_ws, with the grid sized
+ * so that each thread block gets about `split_tokens` cached positions when
+ * every sequence is full (rounded up to the kernel's tile of 32..128
+ * positions; 0 = the automatic one-wave grid).  For tests of the split/merge
+ * path and for tuning.  split_tokens < 0 is rejected.
  * gqa_decode_workspace_bytes_ex gives the workspace that choice needs.
  */
 size_t gqa_decode_workspace_bytes_ex(int B, int H, int G, int d, int Nmax, gqa_dtype_t dtype,
