@@ -103,9 +103,9 @@ KernelChoice make_choice() {
 // kernel (tensor-core MMAs with TMEM accumulators); smaller groups use the
 // warp-level MMA kernel, groups of one or two the CUDA-core kernel.
 constexpr int kTcMinNrep = 8;
-using TcD128x16 = TcCfg<16, 3>;
-using TcD128x32 = TcCfg<32, 3>;
-using TcD128x64 = TcCfg<64, 3>;
+using TcD128x16 = TcCfg<16, 3, 2>;
+using TcD128x32 = TcCfg<32, 3, 2>;
+using TcD128x64 = TcCfg<64, 3, 1>;
 
 KernelChoice choose_kernel(gqa_dtype_t dt, int d, int n_rep) {
   if (dt == GQA_BF16) {

@@ -3,17 +3,18 @@
 // n_rep >= 8 query heads per KV head (GQA-8 and coarser, MQA).
 //
 // Per tile of 128 cached positions of one unit (batch b, KV head g), with
-// the group's query heads (up to 64 per unit, padded to N = 64) as N:
-//   S^T  = K_tile . Q^T     M = 128 positions, N = 64 heads, K = d = 128
+// the group's query heads (up to 64 per unit, padded to N = 16, 32 or 64) as
+// N:
+//   S^T  = K_tile . Q^T     M = 128 positions, N = heads, K = d = 128
 //                           A = K tile as TMA landed it (K-major, 128-byte
 //                           swizzle), B = Q (K-major, swizzled by the kernel)
-//   O^T += V_tile^T . P^T   M = d = 128, N = 64 heads, K = 128 positions
+//   O^T += V_tile^T . P^T   M = d = 128, N = heads, K = 128 positions
 //                           A = V tile as TMA landed it (MN-major: d runs
 //                           along the 128-byte rows), B = P^T written by the
-//                           softmax threads (MN-major: heads along the rows)
+//                           softmax threads (K-major: one row per head)
 // Each K/V byte read from HBM serves every query head of the group (the
 // point of GQA: GQA paper, section 2.2), and the MMA work per tile is the
-// same 4.2 MFLOP whatever n_rep, well under the tensor pipe's rate.
+// 2 x 128 x 128 x 2 x N flop, well under the tensor pipe's rate.
 //
 // Softmax: thread R of the four softmax warps owns TMEM lane R, which is
 // cached position R of the tile in S^T and output dimension R in O^T.  For
@@ -22,7 +23,9 @@
 // any logit exceeds m[h] + 8; only then (always on a unit's first tile) the
 // tile's per-head maxima are reduced across the 128 threads and m moves,
 // with O^T rescaled in TMEM.  P = 2^(S - m) is written to shared memory as
-// bf16; the l_R[h] are summed across threads once per unit.
+// bf16 (double-buffered where shared memory allows, so that the softmax of
+// tile t+1 need not wait for the P.V of tile t); the l_R[h] are summed
+// across threads once per unit.
 //
 // Warp roles (192 threads, one CTA per SM):
 //   warp 0     TMA producer of the CTA's stream-K range (gqa_pipeline.cuh)
@@ -41,34 +44,40 @@
 
 namespace gqa {
 
-template <int NR_, int STAGES_>
+template <int NR_, int STAGES_, int PB_>
 struct TcCfg {
   static constexpr int D = 128;
   static constexpr int BLOCK_N = 128;  // positions per tile: M of S^T, K of P.V
   static constexpr int STAGES = STAGES_;
-  static constexpr int NQ = 64;        // N of both MMAs: heads per unit, zero-padded
-  static constexpr int NR = NR_;       // heads a softmax thread processes (>= heads per unit)
+  static constexpr int NR = NR_;       // heads per unit, padded to a multiple of 16: N of both MMAs
+  static constexpr int NQ = NR;
   static constexpr int HEADS = NR;
-  static_assert(NR == 16 || NR == 32 || NR == 64, "per-thread head count");
+  static constexpr int PB = PB_;       // P^T buffers
+  static_assert(NR == 16 || NR == 32 || NR == 64, "heads per unit");
+  static_assert(PB == 1 || PB == 2, "P^T buffers");
   using Pipe = KVPipe<2, BLOCK_N, STAGES, 1>;  // one "empty" arrival per tile: the MMA commit
   static constexpr int THREADS = 6 * 32;
   static constexpr int SOFT = 128;             // softmax threads
-  // TMEM columns: S^T buffers [0, 2*NQ), O^T buffers [2*NQ, 4*NQ)
+  // TMEM columns: S^T buffers [0, 2*NR), O^T buffers [2*NR, 4*NR)
   static constexpr int TM_S = 0;
-  static constexpr int TM_O = 2 * NQ;
-  static constexpr int TM_COLS = 4 * NQ;  // 256: a power of two
+  static constexpr int TM_O = 2 * NR;
+  static constexpr int TM_COLS = 4 * NR < 32 ? 32 : 4 * NR;  // 64, 128 or 256: a power of two
   // shared memory
-  static constexpr int Q_OFF = Pipe::PIPE_BYTES;  // Q: two 128-byte-wide boxes of NQ rows
-  static constexpr int Q_BOX = NQ * 128;
-  static constexpr int P_OFF = Q_OFF + 2 * Q_BOX;  // P^T: BLOCK_N rows of NQ bf16 (128 B)
-  static constexpr int RED_OFF = P_OFF + BLOCK_N * 128;  // [4][NQ] cross-warp reduction
+  static constexpr int Q_OFF = Pipe::PIPE_BYTES;  // Q: two 128-byte-wide boxes (d 0-63, 64-127) of NR rows
+  static constexpr int Q_BOX = NR * 128;
+  // P^T buffers, K-major like Q: one row of 128 positions per head, as two
+  // 128-byte-wide boxes (positions 0-63, 64-127), 128-byte swizzled
+  static constexpr int P_OFF = Q_OFF + 2 * Q_BOX;
+  static constexpr int P_BOX = NR * 128;
+  static constexpr int P_BYTES = 2 * P_BOX;
+  static constexpr int RED_OFF = P_OFF + PB * P_BYTES;  // [4][NQ] cross-warp reduction
   static constexpr int FIN_OFF = RED_OFF + 4 * NQ * 4;   // [NQ] reduced value
   static constexpr int M_OFF = FIN_OFF + NQ * 4;         // [NQ] running max of the unit
   static constexpr int CORR_OFF = M_OFF + NQ * 4;        // [NQ] rescale factor of a tile
   static constexpr int BAR_OFF = CORR_OFF + NQ * 4;
-  // pipe full[STAGES], empty[STAGES]; then s_full[2], s_free[2], p_full,
-  // pv_done, o_free[2], q_full, mma_done
-  static constexpr int NBAR = 2 * STAGES + 10;
+  // pipe full[STAGES], empty[STAGES]; then s_full[2], s_free[2], p_full[2],
+  // pv_done[2], o_free[2], q_full, mma_done
+  static constexpr int NBAR = 2 * STAGES + 12;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBAR * 8;
   static constexpr int RANGE_OFF = TMEM_SLOT_OFF + 16;
   static constexpr int MERGE_OFF = RANGE_OFF + 64;
@@ -82,11 +91,11 @@ struct TcBars {
   uint32_t b0;
   __device__ __forceinline__ uint32_t s_full(int i) const { return b0 + 8 * i; }
   __device__ __forceinline__ uint32_t s_free(int i) const { return b0 + 16 + 8 * i; }
-  __device__ __forceinline__ uint32_t p_full() const { return b0 + 32; }
-  __device__ __forceinline__ uint32_t pv_done() const { return b0 + 40; }
-  __device__ __forceinline__ uint32_t o_free(int i) const { return b0 + 48 + 8 * i; }
-  __device__ __forceinline__ uint32_t q_full() const { return b0 + 64; }
-  __device__ __forceinline__ uint32_t mma_done() const { return b0 + 72; }
+  __device__ __forceinline__ uint32_t p_full(int i) const { return b0 + 32 + 8 * i; }
+  __device__ __forceinline__ uint32_t pv_done(int i) const { return b0 + 48 + 8 * i; }
+  __device__ __forceinline__ uint32_t o_free(int i) const { return b0 + 64 + 8 * i; }
+  __device__ __forceinline__ uint32_t q_full() const { return b0 + 80; }
+  __device__ __forceinline__ uint32_t mma_done() const { return b0 + 88; }
 };
 
 // All lanes of a warp wait; a wait that timed out in any lane counts as
@@ -200,8 +209,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       mbar_init(bars.s_free(i), 4);
       mbar_init(bars.o_free(i), 4);
     }
-    mbar_init(bars.p_full(), 4);
-    mbar_init(bars.pv_done(), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bars.p_full(i), 4);
+      mbar_init(bars.pv_done(i), 1);
+    }
     mbar_init(bars.q_full(), 4);
     mbar_init(bars.mma_done(), 1);
     fence_barrier_init();
@@ -233,8 +244,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
       if (lane == 0) {
-        constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(BN, NQ, false, false);
-        constexpr uint32_t IDESC_PV = tc::idesc_bf16_f32(D, NQ, true, true);
+        constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(BN, NR, false, false);
+        constexpr uint32_t IDESC_PV = tc::idesc_bf16_f32(D, NR, true, false);
         // Two walks over the CTA's tiles: S^T of tile ts may start once its K
         // tile landed, its S buffer is free and (first tile of a unit) the
         // unit's Q is in place; P.V of tile tp once its P is written and
@@ -276,7 +287,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               for (int ks = 0; ks < D / 16; ++ks) {
                 const uint64_t a = tc::smem_desc_sw128(kt + (ks >> 2) * Pipe::BOX_BYTES + (ks & 3) * 32, 16, 1024);
                 const uint64_t b = tc::smem_desc_sw128(qbase + (ks >> 2) * C::Q_BOX + (ks & 3) * 32, 16, 1024);
-                tc::mma_ss(tmem + C::TM_S + (tg & 1) * NQ, a, b, IDESC_S, ks > 0);
+                tc::mma_ss(tmem + C::TM_S + (tg & 1) * NR, a, b, IDESC_S, ks > 0);
               }
               tc::commit(bars.s_full(tg & 1));
               ws.advance(sp);
@@ -285,18 +296,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
           if (wp.tg < ws.tg) {
             const int tg = wp.tg, ob = wp.unit & 1;
-            if (mbar_test(bars.p_full(), tg & 1) &&
+            const int pb = tg % C::PB, use = tg / C::PB;
+            if (mbar_test(bars.p_full(pb), use & 1) &&
                 (wp.i != 0 || wp.unit < 2 || mbar_test(bars.o_free(ob), ((wp.unit >> 1) - 1) & 1))) {
               tc::fence_after();
               const uint32_t vt = pipe.v_tile(tg % ST);
 #pragma unroll
               for (int ks = 0; ks < BN / 16; ++ks) {
                 const uint64_t a = tc::smem_desc_sw128(vt + ks * 2048, Pipe::BOX_BYTES, 1024);
-                const uint64_t b = tc::smem_desc_sw128(pbase + ks * 2048, 8192, 1024);
-                tc::mma_ss(tmem + C::TM_O + ob * NQ, a, b, IDESC_PV, wp.i > 0 || ks > 0);
+                const uint64_t b =
+                    tc::smem_desc_sw128(pbase + pb * C::P_BYTES + (ks >> 2) * C::P_BOX + (ks & 3) * 32, 16, 1024);
+                tc::mma_ss(tmem + C::TM_O + ob * NR, a, b, IDESC_PV, wp.i > 0 || ks > 0);
               }
               tc::commit(pipe.empty(tg % ST));
-              tc::commit(bars.pv_done());
+              tc::commit(bars.pv_done(pb));
               wp.advance(sp);
               progressed = true;
             }
@@ -339,6 +352,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         unit_heads(s, h_first, nh);
         const int row = R >> 1, half = R & 1;
         const bool real = row < nh;
+        if (row < NR) {
         const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(p.q) +
                                                            ((size_t)s.b * p.H + h_first + min(row, nh - 1)) * D +
                                                            half * 64);
@@ -349,6 +363,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst + ((c ^ (row & 7)) << 4)), "r"(v.x),
                        "r"(v.y), "r"(v.z), "r"(v.w)
                        : "memory");
+        }
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -388,9 +403,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             for (int c0 = 0; c0 < NR; c0 += (NR < 32 ? NR : 32)) {
               uint32_t r[32];
               if constexpr (NR >= 32) {
-                tc::ld_32x32b_x32(trow + C::TM_S + sb * NQ + c0, r);
+                tc::ld_32x32b_x32(trow + C::TM_S + sb * NR + c0, r);
               } else {
-                tc::ld_32x32b_x16(trow + C::TM_S + sb * NQ + c0, r);
+                tc::ld_32x32b_x16(trow + C::TM_S + sb * NR + c0, r);
               }
               tc::wait_ld();
 #pragma unroll
@@ -426,52 +441,49 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (i > 0 && moved) {
               // O^T holds P.V of the unit's tiles so far: rescale it once the
               // last of them landed (the same decision in every thread)
-              wait(bars.pv_done(), (tg - 1) & 1);
+              wait(bars.pv_done((tg - 1) % C::PB), ((tg - 1) / C::PB) & 1);
               tc::fence_after();
 #pragma unroll
               for (int c0 = 0; c0 < NR; c0 += (NR < 32 ? NR : 32)) {
                 uint32_t r[32];
                 if constexpr (NR >= 32) {
-                  tc::ld_32x32b_x32(trow + C::TM_O + ob * NQ + c0, r);
+                  tc::ld_32x32b_x32(trow + C::TM_O + ob * NR + c0, r);
                 } else {
-                  tc::ld_32x32b_x16(trow + C::TM_O + ob * NQ + c0, r);
+                  tc::ld_32x32b_x16(trow + C::TM_O + ob * NR + c0, r);
                 }
                 tc::wait_ld();
 #pragma unroll
                 for (int c = 0; c < (NR < 32 ? NR : 32); ++c)
                   r[c] = __float_as_uint(__uint_as_float(r[c]) * corr_s[c0 + c]);
                 if constexpr (NR >= 32) {
-                  tc::st_32x32b_x32(trow + C::TM_O + ob * NQ + c0, r);
+                  tc::st_32x32b_x32(trow + C::TM_O + ob * NR + c0, r);
                 } else {
-                  tc::st_32x32b_x16(trow + C::TM_O + ob * NQ + c0, r);
+                  tc::st_32x32b_x16(trow + C::TM_O + ob * NR + c0, r);
                 }
               }
               tc::wait_st();
             }
             load_s();
           }
-          // P^T row R: 2^(x - m) as bf16, heads along the 128-byte row (zero
-          // for padding heads)
-          uint32_t pk[NQ / 2];
+          // column R of P^T (position R of every head row): 2^(x - m) as bf16
+          uint16_t pb16[NR];
 #pragma unroll
-          for (int h = 0; h < NQ; h += 2) {
-            if (h < NR) {
-              const float p0 = h < nh ? tc::ex2(x[h] - m_s[h]) : 0.f;
-              const float p1 = h + 1 < nh ? tc::ex2(x[h + 1] - m_s[h + 1]) : 0.f;
-              lp[h] += p0;
-              lp[h + 1] += p1;
-              pk[h / 2] = pack_bf16x2(p0, p1);
-            } else {
-              pk[h / 2] = 0u;
-            }
+          for (int h = 0; h < NR; ++h) {
+            const float pv = h < nh ? tc::ex2(x[h] - m_s[h]) : 0.f;
+            lp[h] += pv;
+            pb16[h] = __bfloat16_as_ushort(__float2bfloat16_rn(pv));
           }
-          // the P buffer was last read by the P.V of tile tg-1
-          if (tg >= 1) wait(bars.pv_done(), (tg - 1) & 1);
+          // the P buffer was last read by the P.V of tile tg - PB
+          const int pb = tg % C::PB;
+          if (tg >= C::PB) wait(bars.pv_done(pb), ((tg / C::PB) - 1) & 1);
+          {
+            const uint32_t col = pbase + pb * C::P_BYTES + (R >> 6) * C::P_BOX + (R & 7) * 2;
+            const int chunk = (R & 63) >> 3;
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(pbase + R * 128 + ((c ^ (R & 7)) << 4)),
-                         "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                         : "memory");
+            for (int h = 0; h < NR; ++h)
+              asm volatile("st.shared.u16 [%0], %1;" ::"r"(col + h * 128 + ((chunk ^ (h & 7)) << 4)), "h"(pb16[h])
+                           : "memory");
+          }
           if (!valid && !dead && mbar_wait(pipe.full(st), (tg / ST) & 1)) {
             // position past L: its V row may hold anything (NaN included) and
             // 0 * NaN = NaN inside the MMA, so clear it (after it landed)
@@ -488,7 +500,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           __syncwarp();
           if (lane == 0) {
             mbar_arrive(bars.s_free(sb));
-            mbar_arrive(bars.p_full());
+            mbar_arrive(bars.p_full(tg % C::PB));
           }
         }
         t += ntl;
@@ -500,7 +512,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const float mR = R < NQ ? m_s[R] : 0.f;
         soft_reduce<C, false>(lp, sub, lane, red, fin, R);
         // O^T of this unit is final once the P.V of its last tile landed
-        wait(bars.pv_done(), (t - 1) & 1);
+        wait(bars.pv_done((t - 1) % C::PB), ((t - 1) / C::PB) & 1);
         tc::fence_after();
         const bool whole = seg.t0 == 0 && seg.t1 == seg.tiles;
         const int slot = partial_slot(unit);
@@ -509,9 +521,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         for (int c0 = 0; c0 < NR; c0 += (NR < 32 ? NR : 32)) {
           uint32_t r[32];
           if constexpr (NR >= 32) {
-            tc::ld_32x32b_x32(trow + C::TM_O + ob * NQ + c0, r);
+            tc::ld_32x32b_x32(trow + C::TM_O + ob * NR + c0, r);
           } else {
-            tc::ld_32x32b_x16(trow + C::TM_O + ob * NQ + c0, r);
+            tc::ld_32x32b_x16(trow + C::TM_O + ob * NR + c0, r);
           }
           tc::wait_ld();
 #pragma unroll

@@ -236,3 +236,94 @@ FULL = ["tiny", "mha", "gqa8", "mqa", "long"] + workloads.sweep_names()
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_config_matches_oracle(name):
     check_case(workloads.workload(name))
+
+
+# ------------------------------------------------------------ persistent schedule and merges
+@pytest.mark.parametrize("split_tokens", [128, 256, 1000])
+@pytest.mark.parametrize("H,G", [(64, 8), (32, 1), (128, 1), (16, 2)])
+def test_forced_splits_on_the_tensor_core_kernel(H, G, split_tokens):
+    """Groups of >= 8 heads run on the tcgen05 kernel; small splits cut
+    every sequence between many CTAs, whose partials the merge kernel joins."""
+    N = 900
+    lens = torch.tensor([900, 2, 511, 513, 64, 129], dtype=torch.int32)
+    w = _small(H, G, 128, N, "bf16", lens.tolist(), 7000 + H + G)
+    check_case(w, lens, split_tokens)
+
+
+@pytest.mark.parametrize("H,G", [(8, 8), (16, 4), (16, 2), (64, 1)])
+def test_more_than_64_sequences(H, G):
+    """B > 64 takes the second pass of the schedule's length scan."""
+    B, N = 97, 260
+    lens = torch.randint(1, N + 1, (B,), generator=torch.Generator().manual_seed(7100 + H + G),
+                         dtype=torch.int64).to(torch.int32)
+    w = workloads.Workload("many_b", B, H, G, 128, N, "bf16", ("fixed", N), 7100 + H + G)
+    check_case(w, lens)
+
+
+@pytest.mark.parametrize("H,G", [(8, 8), (8, 2), (16, 2), (64, 1)])
+def test_empty_sequences_on_every_kernel(H, G):
+    """L = 0 rows are zero-filled by the CTA that owns them, whatever kernel
+    family the group size selects (CUDA-core, mma.sync, tcgen05)."""
+    w = _small(H, G, 128, 400, "bf16", [0] * 5, 7200 + H + G)
+    x = workloads.make_inputs(w, seq_lens=torch.tensor([400, 400, 400, 400, 400], dtype=torch.int32), poison=False)
+    x["seq_lens"] = torch.tensor([0, 333, 0, 1, 400], dtype=torch.int32)
+    ref = oracle.decode_attention(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], w.scale)
+    got = gpu_attention(x, w.scale)
+    assert np.all(got[0] == 0) and np.all(got[2] == 0)
+    assert_parity(got, ref, f"empty rows H={H} G={G}")
+    assert gqa.gqa_get_device_error() & gqa.DEVERR_ATTN_LEN
+
+
+@pytest.mark.parametrize("H,G", [(8, 8), (16, 2), (64, 1)])
+def test_workspace_reused_by_calls_with_other_inputs(H, G):
+    """The merge bookkeeping left in a workspace by one call (counters of
+    another epoch, old unit records) must not leak into the next call."""
+    dev = torch.device("cuda")
+    N = 1500
+    w = _small(H, G, 128, N, "bf16", [N] * 6, 7300 + H + G)
+    need = gqa.gqa_decode_workspace_bytes_ex(6, H, G, 128, N, torch.bfloat16, 128)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    for trial, lens in enumerate(([1500, 7, 700, 1499, 128, 1], [3, 1500, 64, 900, 1, 1200])):
+        sl = torch.tensor(lens, dtype=torch.int32)
+        x = workloads.make_inputs(w.replace(index=7300 + H + G + trial), seq_lens=sl)
+        ref = oracle.decode_attention(x["q"], x["k_cache"], x["v_cache"], sl, w.scale)
+        q, k, v = x["q"].to(dev), x["k_cache"].to(dev), x["v_cache"].to(dev)
+        out = torch.full_like(q, float("nan"))
+        gqa.gqa_decode_attention_ex(q, k, v, sl.to(dev), w.scale, out, 128, ws)
+        torch.cuda.synchronize()
+        assert_parity(out.double().cpu().numpy(), ref, f"reuse {trial} H={H} G={G}")
+    assert gqa.gqa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("H,G", [(8, 8), (16, 2), (64, 1)])
+def test_graph_replay_matches_eager(H, G):
+    """A decode step captured in a CUDA graph (its call epoch fixed at capture)
+    gives the eager result on every replay: the in-kernel merge puts its
+    counters back to zero."""
+    dev = torch.device("cuda")
+    N = 2000
+    w = _small(H, G, 128, N, "bf16", [N] * 4, 7400 + H + G)
+    sl = torch.tensor([2000, 1234, 77, 1999], dtype=torch.int32)
+    x = workloads.make_inputs(w, seq_lens=sl, poison=False)
+    q, k, v, sld = x["q"].to(dev), x["k_cache"].to(dev), x["v_cache"].to(dev), sl.to(dev)
+    need = gqa.gqa_decode_workspace_bytes_ex(4, H, G, 128, N, torch.bfloat16, 128)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    eager = torch.empty_like(q)
+    gqa.gqa_decode_attention_ex(q, k, v, sld, w.scale, eager, 128, ws)
+    torch.cuda.synchronize()
+    out = torch.zeros_like(q)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        gqa.gqa_decode_attention_ex(q, k, v, sld, w.scale, out, 128, ws)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        gqa.gqa_decode_attention_ex(q, k, v, sld, w.scale, out, 128, ws)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
+    assert gqa.gqa_get_device_error() == 0
