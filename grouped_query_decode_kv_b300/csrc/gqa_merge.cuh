@@ -48,12 +48,14 @@ __device__ __forceinline__ unsigned arrive_unit(unsigned long long *cnt, unsigne
 // b), after those writes; `bar` synchronises the group.  When this CTA is the
 // unit's last, the group merges all its partials into out.
 template <typename T, int D, class Bar>
-__device__ __forceinline__ void finish_split_unit(const SplitParams &p, const Segment &seg, long long T_total, int b,
-                                                  int h_first, int nh, int tid, int nthr, UnitMerge *um, Bar bar) {
+__device__ __forceinline__ void finish_split_unit(const SplitParams &p, const Segment &seg, const CtaRange &range,
+                                                  int b, int h_first, int nh, int tid, int nthr, UnitMerge *um,
+                                                  Bar bar) {
+  const long long T_total = range.T;
   __threadfence();
   bar();
   if (tid == 0) {
-    const int P = gridDim.x;
+    const int P = range.P;
     const int c_lo = cta_of_tile(seg.unit_first, T_total, P);
     const int c_hi = cta_of_tile(seg.unit_first + seg.tiles - 1, T_total, P);
     const size_t u = (size_t)b * p.G * p.head_chunks + seg.uib;
@@ -103,11 +105,11 @@ __device__ __forceinline__ void finish_split_unit(const SplitParams &p, const Se
 // Combine-mode bookkeeping of a finished segment (one thread): the unit's
 // first CTA records where its partials are, or that it was finished whole.
 __device__ __forceinline__ void record_unit(const SplitParams &p, const Segment &seg, bool whole, int slot,
-                                            long long T_total, int b) {
+                                            const CtaRange &range, int b) {
   if (!p.unit_info || seg.t0 != 0) return;
   const size_t u = (size_t)b * p.G * p.head_chunks + seg.uib;
   p.unit_info[u] = whole ? make_int2(-1, -1)
-                         : make_int2(slot, cta_of_tile(seg.unit_first + seg.tiles - 1, T_total, gridDim.x));
+                         : make_int2(slot, cta_of_tile(seg.unit_first + seg.tiles - 1, range.T, range.P));
 }
 
 // One warp per (b, h): the merge of the unit that holds head h when the

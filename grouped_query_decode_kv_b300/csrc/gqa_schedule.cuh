@@ -19,6 +19,12 @@
 // and 2c for every later c, and the last of them to finish merges them
 // (gqa_merge.cuh).
 //
+// When every non-empty sequence has the same length and there are no more
+// units than CTAs, fewer than all CTAs may take part, so that range
+// boundaries fall on unit boundaries (see aligned_cta_count): a CTA that ends
+// one unit and starts another pays two epilogues and leaves two partials,
+// which costs more than a few idle CTAs.
+//
 // The lengths live in device memory, so each CTA derives T and its own
 // starting row from seq_lens with a warp scan (O(B/32) steps per CTA; the
 // first 64 rows are read once).
@@ -69,15 +75,29 @@ struct CtaRange {
   long long end;    // one past its last tile
   long long pre_b;  // global index of the first tile of row b
   int b;            // row holding `begin` (valid when begin < end)
+  int P;            // CTAs that take part (<= gridDim.x); the rest have empty ranges
 };
+
+// CTAs used for T tiles when every non-empty unit holds the same number of
+// tiles and there are no more units than CTAs: k = floor(P / units) CTAs per
+// unit, each taking an equal piece of one unit, so that no CTA works on two
+// units (two epilogues, two partials).  Measured on B300 this beats the
+// plain split over all P CTAs even when it leaves some CTAs idle, because
+// the K/V stream stays saturated.  With more units than CTAs, or units of
+// unequal length, the plain tile-level split over all P CTAs is kept.
+__device__ __forceinline__ int aligned_cta_count(long long units, int P) {
+  return (units > 0 && units <= P) ? (int)(units * (P / units)) : P;
+}
 
 // All 32 lanes of one warp call this.  Also flags out-of-range lengths and
 // zero-fills the output rows of empty sequences (L_b = 0) that this CTA owns
 // (row b is owned by CTA b % P), writing `row_bytes` bytes per row of `out`.
 __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int lane, void *out, size_t row_bytes) {
-  const int P = gridDim.x, c = blockIdx.x;
+  const int c = blockIdx.x;
+  int P = gridDim.x;
   long long T = 0;
   long long keep0 = 0, keep1 = 0;  // this lane's tile counts of rows lane and 32 + lane
+  int tmin = 0x7fffffff, tmax = 0, rows = 0;  // per-unit tile counts of the non-empty rows
   for (int base = 0; base < s.B; base += 32) {
     const int b = base + lane;
     long long t = 0;
@@ -86,7 +106,13 @@ __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int la
       const int Lraw = __ldg(s.seq_lens + b);
       const int L = clamp_len(Lraw, s.Nmax);
       t = (long long)((L + s.block_n - 1) / s.block_n) * s.units_per_b;
-      const bool mine = (b % P) == c;
+      const bool mine = (b % gridDim.x) == c;
+      const int tu = (L + s.block_n - 1) / s.block_n;
+      if (tu > 0) {
+        tmin = min(tmin, tu);
+        tmax = max(tmax, tu);
+        ++rows;
+      }
       if (mine && (Lraw <= 0 || Lraw > s.Nmax)) flag_error(GQA_DEVERR_ATTN_LEN);
       zero_mine = mine && L == 0;
     }
@@ -102,10 +128,18 @@ __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int la
     const long long incl = warp_incl_scan(t, lane);
     T += __shfl_sync(0xffffffffu, incl, 31);
   }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    tmin = min(tmin, __shfl_xor_sync(0xffffffffu, tmin, off));
+    tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+    rows += __shfl_xor_sync(0xffffffffu, rows, off);
+  }
+  if (rows > 0 && tmin == tmax) P = aligned_cta_count((long long)rows * s.units_per_b, P);
   CtaRange r;
   r.T = T;
-  r.begin = cta_start(c, T, P);
-  r.end = cta_start(c + 1, T, P);
+  r.P = P;
+  r.begin = c < P ? cta_start(c, T, P) : T;
+  r.end = c < P ? cta_start(c + 1, T, P) : T;
   r.b = 0;
   r.pre_b = 0;
   if (r.begin >= r.end) return r;

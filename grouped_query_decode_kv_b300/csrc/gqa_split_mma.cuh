@@ -370,9 +370,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
     if (!whole)
       for (int hl = threadIdx.x; hl < nh; hl += NCONS)
         reinterpret_cast<float2 *>(p.ml_part)[(size_t)slot * p.heads_per_cta + hl] = fin_s[hl];
-    if (threadIdx.x == 0) record_unit(p, seg, whole, slot, range.T, b);
+    if (threadIdx.x == 0) record_unit(p, seg, whole, slot, range, b);
     if (!whole && p.unit_cnt)
-      finish_split_unit<__nv_bfloat16, D>(p, seg, range.T, b, h_first, nh, threadIdx.x, NCONS, um,
+      finish_split_unit<__nv_bfloat16, D>(p, seg, range, b, h_first, nh, threadIdx.x, NCONS, um,
                                           [] { consumer_bar_sync(NCONS); });
     consumer_bar_sync(NCONS);  // scratch free for the next unit
   }

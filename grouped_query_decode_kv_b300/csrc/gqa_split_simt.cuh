@@ -321,9 +321,9 @@ __global__ void __launch_bounds__(C::THREADS)
       }
     }
     const bool whole = seg.t0 == 0 && seg.t1 == seg.tiles;
-    if (threadIdx.x == 0) record_unit(p, seg, whole, partial_slot(seg_index), range.T, b);
+    if (threadIdx.x == 0) record_unit(p, seg, whole, partial_slot(seg_index), range, b);
     if (!whole && p.unit_cnt)
-      finish_split_unit<T, D>(p, seg, range.T, b, h_first, nh, threadIdx.x, C::CONSUMER_WARPS * 32, um,
+      finish_split_unit<T, D>(p, seg, range, b, h_first, nh, threadIdx.x, C::CONSUMER_WARPS * 32, um,
                               [] { consumer_bar_sync(C::CONSUMER_WARPS * 32); });
     consumer_bar_sync(C::CONSUMER_WARPS * 32);  // scratch free for the next unit
   }

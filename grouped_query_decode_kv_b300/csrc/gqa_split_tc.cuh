@@ -540,9 +540,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         if (!whole && R < nh)
           reinterpret_cast<float2 *>(p.ml_part)[(size_t)slot * p.heads_per_cta + R] = make_float2(mR, fin[R]);
-        if (R == 0) record_unit(p, seg, whole, slot, range.T, b);
+        if (R == 0) record_unit(p, seg, whole, slot, range, b);
         if (!whole && p.unit_cnt)
-          finish_split_unit<__nv_bfloat16, D>(p, seg, range.T, b, h_first, nh, R, C::SOFT, um, [] { soft_bar(); });
+          finish_split_unit<__nv_bfloat16, D>(p, seg, range, b, h_first, nh, R, C::SOFT, um, [] { soft_bar(); });
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.o_free(ob));
