@@ -1,10 +1,11 @@
 #!/usr/bin/env python
 """Benchmark of one grouped-query decode step on B300.
 
-A step is one pass of the whole decode path over one batch: ``kv_append``
-(the new token's K/V written into the cache) followed by
-``gqa_decode_attention`` (split-KV kernel + log-sum-exp combine), both
-through the C ABI of ``libgqa.so``.  Inputs are seeded synthetic N(0, 1)
+A step is one pass of the whole decode path over one batch: the new
+token's K/V appended to the cache, then split-KV attention over the grown
+cache with its log-sum-exp merge -- one ``gqa_decode_step`` call of the C ABI
+of ``libgqa.so`` (one launch; a second, merge launch only for many-head
+groups whose sequences the split cuts).  Inputs are seeded synthetic N(0, 1)
 tensors resident in HBM.  Every step gets its own copy of the lengths
 ``seq_lens = L - 1``, so that each step appends at row L-1 and attends over
 exactly the workload's L_b positions; the caches rotate through enough
@@ -221,6 +222,8 @@ class DecodeState:
         self.lens_after = torch.clamp(self.lens - 1, min=0) + 1
         from grouped_query_decode_kv_b300 import gqa_decode_workspace_bytes
         self.ws_bytes = gqa_decode_workspace_bytes(w.B, w.H, w.G, w.d, w.Nmax, dt)
+        # the step's workspace: zero-filled once, each call leaves it ready
+        self.ws = torch.zeros(max(self.ws_bytes, 1), dtype=torch.uint8, device=device)
 
     def reset_lengths(self):
         pre = torch.clamp(self.lens - 1, min=0).to(torch.int32)
@@ -234,10 +237,6 @@ class DecodeState:
     def append_bytes(self) -> int:
         return cost.kv_append_bytes(self.w.B, self.w.G, self.w.d, self.w.elt)
 
-    @property
-    def launches_per_step(self) -> int:
-        return 2 + (1 if self.ws_bytes > 0 else 0)
-
 
 def copies_for(w: workloads.Workload, l2_bytes: int, mem_budget: int) -> int:
     cache = cost.kv_cache_bytes(w.B, w.G, w.Nmax, w.d, w.elt)
@@ -246,18 +245,18 @@ def copies_for(w: workloads.Workload, l2_bytes: int, mem_budget: int) -> int:
 
 
 def run_steps(st: DecodeState, first: int, count: int, ev=None):
-    """`count` decode steps; step i uses cache copy i % copies and lengths row
-    i.  With `ev` (a list of event pairs) the attention call of every step is
-    bracketed by CUDA events on the current stream."""
+    """`count` decode steps (gqa_decode_step_ws: append + attention in one call);
+    step i uses cache copy i % copies and lengths row i.  With `ev` (a list of
+    event pairs) every step call is bracketed by CUDA events on the current
+    stream."""
     import grouped_query_decode_kv_b300 as gqa
     w = st.w
     for i in range(first, first + count):
         c = i % st.copies
         sl = st.sl[i]
-        gqa.kv_append(st.kn[c], st.vn[c], st.k[c], st.v[c], sl)
         if ev is not None:
             ev[i - first][0].record()
-        gqa.gqa_decode_attention(st.q[c], st.k[c], st.v[c], sl, w.scale, st.out[c])
+        gqa.gqa_decode_step_ws(st.q[c], st.kn[c], st.vn[c], st.k[c], st.v[c], sl, w.scale, st.out[c], st.ws)
         if ev is not None:
             ev[i - first][1].record()
 
@@ -301,7 +300,7 @@ def time_attention_only(w: workloads.Workload, device, iters: int, warm: int, l2
     copies = copies_for(w, l2_bytes, mem_budget)
     st = DecodeState(w, iters, device, copies, seed=17)
     full = st.lens.to(torch.int32).to(device)
-    ws = torch.empty(max(st.ws_bytes, 1), dtype=torch.uint8, device=device)
+    ws = torch.zeros(max(st.ws_bytes, 1), dtype=torch.uint8, device=device)
 
     def attn_seq():
         for i in range(iters):
@@ -315,11 +314,18 @@ def time_attention_only(w: workloads.Workload, device, iters: int, warm: int, l2
             gqa.kv_append(st.kn[c], st.vn[c], st.k[c], st.v[c], st.sl[i])
         return iters
 
+    def step_seq():
+        for i in range(iters):
+            c = i % copies
+            gqa.gqa_decode_step_ws(st.q[c], st.kn[c], st.vn[c], st.k[c], st.v[c], st.sl[i], w.scale, st.out[c], ws)
+        return iters
+
     for i in range(warm):
         c = i % copies
         gqa.gqa_decode_attention_ws(st.q[c], st.k[c], st.v[c], full, w.scale, st.out[c], ws)
     us = _graph_time(attn_seq)
     us_append = _graph_time(append_seq, reset=st.reset_lengths)
+    us_step = _graph_time(step_seq, reset=st.reset_lengths)
     err = gqa.gqa_get_device_error()
     lens_full = st.lens.tolist()
     abytes = cost.decode_attention_bytes(lens_full, w.H, w.G, w.d, w.elt)
@@ -330,7 +336,8 @@ def time_attention_only(w: workloads.Workload, device, iters: int, warm: int, l2
         "frac_measured": round(abytes / us / 1e3 / peak, 3),
         "frac_8tbs": round(abytes / us / 1e3 / NOMINAL_HBM_GBS, 3),
         "tflops": round(cost.decode_attention_flops(lens_full, w.H, w.d) / us / 1e6, 1),
-        "kv_append_us": round(us_append, 2), "copies": copies, "device_error": err,
+        "kv_append_us": round(us_append, 2), "step_us": round(us_step, 2), "copies": copies,
+        "device_error": err,
     }
     del st, ws
     torch.cuda.empty_cache()
@@ -501,7 +508,7 @@ def run_ours(args, world, rank, local):
     value = aggregate(step_bytes * steps, secs_max, world)
     peak, peak_src = hbm_peak()
     attn_mean = statistics.mean(attn_us)
-    achieved = st.attention_bytes / attn_mean / 1e3
+    achieved = step_bytes / attn_mean / 1e3
 
     # ---- end to end through host buffers: q, k_new, v_new in, out back
     pin = lambda t: t.cpu().pin_memory()  # noqa: E731
@@ -517,9 +524,7 @@ def run_ours(args, world, rank, local):
         st.q[c].copy_(hq[c], non_blocking=True)
         st.kn[c].copy_(hk[c], non_blocking=True)
         st.vn[c].copy_(hv[c], non_blocking=True)
-        sl = st.sl[i]
-        gqa.kv_append(st.kn[c], st.vn[c], st.k[c], st.v[c], sl)
-        gqa.gqa_decode_attention(st.q[c], st.k[c], st.v[c], sl, w.scale, st.out[c])
+        gqa.gqa_decode_step_ws(st.q[c], st.kn[c], st.vn[c], st.k[c], st.v[c], st.sl[i], w.scale, st.out[c], st.ws)
         ho[c].copy_(st.out[c], non_blocking=True)
 
     for i in range(warm):
@@ -585,21 +590,21 @@ def run_ours(args, world, rank, local):
             "parallelism": f"replicas x{world}",
             "l2": f"rotating {copies} cache copies ({copies * cost.kv_cache_bytes(w.B, w.G, w.Nmax, w.d, w.elt) / 2**20:.0f} MiB"
                   f" >= 3 x L2 {l2 / 2**20:.0f} MiB)",
-            "step": "kv_append + gqa_decode_attention (split-KV + combine)",
+            "step": "gqa_decode_step: kv_append + split-KV attention + LSE merge, one launch",
             "timing": f"{args.prewarm:.1f} s untimed pre-warm, W warm-up steps, then K steps bracketed by "
                       "CUDA events with nothing else in the stream; the roofline's per-call time comes from "
-                      "a second pass of K steps with events around each attention call",
+                      "a second pass of K steps with events around each step call",
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "gqa_decode_attention call (split-KV kernel + LSE combine)",
+            "kernel": "gqa_decode_step call (split-KV kernel with the append fused; in-kernel merge)",
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_source": peak_src,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
-            "bytes_per_call": st_bytes(w),
+            "bytes_per_call": step_bytes,
             "us_per_call": round(attn_mean, 2),
             "us_per_call_p10_p90": [round(sorted(attn_us)[len(attn_us) // 10], 2),
                                     round(sorted(attn_us)[(9 * len(attn_us)) // 10], 2)],
@@ -608,8 +613,7 @@ def run_ours(args, world, rank, local):
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "us_per_step": round(e_secs / e_steps * 1e6, 2)},
-        "gpu_launches": (2 + (1 if gqa.gqa_decode_workspace_bytes(w.B, w.H, w.G, w.d, w.Nmax, w.torch_dtype) else 0))
-        * steps,
+        "gpu_launches": launches_per_step(w) * steps,
         "clocks": clocks,
         "device_error": dev_err,
         "read_ceiling_gbs": ceiling,
@@ -617,6 +621,17 @@ def run_ours(args, world, rank, local):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def launches_per_step(w: workloads.Workload) -> int:
+    """Kernels one gqa_decode_step launches: the split kernel, plus the merge
+    kernel for groups of three or more heads (bf16) whose sequences a split
+    may cut (the merge of one- and two-head groups runs inside the split
+    kernel)."""
+    import grouped_query_decode_kv_b300 as gqa
+    ws = gqa.gqa_decode_workspace_bytes(w.B, w.H, w.G, w.d, w.Nmax, w.torch_dtype)
+    many_heads = w.dtype == "bf16" and w.n_rep >= 3
+    return 1 + (1 if (ws > 0 and many_heads) else 0)
 
 
 def st_bytes(w: workloads.Workload) -> int:

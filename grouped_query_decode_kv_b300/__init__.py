@@ -13,6 +13,8 @@ Entry points (see ``include/gqa.h`` for the full contract):
   gqa_decode_attention_ex(..., split_tokens, workspace)
   gqa_decode_workspace_bytes(B, H, G, d, Nmax, dtype)
   gqa_decode_attention_noalloc(...)              no allocation: fixed in-library scratch
+  gqa_decode_step(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out)
+  gqa_decode_step_ws(..., workspace)             append + attention in one launch
   kv_append(k_new, v_new, k_cache, v_cache, seq_lens)
   mha_to_gqa_meanpool(w, w_out)
   gqa_get_device_error()
@@ -35,6 +37,7 @@ __all__ = [
     "gqa_decode_workspace_bytes", "gqa_decode_workspace_bytes_ex", "kv_append",
     "mha_to_gqa_meanpool", "gqa_get_device_error", "gqa_status_string",
     "gqa_decode_attention_noalloc", "NOALLOC_SCRATCH_BYTES", "ERR_SCRATCH_LIMIT",
+    "gqa_decode_step", "gqa_decode_step_ws",
     "DEVERR_ATTN_LEN", "DEVERR_APPEND_LEN", "DEVERR_TIMEOUT", "EXPORTED_SYMBOLS",
 ]
 
@@ -47,7 +50,7 @@ EXPORTED_SYMBOLS = (
     "gqa_decode_attention", "gqa_decode_workspace_bytes", "gqa_decode_attention_ws",
     "gqa_decode_workspace_bytes_ex", "gqa_decode_attention_ex", "kv_append",
     "mha_to_gqa_meanpool", "gqa_get_device_error", "gqa_status_string",
-    "gqa_decode_attention_noalloc",
+    "gqa_decode_attention_noalloc", "gqa_decode_step", "gqa_decode_step_ws",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -82,6 +85,11 @@ def load_library():
         lib.gqa_decode_attention_ws.argtypes = attn + [vp, sz, vp]
         lib.gqa_decode_attention_ex.argtypes = attn + [ci, vp, sz, vp]
         lib.gqa_decode_attention_noalloc.argtypes = attn + [vp]
+        step = [vp, vp, vp, vp, vp, vp, cf, vp, ci, ci, ci, ci, ci, ci]
+        lib.gqa_decode_step.argtypes = step + [vp]
+        lib.gqa_decode_step.restype = ci
+        lib.gqa_decode_step_ws.argtypes = step + [vp, sz, vp]
+        lib.gqa_decode_step_ws.restype = ci
         for f in ("gqa_decode_attention", "gqa_decode_attention_ws", "gqa_decode_attention_ex",
                   "gqa_decode_attention_noalloc"):
             getattr(lib, f).restype = ci
@@ -215,6 +223,41 @@ def gqa_decode_attention_noalloc(q, k_cache, v_cache, seq_lens, scale, out, stre
     _check("gqa_decode_attention_noalloc",
            lib.gqa_decode_attention_noalloc(*_attn_args(q, k_cache, v_cache, seq_lens, scale, out),
                                             _stream(q, stream)))
+    return out
+
+
+def _step_args(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out):
+    B, H, G, d, Nmax = _attn_shapes(q, k_cache, v_cache, seq_lens, out)
+    if tuple(k_new.shape) != (B, G, d) or tuple(v_new.shape) != (B, G, d):
+        raise ValueError("k_new and v_new must be [B, G, d]")
+    if not (k_new.dtype == v_new.dtype == q.dtype):
+        raise ValueError("k_new and v_new must have the caches' dtype")
+    return [_dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(k_cache, "k_cache"),
+            _dev(v_cache, "v_cache"), _dev(seq_lens, "seq_lens"), float(scale), _dev(out, "out"),
+            B, H, G, d, Nmax, _dtype_code(q)]
+
+
+def gqa_decode_step(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out, stream=None):
+    """One decode step in one launch: k_new/v_new [B,G,d] appended at row
+    seq_lens[b] of the caches, attention over the grown cache into out, then
+    seq_lens[b] += 1 (all on the device).  Same result as kv_append followed
+    by gqa_decode_attention."""
+    lib = load_library()
+    _check("gqa_decode_step",
+           lib.gqa_decode_step(*_step_args(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out),
+                               _stream(q, stream)))
+    return out
+
+
+def gqa_decode_step_ws(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out, workspace, stream=None):
+    """As gqa_decode_step with a caller-owned workspace of at least
+    gqa_decode_workspace_bytes(...) bytes, zero-filled once before its first
+    use here (every call leaves it ready for the next)."""
+    lib = load_library()
+    wp, wn = _ws(workspace)
+    _check("gqa_decode_step_ws",
+           lib.gqa_decode_step_ws(*_step_args(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out), wp, wn,
+                                  _stream(q, stream)))
     return out
 
 

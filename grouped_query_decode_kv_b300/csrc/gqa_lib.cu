@@ -245,11 +245,17 @@ unsigned next_epoch() {
   return e;
 }
 
+size_t ws_book_bytes(const Plan &pl) { return align256((size_t)pl.units * sizeof(unsigned long long)); }
+size_t step_counter_offset(const Plan &pl, int d) { return ws_opart_bytes(pl, d) + ws_ml_bytes(pl) + ws_book_bytes(pl); }
+
+// ... plus one 32-bit counter of finished CTAs for a fused decode step, which
+// must be zero before the workspace's first gqa_decode_step_ws call (each
+// call leaves it at zero).
 size_t workspace_for(const Plan &pl, int B, int H, int d) {
   (void)B;
   (void)H;
   if (pl.P <= 1) return 0;
-  return ws_opart_bytes(pl, d) + ws_ml_bytes(pl) + align256((size_t)pl.units * sizeof(unsigned long long));
+  return ws_opart_bytes(pl, d) + ws_ml_bytes(pl) + ws_book_bytes(pl) + 256;
 }
 
 // ----------------------------------------------------------- TMA descriptors
@@ -323,8 +329,16 @@ int ensure_smem_attr(const KernelChoice &kc) {
   return GQA_OK;
 }
 
+// Rows appended by a fused decode step (null for attention alone).
+struct StepAppend {
+  const void *k_new = nullptr, *v_new = nullptr;
+  void *k_cache = nullptr, *v_cache = nullptr;
+  int32_t *seq_lens = nullptr;
+};
+
 int run_attention(const void *q, const void *k, const void *v, const int32_t *sl, float scale, void *out, int B,
-                  int H, int G, int d, int Nmax, gqa_dtype_t dt, const Plan &pl, void *ws, cudaStream_t st) {
+                  int H, int G, int d, int Nmax, gqa_dtype_t dt, const Plan &pl, void *ws, cudaStream_t st,
+                  const StepAppend &app = StepAppend()) {
   CUtensorMap mk, mv;
   if (!encode_cache_map(&mk, k, dt, d, Nmax, B * G, pl.k.block_n, pl.k.box_elems) ||
       !encode_cache_map(&mv, v, dt, d, Nmax, B * G, pl.k.block_n, pl.k.box_elems))
@@ -345,6 +359,14 @@ int run_attention(const void *q, const void *k, const void *v, const int32_t *sl
   p.unit_cnt = merge_in_kernel ? reinterpret_cast<unsigned long long *>(book) : nullptr;
   p.unit_info = merge_in_kernel ? nullptr : reinterpret_cast<int2 *>(book);
   p.epoch = next_epoch();
+  p.append = app.k_new != nullptr;
+  p.k_new = app.k_new;
+  p.v_new = app.v_new;
+  p.k_cache = app.k_cache;
+  p.v_cache = app.v_cache;
+  p.seq_lens_w = app.seq_lens;
+  p.row_chunks = d * (dt == GQA_BF16 ? 2 : 4) / 16;
+  p.done_cnt = split ? reinterpret_cast<unsigned *>(w + step_counter_offset(pl, d)) : nullptr;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.B = B;
   p.H = H;
@@ -465,6 +487,59 @@ int gqa_decode_attention(const void *q, const void *k_cache, const void *v_cache
   int rc = run_attention(q, k_cache, v_cache, seq_lens, scale, out, B, H, G, d, Nmax, dtype, pl, ws, stream);
   if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && rc == GQA_OK) rc = GQA_ERR_CUDA;
   return rc;
+}
+
+namespace {
+int decode_step(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                int32_t *seq_lens, float scale, void *out, int B, int H, int G, int d, int Nmax, gqa_dtype_t dtype,
+                void *workspace, size_t workspace_bytes, bool allocate, cudaStream_t stream) {
+  if (int rc = check_attention_args(q, k_cache, v_cache, seq_lens, out, B, H, G, d, Nmax, dtype)) return rc;
+  if (!k_new || !v_new) return GQA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new)) return GQA_ERR_INVALID_ARG;
+  const Plan pl = make_plan(B, H, G, d, Nmax, dtype, 0);
+  if (!plan_fits(pl, B, G)) return GQA_ERR_UNSUPPORTED;
+  const size_t need = workspace_for(pl, B, H, d);
+  void *ws = workspace;
+  if (allocate) {
+    ws = nullptr;
+    if (need > 0 && cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return GQA_ERR_NO_MEMORY;
+    }
+    if (need > 0 &&
+        cudaMemsetAsync(reinterpret_cast<char *>(ws) + step_counter_offset(pl, d), 0, sizeof(unsigned), stream) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      cudaFreeAsync(ws, stream);
+      return GQA_ERR_CUDA;
+    }
+  } else if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))) {
+    return GQA_ERR_INVALID_ARG;
+  }
+  StepAppend app;
+  app.k_new = k_new;
+  app.v_new = v_new;
+  app.k_cache = k_cache;
+  app.v_cache = v_cache;
+  app.seq_lens = seq_lens;
+  int rc = run_attention(q, k_cache, v_cache, seq_lens, scale, out, B, H, G, d, Nmax, dtype, pl, ws, stream, app);
+  if (allocate && ws && cudaFreeAsync(ws, stream) != cudaSuccess && rc == GQA_OK) rc = GQA_ERR_CUDA;
+  return rc;
+}
+}  // namespace
+
+int gqa_decode_step(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                    int32_t *seq_lens, float scale, void *out, int B, int H, int G, int d, int Nmax,
+                    gqa_dtype_t dtype, cudaStream_t stream) {
+  return decode_step(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out, B, H, G, d, Nmax, dtype, nullptr, 0,
+                     true, stream);
+}
+
+int gqa_decode_step_ws(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                       int32_t *seq_lens, float scale, void *out, int B, int H, int G, int d, int Nmax,
+                       gqa_dtype_t dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return decode_step(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out, B, H, G, d, Nmax, dtype, workspace,
+                     workspace_bytes, false, stream);
 }
 
 int gqa_decode_attention_noalloc(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,

@@ -102,6 +102,35 @@ __device__ __forceinline__ void finish_split_unit(const SplitParams &p, const Se
   }
 }
 
+// End of a fused decode step, called by all `nthr` threads of a CTA after all
+// of the CTA's work (every CTA comes, busy or idle).  The last CTA of the
+// grid to get here advances seq_lens[b] to L_b + 1 for every row that took
+// the append, and puts the counter back to zero for the next call.  No CTA
+// reads the lengths after its own arrival, so the update cannot be seen half
+// way through the call.  A plain atomic add (no retry loop): all CTAs of the
+// grid arrive within a few microseconds of each other.  `flag` is a shared
+// word that broadcasts thread 0's finding.
+__device__ __forceinline__ void finish_step(const SplitParams &p, int tid, int nthr, volatile int *flag) {
+  if (tid == 0) {
+    bool last = true;
+    if (p.done_cnt) {
+      __threadfence();
+      last = atomicAdd(p.done_cnt, 1u) == gridDim.x - 1;
+      if (last) {
+        __threadfence();
+        atomicExch(p.done_cnt, 0u);
+      }
+    }
+    *flag = last;
+  }
+  __syncthreads();
+  if (!*flag) return;
+  for (int b = tid; b < p.B; b += nthr) {
+    const int L = __ldcg(p.seq_lens_w + b);
+    if (append_ok(L, p.Nmax)) p.seq_lens_w[b] = L + 1;
+  }
+}
+
 // Combine-mode bookkeeping of a finished segment (one thread): the unit's
 // first CTA records where its partials are, or that it was finished whole.
 __device__ __forceinline__ void record_unit(const SplitParams &p, const Segment &seg, bool whole, int slot,

@@ -19,6 +19,15 @@ struct SplitParams {
   unsigned long long *unit_cnt;  // [B*G*HC] in-kernel merge: (call epoch << 32) | CTAs of the unit done
   int2 *unit_info;          // [B*G*HC] merge kernel: (first slot, last CTA) of a split unit, or -1
   unsigned epoch;           // nonzero, different for every call
+  // Fused decode step (append != 0): the new token's K/V rows k_new/v_new
+  // [B*G, D] go to cache row L_b of every (b, g) before attention over
+  // L_b + 1 positions; the last CTA to finish then sets seq_lens[b] = L_b + 1.
+  int append;
+  const void *k_new, *v_new;
+  void *k_cache, *v_cache;  // [B*G, Nmax, D]
+  int32_t *seq_lens_w;      // the same array as seq_lens
+  int row_chunks;           // 16-byte chunks per cache row (D * element size / 16)
+  unsigned *done_cnt;       // CTAs finished, zero between calls; null with one CTA
   float scale_log2;         // scale * log2(e): softmax is evaluated with exp2
   int B, H, G, Nmax;
   int n_rep;                // H / G

@@ -11,6 +11,7 @@
 #pragma once
 
 #include "gqa_device.cuh"
+#include "gqa_params.cuh"
 #include "gqa_schedule.cuh"
 
 namespace gqa {
@@ -78,31 +79,77 @@ struct KVPipe {
   __device__ __forceinline__ void release(int r) const { mbar_arrive(empty(r % STAGES)); }
 };
 
-// The producer thread's whole job: stream the K/V tiles of every segment of
-// this CTA's range, in order, through the ring.  Unit u = (b, g*HC + hc)
-// reads K/V head b*G + g.
+// Fused decode step, whole producer warp: copies the new token's K and V
+// rows of KV head bg (batch row b) into cache row L_b.  The CTA that loads a
+// unit's last tile is the only one that reads the row, and it copies the row
+// before that load (after a fence.proxy.async for the TMA to see it).
+__device__ __forceinline__ void append_rows(const SplitParams &p, int b, int bg, int lane) {
+  const int L = __ldg(p.seq_lens + b);
+  if (!append_ok(L, p.Nmax)) return;
+  const uint4 *kn = reinterpret_cast<const uint4 *>(p.k_new) + (size_t)bg * p.row_chunks;
+  const uint4 *vn = reinterpret_cast<const uint4 *>(p.v_new) + (size_t)bg * p.row_chunks;
+  uint4 *kc = reinterpret_cast<uint4 *>(p.k_cache) + ((size_t)bg * p.Nmax + L) * p.row_chunks;
+  uint4 *vc = reinterpret_cast<uint4 *>(p.v_cache) + ((size_t)bg * p.Nmax + L) * p.row_chunks;
+  for (int i = lane; i < 2 * p.row_chunks; i += 32) {
+    if (i < p.row_chunks)
+      kc[i] = __ldg(kn + i);
+    else
+      vc[i - p.row_chunks] = __ldg(vn + i - p.row_chunks);
+  }
+}
+
+__device__ __forceinline__ void fence_global_for_async_proxy() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// The producer warp's whole job: stream the K/V tiles of every segment of
+// this CTA's range, in order, through the ring (lane 0 issues the copies).
+// Unit u = (b, g*HC + hc) reads K/V head b*G + g.  In a fused step the warp
+// also writes the appended rows: the rows of units whose last tile falls in
+// the ring's first STAGES loads right before that load, all the others in one
+// batch once those first loads are in flight (their latency then overlaps).
 template <class Pipe>
 __device__ __forceinline__ void produce_range(const Pipe &pipe, const SchedParams &s, const CtaRange &range,
                                               const CUtensorMap *tmK, const CUtensorMap *tmV, int box_elems, int G,
-                                              int HC) {
+                                              int HC, const SplitParams &p, int lane) {
   const uint64_t pol = l2_policy_evict_first();
   SegmentCursor cur;
   cur.init(s, range);
   Segment seg;
   int r = 0;
   bool ok = true;
+  bool batch_done = !p.append;
   while (ok && cur.next(s, seg)) {
     const int bg = seg.b * G + seg.uib / HC;
     for (int t = seg.t0; t < seg.t1; ++t) {
-      if (!pipe.acquire(r)) {
-        ok = false;
-        break;
+      if (!batch_done && r == Pipe::STAGES) {
+        // every remaining unit of the range whose last tile is this CTA's
+        SegmentCursor rest = cur;
+        Segment rs = seg;
+        bool more = true;
+        while (more) {
+          if (rs.t1 == rs.tiles) append_rows(p, rs.b, rs.b * G + rs.uib / HC, lane);
+          more = rest.next(s, rs);
+        }
+        fence_global_for_async_proxy();
+        batch_done = true;
       }
-      pipe.load(r, tmK, tmV, box_elems, bg, t * Pipe::BLOCK_N, pol);
+      if (!batch_done && t == seg.tiles - 1) {
+        append_rows(p, seg.b, bg, lane);
+        fence_global_for_async_proxy();
+      }
+      __syncwarp();
+      if (lane == 0) {
+        ok = pipe.acquire(r);
+        if (ok) pipe.load(r, tmK, tmV, box_elems, bg, t * Pipe::BLOCK_N, pol);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
       ++r;
     }
   }
-  pipe.drain(r);
+  if (lane == 0) pipe.drain(r);
+  __syncwarp();
 }
 
 __device__ __forceinline__ void consumer_bar_sync(int nthreads) {

@@ -40,13 +40,23 @@ struct SchedParams {
   int Nmax;
   int units_per_b;  // G * HC
   int block_n;      // positions per tile
+  int append;       // fused decode step: the call appends one token first
 };
 
 __device__ __forceinline__ int clamp_len(int L, int Nmax) { return max(0, min(L, Nmax)); }
 
+// A stored length L_b takes the step's append when 0 <= L_b < Nmax.
+__device__ __forceinline__ bool append_ok(int L, int Nmax) { return L >= 0 && L < Nmax; }
+
+// The number of cached positions attention covers for row b: the stored
+// length, plus the appended token in a fused step, clamped to [0, Nmax].
+__device__ __forceinline__ int attn_len(const int32_t *seq_lens, int b, int Nmax, int append) {
+  const int L = __ldg(seq_lens + b);
+  return clamp_len(append && append_ok(L, Nmax) ? L + 1 : L, Nmax);
+}
+
 __device__ __forceinline__ int row_tiles(const SchedParams &s, int b) {
-  const int L = clamp_len(__ldg(s.seq_lens + b), s.Nmax);
-  return (L + s.block_n - 1) / s.block_n;
+  return (attn_len(s.seq_lens, b, s.Nmax, s.append) + s.block_n - 1) / s.block_n;
 }
 
 __device__ __forceinline__ long long cta_start(long long c, long long T, long long P) {
@@ -103,7 +113,9 @@ __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int la
     long long t = 0;
     bool zero_mine = false;
     if (b < s.B) {
-      const int Lraw = __ldg(s.seq_lens + b);
+      const int Lstored = __ldg(s.seq_lens + b);
+      const bool appends = s.append && append_ok(Lstored, s.Nmax);
+      const int Lraw = appends ? Lstored + 1 : Lstored;
       const int L = clamp_len(Lraw, s.Nmax);
       t = (long long)((L + s.block_n - 1) / s.block_n) * s.units_per_b;
       const bool mine = (b % gridDim.x) == c;
@@ -114,6 +126,7 @@ __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int la
         ++rows;
       }
       if (mine && (Lraw <= 0 || Lraw > s.Nmax)) flag_error(GQA_DEVERR_ATTN_LEN);
+      if (mine && s.append && !appends) flag_error(GQA_DEVERR_APPEND_LEN);
       zero_mine = mine && L == 0;
     }
     unsigned zero_rows = __ballot_sync(0xffffffffu, zero_mine);

@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   sp.Nmax = p.Nmax;
   sp.units_per_b = p.G * p.head_chunks;
   sp.block_n = C::BLOCK_N;
+  sp.append = p.append;
 
   if (threadIdx.x == 0) pipe.init();
   griddep_wait();  // lengths and cache rows written by earlier kernels are visible
@@ -94,16 +95,14 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   __syncthreads();
   griddep_launch_dependents();
   const CtaRange range = *range_smem;
-  if (range.begin >= range.end) return;
-
-  if (warp == C::CONSUMER_WARPS) {  // producer warp
+  if (range.begin < range.end && warp == C::CONSUMER_WARPS) {
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      produce_range(pipe, sp, range, &tmK, &tmV, 64, p.G, p.head_chunks);
     }
-    return;
+    produce_range(pipe, sp, range, &tmK, &tmV, 64, p.G, p.head_chunks, p, lane);
   }
+  if (range.begin < range.end && warp != C::CONSUMER_WARPS) {
 
   const int wh = warp >> 2, wn = warp & 3;
   const int gq = lane >> 2, tq = lane & 3;
@@ -117,7 +116,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
     const int b = seg.b;
     const int h_first = g * p.n_rep + hc * C::HEADS;
     const int nh = min(C::HEADS, p.n_rep - hc * C::HEADS);
-    const int L = clamp_len(__ldg(p.seq_lens + b), p.Nmax);
+    const int L = attn_len(p.seq_lens, b, p.Nmax, p.append);
 
     // Q fragments (A operand, row-major 16x16 per k-step), kept in registers.
     uint32_t qa[MFW][KS][4];
@@ -375,6 +374,11 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
       finish_split_unit<__nv_bfloat16, D>(p, seg, range, b, h_first, nh, threadIdx.x, NCONS, um,
                                           [] { consumer_bar_sync(NCONS); });
     consumer_bar_sync(NCONS);  // scratch free for the next unit
+  }
+  }
+  if (p.append) {
+    __syncthreads();
+    finish_step(p, threadIdx.x, blockDim.x, &um->last);
   }
 }
 

@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(C::THREADS)
   sp.Nmax = p.Nmax;
   sp.units_per_b = p.G * p.head_chunks;
   sp.block_n = C::BLOCK_N;
+  sp.append = p.append;
 
   if (threadIdx.x == 0) pipe.init();
   griddep_wait();  // lengths and cache rows written by earlier kernels are visible
@@ -124,16 +125,14 @@ __global__ void __launch_bounds__(C::THREADS)
   __syncthreads();
   griddep_launch_dependents();
   const CtaRange range = *range_smem;
-  if (range.begin >= range.end) return;
-
-  if (warp == C::CONSUMER_WARPS) {
+  if (range.begin < range.end && warp == C::CONSUMER_WARPS) {
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      produce_range(pipe, sp, range, &tmK, &tmV, C::BOX_ELEMS, p.G, p.head_chunks);
     }
-    return;
+    produce_range(pipe, sp, range, &tmK, &tmV, C::BOX_ELEMS, p.G, p.head_chunks, p, lane);
   }
+  if (range.begin < range.end && warp != C::CONSUMER_WARPS) {
 
   const int tg = lane >> 3, j = lane & 7;
   float *scratch = reinterpret_cast<float *>(smem + C::EPI_OFF);
@@ -147,7 +146,7 @@ __global__ void __launch_bounds__(C::THREADS)
     const int b = seg.b;
     const int h_first = g * p.n_rep + hc * NH;
     const int nh = min(NH, p.n_rep - hc * NH);
-    const int L = clamp_len(__ldg(p.seq_lens + b), p.Nmax);
+    const int L = attn_len(p.seq_lens, b, p.Nmax, p.append);
 
     // this lane's slice of q: element e of box bx is d = bx*BOX_ELEMS + j*EPC + e
     float qf[NH][EPL];
@@ -326,6 +325,11 @@ __global__ void __launch_bounds__(C::THREADS)
       finish_split_unit<T, D>(p, seg, range, b, h_first, nh, threadIdx.x, C::CONSUMER_WARPS * 32, um,
                               [] { consumer_bar_sync(C::CONSUMER_WARPS * 32); });
     consumer_bar_sync(C::CONSUMER_WARPS * 32);  // scratch free for the next unit
+  }
+  }
+  if (p.append) {
+    __syncthreads();
+    finish_step(p, threadIdx.x, blockDim.x, &um->last);
   }
 }
 

@@ -201,6 +201,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   sp.Nmax = p.Nmax;
   sp.units_per_b = p.G * p.head_chunks;
   sp.block_n = BN;
+  sp.append = p.append;
 
   if (threadIdx.x == 0) {
     pipe.init();
@@ -239,8 +240,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (lane == 0) {
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
-        produce_range(pipe, sp, range, &tmK, &tmV, 64, p.G, p.head_chunks);
       }
+      produce_range(pipe, sp, range, &tmK, &tmV, 64, p.G, p.head_chunks, p, lane);
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
       if (lane == 0) {
@@ -383,7 +384,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         int h_first, nh;
         unit_heads(seg, h_first, nh);
         const int b = seg.b;
-        const int L = clamp_len(__ldg(p.seq_lens + b), p.Nmax);
+        const int L = attn_len(p.seq_lens, b, p.Nmax, p.append);
         const int ob = unit & 1;
         const int ntl = seg.t1 - seg.t0;
         float lp[NR];
@@ -560,6 +561,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     tc::fence_after();
     tc::tmem_dealloc(tmem, C::TM_COLS);
   }
+  if (p.append) finish_step(p, threadIdx.x, blockDim.x, &um->last);
 }
 
 }  // namespace gqa

@@ -128,6 +128,39 @@ int gqa_decode_attention_ex(const void *q, const void *k_cache, const void *v_ca
                             cudaStream_t stream);
 
 /*
+ * gqa_decode_step — one whole autoregressive decode step in one launch: the
+ * cache concatenation of kv_append followed by gqa_decode_attention over the
+ * grown cache (fogdragon's CSDN blog on MQA/GQA, section "KV Cache": K =
+ * cat([K_prev, k]), V = cat([V_prev, v]), then logits / softmax / weighted
+ * sum over all positions including the new one).  Same result as
+ *   kv_append(k_new, v_new, k_cache, v_cache, seq_lens, ...);
+ *   gqa_decode_attention(q, k_cache, v_cache, seq_lens, scale, out, ...);
+ * on the same stream (bit for bit), without the second launch: the thread
+ * block that loads the tile holding row L_b writes k_new/v_new there first,
+ * and the last block to finish advances seq_lens.
+ *
+ *   q [B,H,d], k_new/v_new [B,G,d], k_cache/v_cache [B,G,Nmax,d] (updated),
+ *   seq_lens [B] int32 DEVICE memory (read, then L_b + 1 where appended),
+ *   out [B,H,d].  Pointers 16-byte aligned; d in {64, 128}; H % G == 0.
+ * A row with L_b < 0 or L_b >= Nmax gets no append (GQA_DEVERR_APPEND_LEN)
+ * and attention over its clamped stored length (GQA_DEVERR_ATTN_LEN when
+ * that is <= 0 or > Nmax), exactly as the two separate calls would do.
+ * gqa_decode_step takes its workspace from the stream-ordered allocator;
+ * gqa_decode_step_ws from the caller: gqa_decode_workspace_bytes bytes,
+ * 256-byte aligned, ZERO-FILLED once before its first gqa_decode_step_ws
+ * call (the blocks count their arrivals in it; every call leaves the count
+ * at zero, so later calls need no clearing unless a call failed with a
+ * device error).  The same workspace also serves gqa_decode_attention_ws.
+ * Calls sharing one workspace must not overlap on the device.
+ */
+int gqa_decode_step(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                    int32_t *seq_lens, float scale, void *out, int B, int H, int G, int d, int Nmax,
+                    gqa_dtype_t dtype, cudaStream_t stream);
+int gqa_decode_step_ws(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                       int32_t *seq_lens, float scale, void *out, int B, int H, int G, int d, int Nmax,
+                       gqa_dtype_t dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * gqa_decode_attention_noalloc — gqa_decode_attention for callers that must
  * not allocate device memory during the call.  The paper has no counterpart:
  * this is an integration entry point, not part of the method.

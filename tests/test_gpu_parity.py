@@ -327,3 +327,67 @@ def test_graph_replay_matches_eager(H, G):
         torch.cuda.synchronize()
         assert torch.equal(out, eager)
     assert gqa.gqa_get_device_error() == 0
+
+
+# ------------------------------------------------------------ fused decode step
+@pytest.mark.parametrize("H,G,d,dtype", [(8, 8, 128, "bf16"), (16, 8, 128, "bf16"), (8, 2, 128, "bf16"),
+                                         (16, 2, 128, "bf16"), (64, 1, 128, "bf16"), (8, 2, 64, "bf16"),
+                                         (8, 2, 64, "f32")])
+@pytest.mark.parametrize("use_ws", [False, True])
+def test_decode_step_equals_append_then_attention(H, G, d, dtype, use_ws):
+    """gqa_decode_step (one launch) against kv_append + gqa_decode_attention:
+    output, caches and lengths bit for bit, also for rows that cannot append
+    (L = Nmax, L < 0) and for a sequence that starts empty."""
+    dev = torch.device("cuda")
+    B, N = 7, 700
+    w = workloads.Workload("step", B, H, G, d, N, dtype, ("fixed", N), 7500 + H + G + d)
+    lens = torch.tensor([699, 0, 128, 127, N, -1, 350], dtype=torch.int32)
+    x = workloads.make_inputs(w, seq_lens=torch.clamp(lens, 0, N), poison=True)
+    x["seq_lens"] = lens
+    q, kn, vn = x["q"].to(dev), x["k_new"].to(dev), x["v_new"].to(dev)
+    k1, v1, sl1 = x["k_cache"].to(dev), x["v_cache"].to(dev), lens.to(dev)
+    k2, v2, sl2 = k1.clone(), v1.clone(), sl1.clone()
+    out1, out2 = torch.full_like(q, float("nan")), torch.full_like(q, float("nan"))
+    gqa.gqa_get_device_error()
+    gqa.kv_append(kn, vn, k1, v1, sl1)
+    gqa.gqa_decode_attention(q, k1, v1, sl1, w.scale, out1)
+    e1 = gqa.gqa_get_device_error()
+    if use_ws:
+        ws = torch.zeros(max(gqa.gqa_decode_workspace_bytes(B, H, G, d, N, q.dtype), 1), dtype=torch.uint8,
+                         device=dev)
+        gqa.gqa_decode_step_ws(q, kn, vn, k2, v2, sl2, w.scale, out2, ws)
+    else:
+        gqa.gqa_decode_step(q, kn, vn, k2, v2, sl2, w.scale, out2)
+    e2 = gqa.gqa_get_device_error()
+    torch.cuda.synchronize()
+    assert torch.equal(sl1, sl2)
+    assert torch.equal(k1.view(torch.uint8), k2.view(torch.uint8))
+    assert torch.equal(v1.view(torch.uint8), v2.view(torch.uint8))
+    np.testing.assert_array_equal(out1.double().cpu().numpy(), out2.double().cpu().numpy())
+    assert e1 == e2 and e2 & gqa.DEVERR_APPEND_LEN and e2 & gqa.DEVERR_ATTN_LEN
+
+
+@pytest.mark.parametrize("name", ["mha", "gqa8", "mqa", "sweep_g1"])
+def test_decode_step_matches_oracle(name):
+    """Three consecutive fused decode steps on a full-size workload against the
+    oracle's append-then-attend, step by step."""
+    dev = torch.device("cuda")
+    w = workloads.workload(name)
+    sl0 = torch.clamp(workloads.make_seq_lens(w) - 3, min=0)
+    x = workloads.make_inputs(w, seq_lens=sl0)
+    k, v, sl = x["k_cache"].to(dev), x["v_cache"].to(dev), sl0.to(dev)
+    kc, vc, slc = x["k_cache"], x["v_cache"], sl0
+    g = torch.Generator().manual_seed(7600 + w.index)
+    for step in range(3):
+        kn = torch.randn(w.B, w.G, w.d, generator=g).to(w.torch_dtype)
+        vn = torch.randn(w.B, w.G, w.d, generator=g).to(w.torch_dtype)
+        q = torch.randn(w.B, w.H, w.d, generator=g).to(w.torch_dtype)
+        kc, vc, slc, skipped = oracle.kv_append(kn, vn, kc, vc, slc)
+        assert skipped == 0
+        ref = oracle.decode_attention(q, kc, vc, slc, w.scale)
+        out = torch.empty(w.B, w.H, w.d, dtype=w.torch_dtype, device=dev)
+        gqa.gqa_decode_step(q.to(dev), kn.to(dev), vn.to(dev), k, v, sl, w.scale, out)
+        torch.cuda.synchronize()
+        assert torch.equal(sl.cpu(), slc)
+        assert_parity(out.double().cpu().numpy(), ref, f"{name} step {step}")
+    assert gqa.gqa_get_device_error() == 0
