@@ -47,6 +47,8 @@ def _bind(path: str):
     ci, cd = ctypes.c_int, ctypes.c_double
     lib.oracle_decode_attention.argtypes = [vp, vp, vp, i32p, cd, f64p, ci, ci, ci, ci, ci, ci, ci]
     lib.oracle_decode_attention.restype = ci
+    lib.oracle_decode_attention_multi.argtypes = [vp, vp, vp, i32p, cd, f64p, ci, ci, ci, ci, ci, ci, ci, ci]
+    lib.oracle_decode_attention_multi.restype = ci
     lib.oracle_softmax_weights.argtypes = [vp, vp, i32p, cd, ci, ci, ci, ci, ci, ci, ci, ci, f64p]
     lib.oracle_softmax_weights.restype = ci
     lib.oracle_kv_append.argtypes = [vp, vp, vp, vp, i32p, ci, ci, ci, ci, ci]
@@ -116,6 +118,24 @@ def decode_attention(q, k_cache, v_cache, seq_lens, scale, nthreads: int = 0) ->
                                          _dtype_code(q), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_decode_attention rejected its arguments")
+    return out
+
+
+def decode_attention_multi(q, k_cache, v_cache, seq_lens, scale, nthreads: int = 0) -> np.ndarray:
+    """out[b,t,h,:] in fp64 (numpy [B,T,H,d]) for q [B,T,H,d]: token t of
+    sequence b sits at position L_b - T + t and attends causally to
+    positions n < L_b - T + 1 + t."""
+    q, k, v = _cpu(q), _cpu(k_cache), _cpu(v_cache)
+    sl = _cpu(seq_lens).to(torch.int32)
+    B, T, H, d = q.shape
+    G, Nmax = k.shape[1], k.shape[2]
+    assert k.dtype == q.dtype == v.dtype and k.shape == v.shape == (B, G, Nmax, d)
+    out = np.zeros((B, T, H, d), dtype=np.float64)
+    rc = _load().oracle_decode_attention_multi(q.data_ptr(), k.data_ptr(), v.data_ptr(), _i32p(sl),
+                                               float(scale), _f64p(out), B, T, H, G, d, Nmax,
+                                               _dtype_code(q), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_decode_attention_multi rejected its arguments")
     return out
 
 

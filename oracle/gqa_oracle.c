@@ -26,6 +26,9 @@
  *    section "MQA 的推导" gives the shared-K/V (G = 1) form.
  *  - CSDN interview post on GQA, section 03: the key/value pair is repeated
  *    n_rep times, n_rep being the number of query heads sharing it.
+ *  - GQA paper, section 4: speculative sampling scores several proposed
+ *    tokens in one pass (oracle_decode_attention_multi; the causal rule among
+ *    the T new tokens is the plain reading of scoring a proposed run).
  */
 #include <math.h>
 #include <stdint.h>
@@ -119,6 +122,52 @@ int oracle_decode_attention(const void *q, const void *k, const void *v, const i
         for (int n = 0; n < L; ++n)
             for (int i = 0; i < d; ++i)
                 o[i] += w[n] * load_value(v, kv_off[bh] + (size_t)n * d + i, dtype);
+        free(w);
+    }
+    free(kv_off);
+    return fail ? -1 : 0;
+}
+
+/*
+ * Several new query tokens per sequence.  The GQA paper, section 4 (related
+ * work), notes that speculative sampling eases the bandwidth bound by having
+ * a small model propose several tokens that the large model then scores in
+ * one parallel pass; that pass is this call.  q [B,T,H,d] holds the
+ * queries of the last T cached positions, token t at position L_b - T + t,
+ * and token t attends causally to the positions it may see,
+ *   n < L_b - T + 1 + t   (clamped to [0, L_b]),
+ * with the same grouped softmax as oracle_decode_attention.  A token that
+ * sees no position gets out = 0.  out [B,T,H,d] fp64.
+ */
+int oracle_decode_attention_multi(const void *q, const void *k, const void *v, const int32_t *seq_lens,
+                                  double scale, double *out, int B, int T, int H, int G, int d, int Nmax,
+                                  int dtype, int nthreads) {
+    if (B <= 0 || T <= 0 || H <= 0 || G <= 0 || d <= 0 || Nmax <= 0 || H % G != 0) return -1;
+    size_t *kv_off = repeat_kv_offsets(B, H, G, d, Nmax);
+    if (!kv_off) return -1;
+    int fail = 0;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : fail)
+#endif
+    for (long bth = 0; bth < (long)B * T * H; ++bth) {
+        int b = (int)(bth / ((long)T * H));
+        int t = (int)((bth / H) % T);
+        int h = (int)(bth % H);
+        int L = clamp_len(seq_lens[b], Nmax);
+        int vis = L - T + 1 + t;
+        if (vis < 0) vis = 0;
+        if (vis > L) vis = L;
+        double *o = out + (size_t)bth * d;
+        for (int i = 0; i < d; ++i) o[i] = 0.0;
+        if (vis == 0) continue;
+        double *w = (double *)malloc((size_t)vis * sizeof(double));
+        if (!w) { fail |= 1; continue; }
+        size_t kvo = kv_off[(size_t)b * H + h];
+        head_weights(q, k, (size_t)bth * d, kvo, vis, d, scale, dtype, w);
+        for (int n = 0; n < vis; ++n)
+            for (int i = 0; i < d; ++i)
+                o[i] += w[n] * load_value(v, kvo + (size_t)n * d + i, dtype);
         free(w);
     }
     free(kv_off);

@@ -289,3 +289,61 @@ def test_meanpool_is_the_group_mean_of_projections():
     per_head = np.einsum("hdD,D->hd", w.double().numpy(), x)
     for g in range(G):
         np.testing.assert_allclose(pooled[g] @ x, per_head[g * 4:(g + 1) * 4].mean(0), rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------------- several query tokens
+def test_multi_token_single_token_is_the_decode_oracle():
+    """T = 1 is the single-token step (checked against the independent
+    grouped-einsum oracle)."""
+    q, k, v, sl = _rand_case(3, 8, 2, 16, 30, [30, 1, 17], seed=30)
+    out = oracle.decode_attention_multi(q.unsqueeze(1), k, v, sl, 0.25)
+    ref = decode_attention_grouped(q.double().numpy(), k.double().numpy(), v.double().numpy(), sl.numpy(), 0.25)
+    np.testing.assert_allclose(out[:, 0], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_multi_token_is_causal_prefix_attention():
+    """Token t of a run of T equals single-token attention over the
+    L - T + 1 + t positions it may see (library SDPA in fp64, an independent
+    implementation)."""
+    B, T, H, G, d, N = 2, 4, 8, 2, 16, 20
+    g = torch.Generator().manual_seed(31)
+    q = torch.randn(B, T, H, d, generator=g)
+    k = torch.randn(B, G, N, d, generator=g)
+    v = torch.randn(B, G, N, d, generator=g)
+    sl = torch.tensor([20, 9], dtype=torch.int32)
+    out = oracle.decode_attention_multi(q, k, v, sl, 0.3)
+    for t in range(T):
+        vis = torch.clamp(sl - T + 1 + t, min=0)
+        ref = _sdpa_reference(q[:, t], k, v, vis, 0.3)
+        np.testing.assert_allclose(out[:, t], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_multi_token_sees_nothing_before_the_cache():
+    """With L < T the earliest tokens see no position and give 0."""
+    q, k, v, _ = _rand_case(1, 4, 4, 8, 10, [2], seed=32)
+    q = q.unsqueeze(1).repeat(1, 5, 1, 1)
+    out = oracle.decode_attention_multi(q, k, v, torch.tensor([2], dtype=torch.int32), 0.5)
+    assert np.all(out[0, :3] == 0)                          # tokens 0..2 see nothing
+    np.testing.assert_array_equal(out[0, 3], v[0, :, 0].double().numpy()[np.arange(4) // 1])  # sees row 0 only
+
+
+def test_multi_token_brute_force():
+    import mpmath
+    mpmath.mp.dps = 40
+    B, T, H, G, d, N = 1, 3, 4, 2, 3, 6
+    g = torch.Generator().manual_seed(33)
+    q = torch.randn(B, T, H, d, generator=g)
+    k = torch.randn(B, G, N, d, generator=g)
+    v = torch.randn(B, G, N, d, generator=g)
+    L = 5
+    out = oracle.decode_attention_multi(q, k, v, torch.tensor([L], dtype=torch.int32), 0.7)
+    for t in range(T):
+        vis = L - T + 1 + t
+        for h in range(H):
+            gg = h // (H // G)
+            e = [mpmath.exp(0.7 * mpmath.fsum(mpmath.mpf(float(q[0, t, h, i])) * mpmath.mpf(float(k[0, gg, n, i]))
+                                               for i in range(d))) for n in range(vis)]
+            z = mpmath.fsum(e)
+            for i in range(d):
+                ref = mpmath.fsum(e[n] * mpmath.mpf(float(v[0, gg, n, i])) for n in range(vis)) / z
+                assert abs(out[0, t, h, i] - float(ref)) < 1e-14
