@@ -344,6 +344,51 @@ def time_attention_only(w: workloads.Workload, device, iters: int, warm: int, l2
     return row
 
 
+def time_multi(w: workloads.Workload, device, iters: int, warm: int, l2_bytes: int, mem_budget: int):
+    """Table row of a several-token workload (w.tokens query tokens per
+    sequence, one gqa_decode_attention_multi_ex call): device time per call
+    from CUDA-graph replays over rotating cache copies, the algorithmic bytes
+    (cache once, q and out of every token) and query tokens per second."""
+    import grouped_query_decode_kv_b300 as gqa
+    T = w.tokens
+    copies = copies_for(w, l2_bytes, mem_budget)
+    dt = w.torch_dtype
+    lens = workloads.make_seq_lens(w)
+    g = torch.Generator(device=device).manual_seed(1000 + w.index + 17)
+    k = [torch.randn(w.B, w.G, w.Nmax, w.d, generator=g, device=device).to(dt) for _ in range(copies)]
+    v = [torch.randn(w.B, w.G, w.Nmax, w.d, generator=g, device=device).to(dt) for _ in range(copies)]
+    q = [torch.randn(w.B, T, w.H, w.d, generator=g, device=device).to(dt) for _ in range(copies)]
+    out = [torch.empty(w.B, T, w.H, w.d, dtype=dt, device=device) for _ in range(copies)]
+    sl = lens.to(device)
+    need = gqa.gqa_decode_workspace_bytes_ex(w.B, T * w.H, w.G, w.d, w.Nmax, dt, 0)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+
+    def seq():
+        for i in range(iters):
+            c = i % copies
+            gqa.gqa_decode_attention_multi_ex(q[c], k[c], v[c], sl, w.scale, out[c], 0, ws)
+        return iters
+
+    for i in range(warm):
+        c = i % copies
+        gqa.gqa_decode_attention_multi_ex(q[c], k[c], v[c], sl, w.scale, out[c], 0, ws)
+    us = _graph_time(seq)
+    err = gqa.gqa_get_device_error()
+    lens_l = lens.tolist()
+    abytes = cost.decode_attention_bytes(lens_l, w.H, w.G, w.d, w.elt, tokens=T)
+    peak, _ = hbm_peak()
+    row = {
+        "B": w.B, "T": T, "H": w.H, "G": w.G, "d": w.d, "Nmax": w.Nmax, "dtype": w.dtype, "sum_L": int(sum(lens_l)),
+        "us": round(us, 2), "bytes": abytes, "gbs": round(abytes / us / 1e3, 1),
+        "frac_measured": round(abytes / us / 1e3 / peak, 3),
+        "tflops": round(cost.decode_attention_flops(lens_l, w.H, w.d, tokens=T) / us / 1e6, 1),
+        "query_tokens_per_s": round(w.B * T / us * 1e6, 1), "copies": copies, "device_error": err,
+    }
+    del k, v, q, out, ws
+    torch.cuda.empty_cache()
+    return row
+
+
 def read_ceiling(device) -> float:
     """Read-only streaming ceiling (library reduction over 4 GiB), GB/s."""
     x = torch.ones(2 ** 31, dtype=torch.bfloat16, device=device)
@@ -547,6 +592,7 @@ def run_ours(args, world, rank, local):
 
     # ---- per-workload table and the read-only ceiling (rank 0 only)
     table = None
+    table_multi = None
     ceiling = None
     del st
     torch.cuda.empty_cache()
@@ -555,6 +601,9 @@ def run_ours(args, world, rank, local):
         table = {}
         for name in TABLE_WORKLOADS:
             table[name] = time_attention_only(workloads.workload(name), device, args.table_iters, 5, l2, mem_budget)
+        table_multi = {}
+        for name in workloads.multi_names():
+            table_multi[name] = time_multi(workloads.workload(name), device, args.table_iters, 5, l2, mem_budget)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -618,6 +667,7 @@ def run_ours(args, world, rank, local):
         "device_error": dev_err,
         "read_ceiling_gbs": ceiling,
         "table": table,
+        "table_multi_token": table_multi,
     }
     print(json.dumps(line), flush=True)
     return 0

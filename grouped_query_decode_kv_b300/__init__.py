@@ -15,6 +15,8 @@ Entry points (see ``include/gqa.h`` for the full contract):
   gqa_decode_attention_noalloc(...)              no allocation: fixed in-library scratch
   gqa_decode_step(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out)
   gqa_decode_step_ws(..., workspace)             append + attention in one launch
+  gqa_decode_attention_multi(q[B,T,H,d], ..., out[B,T,H,d])   T query tokens per sequence
+  gqa_decode_attention_multi_ex(..., split_tokens, workspace)
   kv_append(k_new, v_new, k_cache, v_cache, seq_lens)
   mha_to_gqa_meanpool(w, w_out)
   gqa_get_device_error()
@@ -38,6 +40,7 @@ __all__ = [
     "mha_to_gqa_meanpool", "gqa_get_device_error", "gqa_status_string",
     "gqa_decode_attention_noalloc", "NOALLOC_SCRATCH_BYTES", "ERR_SCRATCH_LIMIT",
     "gqa_decode_step", "gqa_decode_step_ws",
+    "gqa_decode_attention_multi", "gqa_decode_attention_multi_ex",
     "DEVERR_ATTN_LEN", "DEVERR_APPEND_LEN", "DEVERR_TIMEOUT", "EXPORTED_SYMBOLS",
 ]
 
@@ -51,6 +54,7 @@ EXPORTED_SYMBOLS = (
     "gqa_decode_workspace_bytes_ex", "gqa_decode_attention_ex", "kv_append",
     "mha_to_gqa_meanpool", "gqa_get_device_error", "gqa_status_string",
     "gqa_decode_attention_noalloc", "gqa_decode_step", "gqa_decode_step_ws",
+    "gqa_decode_attention_multi", "gqa_decode_attention_multi_ex",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -90,8 +94,12 @@ def load_library():
         lib.gqa_decode_step.restype = ci
         lib.gqa_decode_step_ws.argtypes = step + [vp, sz, vp]
         lib.gqa_decode_step_ws.restype = ci
+        multi = [vp, vp, vp, vp, cf, vp, ci, ci, ci, ci, ci, ci, ci]
+        lib.gqa_decode_attention_multi.argtypes = multi + [vp]
+        lib.gqa_decode_attention_multi_ex.argtypes = multi + [ci, vp, sz, vp]
         for f in ("gqa_decode_attention", "gqa_decode_attention_ws", "gqa_decode_attention_ex",
-                  "gqa_decode_attention_noalloc"):
+                  "gqa_decode_attention_noalloc", "gqa_decode_attention_multi",
+                  "gqa_decode_attention_multi_ex"):
             getattr(lib, f).restype = ci
         lib.gqa_decode_workspace_bytes.argtypes = [ci] * 6
         lib.gqa_decode_workspace_bytes.restype = sz
@@ -223,6 +231,42 @@ def gqa_decode_attention_noalloc(q, k_cache, v_cache, seq_lens, scale, out, stre
     _check("gqa_decode_attention_noalloc",
            lib.gqa_decode_attention_noalloc(*_attn_args(q, k_cache, v_cache, seq_lens, scale, out),
                                             _stream(q, stream)))
+    return out
+
+
+def _multi_args(q, k_cache, v_cache, seq_lens, scale, out):
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, d]")
+    B, T, H, d = q.shape
+    if tuple(out.shape) != (B, T, H, d):
+        raise ValueError("out must be [B, T, H, d]")
+    # the per-token view [B, H, d] checks the caches, lengths and dtypes
+    _attn_shapes(q[:, 0], k_cache, v_cache, seq_lens, out[:, 0])
+    G, Nmax = k_cache.shape[1], k_cache.shape[2]
+    return [_dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _dev(seq_lens, "seq_lens"),
+            float(scale), _dev(out, "out"), B, T, H, G, d, Nmax, _dtype_code(q)]
+
+
+def gqa_decode_attention_multi(q, k_cache, v_cache, seq_lens, scale, out, stream=None):
+    """T query tokens per sequence (q, out [B,T,H,d]) whose K/V rows are the
+    last T of the cache: token t attends to positions n < seq_lens[b]-T+1+t.
+    Workspace from the stream-ordered allocator."""
+    lib = load_library()
+    _check("gqa_decode_attention_multi",
+           lib.gqa_decode_attention_multi(*_multi_args(q, k_cache, v_cache, seq_lens, scale, out),
+                                          _stream(q, stream)))
+    return out
+
+
+def gqa_decode_attention_multi_ex(q, k_cache, v_cache, seq_lens, scale, out, split_tokens, workspace, stream=None):
+    """As gqa_decode_attention_multi with a caller-owned workspace of
+    gqa_decode_workspace_bytes_ex(B, T*H, G, d, Nmax, dtype, split_tokens)
+    bytes and the positions per split forced (0 = automatic)."""
+    lib = load_library()
+    wp, wn = _ws(workspace)
+    _check("gqa_decode_attention_multi_ex",
+           lib.gqa_decode_attention_multi_ex(*_multi_args(q, k_cache, v_cache, seq_lens, scale, out),
+                                             int(split_tokens), wp, wn, _stream(q, stream)))
     return out
 
 

@@ -34,18 +34,25 @@ def cache_ratio(H: int, G: int) -> int:
     return H // G
 
 
-def decode_attention_bytes(seq_lens: Iterable[int], H: int, G: int, d: int, elt: int) -> int:
+def decode_attention_bytes(seq_lens: Iterable[int], H: int, G: int, d: int, elt: int, tokens: int = 1) -> int:
     """Algorithmic HBM bytes of one decode-attention call: every cached K and V
-    row of every sequence read once, q read once and out written once."""
+    row of every sequence read once, q read once and out written once (with
+    ``tokens`` query tokens per sequence, q and out hold tokens * H rows per
+    sequence; the cache is still read once)."""
     lens = [int(x) for x in seq_lens]
     B = len(lens)
-    return 2 * G * sum(lens) * d * elt + 2 * B * H * d * elt
+    return 2 * G * sum(lens) * d * elt + 2 * B * tokens * H * d * elt
 
 
-def decode_attention_flops(seq_lens: Iterable[int], H: int, d: int) -> int:
+def decode_attention_flops(seq_lens: Iterable[int], H: int, d: int, tokens: int = 1) -> int:
     """Flops of one decode-attention call: q.K and weights.V, 2*d flops per
-    (head, position) each."""
-    return 4 * H * d * sum(int(x) for x in seq_lens)
+    (head, visible position) each.  With several tokens, token t of a run of
+    T sees min(L, L - T + 1 + t) positions."""
+    vis = 0
+    for x in seq_lens:
+        L = int(x)
+        vis += sum(max(0, min(L, L - tokens + 1 + t)) for t in range(tokens))
+    return 4 * H * d * vis
 
 
 def kv_append_bytes(B: int, G: int, d: int, elt: int) -> int:

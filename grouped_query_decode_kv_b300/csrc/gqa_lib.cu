@@ -336,9 +336,11 @@ struct StepAppend {
   int32_t *seq_lens = nullptr;
 };
 
+// `tokens` query tokens per sequence: q and out are [B, tokens, H, d] and the
+// plan was made for tokens * H query rows.
 int run_attention(const void *q, const void *k, const void *v, const int32_t *sl, float scale, void *out, int B,
                   int H, int G, int d, int Nmax, gqa_dtype_t dt, const Plan &pl, void *ws, cudaStream_t st,
-                  const StepAppend &app = StepAppend()) {
+                  const StepAppend &app = StepAppend(), int tokens = 1) {
   CUtensorMap mk, mv;
   if (!encode_cache_map(&mk, k, dt, d, Nmax, B * G, pl.k.block_n, pl.k.box_elems) ||
       !encode_cache_map(&mv, v, dt, d, Nmax, B * G, pl.k.block_n, pl.k.box_elems))
@@ -369,18 +371,21 @@ int run_attention(const void *q, const void *k, const void *v, const int32_t *sl
   p.done_cnt = split ? reinterpret_cast<unsigned *>(w + step_counter_offset(pl, d)) : nullptr;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.B = B;
-  p.H = H;
+  p.H = tokens * H;
   p.G = G;
   p.Nmax = Nmax;
-  p.n_rep = H / G;
+  p.n_rep = tokens * (H / G);
   p.heads_per_cta = pl.heads;
   p.head_chunks = pl.head_chunks;
+  p.tokens = tokens;
+  p.heads_q = H;
+  p.rep_kv = H / G;
   if (pl.k.launch(dim3(pl.P), mk, mv, p, st) != cudaSuccess) {
     cudaGetLastError();
     return GQA_ERR_CUDA;
   }
   if (split && !merge_in_kernel) {
-    const dim3 blocks(ceil_div((long long)B * H, 4));
+    const dim3 blocks(ceil_div((long long)B * p.H, 4));
     cudaError_t e;
     if (dt == GQA_BF16)
       e = d == 128 ? launch_pdl(gqa_combine_kernel<__nv_bfloat16, 128>, blocks, dim3(128), 0, st, p)
@@ -555,6 +560,51 @@ int gqa_decode_attention_noalloc(const void *q, const void *k_cache, const void 
     if (int rc = noalloc_scratch(&ws)) return rc;
   }
   return run_attention(q, k_cache, v_cache, seq_lens, scale, out, B, H, G, d, Nmax, dtype, pl, ws, stream);
+}
+
+namespace {
+// Arguments of the several-token calls; the plan is the one for T * H query
+// rows per sequence.
+int check_multi_args(const void *q, const void *k, const void *v, const int32_t *sl, const void *out, int B, int T,
+                     int H, int G, int d, int Nmax, gqa_dtype_t dt) {
+  if (T <= 0) return GQA_ERR_INVALID_ARG;
+  if (int rc = check_attention_args(q, k, v, sl, out, B, H, G, d, Nmax, dt)) return rc;
+  if ((long long)T * H > (1 << 20)) return GQA_ERR_UNSUPPORTED;
+  return GQA_OK;
+}
+}  // namespace
+
+int gqa_decode_attention_multi_ex(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
+                                  float scale, void *out, int B, int T, int H, int G, int d, int Nmax,
+                                  gqa_dtype_t dtype, int split_tokens, void *workspace, size_t workspace_bytes,
+                                  cudaStream_t stream) {
+  if (int rc = check_multi_args(q, k_cache, v_cache, seq_lens, out, B, T, H, G, d, Nmax, dtype)) return rc;
+  if (split_tokens < 0) return GQA_ERR_INVALID_ARG;
+  const Plan pl = make_plan(B, T * H, G, d, Nmax, dtype, split_tokens);
+  if (!plan_fits(pl, B, G)) return GQA_ERR_UNSUPPORTED;
+  const size_t need = workspace_for(pl, B, T * H, d);
+  if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+    return GQA_ERR_INVALID_ARG;
+  return run_attention(q, k_cache, v_cache, seq_lens, scale, out, B, H, G, d, Nmax, dtype, pl, workspace, stream,
+                       StepAppend(), T);
+}
+
+int gqa_decode_attention_multi(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
+                               float scale, void *out, int B, int T, int H, int G, int d, int Nmax, gqa_dtype_t dtype,
+                               cudaStream_t stream) {
+  if (int rc = check_multi_args(q, k_cache, v_cache, seq_lens, out, B, T, H, G, d, Nmax, dtype)) return rc;
+  const Plan pl = make_plan(B, T * H, G, d, Nmax, dtype, 0);
+  if (!plan_fits(pl, B, G)) return GQA_ERR_UNSUPPORTED;
+  const size_t need = workspace_for(pl, B, T * H, d);
+  void *ws = nullptr;
+  if (need > 0 && cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GQA_ERR_NO_MEMORY;
+  }
+  int rc = run_attention(q, k_cache, v_cache, seq_lens, scale, out, B, H, G, d, Nmax, dtype, pl, ws, stream,
+                         StepAppend(), T);
+  if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && rc == GQA_OK) rc = GQA_ERR_CUDA;
+  return rc;
 }
 
 int kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache, int32_t *seq_lens, int B, int G,

@@ -93,8 +93,8 @@ __device__ __forceinline__ void finish_split_unit(const SplitParams &p, const Se
       a2 += w * o.z;
       a3 += w * o.w;
     }
-    const float inv = 1.f / L;
-    T *dst = reinterpret_cast<T *>(p.out) + ((size_t)b * p.H + h_first + h) * D + d0;
+    const float inv = L > 0.f ? 1.f / L : 0.f;  // 0: a query row that sees no position
+    T *dst = reinterpret_cast<T *>(p.out) + query_row(p, b, h_first + h) * D + d0;
     dst[0] = from_float<T>(a0 * inv);
     dst[1] = from_float<T>(a1 * inv);
     dst[2] = from_float<T>(a2 * inv);
@@ -190,8 +190,8 @@ __global__ void __launch_bounds__(128) gqa_combine_kernel(const SplitParams p) {
       acc[1] += w * v.y;
     }
   }
-  const float inv = 1.f / l;
-  T *o = reinterpret_cast<T *>(p.out) + (size_t)bh * D + lane * PER_LANE;
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  T *o = reinterpret_cast<T *>(p.out) + query_row(p, b, h) * D + lane * PER_LANE;
 #pragma unroll
   for (int e = 0; e < PER_LANE; ++e) o[e] = from_float<T>(acc[e] * inv);
 }

@@ -33,6 +33,32 @@ struct SplitParams {
   int n_rep;                // H / G
   int heads_per_cta;
   int head_chunks;          // HC = ceil(n_rep / heads_per_cta)
+  // Several query tokens per sequence (tokens > 1): q and out are
+  // [B, tokens, heads_q, D] and token t sits at cached position
+  // L_b - tokens + t, seeing positions n < L_b - (tokens - 1 - t).  The
+  // kernels then treat the tokens * heads_q query rows of a sequence as its
+  // "heads": H = tokens * heads_q and n_rep = tokens * rep_kv rows per KV
+  // head, row v of group g being token (v - g*n_rep) / rep_kv, head
+  // g*rep_kv + (v - g*n_rep) % rep_kv.  With tokens = 1 this is the plain
+  // [B, H, D] layout.
+  int tokens;
+  int heads_q;              // query heads of one token
+  int rep_kv;               // query heads of one token per KV head
 };
+
+// Row (of D elements) of q and out that holds query row v of batch row b.
+__device__ __forceinline__ size_t query_row(const SplitParams &p, int b, int v) {
+  if (p.tokens == 1) return (size_t)b * p.H + v;
+  const int g = v / p.n_rep, r = v - g * p.n_rep;
+  const int t = r / p.rep_kv;
+  return ((size_t)b * p.tokens + t) * p.heads_q + g * p.rep_kv + (r - t * p.rep_kv);
+}
+
+// Cached positions at the end of the sequence that query row v may not see
+// (the later tokens of its own run): tokens - 1 - t.  0 with one token.
+__device__ __forceinline__ int query_lag(const SplitParams &p, int v) {
+  if (p.tokens == 1) return 0;
+  return p.tokens - 1 - (v % p.n_rep) / p.rep_kv;
+}
 
 }  // namespace gqa

@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
         for (int half = 0; half < 2; ++half) {
           const int hl = wh * 16 * MFW + mf * 16 + gq + 8 * half;
           const bool ok = hl < nh;
-          const size_t row = ((size_t)b * p.H + h_first + (ok ? hl : 0)) * (D / 2);
+          const size_t row = query_row(p, b, h_first + (ok ? hl : 0)) * (D / 2);
 #pragma unroll
           for (int ks = 0; ks < KS; ++ks) {
             qa[mf][ks][half] = ok ? __ldg(q32 + row + ks * 8 + tq) : 0u;
@@ -136,6 +136,18 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
           }
         }
     }
+
+    // positions n < lim of each of this thread's rows are visible to it
+    // (L, less the later tokens of the row's own run)
+    int lim[MFW][2];
+#pragma unroll
+    for (int mf = 0; mf < MFW; ++mf)
+#pragma unroll
+      for (int rh = 0; rh < 2; ++rh) {
+        const int hl = wh * 16 * MFW + mf * 16 + gq + 8 * rh;
+        lim[mf][rh] = L - query_lag(p, h_first + (hl < nh ? hl : 0));
+      }
+    const int L_all = L - (p.tokens - 1);  // positions below this are visible to every row
 
     float o[MFW][NF][4];
     float m_run[MFW][2], l_run[MFW][2];
@@ -156,7 +168,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
       const uint32_t kt = pipe.k_tile(st), vt = pipe.v_tile(st);
       const int n0 = t * C::BLOCK_N;
       const int end = min(n0 + C::BLOCK_N, L);
-      const bool tail = n0 + C::BLOCK_N > end;
+      const bool tail = n0 + C::BLOCK_N > L_all;
 #pragma unroll
       for (int sub = 0; sub < C::SUB; ++sub) {
         const int r0 = wn * C::ROWS_PER_WARP + sub * 16;  // first row of this sub-tile in the stage
@@ -196,7 +208,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
           }
         }
 
-        // scale to log2 units, mask positions outside [n0, end), row max
+        // scale to log2 units, mask positions a row may not see, row max
         float tmax[MFW][2];
 #pragma unroll
         for (int mf = 0; mf < MFW; ++mf) {
@@ -208,7 +220,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
               float x = sacc[mf][nf][e] * p.scale_log2;
               if (tail) {
                 const int tok = tok0 + nf * 8 + 2 * tq + (e & 1);
-                x = tok < end ? x : -INFINITY;
+                x = tok < lim[mf][e >> 1] ? x : -INFINITY;
               }
               sacc[mf][nf][e] = x;
               tmax[mf][e >> 1] = fmaxf(tmax[mf][e >> 1], x);
@@ -352,14 +364,14 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
       const float4 a = *reinterpret_cast<const float4 *>(src);
       const float4 c = *reinterpret_cast<const float4 *>(src + 4);
       if (whole) {
-        const float inv = 1.f / fin_s[hl].y;
+        const float inv = fin_s[hl].y > 0.f ? 1.f / fin_s[hl].y : 0.f;
         uint4 pk;
         pk.x = pack_bf16x2(a.x * inv, a.y * inv);
         pk.y = pack_bf16x2(a.z * inv, a.w * inv);
         pk.z = pack_bf16x2(c.x * inv, c.y * inv);
         pk.w = pack_bf16x2(c.z * inv, c.w * inv);
         *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) +
-                                   ((size_t)b * p.H + h_first + hl) * D + d0) = pk;
+                                   query_row(p, b, h_first + hl) * D + d0) = pk;
       } else {
         float *dst = p.o_part + ((size_t)slot * p.heads_per_cta + hl) * D + d0;
         *reinterpret_cast<float4 *>(dst) = a;

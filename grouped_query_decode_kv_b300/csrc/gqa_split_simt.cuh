@@ -150,10 +150,12 @@ __global__ void __launch_bounds__(C::THREADS)
 
     // this lane's slice of q: element e of box bx is d = bx*BOX_ELEMS + j*EPC + e
     float qf[NH][EPL];
+    int lim[NH];  // positions n < lim[h] are visible to row h
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
       const int hh = h_first + (h < nh ? h : 0);
-      const T *qrow = reinterpret_cast<const T *>(p.q) + ((size_t)b * p.H + hh) * D;
+      lim[h] = L - query_lag(p, hh);
+      const T *qrow = reinterpret_cast<const T *>(p.q) + query_row(p, b, hh) * D;
 #pragma unroll
       for (int bx = 0; bx < NBOX; ++bx) {
         const uint4 c = __ldg(reinterpret_cast<const uint4 *>(qrow + bx * C::BOX_ELEMS + j * EPC));
@@ -207,6 +209,7 @@ __global__ void __launch_bounds__(C::THREADS)
             widen_chunk<T>(lds128(swz128(vt + bx * Pipe::BOX_BYTES, row, j)), &vf[bx * EPC]);
 #pragma unroll
           for (int h = 0; h < NH; ++h) {
+            if (tok >= lim[h]) continue;  // a later token of row h's own run
             if (x[h] > m_run[h]) {
               const float corr = merge_weight(m_run[h], x[h]);
               m_run[h] = x[h];
@@ -294,9 +297,9 @@ __global__ void __launch_bounds__(C::THREADS)
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
         if (h >= nh) break;
-        const size_t bh = (size_t)b * p.H + h_first + h;
+        const size_t bh = query_row(p, b, h_first + h);
         if (whole) {
-          const float inv = 1.f / l_run[h];
+          const float inv = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
           T *orow = reinterpret_cast<T *>(p.out) + bh * D;
 #pragma unroll
           for (int bx = 0; bx < NBOX; ++bx) {

@@ -171,6 +171,12 @@ __device__ __forceinline__ void soft_reduce(float (&v)[C::NR], int sub, int lane
   soft_bar();
 }
 
+// Floor of the running max (log2 units): far below any logit, finite so
+// that 2^(x - floor) is 0 for x = -inf.  A partial left with it (a row with
+// no visible position in its segment) gets weight 0 in the merge unless every
+// partial of the row has it, and a row whose sum stays 0 is written as 0.
+constexpr float kNoMax = -1e30f;
+
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
     gqa_split_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -355,7 +361,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const bool real = row < nh;
         if (row < NR) {
         const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(p.q) +
-                                                           ((size_t)s.b * p.H + h_first + min(row, nh - 1)) * D +
+                                                           query_row(p, s.b, h_first + min(row, nh - 1)) * D +
                                                            half * 64);
         const uint32_t dst = qbase + half * C::Q_BOX + row * 128;
 #pragma unroll
@@ -390,16 +396,32 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         float lp[NR];
 #pragma unroll
         for (int h = 0; h < NR; ++h) lp[h] = 0.f;
-        if (R < NQ) m_s[R] = -INFINITY;
+        // The running max starts at a finite floor rather than -inf, so that
+        // a row that has seen no visible position yet (a query token whose
+        // whole view lies in later tiles) gets 2^(-inf - floor) = 0, not NaN.
+        if (R < NQ) m_s[R] = kNoMax;
         soft_bar();
+        // Row h of the unit is query token t(h) = (row0 + h) / rep_kv of its
+        // run and sees positions n < L_all + t(h); positions below L_all are
+        // visible to every row.
+        const int L_all = L - (p.tokens - 1);
+        const int row0 = h_first % p.n_rep;
+        const int t_first = row0 / p.rep_kv, k_first = row0 % p.rep_kv;
         for (int i = 0; i < ntl; ++i) {
           const int tg = t + i, sb = tg & 1, st = tg % ST;
           const bool valid = (seg.t0 + i) * BN + R < L;
+          // a tile that reaches L_all needs the per-row limits; before it,
+          // every position is visible to every real row
+          const bool edge = (seg.t0 + i + 1) * BN > L_all;
+          const int pos = (seg.t0 + i) * BN + R;
           wait(bars.s_full(sb), (tg >> 1) & 1);
           tc::fence_after();
-          // this position's logits (log2 units), -inf past L and for padding heads
+          // this position's logits (log2 units); -inf where the row may not
+          // see it (past L, or a later token of the row's own run) and for
+          // padding rows
           float x[NR];
           auto load_s = [&]() {
+            int tk = t_first, kk = k_first;  // token of row h and its place in the token's run
 #pragma unroll
             for (int c0 = 0; c0 < NR; c0 += (NR < 32 ? NR : 32)) {
               uint32_t r[32];
@@ -412,7 +434,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
               for (int c = 0; c < (NR < 32 ? NR : 32); ++c) {
                 const int h = c0 + c;
-                x[h] = (valid && h < nh) ? __uint_as_float(r[c]) * p.scale_log2 : -INFINITY;
+                bool vis = h < nh;
+                if (edge) {
+                  vis = vis && pos < L_all + tk;
+                  if (++kk == p.rep_kv) {
+                    kk = 0;
+                    ++tk;
+                  }
+                }
+                x[h] = vis ? __uint_as_float(r[c]) * p.scale_log2 : -INFINITY;
               }
             }
           };
@@ -510,14 +540,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const bool next = cur.next(sp, nseg);
         if (next) load_q(nseg);
         // ---- epilogue: l[h] summed over the 128 positions' partials
-        const float mR = R < NQ ? m_s[R] : 0.f;
+        const float mR = R < NQ ? m_s[R] : 0.f;  // kNoMax when the row saw no position
         soft_reduce<C, false>(lp, sub, lane, red, fin, R);
         // O^T of this unit is final once the P.V of its last tile landed
         wait(bars.pv_done((t - 1) % C::PB), ((t - 1) / C::PB) & 1);
         tc::fence_after();
         const bool whole = seg.t0 == 0 && seg.t1 == seg.tiles;
         const int slot = partial_slot(unit);
-        const size_t bh0 = (size_t)b * p.H + h_first;
 #pragma unroll
         for (int c0 = 0; c0 < NR; c0 += (NR < 32 ? NR : 32)) {
           uint32_t r[32];
@@ -533,7 +562,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (h < nh) {
               const float o = __uint_as_float(r[c]);
               if (whole)
-                reinterpret_cast<__nv_bfloat16 *>(p.out)[(bh0 + h) * D + R] = __float2bfloat16_rn(o / fin[h]);
+                reinterpret_cast<__nv_bfloat16 *>(p.out)[query_row(p, b, h_first + h) * D + R] =
+                    __float2bfloat16_rn(fin[h] > 0.f ? o / fin[h] : 0.f);
               else
                 p.o_part[((size_t)slot * p.heads_per_cta + h) * D + R] = o;
             }

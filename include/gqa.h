@@ -195,6 +195,42 @@ int gqa_decode_attention_noalloc(const void *q, const void *k_cache, const void 
                                  cudaStream_t stream);
 
 /*
+ * gqa_decode_attention_multi — attention of T new query tokens per sequence
+ * in one pass, as when a large model scores a run of T tokens proposed by a
+ * smaller one (speculative sampling: GQA paper, section 4, related work).
+ * The T tokens' K/V rows are already in the cache: token t sits at cached
+ * position L_b - T + t and attends to the positions up to and including its
+ * own,
+ *
+ *   out[b,t,h,:] = sum_{n < L_b-T+1+t} softmax_n( scale * <q[b,t,h,:], K[b,g,n,:]> ) * V[b,g,n,:]
+ *
+ * with g = h / (H/G).  A token that sees no position (L_b - T + 1 + t <= 0)
+ * gets out = 0.  T = 1 is gqa_decode_attention exactly (bit for bit).
+ *
+ *   q   [B, T, H, d]   queries of the T tokens
+ *   out [B, T, H, d]   result, rounded to nearest even in `dtype`
+ *   k_cache, v_cache, seq_lens, scale, d, dtype, alignment and the length
+ *   errors as for gqa_decode_attention.  T >= 1 and T * H <= 2^20.
+ *
+ * Each K/V tile read from HBM serves all T * (H/G) query rows of its group,
+ * so the call reads the same bytes as a one-token call.
+ * gqa_decode_attention_multi takes its workspace from the stream-ordered
+ * allocator.  gqa_decode_attention_multi_ex takes it from the caller, with
+ * the grid choice of gqa_decode_attention_ex.  Its size is
+ * gqa_decode_workspace_bytes_ex(B, T * H, G, d, Nmax, dtype, split_tokens),
+ * 256-byte aligned, needing no initialisation.
+ */
+int gqa_decode_attention_multi(const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *seq_lens, float scale, void *out,
+                               int B, int T, int H, int G, int d, int Nmax, gqa_dtype_t dtype,
+                               cudaStream_t stream);
+int gqa_decode_attention_multi_ex(const void *q, const void *k_cache, const void *v_cache,
+                                  const int32_t *seq_lens, float scale, void *out,
+                                  int B, int T, int H, int G, int d, int Nmax, gqa_dtype_t dtype,
+                                  int split_tokens, void *workspace, size_t workspace_bytes,
+                                  cudaStream_t stream);
+
+/*
  * kv_append — the cache concatenation of one decode step (fogdragon's CSDN
  * blog, section "KV Cache": K = cat([K_prev, k]), V = cat([V_prev, v])).
  *

@@ -127,3 +127,23 @@ def test_binding_raises_without_cuda_tensors():
     k = torch.zeros(1, 2, 16, 64)
     with pytest.raises((ValueError, RuntimeError)):
         gqa.gqa_decode_attention(q, k, k, torch.zeros(1, dtype=torch.int32), 0.1, q.clone())
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=0), -1), (dict(T=-2), -1), (dict(q=0), -1), (dict(H=8, G=3), -1), (dict(d=96), -2),
+    (dict(T=1 << 18, H=8), -2), (dict(out=FAKE + 4), -1),
+])
+def test_multi_token_rejects_bad_arguments(lib, kw, status):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, sl=FAKE, out=FAKE, B=2, T=4, H=8, G=2, d=128, N=64, dt=1)
+    a.update(kw)
+    assert lib.gqa_decode_attention_multi(a["q"], a["k"], a["v"], a["sl"], 0.1, a["out"], a["B"], a["T"], a["H"],
+                                          a["G"], a["d"], a["N"], a["dt"], None) == status
+
+
+def test_multi_token_ex_rejects_missing_workspace(lib):
+    # the workspace of T tokens is the one of T * H query rows
+    need = lib.gqa_decode_workspace_bytes_ex(2, 4 * 8, 2, 128, 4096, 1, 256)
+    assert need > 0
+    args = (FAKE, FAKE, FAKE, FAKE, 0.1, FAKE, 2, 4, 8, 2, 128, 4096, 1, 256)
+    assert lib.gqa_decode_attention_multi_ex(*args, None, 0, None) == -1
+    assert lib.gqa_decode_attention_multi_ex(*args, FAKE, need - 1, None) == -1

@@ -30,6 +30,10 @@ PIN_BATTERY = [
     pins.test_meanpool_identity_when_groups_equal_heads,
     pins.test_meanpool_single_group_is_mean_of_all_heads,
     pins.test_meanpool_is_the_group_mean_of_projections,
+    pins.test_multi_token_single_token_is_the_decode_oracle,
+    pins.test_multi_token_is_causal_prefix_attention,
+    pins.test_multi_token_sees_nothing_before_the_cache,
+    pins.test_multi_token_brute_force,
 ]
 
 # (name, text in the oracle source, replacement)
@@ -41,7 +45,12 @@ MUTANTS = [
     ("reads one position past L", "int b = (int)(bh / H);\n        int L = clamp_len(seq_lens[b], Nmax);",
      "int b = (int)(bh / H);\n        int L = clamp_len(seq_lens[b] + 1, Nmax);"),
     ("softmax not normalised", "for (int n = 0; n < L; ++n) w[n] /= z;", "(void)z;"),
-    ("K used in place of V", "o[i] += w[n] * load_value(v,", "o[i] += w[n] * load_value(k,"),
+    ("K used in place of V", "o[i] += w[n] * load_value(v, kv_off[bh]", "o[i] += w[n] * load_value(k, kv_off[bh]"),
+    ("several tokens: a token also sees the next one", "int vis = L - T + 1 + t;", "int vis = L - T + 2 + t;"),
+    ("several tokens: views in reverse token order", "int vis = L - T + 1 + t;", "int vis = L - t;"),
+    ("several tokens: every token reads token 0's query", "head_weights(q, k, (size_t)bth * d,",
+     "head_weights(q, k, ((size_t)b * T * H + h) * d,"),
+    ("several tokens: K used in place of V", "o[i] += w[n] * load_value(v, kvo", "o[i] += w[n] * load_value(k, kvo"),
     ("q read reversed", "load_value(q, q_off + i, dtype)", "load_value(q, q_off + (d - 1 - i), dtype)"),
     ("wrong sign of logits", "w[n] = dot * scale;", "w[n] = -dot * scale;"),
     ("meanpool sums instead of averaging", "w_out[(size_t)g * per_head + e] = s / n_rep;",

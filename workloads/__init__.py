@@ -19,6 +19,13 @@ whose datasets and checkpoints are not used):
 
 Config indices: the five listed workloads are 0..4 (the group-count sweep
 points use 500 + G and the long-context case 599).
+
+Several query tokens per sequence (``tokens`` = T > 1, the scoring pass of
+speculative sampling): q is drawn as one ``randn(B, T, H, d)`` in place of
+``randn(B, H, d)``, the rest as above.  The T tokens' K/V rows are the last
+T cached rows, so these workloads need L_b >= T only where every token
+should see something; shorter rows are the edge case of tokens that see
+nothing.  Indices 604 (gqa8_t4) and 614 (mha_t4).
 """
 from __future__ import annotations
 
@@ -27,7 +34,7 @@ from typing import Dict, Optional, Tuple
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "workload", "make_inputs", "sweep_names"]
+__all__ = ["Workload", "WORKLOADS", "workload", "make_inputs", "sweep_names", "multi_names"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -42,6 +49,7 @@ class Workload:
     lens: Tuple           # ("fixed", L) or ("uniform", lo, hi) inclusive
     index: int            # seed index
     description: str = ""
+    tokens: int = 1       # query tokens per sequence
 
     @property
     def n_rep(self) -> int:
@@ -83,6 +91,19 @@ for _g in SWEEP_G:
         f"group-count sweep B=32 H=64 G={_g} d=128 N=4096 bf16")
 
 
+WORKLOADS["gqa8_t4"] = dataclasses.replace(
+    WORKLOADS["gqa8"], name="gqa8_t4", index=604, tokens=4,
+    description="GQA-8 decode, 4 query tokens per sequence: B=16 T=4 H=64 G=8 d=128 Nmax=8192 "
+                "L~U[1,8192] bf16")
+WORKLOADS["mha_t4"] = dataclasses.replace(
+    WORKLOADS["mha"], name="mha_t4", index=614, tokens=4,
+    description="MHA decode, 4 query tokens per sequence: B=8 T=4 H=G=32 d=128 N=4096 bf16")
+
+
+def multi_names():
+    return ["gqa8_t4", "mha_t4"]
+
+
 def sweep_names():
     return [f"sweep_g{g}" for g in SWEEP_G]
 
@@ -104,13 +125,14 @@ def make_inputs(w: Workload, seq_lens: Optional[torch.Tensor] = None,
                 poison: bool = True) -> Dict[str, torch.Tensor]:
     """All inputs of one decode step, on the CPU, in the workload's dtype.
 
-    Returns q [B,H,d], k_cache / v_cache [B,G,Nmax,d], k_new / v_new [B,G,d]
-    and seq_lens [B] (int32).  With ``poison`` the cache rows at positions
-    >= L_b hold NaN.
+    Returns q [B,H,d] ([B,T,H,d] with T = w.tokens > 1), k_cache / v_cache
+    [B,G,Nmax,d], k_new / v_new [B,G,d] and seq_lens [B] (int32).  With
+    ``poison`` the cache rows at positions >= L_b hold NaN.
     """
     dt = w.torch_dtype
     g = torch.Generator().manual_seed(1000 + w.index)
-    q = torch.randn(w.B, w.H, w.d, generator=g).to(dt)
+    qshape = (w.B, w.H, w.d) if w.tokens == 1 else (w.B, w.tokens, w.H, w.d)
+    q = torch.randn(*qshape, generator=g).to(dt)
     k = torch.empty(w.B, w.G, w.Nmax, w.d, dtype=dt)
     v = torch.empty(w.B, w.G, w.Nmax, w.d, dtype=dt)
     for b in range(w.B):
