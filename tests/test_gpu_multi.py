@@ -44,12 +44,12 @@ def gpu_multi(x, scale, split_tokens=None):
     return out.double().cpu().numpy()
 
 
-def check_multi(w, seq_lens=None, split_tokens=None):
+def check_multi(w, seq_lens=None, split_tokens=None, expect_err=0):
     x = workloads.make_inputs(w, seq_lens=seq_lens)
     ref = oracle.decode_attention_multi(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], w.scale)
     got = gpu_multi(x, w.scale, split_tokens)
     assert_parity(got, ref, f"{w.name} T={w.tokens} split={split_tokens}")
-    assert gqa.gqa_get_device_error() == 0
+    assert gqa.gqa_get_device_error() == expect_err
     return got, ref
 
 
@@ -119,7 +119,7 @@ def test_last_token_equals_single_token_attention(H, G, T):
 def test_empty_rows_and_tokens_that_see_nothing_are_zero():
     w = _small(64, 8, 128, 300, "bf16", 4, 8500, B=4)
     lens = torch.tensor([0, 2, 3, 300], dtype=torch.int32)
-    got, _ = check_multi(w, lens)
+    got, _ = check_multi(w, lens, expect_err=gqa.DEVERR_ATTN_LEN)  # L = 0 is flagged, as for one token
     assert np.all(got[0] == 0)            # empty sequence
     assert np.all(got[1, :2] == 0)        # L = 2 < T = 4: tokens 0, 1 see nothing
     assert np.all(got[2, :1] == 0)
