@@ -66,26 +66,28 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
 
 enum Family { kSimt = 0, kMma = 1, kTc = 2 };
 
-template <class C, int F>
+// MULTI: the instantiation for several query tokens per sequence; the
+// one-token kernels are compiled without any of that code.
+template <class C, int F, bool MULTI>
 auto split_kernel_ptr() {
   if constexpr (F == kMma)
-    return &gqa_split_mma_kernel<C>;
+    return &gqa_split_mma_kernel<C, MULTI>;
   else if constexpr (F == kTc)
-    return &gqa_split_tc_kernel<C>;
+    return &gqa_split_tc_kernel<C, MULTI>;
   else
-    return &gqa_split_simt_kernel<C>;
+    return &gqa_split_simt_kernel<C, MULTI>;
 }
 
-template <class C, int F>
+template <class C, int F, bool MULTI>
 cudaError_t launch_split(dim3 grid, const CUtensorMap &k, const CUtensorMap &v, const SplitParams &p,
                          cudaStream_t st) {
-  return launch_pdl(split_kernel_ptr<C, F>(), grid, dim3(C::THREADS), C::SMEM_BYTES, st, k, v, p);
+  return launch_pdl(split_kernel_ptr<C, F, MULTI>(), grid, dim3(C::THREADS), C::SMEM_BYTES, st, k, v, p);
 }
 
-template <class C, int F>
+template <class C, int F, bool MULTI>
 KernelChoice make_choice() {
   KernelChoice c;
-  c.func = reinterpret_cast<const void *>(split_kernel_ptr<C, F>());
+  c.func = reinterpret_cast<const void *>(split_kernel_ptr<C, F, MULTI>());
   c.family = F;
   c.threads = C::THREADS;
   c.smem = C::SMEM_BYTES;
@@ -95,7 +97,7 @@ KernelChoice make_choice() {
     c.box_elems = C::BOX_ELEMS;
   else
     c.box_elems = 64;
-  c.launch = &launch_split<C, F>;
+  c.launch = &launch_split<C, F, MULTI>;
   return c;
 }
 
@@ -107,34 +109,35 @@ using TcD128x16 = TcCfg<16, 3, 2>;
 using TcD128x32 = TcCfg<32, 3, 2>;
 using TcD128x64 = TcCfg<64, 3, 1>;
 
+template <bool M>
 KernelChoice choose_kernel(gqa_dtype_t dt, int d, int n_rep) {
   if (dt == GQA_BF16) {
     if (d == 128) {
-      if (n_rep == 1) return make_choice<SimtFor<__nv_bfloat16, 128, 1>, kSimt>();
-      if (n_rep == 2) return make_choice<SimtFor<__nv_bfloat16, 128, 2>, kSimt>();
+      if (n_rep == 1) return make_choice<SimtFor<__nv_bfloat16, 128, 1>, kSimt, M>();
+      if (n_rep == 2) return make_choice<SimtFor<__nv_bfloat16, 128, 2>, kSimt, M>();
       if (n_rep >= kTcMinNrep) {
-        if (n_rep <= 16) return make_choice<TcD128x16, kTc>();
-        if (n_rep <= 32) return make_choice<TcD128x32, kTc>();
-        return make_choice<TcD128x64, kTc>();
+        if (n_rep <= 16) return make_choice<TcD128x16, kTc, M>();
+        if (n_rep <= 32) return make_choice<TcD128x32, kTc, M>();
+        return make_choice<TcD128x64, kTc, M>();
       }
-      if (n_rep <= 16) return make_choice<MmaD128x1, kMma>();
-      if (n_rep <= 32) return make_choice<MmaD128x2, kMma>();
-      return make_choice<MmaD128x4, kMma>();
+      if (n_rep <= 16) return make_choice<MmaD128x1, kMma, M>();
+      if (n_rep <= 32) return make_choice<MmaD128x2, kMma, M>();
+      return make_choice<MmaD128x4, kMma, M>();
     }
-    if (n_rep == 1) return make_choice<SimtFor<__nv_bfloat16, 64, 1>, kSimt>();
-    if (n_rep == 2) return make_choice<SimtFor<__nv_bfloat16, 64, 2>, kSimt>();
-    if (n_rep <= 16) return make_choice<MmaD64x1, kMma>();
-    if (n_rep <= 32) return make_choice<MmaD64x2, kMma>();
-    return make_choice<MmaD64x4, kMma>();
+    if (n_rep == 1) return make_choice<SimtFor<__nv_bfloat16, 64, 1>, kSimt, M>();
+    if (n_rep == 2) return make_choice<SimtFor<__nv_bfloat16, 64, 2>, kSimt, M>();
+    if (n_rep <= 16) return make_choice<MmaD64x1, kMma, M>();
+    if (n_rep <= 32) return make_choice<MmaD64x2, kMma, M>();
+    return make_choice<MmaD64x4, kMma, M>();
   }
   if (d == 128) {
-    if (n_rep == 1) return make_choice<SimtFor<float, 128, 1>, kSimt>();
-    if (n_rep == 2) return make_choice<SimtFor<float, 128, 2>, kSimt>();
-    return make_choice<SimtFor<float, 128, 4>, kSimt>();
+    if (n_rep == 1) return make_choice<SimtFor<float, 128, 1>, kSimt, M>();
+    if (n_rep == 2) return make_choice<SimtFor<float, 128, 2>, kSimt, M>();
+    return make_choice<SimtFor<float, 128, 4>, kSimt, M>();
   }
-  if (n_rep == 1) return make_choice<SimtFor<float, 64, 1>, kSimt>();
-  if (n_rep == 2) return make_choice<SimtFor<float, 64, 2>, kSimt>();
-  return make_choice<SimtFor<float, 64, 4>, kSimt>();
+  if (n_rep == 1) return make_choice<SimtFor<float, 64, 1>, kSimt, M>();
+  if (n_rep == 2) return make_choice<SimtFor<float, 64, 2>, kSimt, M>();
+  return make_choice<SimtFor<float, 64, 4>, kSimt, M>();
 }
 
 // ----------------------------------------------------------- split plan
@@ -205,10 +208,15 @@ int ctas_per_sm(const KernelChoice &kc) {
 // the lengths.  split_tokens > 0 instead asks for about that many positions
 // per CTA when every sequence is full (for tests of the merge and for
 // tuning).
-Plan make_plan(int B, int H, int G, int d, int Nmax, gqa_dtype_t dt, int split_tokens) {
+// `multi`: the plan of a several-token call (H counts its tokens * heads
+// query rows); it picks the kernels compiled for that case.
+Plan make_plan(int B, int H, int G, int d, int Nmax, gqa_dtype_t dt, int split_tokens, bool multi = false) {
   Plan pl;
   const int n_rep = H / G;
-  pl.k = choose_kernel(dt, d, n_rep);
+  // the grid (and so the workspace) is sized from the one-token kernel, so
+  // that both instantiations share gqa_decode_workspace_bytes_ex
+  const KernelChoice base = choose_kernel<false>(dt, d, n_rep);
+  pl.k = multi ? choose_kernel<true>(dt, d, n_rep) : base;
   // the tcgen05 kernel takes a group of up to 64 heads per unit (its MMA N);
   // the others have a fixed number of heads per CTA
   pl.heads = pl.k.family == kTc ? std::min(n_rep, pl.k.heads) : pl.k.heads;
@@ -220,7 +228,7 @@ Plan make_plan(int B, int H, int G, int d, int Nmax, gqa_dtype_t dt, int split_t
     const long long per_cta = std::max(1, ceil_div(split_tokens, pl.k.block_n));
     P = (tiles_full + per_cta - 1) / per_cta;
   } else {
-    P = (long long)device_sm_count() * ctas_per_sm(pl.k);
+    P = (long long)device_sm_count() * ctas_per_sm(base);
   }
   P = std::max<long long>(1, std::min<long long>(P, std::min<long long>(tiles_full, 1 << 20)));
   pl.P = (int)P;
@@ -580,7 +588,7 @@ int gqa_decode_attention_multi_ex(const void *q, const void *k_cache, const void
                                   cudaStream_t stream) {
   if (int rc = check_multi_args(q, k_cache, v_cache, seq_lens, out, B, T, H, G, d, Nmax, dtype)) return rc;
   if (split_tokens < 0) return GQA_ERR_INVALID_ARG;
-  const Plan pl = make_plan(B, T * H, G, d, Nmax, dtype, split_tokens);
+  const Plan pl = make_plan(B, T * H, G, d, Nmax, dtype, split_tokens, true);
   if (!plan_fits(pl, B, G)) return GQA_ERR_UNSUPPORTED;
   const size_t need = workspace_for(pl, B, T * H, d);
   if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
@@ -593,7 +601,7 @@ int gqa_decode_attention_multi(const void *q, const void *k_cache, const void *v
                                float scale, void *out, int B, int T, int H, int G, int d, int Nmax, gqa_dtype_t dtype,
                                cudaStream_t stream) {
   if (int rc = check_multi_args(q, k_cache, v_cache, seq_lens, out, B, T, H, G, d, Nmax, dtype)) return rc;
-  const Plan pl = make_plan(B, T * H, G, d, Nmax, dtype, 0);
+  const Plan pl = make_plan(B, T * H, G, d, Nmax, dtype, 0, true);
   if (!plan_fits(pl, B, G)) return GQA_ERR_UNSUPPORTED;
   const size_t need = workspace_for(pl, B, T * H, d);
   void *ws = nullptr;

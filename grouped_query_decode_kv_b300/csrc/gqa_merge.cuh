@@ -47,7 +47,7 @@ __device__ __forceinline__ unsigned arrive_unit(unsigned long long *cnt, unsigne
 // CTA's partial of a split unit (heads [h_first, h_first + nh) of batch row
 // b), after those writes; `bar` synchronises the group.  When this CTA is the
 // unit's last, the group merges all its partials into out.
-template <typename T, int D, class Bar>
+template <typename T, int D, bool MULTI, class Bar>
 __device__ __forceinline__ void finish_split_unit(const SplitParams &p, const Segment &seg, const CtaRange &range,
                                                   int b, int h_first, int nh, int tid, int nthr, UnitMerge *um,
                                                   Bar bar) {
@@ -93,8 +93,8 @@ __device__ __forceinline__ void finish_split_unit(const SplitParams &p, const Se
       a2 += w * o.z;
       a3 += w * o.w;
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;  // 0: a query row that sees no position
-    T *dst = reinterpret_cast<T *>(p.out) + query_row(p, b, h_first + h) * D + d0;
+    const float inv = (!MULTI || L > 0.f) ? 1.f / L : 0.f;  // 0: a query row that sees no position
+    T *dst = reinterpret_cast<T *>(p.out) + query_row<MULTI>(p, b, h_first + h) * D + d0;
     dst[0] = from_float<T>(a0 * inv);
     dst[1] = from_float<T>(a1 * inv);
     dst[2] = from_float<T>(a2 * inv);
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(128) gqa_combine_kernel(const SplitParams p) {
     }
   }
   const float inv = l > 0.f ? 1.f / l : 0.f;
-  T *o = reinterpret_cast<T *>(p.out) + query_row(p, b, h) * D + lane * PER_LANE;
+  T *o = reinterpret_cast<T *>(p.out) + query_row<true>(p, b, h) * D + lane * PER_LANE;
 #pragma unroll
   for (int e = 0; e < PER_LANE; ++e) o[e] = from_float<T>(acc[e] * inv);
 }

@@ -47,8 +47,10 @@ struct SplitParams {
 };
 
 // Row (of D elements) of q and out that holds query row v of batch row b.
+// MULTI = false: the kernel was compiled for one token per sequence.
+template <bool MULTI>
 __device__ __forceinline__ size_t query_row(const SplitParams &p, int b, int v) {
-  if (p.tokens == 1) return (size_t)b * p.H + v;
+  if (!MULTI || p.tokens == 1) return (size_t)b * p.H + v;
   const int g = v / p.n_rep, r = v - g * p.n_rep;
   const int t = r / p.rep_kv;
   return ((size_t)b * p.tokens + t) * p.heads_q + g * p.rep_kv + (r - t * p.rep_kv);
@@ -56,8 +58,9 @@ __device__ __forceinline__ size_t query_row(const SplitParams &p, int b, int v) 
 
 // Cached positions at the end of the sequence that query row v may not see
 // (the later tokens of its own run): tokens - 1 - t.  0 with one token.
+template <bool MULTI>
 __device__ __forceinline__ int query_lag(const SplitParams &p, int v) {
-  if (p.tokens == 1) return 0;
+  if (!MULTI || p.tokens == 1) return 0;
   return p.tokens - 1 - (v % p.n_rep) / p.rep_kv;
 }
 

@@ -58,7 +58,7 @@ struct MmaCfg {
   static_assert(D == 64 || D == 128, "head dimension");
 };
 
-template <class C>
+template <class C, bool MULTI>
 __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
     gqa_split_mma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                          const SplitParams p) {
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
         for (int half = 0; half < 2; ++half) {
           const int hl = wh * 16 * MFW + mf * 16 + gq + 8 * half;
           const bool ok = hl < nh;
-          const size_t row = query_row(p, b, h_first + (ok ? hl : 0)) * (D / 2);
+          const size_t row = query_row<MULTI>(p, b, h_first + (ok ? hl : 0)) * (D / 2);
 #pragma unroll
           for (int ks = 0; ks < KS; ++ks) {
             qa[mf][ks][half] = ok ? __ldg(q32 + row + ks * 8 + tq) : 0u;
@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
 #pragma unroll
       for (int rh = 0; rh < 2; ++rh) {
         const int hl = wh * 16 * MFW + mf * 16 + gq + 8 * rh;
-        lim[mf][rh] = L - query_lag(p, h_first + (hl < nh ? hl : 0));
+        lim[mf][rh] = L - query_lag<MULTI>(p, h_first + (hl < nh ? hl : 0));
       }
     const int L_all = L - (p.tokens - 1);  // positions below this are visible to every row
 
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
       const uint32_t kt = pipe.k_tile(st), vt = pipe.v_tile(st);
       const int n0 = t * C::BLOCK_N;
       const int end = min(n0 + C::BLOCK_N, L);
-      const bool tail = n0 + C::BLOCK_N > L_all;
+      const bool tail = n0 + C::BLOCK_N > (MULTI ? L_all : end);
 #pragma unroll
       for (int sub = 0; sub < C::SUB; ++sub) {
         const int r0 = wn * C::ROWS_PER_WARP + sub * 16;  // first row of this sub-tile in the stage
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
               float x = sacc[mf][nf][e] * p.scale_log2;
               if (tail) {
                 const int tok = tok0 + nf * 8 + 2 * tq + (e & 1);
-                x = tok < lim[mf][e >> 1] ? x : -INFINITY;
+                x = tok < (MULTI ? lim[mf][e >> 1] : end) ? x : -INFINITY;
               }
               sacc[mf][nf][e] = x;
               tmax[mf][e >> 1] = fmaxf(tmax[mf][e >> 1], x);
@@ -364,14 +364,14 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
       const float4 a = *reinterpret_cast<const float4 *>(src);
       const float4 c = *reinterpret_cast<const float4 *>(src + 4);
       if (whole) {
-        const float inv = fin_s[hl].y > 0.f ? 1.f / fin_s[hl].y : 0.f;
+        const float inv = (!MULTI || fin_s[hl].y > 0.f) ? 1.f / fin_s[hl].y : 0.f;
         uint4 pk;
         pk.x = pack_bf16x2(a.x * inv, a.y * inv);
         pk.y = pack_bf16x2(a.z * inv, a.w * inv);
         pk.z = pack_bf16x2(c.x * inv, c.y * inv);
         pk.w = pack_bf16x2(c.z * inv, c.w * inv);
         *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) +
-                                   query_row(p, b, h_first + hl) * D + d0) = pk;
+                                   query_row<MULTI>(p, b, h_first + hl) * D + d0) = pk;
       } else {
         float *dst = p.o_part + ((size_t)slot * p.heads_per_cta + hl) * D + d0;
         *reinterpret_cast<float4 *>(dst) = a;
@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
         reinterpret_cast<float2 *>(p.ml_part)[(size_t)slot * p.heads_per_cta + hl] = fin_s[hl];
     if (threadIdx.x == 0) record_unit(p, seg, whole, slot, range, b);
     if (!whole && p.unit_cnt)
-      finish_split_unit<__nv_bfloat16, D>(p, seg, range, b, h_first, nh, threadIdx.x, NCONS, um,
+      finish_split_unit<__nv_bfloat16, D, MULTI>(p, seg, range, b, h_first, nh, threadIdx.x, NCONS, um,
                                           [] { consumer_bar_sync(NCONS); });
     consumer_bar_sync(NCONS);  // scratch free for the next unit
   }

@@ -91,7 +91,7 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
   return v;
 }
 
-template <class C>
+template <class C, bool MULTI>
 __global__ void __launch_bounds__(C::THREADS)
     gqa_split_simt_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                           const SplitParams p) {
@@ -151,11 +151,12 @@ __global__ void __launch_bounds__(C::THREADS)
     // this lane's slice of q: element e of box bx is d = bx*BOX_ELEMS + j*EPC + e
     float qf[NH][EPL];
     int lim[NH];  // positions n < lim[h] are visible to row h
+    const int L_all = L - (p.tokens - 1);  // ... and all positions below L_all to every row
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
       const int hh = h_first + (h < nh ? h : 0);
-      lim[h] = L - query_lag(p, hh);
-      const T *qrow = reinterpret_cast<const T *>(p.q) + query_row(p, b, hh) * D;
+      lim[h] = L - query_lag<MULTI>(p, hh);
+      const T *qrow = reinterpret_cast<const T *>(p.q) + query_row<MULTI>(p, b, hh) * D;
 #pragma unroll
       for (int bx = 0; bx < NBOX; ++bx) {
         const uint4 c = __ldg(reinterpret_cast<const uint4 *>(qrow + bx * C::BOX_ELEMS + j * EPC));
@@ -203,13 +204,16 @@ __global__ void __launch_bounds__(C::THREADS)
           x[h] = dot * p.scale_log2;
         }
         if (valid) {
+          const bool lagged = tok >= L_all;  // only with several tokens
           float vf[EPL];
 #pragma unroll
           for (int bx = 0; bx < NBOX; ++bx)
             widen_chunk<T>(lds128(swz128(vt + bx * Pipe::BOX_BYTES, row, j)), &vf[bx * EPC]);
 #pragma unroll
           for (int h = 0; h < NH; ++h) {
-            if (tok >= lim[h]) continue;  // a later token of row h's own run
+            if constexpr (MULTI) {
+              if (lagged && tok >= lim[h]) continue;  // a later token of row h's own run
+            }
             if (x[h] > m_run[h]) {
               const float corr = merge_weight(m_run[h], x[h]);
               m_run[h] = x[h];
@@ -297,9 +301,10 @@ __global__ void __launch_bounds__(C::THREADS)
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
         if (h >= nh) break;
-        const size_t bh = query_row(p, b, h_first + h);
+        const size_t bh = query_row<MULTI>(p, b, h_first + h);
         if (whole) {
-          const float inv = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
+          // a row with no visible position (several tokens only) is 0
+          const float inv = (!MULTI || l_run[h] > 0.f) ? 1.f / l_run[h] : 0.f;
           T *orow = reinterpret_cast<T *>(p.out) + bh * D;
 #pragma unroll
           for (int bx = 0; bx < NBOX; ++bx) {
@@ -325,7 +330,7 @@ __global__ void __launch_bounds__(C::THREADS)
     const bool whole = seg.t0 == 0 && seg.t1 == seg.tiles;
     if (threadIdx.x == 0) record_unit(p, seg, whole, partial_slot(seg_index), range, b);
     if (!whole && p.unit_cnt)
-      finish_split_unit<T, D>(p, seg, range, b, h_first, nh, threadIdx.x, C::CONSUMER_WARPS * 32, um,
+      finish_split_unit<T, D, MULTI>(p, seg, range, b, h_first, nh, threadIdx.x, C::CONSUMER_WARPS * 32, um,
                               [] { consumer_bar_sync(C::CONSUMER_WARPS * 32); });
     consumer_bar_sync(C::CONSUMER_WARPS * 32);  // scratch free for the next unit
   }

@@ -177,7 +177,7 @@ __device__ __forceinline__ void soft_reduce(float (&v)[C::NR], int sub, int lane
 // partial of the row has it, and a row whose sum stays 0 is written as 0.
 constexpr float kNoMax = -1e30f;
 
-template <class C>
+template <class C, bool MULTI>
 __global__ void __launch_bounds__(C::THREADS, 1)
     gqa_split_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const SplitParams p) {
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const bool real = row < nh;
         if (row < NR) {
         const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(p.q) +
-                                                           query_row(p, s.b, h_first + min(row, nh - 1)) * D +
+                                                           query_row<MULTI>(p, s.b, h_first + min(row, nh - 1)) * D +
                                                            half * 64);
         const uint32_t dst = qbase + half * C::Q_BOX + row * 128;
 #pragma unroll
@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // The running max starts at a finite floor rather than -inf, so that
         // a row that has seen no visible position yet (a query token whose
         // whole view lies in later tiles) gets 2^(-inf - floor) = 0, not NaN.
-        if (R < NQ) m_s[R] = kNoMax;
+        if (R < NQ) m_s[R] = MULTI ? kNoMax : -INFINITY;
         soft_bar();
         // Row h of the unit is query token t(h) = (row0 + h) / rep_kv of its
         // run and sees positions n < L_all + t(h); positions below L_all are
@@ -410,8 +410,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         for (int i = 0; i < ntl; ++i) {
           const int tg = t + i, sb = tg & 1, st = tg % ST;
           const bool valid = (seg.t0 + i) * BN + R < L;
-          // a tile that reaches L_all needs the per-row limits; before it,
-          // every position is visible to every real row
+          // a tile that reaches L_all needs the per-row limits of a run of
+          // several tokens; before it every position is visible to every row
           const bool edge = (seg.t0 + i + 1) * BN > L_all;
           const int pos = (seg.t0 + i) * BN + R;
           wait(bars.s_full(sb), (tg >> 1) & 1);
@@ -421,7 +421,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           // padding rows
           float x[NR];
           auto load_s = [&]() {
-            int tk = t_first, kk = k_first;  // token of row h and its place in the token's run
 #pragma unroll
             for (int c0 = 0; c0 < NR; c0 += (NR < 32 ? NR : 32)) {
               uint32_t r[32];
@@ -434,15 +433,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
               for (int c = 0; c < (NR < 32 ? NR : 32); ++c) {
                 const int h = c0 + c;
-                bool vis = h < nh;
-                if (edge) {
-                  vis = vis && pos < L_all + tk;
-                  if (++kk == p.rep_kv) {
-                    kk = 0;
-                    ++tk;
-                  }
-                }
-                x[h] = vis ? __uint_as_float(r[c]) * p.scale_log2 : -INFINITY;
+                x[h] = (valid && h < nh) ? __uint_as_float(r[c]) * p.scale_log2 : -INFINITY;
+              }
+            }
+            if (MULTI && edge) {
+              // row h is token t(h) of its run: it sees positions < L_all + t(h)
+              int tk = t_first, kk = k_first;
+#pragma unroll
+              for (int h = 0; h < NR; ++h) {
+                if (pos >= L_all + tk) x[h] = -INFINITY;
+                const bool wrap = ++kk == p.rep_kv;
+                kk = wrap ? 0 : kk;
+                tk += wrap ? 1 : 0;
               }
             }
           };
@@ -547,6 +549,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         tc::fence_after();
         const bool whole = seg.t0 == 0 && seg.t1 == seg.tiles;
         const int slot = partial_slot(unit);
+        // output row of column h: (b*tokens + t(h))*heads_q + g*rep_kv + k(h),
+        // stepping (t, k) through the unit's rows (query_row without divisions)
+        int tk = t_first, kk = k_first;
+        const size_t orow_b = MULTI ? (size_t)b * p.tokens * p.heads_q + (size_t)(h_first / p.n_rep) * p.rep_kv
+                                    : (size_t)b * p.H + h_first;
 #pragma unroll
         for (int c0 = 0; c0 < NR; c0 += (NR < 32 ? NR : 32)) {
           uint32_t r[32];
@@ -559,11 +566,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
           for (int c = 0; c < (NR < 32 ? NR : 32); ++c) {
             const int h = c0 + c;
+            size_t orow = orow_b + h;
+            if constexpr (MULTI) {
+              orow = orow_b + (size_t)tk * p.heads_q + kk;
+              const bool wrap = ++kk == p.rep_kv;
+              kk = wrap ? 0 : kk;
+              tk += wrap ? 1 : 0;
+            }
             if (h < nh) {
               const float o = __uint_as_float(r[c]);
               if (whole)
-                reinterpret_cast<__nv_bfloat16 *>(p.out)[query_row(p, b, h_first + h) * D + R] =
-                    __float2bfloat16_rn(fin[h] > 0.f ? o / fin[h] : 0.f);
+                reinterpret_cast<__nv_bfloat16 *>(p.out)[orow * D + R] =
+                    __float2bfloat16_rn((!MULTI || fin[h] > 0.f) ? o / fin[h] : 0.f);
               else
                 p.o_part[((size_t)slot * p.heads_per_cta + h) * D + R] = o;
             }
@@ -573,7 +587,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           reinterpret_cast<float2 *>(p.ml_part)[(size_t)slot * p.heads_per_cta + R] = make_float2(mR, fin[R]);
         if (R == 0) record_unit(p, seg, whole, slot, range, b);
         if (!whole && p.unit_cnt)
-          finish_split_unit<__nv_bfloat16, D>(p, seg, range, b, h_first, nh, R, C::SOFT, um, [] { soft_bar(); });
+          finish_split_unit<__nv_bfloat16, D, MULTI>(p, seg, range, b, h_first, nh, R, C::SOFT, um, [] { soft_bar(); });
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.o_free(ob));
