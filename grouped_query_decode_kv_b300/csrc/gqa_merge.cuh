@@ -68,7 +68,9 @@ __device__ __forceinline__ void finish_split_unit(const SplitParams &p, const Se
     um->last = last;
     um->c_lo = c_lo;
     um->n = n;
-    um->slot0 = cta_start(c_lo, T_total, P) == seg.unit_first ? 2 * c_lo : 2 * c_lo + 1;
+    // the unit is c_lo's first segment when c_lo's range starts inside the
+    // unit's span (its charge, then its tiles)
+    um->slot0 = cta_start(c_lo, T_total, P) >= seg.unit_first - range.cost ? 2 * c_lo : 2 * c_lo + 1;
   }
   bar();
   if (!um->last) return;

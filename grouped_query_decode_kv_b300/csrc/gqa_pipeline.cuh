@@ -152,6 +152,28 @@ __device__ __forceinline__ void produce_range(const Pipe &pipe, const SchedParam
   __syncwarp();
 }
 
+// Before the kernel may read what earlier kernels wrote (ahead of
+// griddepcontrol.wait), one lane asks L2 for the first `n` tiles of the
+// range a speculative plan gives this CTA, so that the first loads after
+// the wait find them there.  Only a hint: a stale plan costs some bandwidth,
+// never a wrong result (the real loads still come from global memory).
+__device__ __forceinline__ void prefetch_first_tiles(const SchedParams &s, const CtaRange &range,
+                                                     const CUtensorMap *tmK, const CUtensorMap *tmV, int box_elems,
+                                                     int nbox, int G, int HC, int n) {
+  SegmentCursor cur;
+  cur.init(s, range);
+  Segment seg;
+  while (n > 0 && cur.next(s, seg)) {
+    const int bg = seg.b * G + seg.uib / HC;
+    for (int t = seg.t0; t < seg.t1 && n > 0; ++t, --n) {
+      for (int bx = 0; bx < nbox; ++bx) {
+        tma_prefetch_l2_3d(tmK, bx * box_elems, t * s.block_n, bg);
+        tma_prefetch_l2_3d(tmV, bx * box_elems, t * s.block_n, bg);
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ void consumer_bar_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }

@@ -25,6 +25,14 @@
 // one unit and starts another pays two epilogues and leaves two partials,
 // which costs more than a few idle CTAs.
 //
+// Every unit also costs a fixed amount of work however few tiles it has (Q
+// load, first-tile max, epilogue, partial), so for unequal lengths each
+// non-empty unit is charged `unit_cost` extra virtual tiles ahead of its
+// first real one: the flat space holds span = tiles_b + unit_cost virtual
+// tiles per unit, and a CTA whose range crosses many short units gets fewer
+// real tiles.  A range piece that holds only a unit's charge is no segment.
+// With equal lengths (the aligned plan) the charge is 0.
+//
 // The lengths live in device memory, so each CTA derives T and its own
 // starting row from seq_lens with a warp scan (O(B/32) steps per CTA; the
 // first 64 rows are read once).
@@ -41,6 +49,11 @@ struct SchedParams {
   int units_per_b;  // G * HC
   int block_n;      // positions per tile
   int append;       // fused decode step: the call appends one token first
+  int unit_cost;    // extra virtual tiles charged per unit (see below)
+  // speculative plan (before griddepcontrol.wait): lengths are read with
+  // L1-bypassing loads, so that no stale copy stays in the non-coherent cache
+  // for the real plan to hit
+  int spec = 0;
 };
 
 __device__ __forceinline__ int clamp_len(int L, int Nmax) { return max(0, min(L, Nmax)); }
@@ -56,6 +69,10 @@ __device__ __forceinline__ int attn_len(const int32_t *seq_lens, int b, int Nmax
 }
 
 __device__ __forceinline__ int row_tiles(const SchedParams &s, int b) {
+  if (s.spec) {
+    const int L = *(volatile const int32_t *)(s.seq_lens + b);
+    return (clamp_len(s.append && append_ok(L, s.Nmax) ? L + 1 : L, s.Nmax) + s.block_n - 1) / s.block_n;
+  }
   return (attn_len(s.seq_lens, b, s.Nmax, s.append) + s.block_n - 1) / s.block_n;
 }
 
@@ -80,13 +97,18 @@ __device__ __forceinline__ long long warp_incl_scan(long long v, int lane) {
 
 // This CTA's place in the flat tile space, computed by one warp.
 struct CtaRange {
-  long long T;      // total tiles of the call
+  long long T;      // total (virtual) tiles of the call
   long long begin;  // first tile of this CTA
   long long end;    // one past its last tile
   long long pre_b;  // global index of the first tile of row b
   int b;            // row holding `begin` (valid when begin < end)
   int P;            // CTAs that take part (<= gridDim.x); the rest have empty ranges
+  int cost;         // virtual tiles charged per non-empty unit
+  int tiles_b;      // tiles of each unit of row b
 };
+
+// Virtual tiles of one unit of a row with `tiles` real tiles.
+__device__ __forceinline__ long long unit_span(int tiles, int cost) { return tiles > 0 ? tiles + cost : 0; }
 
 // CTAs used for T tiles when every non-empty unit holds the same number of
 // tiles and there are no more units than CTAs: k = floor(P / units) CTAs per
@@ -102,18 +124,21 @@ __device__ __forceinline__ int aligned_cta_count(long long units, int P) {
 // All 32 lanes of one warp call this.  Also flags out-of-range lengths and
 // zero-fills the output rows of empty sequences (L_b = 0) that this CTA owns
 // (row b is owned by CTA b % P), writing `row_bytes` bytes per row of `out`.
+// SPECULATIVE: a plan from lengths that an earlier kernel may still be
+// changing, used only to pick tiles to prefetch into L2: no flags, no writes.
+template <bool SPECULATIVE = false>
 __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int lane, void *out, size_t row_bytes) {
   const int c = blockIdx.x;
   int P = gridDim.x;
-  long long T = 0;
-  long long keep0 = 0, keep1 = 0;  // this lane's tile counts of rows lane and 32 + lane
+  long long T = 0;                 // real tiles
+  int keep0 = 0, keep1 = 0;        // this lane's per-unit tile counts of rows lane and 32 + lane
   int tmin = 0x7fffffff, tmax = 0, rows = 0;  // per-unit tile counts of the non-empty rows
   for (int base = 0; base < s.B; base += 32) {
     const int b = base + lane;
     long long t = 0;
     bool zero_mine = false;
     if (b < s.B) {
-      const int Lstored = __ldg(s.seq_lens + b);
+      const int Lstored = (SPECULATIVE || s.spec) ? *(volatile const int32_t *)(s.seq_lens + b) : __ldg(s.seq_lens + b);
       const bool appends = s.append && append_ok(Lstored, s.Nmax);
       const int Lraw = appends ? Lstored + 1 : Lstored;
       const int L = clamp_len(Lraw, s.Nmax);
@@ -125,9 +150,9 @@ __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int la
         tmax = max(tmax, tu);
         ++rows;
       }
-      if (mine && (Lraw <= 0 || Lraw > s.Nmax)) flag_error(GQA_DEVERR_ATTN_LEN);
-      if (mine && s.append && !appends) flag_error(GQA_DEVERR_APPEND_LEN);
-      zero_mine = mine && L == 0;
+      if (!SPECULATIVE && mine && (Lraw <= 0 || Lraw > s.Nmax)) flag_error(GQA_DEVERR_ATTN_LEN);
+      if (!SPECULATIVE && mine && s.append && !appends) flag_error(GQA_DEVERR_APPEND_LEN);
+      zero_mine = !SPECULATIVE && mine && L == 0;
     }
     unsigned zero_rows = __ballot_sync(0xffffffffu, zero_mine);
     while (zero_rows) {  // warp-uniform loop over this chunk's empty rows
@@ -136,8 +161,8 @@ __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int la
       uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(out) + (size_t)(base + src) * row_bytes);
       for (size_t i = lane; i < row_bytes / 16; i += 32) o[i] = make_uint4(0, 0, 0, 0);
     }
-    if (base == 0) keep0 = t;
-    if (base == 32) keep1 = t;
+    if (base == 0) keep0 = (int)(t / s.units_per_b);
+    if (base == 32) keep1 = (int)(t / s.units_per_b);
     const long long incl = warp_incl_scan(t, lane);
     T += __shfl_sync(0xffffffffu, incl, 31);
   }
@@ -147,21 +172,25 @@ __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int la
     tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
     rows += __shfl_xor_sync(0xffffffffu, rows, off);
   }
-  if (rows > 0 && tmin == tmax) P = aligned_cta_count((long long)rows * s.units_per_b, P);
+  const bool uniform = rows > 0 && tmin == tmax;
+  if (uniform) P = aligned_cta_count((long long)rows * s.units_per_b, P);
+  const int cost = uniform ? 0 : s.unit_cost;
+  T += (long long)cost * rows * s.units_per_b;
   CtaRange r;
   r.T = T;
   r.P = P;
+  r.cost = cost;
   r.begin = c < P ? cta_start(c, T, P) : T;
   r.end = c < P ? cta_start(c + 1, T, P) : T;
   r.b = 0;
   r.pre_b = 0;
+  r.tiles_b = 0;
   if (r.begin >= r.end) return r;
   long long acc = 0;
   for (int base = 0; base < s.B; base += 32) {
     const int b = base + lane;
-    const long long t = base == 0    ? keep0
-                        : base == 32 ? keep1
-                        : (b < s.B ? (long long)row_tiles(s, b) * s.units_per_b : 0);
+    const int tu = base == 0 ? keep0 : base == 32 ? keep1 : (b < s.B ? row_tiles(s, b) : 0);
+    const long long t = unit_span(tu, cost) * s.units_per_b;
     const long long incl = warp_incl_scan(t, lane);
     const long long lo = acc + incl - t, hi = acc + incl;
     const unsigned hit = __ballot_sync(0xffffffffu, b < s.B && lo <= r.begin && r.begin < hi);
@@ -169,6 +198,7 @@ __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int la
       const int src = __ffs(hit) - 1;
       r.b = base + src;
       r.pre_b = __shfl_sync(0xffffffffu, lo, src);
+      r.tiles_b = __shfl_sync(0xffffffffu, tu, src);
       break;
     }
     acc += __shfl_sync(0xffffffffu, incl, 31);
@@ -181,40 +211,49 @@ struct Segment {
   int b, uib;
   int t0, t1;
   int tiles;             // tiles of every unit of row b
-  long long unit_first;  // global index of the unit's first tile
+  long long unit_first;  // global (virtual) index of the unit's first real tile
 };
 
 // Walks the segments of a range; every thread that calls next() with the
 // same cursor sees the same sequence.
 struct SegmentCursor {
   long long pos, end, pre_b;
-  int b, tiles_b;
+  int b, tiles_b, cost;
 
   __device__ __forceinline__ void init(const SchedParams &s, const CtaRange &r) {
     pos = r.begin;
     end = r.end;
     pre_b = r.pre_b;
     b = r.b;
-    tiles_b = pos < end ? row_tiles(s, b) : 0;
+    cost = r.cost;
+    tiles_b = pos < end ? r.tiles_b : 0;
   }
 
   __device__ __forceinline__ bool next(const SchedParams &s, Segment &seg) {
-    if (pos >= end) return false;
-    while (pos >= pre_b + (long long)tiles_b * s.units_per_b) {
-      pre_b += (long long)tiles_b * s.units_per_b;
-      ++b;
-      tiles_b = row_tiles(s, b);
+    for (;;) {
+      if (pos >= end) return false;
+      long long span = unit_span(tiles_b, cost);
+      while (pos >= pre_b + span * s.units_per_b) {
+        pre_b += span * s.units_per_b;
+        ++b;
+        tiles_b = row_tiles(s, b);
+        span = unit_span(tiles_b, cost);
+      }
+      const long long off = pos - pre_b;
+      const int uib = (int)(off / span);
+      const int v0 = (int)(off % span);
+      const long long left = end - pos;
+      const int v1 = left < span - v0 ? v0 + (int)left : (int)span;
+      pos += v1 - v0;
+      if (v1 <= cost) continue;  // only the unit's charge lies in the range
+      seg.b = b;
+      seg.uib = uib;
+      seg.t0 = v0 > cost ? v0 - cost : 0;
+      seg.t1 = v1 - cost;
+      seg.tiles = tiles_b;
+      seg.unit_first = pre_b + (long long)uib * span + cost;
+      return true;
     }
-    const long long off = pos - pre_b;
-    seg.b = b;
-    seg.uib = (int)(off / tiles_b);
-    seg.t0 = (int)(off % tiles_b);
-    const long long left = end - pos;
-    seg.t1 = (int)(left < (long long)(tiles_b - seg.t0) ? seg.t0 + left : tiles_b);
-    seg.tiles = tiles_b;
-    seg.unit_first = pre_b + (long long)seg.uib * tiles_b;
-    pos += seg.t1 - seg.t0;
-    return true;
   }
 };
 

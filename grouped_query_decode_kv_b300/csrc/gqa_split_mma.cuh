@@ -37,6 +37,7 @@ struct MmaCfg {
   static constexpr int CONSUMER_WARPS = 4 * WH;
   static constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;
   static constexpr int HEADS = 16 * MFW * WH;  // query heads per CTA
+  static constexpr int UNIT_COST = 2;          // stream-K charge per unit, in tiles (gqa_schedule.cuh)
   static constexpr int MIN_BLOCKS = MIN_BLOCKS_;  // resident CTAs per SM the register budget must allow
   using Pipe = KVPipe<D * 2 / 128, BLOCK_N_, STAGES_, CONSUMER_WARPS>;
   static constexpr int BLOCK_N = BLOCK_N_;
@@ -85,8 +86,22 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   sp.units_per_b = p.G * p.head_chunks;
   sp.block_n = C::BLOCK_N;
   sp.append = p.append;
+  sp.unit_cost = C::UNIT_COST;
 
   if (threadIdx.x == 0) pipe.init();
+  if (warp == 0) {
+    // Ahead of the wait for earlier kernels: fetch the tensor maps and ask
+    // L2 for the first tiles of a speculative plan (a hint only).
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    SchedParams spx = sp;
+    spx.spec = 1;
+    const CtaRange r0 = warp_plan_range<true>(spx, lane, nullptr, 0);
+    if (lane == 0 && r0.begin < r0.end)
+      prefetch_first_tiles(spx, r0, &tmK, &tmV, 64, Pipe::NBOX, p.G, p.head_chunks, Pipe::STAGES);
+  }
   griddep_wait();  // lengths and cache rows written by earlier kernels are visible
   if (warp == 0) {
     const CtaRange r = warp_plan_range(sp, lane, p.out, (size_t)p.H * D * sizeof(__nv_bfloat16));
@@ -96,10 +111,6 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   griddep_launch_dependents();
   const CtaRange range = *range_smem;
   if (range.begin < range.end && warp == C::CONSUMER_WARPS) {
-    if (lane == 0) {
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-    }
     produce_range(pipe, sp, range, &tmK, &tmV, 64, p.G, p.head_chunks, p, lane);
   }
   if (range.begin < range.end && warp != C::CONSUMER_WARPS) {

@@ -34,6 +34,7 @@ struct SimtCfg {
   static constexpr int CONSUMER_WARPS = 4;
   static constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;
   static constexpr int HEADS = NH;
+  static constexpr int UNIT_COST = 2;  // stream-K charge per unit, in tiles (gqa_schedule.cuh)
   using Pipe = KVPipe<NBOX, BLOCK_N_, STAGES_, CONSUMER_WARPS>;
   static constexpr int BLOCK_N = BLOCK_N_;
   static constexpr int ROWS_PER_WARP = BLOCK_N / 4;
@@ -115,8 +116,22 @@ __global__ void __launch_bounds__(C::THREADS)
   sp.units_per_b = p.G * p.head_chunks;
   sp.block_n = C::BLOCK_N;
   sp.append = p.append;
+  sp.unit_cost = C::UNIT_COST;
 
   if (threadIdx.x == 0) pipe.init();
+  if (warp == 0) {
+    // Ahead of the wait for earlier kernels: fetch the tensor maps and ask
+    // L2 for the first tiles of a speculative plan (a hint only).
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    SchedParams spx = sp;
+    spx.spec = 1;
+    const CtaRange r0 = warp_plan_range<true>(spx, lane, nullptr, 0);
+    if (lane == 0 && r0.begin < r0.end)
+      prefetch_first_tiles(spx, r0, &tmK, &tmV, C::BOX_ELEMS, NBOX, p.G, p.head_chunks, Pipe::STAGES);
+  }
   griddep_wait();  // lengths and cache rows written by earlier kernels are visible
   if (warp == 0) {
     const CtaRange r = warp_plan_range(sp, lane, p.out, (size_t)p.H * D * sizeof(T));
@@ -126,10 +141,6 @@ __global__ void __launch_bounds__(C::THREADS)
   griddep_launch_dependents();
   const CtaRange range = *range_smem;
   if (range.begin < range.end && warp == C::CONSUMER_WARPS) {
-    if (lane == 0) {
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-    }
     produce_range(pipe, sp, range, &tmK, &tmV, C::BOX_ELEMS, p.G, p.head_chunks, p, lane);
   }
   if (range.begin < range.end && warp != C::CONSUMER_WARPS) {

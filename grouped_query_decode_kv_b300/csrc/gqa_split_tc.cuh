@@ -53,6 +53,7 @@ struct TcCfg {
   static constexpr int NQ = NR;
   static constexpr int HEADS = NR;
   static constexpr int PB = PB_;       // P^T buffers
+  static constexpr int UNIT_COST = 2;  // stream-K charge per unit, in tiles (gqa_schedule.cuh)
   static_assert(NR == 16 || NR == 32 || NR == 64, "heads per unit");
   static_assert(PB == 1 || PB == 2, "P^T buffers");
   using Pipe = KVPipe<2, BLOCK_N, STAGES, 1>;  // one "empty" arrival per tile: the MMA commit
@@ -63,24 +64,31 @@ struct TcCfg {
   static constexpr int TM_O = 2 * NR;
   static constexpr int TM_COLS = 4 * NR < 32 ? 32 : 4 * NR;  // 64, 128 or 256: a power of two
   // shared memory
-  static constexpr int Q_OFF = Pipe::PIPE_BYTES;  // Q: two 128-byte-wide boxes (d 0-63, 64-127) of NR rows
+  // Q: two 128-byte-wide boxes (d 0-63, 64-127) of NR rows per buffer; two
+  // buffers where shared memory allows, so that the next unit's Q lands
+  // while the current one is still in use
+  static constexpr int Q_OFF = Pipe::PIPE_BYTES;
   static constexpr int Q_BOX = NR * 128;
+  static constexpr int Q_BYTES = 2 * Q_BOX;
   // P^T buffers, K-major like Q: one row of 128 positions per head, as two
   // 128-byte-wide boxes (positions 0-63, 64-127), 128-byte swizzled
-  static constexpr int P_OFF = Q_OFF + 2 * Q_BOX;
   static constexpr int P_BOX = NR * 128;
   static constexpr int P_BYTES = 2 * P_BOX;
+  // pipe full[STAGES], empty[STAGES]; then s_full[2], s_free[2], p_full[2],
+  // pv_done[2], o_free[2], q_full[2], mma_done
+  static constexpr int NBAR = 2 * STAGES + 13;
+  static constexpr int RANGE_BYTES = ((int)sizeof(CtaRange) + 15) / 16 * 16;
+  static constexpr int TAIL_BYTES = 4 * NQ * 4 + 3 * NQ * 4 + NBAR * 8 + 16 + RANGE_BYTES + (int)sizeof(UnitMerge);
+  static constexpr int QB = 1024 + Q_OFF + 2 * Q_BYTES + PB * P_BYTES + TAIL_BYTES <= 227 * 1024 ? 2 : 1;
+  static constexpr int P_OFF = Q_OFF + QB * Q_BYTES;
   static constexpr int RED_OFF = P_OFF + PB * P_BYTES;  // [4][NQ] cross-warp reduction
   static constexpr int FIN_OFF = RED_OFF + 4 * NQ * 4;   // [NQ] reduced value
   static constexpr int M_OFF = FIN_OFF + NQ * 4;         // [NQ] running max of the unit
   static constexpr int CORR_OFF = M_OFF + NQ * 4;        // [NQ] rescale factor of a tile
   static constexpr int BAR_OFF = CORR_OFF + NQ * 4;
-  // pipe full[STAGES], empty[STAGES]; then s_full[2], s_free[2], p_full[2],
-  // pv_done[2], o_free[2], q_full, mma_done
-  static constexpr int NBAR = 2 * STAGES + 12;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBAR * 8;
   static constexpr int RANGE_OFF = TMEM_SLOT_OFF + 16;
-  static constexpr int MERGE_OFF = RANGE_OFF + 64;
+  static constexpr int MERGE_OFF = RANGE_OFF + RANGE_BYTES;
   static constexpr int SMEM_BYTES = 1024 + MERGE_OFF + (int)sizeof(UnitMerge);
   // more than half of an SM's shared memory: one CTA per SM, so the TMEM
   // allocation never waits for another CTA
@@ -94,8 +102,8 @@ struct TcBars {
   __device__ __forceinline__ uint32_t p_full(int i) const { return b0 + 32 + 8 * i; }
   __device__ __forceinline__ uint32_t pv_done(int i) const { return b0 + 48 + 8 * i; }
   __device__ __forceinline__ uint32_t o_free(int i) const { return b0 + 64 + 8 * i; }
-  __device__ __forceinline__ uint32_t q_full() const { return b0 + 80; }
-  __device__ __forceinline__ uint32_t mma_done() const { return b0 + 88; }
+  __device__ __forceinline__ uint32_t q_full(int i) const { return b0 + 80 + 8 * i; }
+  __device__ __forceinline__ uint32_t mma_done() const { return b0 + 96; }
 };
 
 // All lanes of a warp wait; a wait that timed out in any lane counts as
@@ -208,6 +216,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   sp.units_per_b = p.G * p.head_chunks;
   sp.block_n = BN;
   sp.append = p.append;
+  sp.unit_cost = C::UNIT_COST;
 
   if (threadIdx.x == 0) {
     pipe.init();
@@ -220,13 +229,26 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       mbar_init(bars.p_full(i), 4);
       mbar_init(bars.pv_done(i), 1);
     }
-    mbar_init(bars.q_full(), 4);
+    mbar_init(bars.q_full(0), 4);  // one arrival per softmax warp
+    mbar_init(bars.q_full(1), 4);
     mbar_init(bars.mma_done(), 1);
     fence_barrier_init();
   }
   if (warp == 1) {
     tc::tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
     tc::tmem_relinquish();
+  }
+  if (warp == 0) {
+    // Ahead of the wait for earlier kernels: fetch the tensor maps and ask
+    // L2 for the first tiles of a speculative plan (a hint only).
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    SchedParams spx = sp;
+    spx.spec = 1;
+    const CtaRange r0 = warp_plan_range<true>(spx, lane, nullptr, 0);
+    if (lane == 0 && r0.begin < r0.end) prefetch_first_tiles(spx, r0, &tmK, &tmV, 64, 2, p.G, p.head_chunks, ST);
   }
   griddep_wait();  // lengths, q and cache rows written by earlier kernels are visible
   if (warp == 0) {
@@ -243,10 +265,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   if (range.begin < range.end) {
     if (warp == 0) {
       // ------------------------------------------------------------ producer
-      if (lane == 0) {
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
-      }
       produce_range(pipe, sp, range, &tmK, &tmV, 64, p.G, p.head_chunks, p, lane);
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
@@ -286,14 +304,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           bool progressed = false;
           if (ws.has && ws.tg < wp.tg + 2) {
             const int tg = ws.tg, st = tg % ST;
-            if ((ws.i != 0 || mbar_test(bars.q_full(), ws.unit & 1)) && mbar_test(pipe.full(st), (tg / ST) & 1) &&
+            // unit u's Q is in buffer u % QB, its (u / QB)-th use
+            const int qb = ws.unit % C::QB;
+            const uint32_t qpar = (ws.unit / C::QB) & 1;
+            if ((ws.i != 0 || mbar_test(bars.q_full(qb), qpar)) && mbar_test(pipe.full(st), (tg / ST) & 1) &&
                 (tg < 2 || mbar_test(bars.s_free(tg & 1), ((tg >> 1) - 1) & 1))) {
               tc::fence_after();
               const uint32_t kt = pipe.k_tile(st);
+              const uint32_t qt = qbase + qb * C::Q_BYTES;
 #pragma unroll
               for (int ks = 0; ks < D / 16; ++ks) {
                 const uint64_t a = tc::smem_desc_sw128(kt + (ks >> 2) * Pipe::BOX_BYTES + (ks & 3) * 32, 16, 1024);
-                const uint64_t b = tc::smem_desc_sw128(qbase + (ks >> 2) * C::Q_BOX + (ks & 3) * 32, 16, 1024);
+                const uint64_t b = tc::smem_desc_sw128(qt + (ks >> 2) * C::Q_BOX + (ks & 3) * 32, 16, 1024);
                 tc::mma_ss(tmem + C::TM_S + (tg & 1) * NR, a, b, IDESC_S, ks > 0);
               }
               tc::commit(bars.s_full(tg & 1));
@@ -324,7 +346,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           if (progressed) {
             idle_since = 0;
           } else {
-            __nanosleep(32);  // leave the issue slots to the softmax warp on this SM sub-partition
+            // Nothing ready: sleep on the barrier most likely to complete
+            // next (the P^T the P.V walk needs, else the K tile the S^T walk
+            // needs), so that the thread wakes the moment it does and leaves
+            // the issue slots to the softmax warp on this sub-partition.
+            if (wp.tg < ws.tg)
+              mbar_try_wait_hint(bars.p_full(wp.tg % C::PB), (wp.tg / C::PB) & 1, 1000);
+            else if (ws.has)
+              mbar_try_wait_hint(pipe.full(ws.tg % ST), (ws.tg / ST) & 1, 1000);
+            else
+              __nanosleep(32);
             const unsigned long long now = global_timer_ns();
             if (idle_since == 0) {
               idle_since = now;
@@ -353,30 +384,46 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         h_first = g * p.n_rep + hc * p.heads_per_cta;
         nh = min(p.heads_per_cta, p.n_rep - hc * p.heads_per_cta);
       };
-      // Q rows of a unit: thread R writes the 128-byte half R & 1 of row R >> 1
-      auto load_q = [&](const Segment &s) {
+      // Q rows of a unit go to buffer u % QB: thread R copies the 128-byte
+      // half R & 1 of row R >> 1 (zeros for padding rows) with cp.async, so
+      // the copy runs while the thread works on.  With two buffers unit
+      // u + 2's copy is issued at the end of unit u and completed (wait,
+      // proxy fence, arrival on q_full) at the end of unit u + 1, a whole
+      // unit later; with one buffer it is issued and completed at the end of
+      // the previous unit.
+      auto issue_q = [&](const Segment &s, int buf) {
         int h_first, nh;
         unit_heads(s, h_first, nh);
         const int row = R >> 1, half = R & 1;
-        const bool real = row < nh;
         if (row < NR) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(p.q) +
-                                                           query_row<MULTI>(p, s.b, h_first + min(row, nh - 1)) * D +
-                                                           half * 64);
-        const uint32_t dst = qbase + half * C::Q_BOX + row * 128;
+          const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(p.q) +
+                                                             query_row<MULTI>(p, s.b, h_first + min(row, nh - 1)) * D +
+                                                             half * 64);
+          const uint32_t dst = qbase + buf * C::Q_BYTES + half * C::Q_BOX + row * 128;
+          const uint32_t bytes = row < nh ? 16u : 0u;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 v = real ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst + ((c ^ (row & 7)) << 4)), "r"(v.x),
-                       "r"(v.y), "r"(v.z), "r"(v.w)
-                       : "memory");
+          for (int c = 0; c < 8; ++c) cp_async_16(dst + ((c ^ (row & 7)) << 4), src + c, bytes);
         }
-        }
+        cp_async_commit();
+      };
+      // `later`: another unit's copy was issued after this one
+      auto complete_q = [&](int buf, bool later) {
+        if (later)
+          cp_async_wait<1>();
+        else
+          cp_async_wait<0>();
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bars.q_full());
+        if (lane == 0) mbar_arrive(bars.q_full(buf));
       };
-      if (have) load_q(seg);
+      if (have) {
+        issue_q(seg, 0);
+        SegmentCursor la = cur;
+        Segment s1;
+        const bool has1 = C::QB == 2 && la.next(sp, s1);
+        if (has1) issue_q(s1, 1);
+        complete_q(0, has1);
+      }
       // After a wait that timed out the thread is "dead": its later waits
       // return at once, but it keeps the same control flow, so the four
       // softmax warps still meet at every named barrier and finish (the
@@ -540,7 +587,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // the S^T of every tile of this unit is done, so Q may take the next unit
         Segment nseg;
         const bool next = cur.next(sp, nseg);
-        if (next) load_q(nseg);
+        if (next) {
+          if constexpr (C::QB == 2) {
+            // unit + 1's Q was issued a unit ago; unit + 2's goes to this
+            // unit's buffer, whose S^T MMAs have all completed
+            SegmentCursor la = cur;
+            Segment s2;
+            const bool has2 = la.next(sp, s2);
+            if (has2) issue_q(s2, unit & 1);
+            complete_q((unit + 1) & 1, has2);
+          } else {
+            issue_q(nseg, 0);
+            complete_q(0, false);
+          }
+        }
         // ---- epilogue: l[h] summed over the 128 positions' partials
         const float mR = R < NQ ? m_s[R] : 0.f;  // kNoMax when the row saw no position
         soft_reduce<C, false>(lp, sub, lane, red, fin, R);

@@ -1,0 +1,120 @@
+"""The stream-K work split of the split kernels, stated as a plain Python
+model and checked for the properties the kernels rely on: every real K/V tile
+of every (sequence, KV head, head chunk) unit is visited by exactly one CTA;
+a unit is cut only at a CTA's first or last segment; the CTAs that hold a cut
+unit are exactly cta_of_tile(first) .. cta_of_tile(last); and the merge's
+rule for the first partial's slot names the slot that CTA wrote.
+
+The model follows the device code (gqa_schedule.cuh, gqa_merge.cuh): per-row
+tile counts, a per-unit charge of `cost` virtual tiles ahead of the unit's
+first real tile when lengths differ (0 when every non-empty row has the same
+tile count, where the aligned CTA count applies), contiguous ranges
+start(c) = floor(c*T/P).  No GPU needed."""
+import random
+
+import pytest
+
+
+def cta_start(c, T, P):
+    return (c * T) // P if T >= P else min(c, T)
+
+
+def cta_of_tile(t, T, P):
+    return t if T < P else ((t + 1) * P + T - 1) // T - 1
+
+
+def span(tiles, cost):
+    return tiles + cost if tiles > 0 else 0
+
+
+def plan(lens, Nmax, BN, U, P0, unit_cost):
+    tiles = [(max(0, min(L, Nmax)) + BN - 1) // BN for L in lens]
+    nz = [t for t in tiles if t > 0]
+    uniform = bool(nz) and min(nz) == max(nz)
+    P = P0
+    if uniform and len(nz) * U <= P:
+        P = len(nz) * U * (P // (len(nz) * U))
+    cost = 0 if uniform else unit_cost
+    return tiles, sum(span(t, cost) * U for t in tiles), P, cost
+
+
+def segments(c, tiles, T, P, U, cost):
+    """The segments CTA c visits, in order (SegmentCursor::next)."""
+    if c >= P:
+        return []
+    pos, end = cta_start(c, T, P), cta_start(c + 1, T, P)
+    pre, b, out = 0, 0, []
+    while pos < end:
+        sp = span(tiles[b], cost)
+        while pos >= pre + sp * U:
+            pre += sp * U
+            b += 1
+            sp = span(tiles[b], cost)
+        off = pos - pre
+        uib, v0 = divmod(off, sp)
+        v1 = min(v0 + (end - pos), sp)
+        pos += v1 - v0
+        if v1 <= cost:
+            continue  # only the unit's charge
+        out.append(dict(b=b, uib=uib, t0=max(v0 - cost, 0), t1=v1 - cost, tiles=tiles[b],
+                        unit_first=pre + uib * sp + cost))
+    return out
+
+
+def _check(lens, Nmax, BN, U, P0, unit_cost):
+    tiles, T, P, cost = plan(lens, Nmax, BN, U, P0, unit_cost)
+    owner, segs = {}, {}
+    for c in range(P0):
+        segs[c] = segments(c, tiles, T, P, U, cost)
+        for i, s in enumerate(segs[c]):
+            assert 0 <= s["t0"] < s["t1"] <= s["tiles"]
+            for t in range(s["t0"], s["t1"]):
+                key = (s["b"], s["uib"], t)
+                assert key not in owner, f"tile {key} visited twice"
+                owner[key] = c
+    assert len(owner) == sum(t * U for t in tiles), "a tile was never visited"
+    for c, ss in segs.items():
+        for i, s in enumerate(ss):
+            if s["t0"] == 0 and s["t1"] == s["tiles"]:
+                continue  # whole unit: finished in place
+            assert i in (0, len(ss) - 1), "a unit cut in the middle of a range"
+            c_lo = cta_of_tile(s["unit_first"], T, P)
+            c_hi = cta_of_tile(s["unit_first"] + s["tiles"] - 1, T, P)
+            holders = sorted({owner[(s["b"], s["uib"], t)] for t in range(s["tiles"])})
+            assert holders == list(range(c_lo, c_hi + 1))
+            first = [k for k, x in enumerate(segs[c_lo]) if (x["b"], x["uib"]) == (s["b"], s["uib"])][0]
+            slot0 = 2 * c_lo if cta_start(c_lo, T, P) >= s["unit_first"] - cost else 2 * c_lo + 1
+            assert slot0 == 2 * c_lo + (0 if first == 0 else 1)
+            for cc in range(c_lo + 1, c_hi + 1):
+                k = [k for k, x in enumerate(segs[cc]) if (x["b"], x["uib"]) == (s["b"], s["uib"])][0]
+                assert k == 0, "a later CTA's piece of a cut unit must be its first segment"
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_schedule_covers_every_tile_once_and_merges_consistently(seed):
+    rng = random.Random(seed)
+    for _ in range(300):
+        B = rng.randint(1, 70)
+        Nmax = rng.choice([128, 300, 1000, 4096])
+        mode = rng.random()
+        if mode < 0.3:
+            lens = [Nmax] * B
+        elif mode < 0.5:
+            lens = [rng.choice([0, Nmax, rng.randint(1, Nmax)]) for _ in range(B)]
+        else:
+            lens = [rng.randint(0, Nmax) for _ in range(B)]
+        _check(lens, Nmax, rng.choice([64, 128]), rng.choice([1, 2, 4, 8, 16]), rng.choice([1, 7, 148, 296]),
+               rng.choice([0, 1, 2, 3]))
+
+
+def test_charge_moves_real_tiles_away_from_ranges_with_many_units():
+    """Ragged lengths: a CTA whose range crosses many short sequences gets
+    fewer real tiles than one inside a long sequence."""
+    lens = [8192] * 4 + [130] * 40
+    tiles, T, P, cost = plan(lens, 8192, 128, 8, 148, 2)
+    assert cost == 2
+    per_cta = [(sum(s["t1"] - s["t0"] for s in segments(c, tiles, T, P, 8, cost)), len(segments(c, tiles, T, P, 8, cost)))
+               for c in range(P)]
+    many = [t for t, n in per_cta if n >= 4]
+    one = [t for t, n in per_cta if n == 1]
+    assert many and one and max(many) < min(one)
