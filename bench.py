@@ -72,16 +72,20 @@ def hbm_peak():
     return FALLBACK_HBM_GBS, "fallback 6.4 TB/s"
 
 
+# Device sources of the decode-attention kernels (split kernels, merge,
+# append): an ncu traffic figure is only reported while it was taken on
+# these exact sources.
+STEP_KERNEL_SOURCES = ("gqa_device.cuh", "gqa_params.cuh", "gqa_schedule.cuh", "gqa_pipeline.cuh", "gqa_merge.cuh",
+                       "gqa_tcgen05.cuh", "gqa_split_simt.cuh", "gqa_split_mma.cuh", "gqa_split_tc.cuh",
+                       "gqa_small_kernels.cuh")
+
+
 def kernel_source_hash() -> str:
-    """Hash of the CUDA sources; an ncu traffic figure is only reported while
-    it was taken on the same sources."""
+    """Hash of the decode-attention kernels' device sources."""
     h = hashlib.sha256()
-    for fn in sorted(os.listdir(CSRC)):
-        if fn.endswith((".cu", ".cuh")):
-            with open(os.path.join(CSRC, fn), "rb") as f:
-                h.update(fn.encode() + f.read())
-    with open(os.path.join(ROOT, "include", "gqa.h"), "rb") as f:
-        h.update(f.read())
+    for fn in STEP_KERNEL_SOURCES:
+        with open(os.path.join(CSRC, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
 
 
