@@ -53,6 +53,8 @@ def _bind(path: str):
     lib.oracle_softmax_weights.restype = ci
     lib.oracle_kv_append.argtypes = [vp, vp, vp, vp, i32p, ci, ci, ci, ci, ci]
     lib.oracle_kv_append.restype = ci
+    lib.oracle_qkv_project.argtypes = [vp, vp, vp, vp, f64p, f64p, f64p, ci, ci, ci, ci, ci, ci, ci]
+    lib.oracle_qkv_project.restype = ci
     lib.oracle_meanpool.argtypes = [vp, f64p, ci, ci, ctypes.c_long, ci]
     lib.oracle_meanpool.restype = ci
     return lib
@@ -162,6 +164,25 @@ def kv_append(k_new, v_new, k_cache, v_cache, seq_lens):
     skipped = _load().oracle_kv_append(kn.data_ptr(), vn.data_ptr(), k.data_ptr(), v.data_ptr(),
                                        _i32p(sl), B, G, d, Nmax, k.element_size())
     return k, v, sl, int(skipped)
+
+
+def qkv_project(x, w_q, w_k, w_v, nthreads: int = 0):
+    """fp64 numpy (q [B,H,d], k [B,G,d], v [B,G,d]) for x [B,A] and the
+    projection weights w_q [H,A,d], w_k / w_v [G,A,d] (one dtype)."""
+    x, wq, wk, wv = _cpu(x), _cpu(w_q), _cpu(w_k), _cpu(w_v)
+    B, A = x.shape
+    H, A2, d = wq.shape
+    G = wk.shape[0]
+    assert A2 == A and tuple(wk.shape) == tuple(wv.shape) == (G, A, d)
+    assert x.dtype == wq.dtype == wk.dtype == wv.dtype
+    q = np.zeros((B, H, d), dtype=np.float64)
+    k = np.zeros((B, G, d), dtype=np.float64)
+    v = np.zeros((B, G, d), dtype=np.float64)
+    rc = _load().oracle_qkv_project(x.data_ptr(), wq.data_ptr(), wk.data_ptr(), wv.data_ptr(), _f64p(q), _f64p(k),
+                                    _f64p(v), B, A, H, G, d, _dtype_code(x), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_qkv_project rejected its arguments")
+    return q, k, v
 
 
 def meanpool(w, G: int) -> np.ndarray:

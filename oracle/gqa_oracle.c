@@ -26,6 +26,8 @@
  *    section "MQA 的推导" gives the shared-K/V (G = 1) form.
  *  - CSDN interview post on GQA, section 03: the key/value pair is repeated
  *    n_rep times, n_rep being the number of query heads sharing it.
+ *  - CSDN blog, section "MQA 的推导", and 2kiu.com explainer, section 3.2:
+ *    the per-head Q and per-group K/V projections (oracle_qkv_project).
  *  - GQA paper, section 4: speculative sampling scores several proposed
  *    tokens in one pass (oracle_decode_attention_multi; the causal rule among
  *    the T new tokens is the plain reading of scoring a proposed run).
@@ -210,6 +212,43 @@ int oracle_kv_append(const void *k_new, const void *v_new, void *k_cache, void *
         seq_lens[b] = L + 1;
     }
     return skipped;
+}
+
+/*
+ * Q/K/V projections of the decode token.  CSDN blog on MQA/GQA, section
+ * "MQA 的推导": q = einsum('ba,had->bhd', x, P_q) with P_q [h, a, d], and
+ * the shared K/V projection loses the head axis for MQA; with G KV heads
+ * (2kiu.com explainer, section 3.2, steps 2-3: every query head computes its
+ * own Q with its own weights, every group one K and one V with the group's
+ * weights) k = einsum('ba,gad->bgd', x, P_k), v likewise.
+ * x [B, A] (A = model width), P_q [H, A, d], P_k and P_v [G, A, d];
+ * q [B, H, d], k and v [B, G, d] in fp64.
+ */
+static void project_heads(const void *x, const void *p, double *out, int B, int A, int nh, int d, int dtype,
+                          int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static)
+#endif
+    for (long bh = 0; bh < (long)B * nh; ++bh) {
+        int b = (int)(bh / nh), h = (int)(bh % nh);
+        for (int j = 0; j < d; ++j) {
+            double s = 0.0;
+            for (int a = 0; a < A; ++a)
+                s += load_value(x, (size_t)b * A + a, dtype) *
+                     load_value(p, ((size_t)h * A + a) * d + j, dtype);
+            out[((size_t)b * nh + h) * d + j] = s;
+        }
+    }
+}
+
+int oracle_qkv_project(const void *x, const void *pq, const void *pk, const void *pv, double *q, double *k,
+                       double *v, int B, int A, int H, int G, int d, int dtype, int nthreads) {
+    if (B <= 0 || A <= 0 || H <= 0 || G <= 0 || d <= 0 || H % G != 0) return -1;
+    project_heads(x, pq, q, B, A, H, d, dtype, nthreads);
+    project_heads(x, pk, k, B, A, G, d, dtype, nthreads);
+    project_heads(x, pv, v, B, A, G, d, dtype, nthreads);
+    return 0;
 }
 
 /*

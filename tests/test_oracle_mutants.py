@@ -34,6 +34,10 @@ PIN_BATTERY = [
     pins.test_multi_token_is_causal_prefix_attention,
     pins.test_multi_token_sees_nothing_before_the_cache,
     pins.test_multi_token_brute_force,
+    pins.test_projection_with_identity_weights_slices_x,
+    pins.test_projection_of_mean_pooled_weights_is_the_group_mean,
+    pins.test_projection_matches_the_blog_einsums,
+    pins.test_projection_brute_force,
 ]
 
 # (name, text in the oracle source, replacement)
@@ -51,6 +55,11 @@ MUTANTS = [
     ("several tokens: every token reads token 0's query", "head_weights(q, k, (size_t)bth * d,",
      "head_weights(q, k, ((size_t)b * T * H + h) * d,"),
     ("several tokens: K used in place of V", "o[i] += w[n] * load_value(v, kvo", "o[i] += w[n] * load_value(k, kvo"),
+    ("projection reads the weight transposed", "load_value(p, ((size_t)h * A + a) * d + j, dtype)",
+     "load_value(p, ((size_t)h * d + j) * A + a, dtype)"),
+    ("K projected with the query weights", "project_heads(x, pk, k,", "project_heads(x, pq, k,"),
+    ("projection drops the last input feature", "for (int a = 0; a < A; ++a)\n                s += load_value(x,",
+     "for (int a = 0; a < A - 1; ++a)\n                s += load_value(x,"),
     ("q read reversed", "load_value(q, q_off + i, dtype)", "load_value(q, q_off + (d - 1 - i), dtype)"),
     ("wrong sign of logits", "w[n] = dot * scale;", "w[n] = -dot * scale;"),
     ("meanpool sums instead of averaging", "w_out[(size_t)g * per_head + e] = s / n_rep;",

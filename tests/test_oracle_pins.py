@@ -347,3 +347,74 @@ def test_multi_token_brute_force():
             for i in range(d):
                 ref = mpmath.fsum(e[n] * mpmath.mpf(float(v[0, gg, n, i])) for n in range(vis)) / z
                 assert abs(out[0, t, h, i] - float(ref)) < 1e-14
+
+
+# ------------------------------------------------------- Q/K/V projections
+def _proj_case(B, A, H, G, d, seed, dtype=torch.float32):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(B, A, generator=g).to(dtype)
+    wq = torch.randn(H, A, d, generator=g).to(dtype)
+    wk = torch.randn(G, A, d, generator=g).to(dtype)
+    wv = torch.randn(G, A, d, generator=g).to(dtype)
+    return x, wq, wk, wv
+
+
+def test_projection_with_identity_weights_slices_x():
+    """P[h, a, j] = 1 where a = h*d + j: head h's output is x's h-th d-slice
+    (the blog's a = h*d layout of the hidden vector)."""
+    B, H, G, d = 3, 4, 2, 8
+    A = H * d
+    x = torch.randn(B, A, generator=torch.Generator().manual_seed(40))
+    eye = torch.zeros(H, A, d)
+    for h in range(H):
+        for j in range(d):
+            eye[h, h * d + j, j] = 1.0
+    q, k, v = oracle.qkv_project(x, eye, eye[:G], eye[G:2 * G].clone() if 2 * G <= H else eye[:G], 0)
+    np.testing.assert_array_equal(q, x.double().numpy().reshape(B, H, d))
+    np.testing.assert_array_equal(k, x.double().numpy().reshape(B, H, d)[:, :G])
+
+
+def test_projection_of_mean_pooled_weights_is_the_group_mean():
+    """GQA paper, section 2.1: K/V heads of a converted checkpoint are the
+    mean-pooled MHA heads; by linearity their projection is the mean of the
+    group's MHA projections (ties the projection to the conversion oracle)."""
+    B, A, H, G, d = 2, 24, 8, 2, 4
+    g = torch.Generator().manual_seed(41)
+    # small integers: every mean of 4 and every product sum is exact in fp32 / fp64
+    x = torch.randint(-4, 5, (B, A), generator=g).float()
+    wq = torch.randint(-4, 5, (H, A, d), generator=g).float()
+    wk_mha = torch.randint(-4, 5, (H, A, d), generator=g).float()
+    wv_mha = torch.randint(-4, 5, (H, A, d), generator=g).float()
+    wk = torch.from_numpy(oracle.meanpool(wk_mha, G)).float()
+    wv = torch.from_numpy(oracle.meanpool(wv_mha, G)).float()
+    _, k_mha, v_mha = oracle.qkv_project(x, wq, wk_mha, wv_mha)
+    _, k, v = oracle.qkv_project(x, wq[:G].contiguous(), wk, wv)
+    np.testing.assert_array_equal(k, k_mha.reshape(B, G, H // G, d).mean(axis=2))
+    np.testing.assert_array_equal(v, v_mha.reshape(B, G, H // G, d).mean(axis=2))
+
+
+def test_projection_matches_the_blog_einsums():
+    """The blog's MHA lines q = einsum('ba,had->bhd') and, for MQA,
+    k = einsum('ba,ad->bd') (P_k without a head axis)."""
+    B, A, H, d = 3, 16, 4, 5
+    x, wq, wk, wv = _proj_case(B, A, H, 1, d, 42)
+    q, k, v = oracle.qkv_project(x, wq, wk, wv)
+    np.testing.assert_allclose(q, np.einsum("ba,had->bhd", x.double().numpy(), wq.double().numpy()), rtol=1e-12)
+    np.testing.assert_allclose(k[:, 0], np.einsum("ba,ad->bd", x.double().numpy(), wk[0].double().numpy()),
+                               rtol=1e-12)
+    np.testing.assert_allclose(v[:, 0], np.einsum("ba,ad->bd", x.double().numpy(), wv[0].double().numpy()),
+                               rtol=1e-12)
+
+
+def test_projection_brute_force():
+    import mpmath
+    mpmath.mp.dps = 40
+    B, A, H, G, d = 2, 5, 4, 2, 3
+    x, wq, wk, wv = _proj_case(B, A, H, G, d, 43, torch.bfloat16)
+    q, k, v = oracle.qkv_project(x, wq, wk, wv)
+    for out, w, nh in ((q, wq, H), (k, wk, G), (v, wv, G)):
+        for b in range(B):
+            for h in range(nh):
+                for j in range(d):
+                    ref = mpmath.fsum(mpmath.mpf(float(x[b, a])) * mpmath.mpf(float(w[h, a, j])) for a in range(A))
+                    assert abs(out[b, h, j] - float(ref)) < 1e-13 * (1 + abs(float(ref)))
