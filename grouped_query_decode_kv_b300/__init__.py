@@ -17,6 +17,8 @@ Entry points (see ``include/gqa.h`` for the full contract):
   gqa_decode_step_ws(..., workspace)             append + attention in one launch
   gqa_decode_attention_multi(q[B,T,H,d], ..., out[B,T,H,d])   T query tokens per sequence
   gqa_decode_attention_multi_ex(..., split_tokens, workspace)
+  gqa_qkv_project(x, w_q, w_k, w_v, q, k_new, v_new)   Q/K/V projections of the token
+  gqa_qkv_project_ws(..., workspace), gqa_qkv_project_workspace_bytes(B, A, H, G, d)
   kv_append(k_new, v_new, k_cache, v_cache, seq_lens)
   mha_to_gqa_meanpool(w, w_out)
   gqa_get_device_error()
@@ -41,6 +43,7 @@ __all__ = [
     "gqa_decode_attention_noalloc", "NOALLOC_SCRATCH_BYTES", "ERR_SCRATCH_LIMIT",
     "gqa_decode_step", "gqa_decode_step_ws",
     "gqa_decode_attention_multi", "gqa_decode_attention_multi_ex",
+    "gqa_qkv_project", "gqa_qkv_project_ws", "gqa_qkv_project_workspace_bytes",
     "DEVERR_ATTN_LEN", "DEVERR_APPEND_LEN", "DEVERR_TIMEOUT", "EXPORTED_SYMBOLS",
 ]
 
@@ -55,6 +58,7 @@ EXPORTED_SYMBOLS = (
     "mha_to_gqa_meanpool", "gqa_get_device_error", "gqa_status_string",
     "gqa_decode_attention_noalloc", "gqa_decode_step", "gqa_decode_step_ws",
     "gqa_decode_attention_multi", "gqa_decode_attention_multi_ex",
+    "gqa_qkv_project", "gqa_qkv_project_ws", "gqa_qkv_project_workspace_bytes",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -105,6 +109,13 @@ def load_library():
         lib.gqa_decode_workspace_bytes.restype = sz
         lib.gqa_decode_workspace_bytes_ex.argtypes = [ci] * 7
         lib.gqa_decode_workspace_bytes_ex.restype = sz
+        proj = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci]
+        lib.gqa_qkv_project.argtypes = proj + [vp]
+        lib.gqa_qkv_project.restype = ci
+        lib.gqa_qkv_project_ws.argtypes = proj + [vp, sz, vp]
+        lib.gqa_qkv_project_ws.restype = ci
+        lib.gqa_qkv_project_workspace_bytes.argtypes = [ci] * 5
+        lib.gqa_qkv_project_workspace_bytes.restype = sz
         lib.kv_append.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, vp]
         lib.kv_append.restype = ci
         lib.mha_to_gqa_meanpool.argtypes = [vp, vp, ci, ci, ci, ci, ci, vp]
@@ -303,6 +314,47 @@ def gqa_decode_step_ws(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out, 
            lib.gqa_decode_step_ws(*_step_args(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out), wp, wn,
                                   _stream(q, stream)))
     return out
+
+
+def _proj_args(x, w_q, w_k, w_v, q, k_new, v_new):
+    if x.dim() != 2 or w_q.dim() != 3 or w_k.dim() != 3 or w_k.shape != w_v.shape:
+        raise ValueError("x [B,A], w_q [H,A,d], w_k and w_v [G,A,d]")
+    B, A = x.shape
+    H, A2, d = w_q.shape
+    G = w_k.shape[0]
+    if A2 != A or w_k.shape[1] != A or w_k.shape[2] != d:
+        raise ValueError("x and the weights disagree on A or d")
+    if tuple(q.shape) != (B, H, d) or tuple(k_new.shape) != (B, G, d) or tuple(v_new.shape) != (B, G, d):
+        raise ValueError("q must be [B,H,d], k_new and v_new [B,G,d]")
+    ts = (x, w_q, w_k, w_v, q, k_new, v_new)
+    if any(t.dtype != x.dtype for t in ts):
+        raise ValueError("all tensors must share one dtype")
+    names = ("x", "w_q", "w_k", "w_v", "q", "k_new", "v_new")
+    return [_dev(t, n) for t, n in zip(ts, names)] + [B, A, H, G, d, _dtype_code(x)]
+
+
+def gqa_qkv_project_workspace_bytes(B, A, H, G, d) -> int:
+    return int(load_library().gqa_qkv_project_workspace_bytes(B, A, H, G, d))
+
+
+def gqa_qkv_project(x, w_q, w_k, w_v, q, k_new, v_new, stream=None):
+    """q[b,h] = x[b] . w_q[h], k_new[b,g] = x[b] . w_k[g], v_new likewise
+    (x [B,A], weights [heads,A,d], bf16).  Workspace from the stream-ordered
+    allocator."""
+    lib = load_library()
+    _check("gqa_qkv_project", lib.gqa_qkv_project(*_proj_args(x, w_q, w_k, w_v, q, k_new, v_new),
+                                                  _stream(x, stream)))
+    return q, k_new, v_new
+
+
+def gqa_qkv_project_ws(x, w_q, w_k, w_v, q, k_new, v_new, workspace, stream=None):
+    """As gqa_qkv_project with a caller-owned workspace of at least
+    gqa_qkv_project_workspace_bytes(B, A, H, G, d) bytes."""
+    lib = load_library()
+    wp, wn = _ws(workspace)
+    _check("gqa_qkv_project_ws", lib.gqa_qkv_project_ws(*_proj_args(x, w_q, w_k, w_v, q, k_new, v_new), wp, wn,
+                                                        _stream(x, stream)))
+    return q, k_new, v_new
 
 
 def kv_append(k_new, v_new, k_cache, v_cache, seq_lens, stream=None):

@@ -13,6 +13,7 @@
 #include "gqa.h"
 #include "gqa_device.cuh"
 #include "gqa_params.cuh"
+#include "gqa_proj_tc.cuh"
 #include "gqa_small_kernels.cuh"
 #include "gqa_split_mma.cuh"
 #include "gqa_split_simt.cuh"
@@ -449,6 +450,149 @@ int noalloc_scratch(void **ptr) {
 }  // namespace
 }  // namespace gqa
 
+namespace gqa {
+namespace {
+// ----------------------------------------------------------- Q/K/V projections
+constexpr int kProjMaxBatch = 256;  // batch rows per launch (N of the MMA); larger batches run in chunks
+
+int proj_nb(int B) {
+  int nb = 16;
+  while (nb < B) nb *= 2;
+  return nb;
+}
+
+struct ProjPlan {
+  int nb;      // padded batch columns of one launch
+  int items;   // projection items (128 output features each)
+  int items_q, items_kv;
+  int ktiles;
+  int P;       // CTAs
+};
+
+ProjPlan make_proj_plan(int B, int A, int H, int G, int d) {
+  ProjPlan pl;
+  pl.nb = proj_nb(std::min(B, kProjMaxBatch));
+  pl.items_q = d == 128 ? H : (H + 1) / 2;
+  pl.items_kv = d == 128 ? G : (G + 1) / 2;
+  pl.items = pl.items_q + 2 * pl.items_kv;
+  pl.ktiles = A / 64;
+  const long long T = (long long)pl.items * pl.ktiles;
+  pl.P = (int)std::max<long long>(1, std::min<long long>(T, device_sm_count()));
+  return pl;
+}
+
+size_t proj_part_bytes(const ProjPlan &pl) { return align256((size_t)2 * pl.P * pl.nb * 128 * sizeof(float)); }
+size_t proj_workspace(const ProjPlan &pl) {
+  if (pl.P <= 1) return 0;
+  return proj_part_bytes(pl) + align256((size_t)pl.items * sizeof(unsigned long long));
+}
+
+int check_proj_args(const void *x, const void *wq, const void *wk, const void *wv, const void *q, const void *k,
+                    const void *v, int B, int A, int H, int G, int d, gqa_dtype_t dt) {
+  if (!x || !wq || !wk || !wv || !q || !k || !v) return GQA_ERR_INVALID_ARG;
+  if (B <= 0 || A <= 0 || H <= 0 || G <= 0 || d <= 0 || H % G != 0) return GQA_ERR_INVALID_ARG;
+  if (dt != GQA_F32 && dt != GQA_BF16) return GQA_ERR_INVALID_ARG;
+  if (dt != GQA_BF16 || (d != 64 && d != 128) || A % 64 != 0) return GQA_ERR_UNSUPPORTED;
+  if ((long long)A * 2 >= (1LL << 40) || H > 65535 || B > (1 << 24)) return GQA_ERR_UNSUPPORTED;
+  for (const void *ptr : {x, wq, wk, wv, q, k, v})
+    if (!aligned16(ptr)) return GQA_ERR_INVALID_ARG;
+  return GQA_OK;
+}
+
+// P [heads, A, d] bf16 as a 3-D tensor (d, A, heads); a box is 64 outputs
+// (128 bytes) by 64 inputs of one head, 128-byte swizzled.
+bool encode_weight_map(CUtensorMap *map, const void *w, int heads, int A, int d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)A, (cuuint64_t)heads};
+  cuuint64_t strides[2] = {(cuuint64_t)(d * 2), (cuuint64_t)((size_t)A * d * 2)};
+  cuuint32_t box[3] = {64, 64, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(w), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// x [B, A] bf16 as a 2-D tensor; a box is 64 inputs by `nb` rows (rows past
+// B read as zeros), 128-byte swizzled: the K-major B operand.
+bool encode_x_map(CUtensorMap *map, const void *x, int B, int A, int nb) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)A, (cuuint64_t)B};
+  cuuint64_t strides[1] = {(cuuint64_t)A * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)nb};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NB>
+int launch_proj(const CUtensorMap &mx, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                const ProjParams &p, int P, cudaStream_t st) {
+  using C = ProjCfg<NB>;
+  static std::once_flag once[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return GQA_ERR_CUDA;
+  bool attr_ok = true;
+  std::call_once(once[dev], [&] {
+    attr_ok = cudaFuncSetAttribute(gqa_qkv_proj_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   C::SMEM_BYTES) == cudaSuccess;
+  });
+  if (!attr_ok ||
+      launch_pdl(gqa_qkv_proj_kernel<C>, dim3(P), dim3(C::THREADS), C::SMEM_BYTES, st, mx, mq, mk, mv, p) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return GQA_ERR_CUDA;
+  }
+  return GQA_OK;
+}
+
+int run_projection(const void *x, const void *wq, const void *wk, const void *wv, void *q, void *k, void *v, int B,
+                   int A, int H, int G, int d, void *ws, cudaStream_t st) {
+  const ProjPlan pl = make_proj_plan(B, A, H, G, d);
+  CUtensorMap mq, mk, mv;
+  if (!encode_weight_map(&mq, wq, H, A, d) || !encode_weight_map(&mk, wk, G, A, d) ||
+      !encode_weight_map(&mv, wv, G, A, d))
+    return GQA_ERR_CUDA;
+  char *w = reinterpret_cast<char *>(ws);
+  for (int b0 = 0; b0 < B; b0 += kProjMaxBatch) {
+    const int nbat = std::min(kProjMaxBatch, B - b0);
+    const int nb = proj_nb(nbat);
+    CUtensorMap mx;
+    if (!encode_x_map(&mx, reinterpret_cast<const char *>(x) + (size_t)b0 * A * 2, nbat, A, nb)) return GQA_ERR_CUDA;
+    ProjParams p;
+    p.out[0] = reinterpret_cast<char *>(q) + (size_t)b0 * H * d * 2;
+    p.out[1] = reinterpret_cast<char *>(k) + (size_t)b0 * G * d * 2;
+    p.out[2] = reinterpret_cast<char *>(v) + (size_t)b0 * G * d * 2;
+    p.heads[0] = H;
+    p.heads[1] = G;
+    p.heads[2] = G;
+    p.item_start[0] = 0;
+    p.item_start[1] = pl.items_q;
+    p.item_start[2] = pl.items_q + pl.items_kv;
+    p.item_start[3] = pl.items;
+    p.ktiles = pl.ktiles;
+    p.B = nbat;
+    p.d = d;
+    p.part = pl.P > 1 ? reinterpret_cast<float *>(w) : nullptr;
+    p.item_cnt = pl.P > 1 ? reinterpret_cast<unsigned long long *>(w + proj_part_bytes(pl)) : nullptr;
+    p.epoch = next_epoch();
+    int rc;
+    switch (nb) {
+      case 16: rc = launch_proj<16>(mx, mq, mk, mv, p, pl.P, st); break;
+      case 32: rc = launch_proj<32>(mx, mq, mk, mv, p, pl.P, st); break;
+      case 64: rc = launch_proj<64>(mx, mq, mk, mv, p, pl.P, st); break;
+      case 128: rc = launch_proj<128>(mx, mq, mk, mv, p, pl.P, st); break;
+      default: rc = launch_proj<256>(mx, mq, mk, mv, p, pl.P, st); break;
+    }
+    if (rc) return rc;
+  }
+  return GQA_OK;
+}
+}  // namespace
+}  // namespace gqa
+
 using namespace gqa;
 
 extern "C" {
@@ -611,6 +755,36 @@ int gqa_decode_attention_multi(const void *q, const void *k_cache, const void *v
   }
   int rc = run_attention(q, k_cache, v_cache, seq_lens, scale, out, B, H, G, d, Nmax, dtype, pl, ws, stream,
                          StepAppend(), T);
+  if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && rc == GQA_OK) rc = GQA_ERR_CUDA;
+  return rc;
+}
+
+
+size_t gqa_qkv_project_workspace_bytes(int B, int A, int H, int G, int d) {
+  if (B <= 0 || A <= 0 || H <= 0 || G <= 0 || H % G != 0 || (d != 64 && d != 128) || A % 64 != 0) return 0;
+  return proj_workspace(make_proj_plan(B, A, H, G, d));
+}
+
+int gqa_qkv_project_ws(const void *x, const void *w_q, const void *w_k, const void *w_v, void *q, void *k_new,
+                       void *v_new, int B, int A, int H, int G, int d, gqa_dtype_t dtype, void *workspace,
+                       size_t workspace_bytes, cudaStream_t stream) {
+  if (int rc = check_proj_args(x, w_q, w_k, w_v, q, k_new, v_new, B, A, H, G, d, dtype)) return rc;
+  const size_t need = proj_workspace(make_proj_plan(B, A, H, G, d));
+  if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+    return GQA_ERR_INVALID_ARG;
+  return run_projection(x, w_q, w_k, w_v, q, k_new, v_new, B, A, H, G, d, workspace, stream);
+}
+
+int gqa_qkv_project(const void *x, const void *w_q, const void *w_k, const void *w_v, void *q, void *k_new,
+                    void *v_new, int B, int A, int H, int G, int d, gqa_dtype_t dtype, cudaStream_t stream) {
+  if (int rc = check_proj_args(x, w_q, w_k, w_v, q, k_new, v_new, B, A, H, G, d, dtype)) return rc;
+  const size_t need = proj_workspace(make_proj_plan(B, A, H, G, d));
+  void *ws = nullptr;
+  if (need > 0 && cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GQA_ERR_NO_MEMORY;
+  }
+  int rc = run_projection(x, w_q, w_k, w_v, q, k_new, v_new, B, A, H, G, d, ws, stream);
   if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && rc == GQA_OK) rc = GQA_ERR_CUDA;
   return rc;
 }

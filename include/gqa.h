@@ -231,6 +231,41 @@ int gqa_decode_attention_multi_ex(const void *q, const void *k_cache, const void
                                   cudaStream_t stream);
 
 /*
+ * gqa_qkv_project — the Q, K and V projections of the decode token, the step
+ * before kv_append: every query head computes its own query with its own
+ * weights, every group one shared key and one shared value with the group's
+ * weights (2kiu.com explainer, section 3.2, steps 2-3; CSDN blog on MQA/GQA,
+ * section "MQA 的推导": q = einsum('ba,had->bhd', x, P_q), with the head axis
+ * of P_k and P_v reduced to the G KV heads).
+ *
+ *   q[b,h,:]     = sum_a x[b,a] * w_q[h,a,:]
+ *   k_new[b,g,:] = sum_a x[b,a] * w_k[g,a,:]
+ *   v_new[b,g,:] = sum_a x[b,a] * w_v[g,a,:]
+ *
+ *   x   [B, A]     the token's hidden vector (A = model width)
+ *   w_q [H, A, d], w_k and w_v [G, A, d]  (the blog's [h, a, d] layout)
+ *   q [B, H, d], k_new and v_new [B, G, d]: the inputs of kv_append /
+ *   gqa_decode_step.  Accumulated in fp32, rounded to nearest even.
+ * bf16 only (GQA_ERR_UNSUPPORTED for fp32); d in {64, 128}; A % 64 == 0;
+ * H % G == 0; pointers 16-byte aligned; any B (batches of more than 256 rows
+ * run in chunks of 256).  The weights are read from HBM once per 256 rows:
+ * the call is bound by those (H + 2G) * A * d * 2 bytes.  Results are
+ * deterministic (a split projection head is summed in a fixed order).
+ * gqa_qkv_project takes its workspace from the stream-ordered allocator;
+ * gqa_qkv_project_ws from the caller: gqa_qkv_project_workspace_bytes
+ * bytes (0 = none needed, or an invalid shape), 256-byte aligned, needing
+ * no initialisation.  Calls sharing a workspace must not overlap.
+ */
+size_t gqa_qkv_project_workspace_bytes(int B, int A, int H, int G, int d);
+int gqa_qkv_project(const void *x, const void *w_q, const void *w_k, const void *w_v,
+                    void *q, void *k_new, void *v_new, int B, int A, int H, int G, int d,
+                    gqa_dtype_t dtype, cudaStream_t stream);
+int gqa_qkv_project_ws(const void *x, const void *w_q, const void *w_k, const void *w_v,
+                       void *q, void *k_new, void *v_new, int B, int A, int H, int G, int d,
+                       gqa_dtype_t dtype, void *workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
+/*
  * kv_append — the cache concatenation of one decode step (fogdragon's CSDN
  * blog, section "KV Cache": K = cat([K_prev, k]), V = cat([V_prev, v])).
  *

@@ -147,3 +147,23 @@ def test_multi_token_ex_rejects_missing_workspace(lib):
     args = (FAKE, FAKE, FAKE, FAKE, 0.1, FAKE, 2, 4, 8, 2, 128, 4096, 1, 256)
     assert lib.gqa_decode_attention_multi_ex(*args, None, 0, None) == -1
     assert lib.gqa_decode_attention_multi_ex(*args, FAKE, need - 1, None) == -1
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=0), -1), (dict(B=0), -1), (dict(H=8, G=3), -1), (dict(dt=0), -2), (dict(d=96), -2),
+    (dict(A=100), -2), (dict(wk=FAKE + 8), -1), (dict(dt=5), -1),
+])
+def test_projection_rejects_bad_arguments(lib, kw, status):
+    a = dict(x=FAKE, wq=FAKE, wk=FAKE, wv=FAKE, q=FAKE, k=FAKE, v=FAKE, B=4, A=256, H=8, G=2, d=128, dt=1)
+    a.update(kw)
+    assert lib.gqa_qkv_project(a["x"], a["wq"], a["wk"], a["wv"], a["q"], a["k"], a["v"], a["B"], a["A"], a["H"],
+                               a["G"], a["d"], a["dt"], None) == status
+
+
+def test_projection_workspace(lib):
+    # one 128-feature item per projection head and A/64 tiles each: 12 items x 4 tiles
+    need = lib.gqa_qkv_project_workspace_bytes(4, 256, 8, 2, 128)
+    assert need >= 2 * 2 * 16 * 128 * 4       # at least two CTAs' partial slots
+    assert lib.gqa_qkv_project_workspace_bytes(4, 100, 8, 2, 128) == 0   # A % 64 != 0
+    args = (FAKE,) * 7 + (4, 256, 8, 2, 128, 1)
+    assert lib.gqa_qkv_project_ws(*args, None, 0, None) == -1

@@ -34,7 +34,8 @@ from typing import Dict, Optional, Tuple
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "workload", "make_inputs", "sweep_names", "multi_names"]
+__all__ = ["Workload", "WORKLOADS", "workload", "make_inputs", "sweep_names", "multi_names", "make_qkv_inputs",
+           "PROJECTIONS"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -159,3 +160,25 @@ def make_projection(H: int, d: int, D: int, seed: int, dtype: torch.dtype) -> to
     mean-pool conversion, from ``manual_seed(seed)``."""
     g = torch.Generator().manual_seed(seed)
     return torch.randn(H, d, D, generator=g).to(dtype)
+
+
+# Q/K/V projection layers (the step before the cache append): model width A =
+# H*d as in the blog's `a = hd`, batch B rows of the decode token.
+PROJECTIONS = {
+    "proj_7b": dict(B=8, A=4096, H=32, G=32, d=128, seed=701),
+    "proj_70b": dict(B=16, A=8192, H=64, G=8, d=128, seed=702),
+}
+
+
+def make_qkv_inputs(B: int, A: int, H: int, G: int, d: int, seed: int,
+                    dtype: torch.dtype = torch.bfloat16) -> Dict[str, torch.Tensor]:
+    """x [B,A] ~ N(0,1) and projection weights w_q [H,A,d], w_k / w_v [G,A,d]
+    ~ N(0, 1/A) (so that the outputs are of unit scale), drawn in that order
+    from ``manual_seed(seed)`` in fp32, then rounded to `dtype`."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(B, A, generator=g)
+    s = A ** -0.5
+    wq = torch.randn(H, A, d, generator=g) * s
+    wk = torch.randn(G, A, d, generator=g) * s
+    wv = torch.randn(G, A, d, generator=g) * s
+    return {"x": x.to(dtype), "w_q": wq.to(dtype), "w_k": wk.to(dtype), "w_v": wv.to(dtype)}
