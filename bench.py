@@ -393,6 +393,46 @@ def time_multi(w: workloads.Workload, device, iters: int, warm: int, l2_bytes: i
     return row
 
 
+def time_projection(name: str, device, iters: int, l2_bytes: int, mem_budget: int):
+    """Table row of a Q/K/V projection layer: device time per
+    gqa_qkv_project_ws call from CUDA-graph replays over rotating weight
+    copies (together >= 3 x L2), GB/s of the weight, x and q/k/v bytes."""
+    import grouped_query_decode_kv_b300 as gqa
+    c = workloads.PROJECTIONS[name]
+    B, A, H, G, d = c["B"], c["A"], c["H"], c["G"], c["d"]
+    wbytes = (H + 2 * G) * A * d * 2
+    copies = max(2, min(64, math.ceil(3 * l2_bytes / wbytes), max(1, mem_budget // wbytes)))
+    g = torch.Generator(device=device).manual_seed(c["seed"])
+    s = A ** -0.5
+    x = torch.randn(B, A, generator=g, device=device).bfloat16()
+    ws_ = [(torch.randn(H, A, d, generator=g, device=device) * s).bfloat16() for _ in range(copies)]
+    wk_ = [(torch.randn(G, A, d, generator=g, device=device) * s).bfloat16() for _ in range(copies)]
+    wv_ = [(torch.randn(G, A, d, generator=g, device=device) * s).bfloat16() for _ in range(copies)]
+    q = torch.empty(B, H, d, dtype=torch.bfloat16, device=device)
+    kn = torch.empty(B, G, d, dtype=torch.bfloat16, device=device)
+    vn = torch.empty(B, G, d, dtype=torch.bfloat16, device=device)
+    need = gqa.gqa_qkv_project_workspace_bytes(B, A, H, G, d)
+    wsp = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+
+    def seq():
+        for i in range(iters):
+            j = i % copies
+            gqa.gqa_qkv_project_ws(x, ws_[j], wk_[j], wv_[j], q, kn, vn, wsp)
+        return iters
+
+    us = _graph_time(seq)
+    err = gqa.gqa_get_device_error()
+    nbytes = cost.qkv_project_bytes(B, A, H, G, d)
+    peak, _ = hbm_peak()
+    row = {"B": B, "A": A, "H": H, "G": G, "d": d, "us": round(us, 2), "bytes": nbytes,
+           "gbs": round(nbytes / us / 1e3, 1), "frac_measured": round(nbytes / us / 1e3 / peak, 3),
+           "tflops": round(cost.qkv_project_flops(B, A, H, G, d) / us / 1e6, 1), "copies": copies,
+           "device_error": err}
+    del ws_, wk_, wv_, wsp
+    torch.cuda.empty_cache()
+    return row
+
+
 def read_ceiling(device) -> float:
     """Read-only streaming ceiling (library reduction over 4 GiB), GB/s."""
     x = torch.ones(2 ** 31, dtype=torch.bfloat16, device=device)
@@ -597,6 +637,7 @@ def run_ours(args, world, rank, local):
     # ---- per-workload table and the read-only ceiling (rank 0 only)
     table = None
     table_multi = None
+    table_proj = None
     ceiling = None
     del st
     torch.cuda.empty_cache()
@@ -608,6 +649,9 @@ def run_ours(args, world, rank, local):
         table_multi = {}
         for name in workloads.multi_names():
             table_multi[name] = time_multi(workloads.workload(name), device, args.table_iters, 5, l2, mem_budget)
+        table_proj = {}
+        for name in sorted(workloads.PROJECTIONS):
+            table_proj[name] = time_projection(name, device, args.table_iters, l2, mem_budget)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -672,6 +716,7 @@ def run_ours(args, world, rank, local):
         "read_ceiling_gbs": ceiling,
         "table": table,
         "table_multi_token": table_multi,
+        "table_qkv_projection": table_proj,
     }
     print(json.dumps(line), flush=True)
     return 0

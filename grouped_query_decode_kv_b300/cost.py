@@ -13,7 +13,7 @@ from __future__ import annotations
 from typing import Iterable
 
 __all__ = ["kv_cache_bytes", "kv_bytes_per_token", "decode_attention_bytes",
-           "decode_attention_flops", "kv_append_bytes", "cache_ratio"]
+           "decode_attention_flops", "kv_append_bytes", "cache_ratio", "qkv_project_bytes", "qkv_project_flops"]
 
 
 def kv_cache_bytes(B: int, G: int, N: int, d: int, elt: int, layers: int = 1) -> int:
@@ -59,3 +59,15 @@ def kv_append_bytes(B: int, G: int, d: int, elt: int) -> int:
     """Algorithmic bytes of one cache append: the new K and V rows read, then
     written into the caches."""
     return 2 * 2 * B * G * d * elt
+
+
+def qkv_project_bytes(B: int, A: int, H: int, G: int, d: int, elt: int = 2) -> int:
+    """Algorithmic bytes of the Q/K/V projections of one decode step (the
+    blog's per-line M terms 'had+ba' for Q and, with G KV heads, 'gad+ba' for
+    K and V): the weights read once, x read, q/k/v written."""
+    return (H + 2 * G) * A * d * elt + B * A * elt + B * (H + 2 * G) * d * elt
+
+
+def qkv_project_flops(B: int, A: int, H: int, G: int, d: int) -> int:
+    """2 flops per multiply-add: 2*B*A*(H + 2G)*d."""
+    return 2 * B * A * (H + 2 * G) * d

@@ -454,6 +454,7 @@ namespace gqa {
 namespace {
 // ----------------------------------------------------------- Q/K/V projections
 constexpr int kProjMaxBatch = 256;  // batch rows per launch (N of the MMA); larger batches run in chunks
+constexpr int kProjKT = 64;         // input features per pipeline stage
 
 int proj_nb(int B) {
   int nb = 16;
@@ -475,7 +476,7 @@ ProjPlan make_proj_plan(int B, int A, int H, int G, int d) {
   pl.items_q = d == 128 ? H : (H + 1) / 2;
   pl.items_kv = d == 128 ? G : (G + 1) / 2;
   pl.items = pl.items_q + 2 * pl.items_kv;
-  pl.ktiles = A / 64;
+  pl.ktiles = A / kProjKT;
   const long long T = (long long)pl.items * pl.ktiles;
   pl.P = (int)std::max<long long>(1, std::min<long long>(T, device_sm_count()));
   return pl;
@@ -492,7 +493,7 @@ int check_proj_args(const void *x, const void *wq, const void *wk, const void *w
   if (!x || !wq || !wk || !wv || !q || !k || !v) return GQA_ERR_INVALID_ARG;
   if (B <= 0 || A <= 0 || H <= 0 || G <= 0 || d <= 0 || H % G != 0) return GQA_ERR_INVALID_ARG;
   if (dt != GQA_F32 && dt != GQA_BF16) return GQA_ERR_INVALID_ARG;
-  if (dt != GQA_BF16 || (d != 64 && d != 128) || A % 64 != 0) return GQA_ERR_UNSUPPORTED;
+  if (dt != GQA_BF16 || (d != 64 && d != 128) || A % kProjKT != 0) return GQA_ERR_UNSUPPORTED;
   if ((long long)A * 2 >= (1LL << 40) || H > 65535 || B > (1 << 24)) return GQA_ERR_UNSUPPORTED;
   for (const void *ptr : {x, wq, wk, wv, q, k, v})
     if (!aligned16(ptr)) return GQA_ERR_INVALID_ARG;
@@ -506,7 +507,7 @@ bool encode_weight_map(CUtensorMap *map, const void *w, int heads, int A, int d)
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)A, (cuuint64_t)heads};
   cuuint64_t strides[2] = {(cuuint64_t)(d * 2), (cuuint64_t)((size_t)A * d * 2)};
-  cuuint32_t box[3] = {64, 64, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)kProjKT, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(w), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -530,7 +531,7 @@ bool encode_x_map(CUtensorMap *map, const void *x, int B, int A, int nb) {
 template <int NB>
 int launch_proj(const CUtensorMap &mx, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                 const ProjParams &p, int P, cudaStream_t st) {
-  using C = ProjCfg<NB>;
+  using C = ProjCfg<NB, kProjKT>;
   static std::once_flag once[kMaxDevices];
   const int dev = current_device();
   if (dev < 0) return GQA_ERR_CUDA;
@@ -761,7 +762,7 @@ int gqa_decode_attention_multi(const void *q, const void *k_cache, const void *v
 
 
 size_t gqa_qkv_project_workspace_bytes(int B, int A, int H, int G, int d) {
-  if (B <= 0 || A <= 0 || H <= 0 || G <= 0 || H % G != 0 || (d != 64 && d != 128) || A % 64 != 0) return 0;
+  if (B <= 0 || A <= 0 || H <= 0 || G <= 0 || H % G != 0 || (d != 64 && d != 128) || A % kProjKT != 0) return 0;
   return proj_workspace(make_proj_plan(B, A, H, G, d));
 }
 

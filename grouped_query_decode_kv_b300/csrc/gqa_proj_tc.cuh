@@ -41,7 +41,7 @@ struct ProjParams {
   void *out[3];                  // q [B,H,d], k [B,G,d], v [B,G,d], bf16
   int heads[3];                  // H, G, G
   int item_start[4];             // first item of each output; item_start[3] = all items
-  int ktiles;                    // A / 64
+  int ktiles;                    // A / KT
   int B;                         // batch rows of this launch (<= NB)
   int d;                         // 64 or 128
   float *part;                   // [2P][NB][128] partial sums (null with one CTA)
@@ -49,14 +49,16 @@ struct ProjParams {
   unsigned epoch;
 };
 
-template <int NB_>
+template <int NB_, int KT_>
 struct ProjCfg {
   static constexpr int NB = NB_;                 // batch columns: N of the MMA
   static_assert(NB == 16 || NB == 32 || NB == 64 || NB == 128 || NB == 256, "batch tile");
-  static constexpr int KT = 64;                  // input features per tile (one 128-byte row of x)
+  static constexpr int KT = KT_;                 // input features per tile
+  static_assert(KT == 64 || KT == 128 || KT == 256, "tile depth");
   static constexpr int W_BOX = KT * 128;         // 64 output features x KT inputs
   static constexpr int W_TILE = 2 * W_BOX;       // 128 output features
-  static constexpr int X_TILE = NB * 128;
+  static constexpr int X_BOX = NB * 128;         // NB rows x 64 inputs (one 128-byte swizzle atom)
+  static constexpr int X_TILE = (KT / 64) * X_BOX;
   static constexpr int STAGE_BYTES = W_TILE + X_TILE;
   static constexpr int STAGES = 196608 / STAGE_BYTES > 10 ? 10 : 196608 / STAGE_BYTES;
   static constexpr int THREADS = 192;
@@ -146,7 +148,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             tma_load_3d(wt, tm, 0, t * C::KT, 2 * idx, full(st), pol);
             tma_load_3d(wt + C::W_BOX, tm, 0, t * C::KT, 2 * idx + 1, full(st), pol);
           }
-          tma_load_2d(wt + C::W_TILE, &tmX, t * C::KT, 0, full(st));
+#pragma unroll
+          for (int xb = 0; xb < C::KT / 64; ++xb)
+            tma_load_2d(wt + C::W_TILE + xb * C::X_BOX, &tmX, t * C::KT + xb * 64, 0, full(st));
         }
         // copies still in flight land before the CTA may end (bounded)
         for (int q = (r > ST ? r - ST : 0); q < r; ++q)
@@ -177,7 +181,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
             for (int ks = 0; ks < C::KT / 16; ++ks) {
               const uint64_t a = tc::smem_desc_sw128(wt + ks * 2048, C::W_BOX, 1024);
-              const uint64_t b = tc::smem_desc_sw128(xt + ks * 32, 16, 1024);
+              const uint64_t b = tc::smem_desc_sw128(xt + (ks >> 2) * C::X_BOX + (ks & 3) * 32, 16, 1024);
               tc::mma_ss(tmem + buf * NB, a, b, IDESC, t > t0 || ks > 0);
             }
             tc::commit(empty(st));
@@ -253,14 +257,25 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
           asm volatile("bar.sync 2, 128;" ::: "memory");
           if (*merge_flag) {
+            // 16 batch rows at a time, so that 16 independent L2 loads of a
+            // partial are in flight together; partials added in slot order
             const int slot0 = cta_start(c_lo, T, P) == first ? 2 * c_lo : 2 * c_lo + 1;
-            for (int b = 0; b < p.B; ++b) {
-              float acc = 0.f;
+            for (int b0 = 0; b0 < p.B; b0 += 16) {
+              float acc[16];
+#pragma unroll
+              for (int n = 0; n < 16; ++n) acc[n] = 0.f;
               for (int k = 0; k <= c_hi - c_lo; ++k) {
-                const int sl = k == 0 ? slot0 : 2 * (c_lo + k);
-                acc += __ldcg(p.part + ((size_t)sl * NB + b) * 128 + R);
+                const float *src = p.part + ((size_t)(k == 0 ? slot0 : 2 * (c_lo + k)) * NB + b0) * 128 + R;
+                float v[16];
+#pragma unroll
+                for (int n = 0; n < 16; ++n) v[n] = b0 + n < p.B ? __ldcg(src + (size_t)n * 128) : 0.f;
+#pragma unroll
+                for (int n = 0; n < 16; ++n) acc[n] += v[n];
               }
-              if (real) out[((size_t)b * p.heads[s] + head) * p.d + j] = __float2bfloat16_rn(acc);
+#pragma unroll
+              for (int n = 0; n < 16; ++n)
+                if (real && b0 + n < p.B)
+                  out[((size_t)(b0 + n) * p.heads[s] + head) * p.d + j] = __float2bfloat16_rn(acc[n]);
             }
           }
           asm volatile("bar.sync 2, 128;" ::: "memory");  // merge_flag is reused
