@@ -53,6 +53,17 @@ def _bind(path: str):
     lib.oracle_softmax_weights.restype = ci
     lib.oracle_kv_append.argtypes = [vp, vp, vp, vp, i32p, ci, ci, ci, ci, ci]
     lib.oracle_kv_append.restype = ci
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    f32p = ctypes.POINTER(ctypes.c_float)
+    lib.oracle_e4m3_decode_array.argtypes = [u8p, f64p, ctypes.c_long]
+    lib.oracle_e4m3_decode_array.restype = None
+    lib.oracle_e4m3_encode_array.argtypes = [f32p, u8p, ctypes.c_long]
+    lib.oracle_e4m3_encode_array.restype = None
+    lib.oracle_kv_append_fp8.argtypes = [vp, vp, u8p, u8p, f32p, f32p, i32p, ci, ci, ci, ci, ci]
+    lib.oracle_kv_append_fp8.restype = ci
+    lib.oracle_decode_attention_fp8.argtypes = [vp, u8p, u8p, f32p, f32p, i32p, cd, f64p, ci, ci, ci, ci, ci, ci,
+                                                ci]
+    lib.oracle_decode_attention_fp8.restype = ci
     lib.oracle_qkv_project.argtypes = [vp, vp, vp, vp, f64p, f64p, f64p, ci, ci, ci, ci, ci, ci, ci]
     lib.oracle_qkv_project.restype = ci
     lib.oracle_meanpool.argtypes = [vp, f64p, ci, ci, ctypes.c_long, ci]
@@ -164,6 +175,63 @@ def kv_append(k_new, v_new, k_cache, v_cache, seq_lens):
     skipped = _load().oracle_kv_append(kn.data_ptr(), vn.data_ptr(), k.data_ptr(), v.data_ptr(),
                                        _i32p(sl), B, G, d, Nmax, k.element_size())
     return k, v, sl, int(skipped)
+
+
+def _u8p(t: torch.Tensor):
+    assert t.dtype == torch.uint8 and t.is_contiguous()
+    return ctypes.cast(t.data_ptr(), ctypes.POINTER(ctypes.c_uint8))
+
+
+def _f32p(t: torch.Tensor):
+    assert t.dtype == torch.float32 and t.is_contiguous()
+    return ctypes.cast(t.data_ptr(), ctypes.POINTER(ctypes.c_float))
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """fp64 values of E4M3 codes (uint8 tensor of any shape)."""
+    c = _cpu(codes).to(torch.uint8).contiguous()
+    out = np.zeros(tuple(c.shape), dtype=np.float64)
+    _load().oracle_e4m3_decode_array(_u8p(c), _f64p(out), c.numel())
+    return out
+
+
+def e4m3_encode(values) -> torch.Tensor:
+    """E4M3 codes (uint8) of fp32 values: nearest, ties to even, saturating
+    at +-448, NaN -> 0x7F."""
+    r = _cpu(values).to(torch.float32).contiguous()
+    out = torch.zeros(tuple(r.shape), dtype=torch.uint8)
+    _load().oracle_e4m3_encode_array(_f32p(r), _u8p(out), r.numel())
+    return out
+
+
+def kv_append_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale, seq_lens):
+    """Copies of the FP8 caches and lengths after the append, and the number
+    of rows skipped."""
+    kn, vn = _cpu(k_new), _cpu(v_new)
+    k, v = _cpu(k_cache).clone().contiguous(), _cpu(v_cache).clone().contiguous()
+    ks, vs = _cpu(k_scale).float().contiguous(), _cpu(v_scale).float().contiguous()
+    sl = _cpu(seq_lens).to(torch.int32).clone()
+    B, G, Nmax, d = k.shape
+    skipped = _load().oracle_kv_append_fp8(kn.data_ptr(), vn.data_ptr(), _u8p(k), _u8p(v), _f32p(ks), _f32p(vs),
+                                           _i32p(sl), B, G, d, Nmax, _dtype_code(kn))
+    return k, v, sl, int(skipped)
+
+
+def decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, seq_lens, scale, nthreads: int = 0) -> np.ndarray:
+    """out[b,h,:] in fp64 for an FP8 cache (uint8 codes [B,G,Nmax,d], fp32
+    scales [G])."""
+    q, k, v = _cpu(q), _cpu(k_cache).contiguous(), _cpu(v_cache).contiguous()
+    ks, vs = _cpu(k_scale).float().contiguous(), _cpu(v_scale).float().contiguous()
+    sl = _cpu(seq_lens).to(torch.int32)
+    B, H, d = q.shape
+    G, Nmax = k.shape[1], k.shape[2]
+    out = np.zeros((B, H, d), dtype=np.float64)
+    rc = _load().oracle_decode_attention_fp8(q.data_ptr(), _u8p(k), _u8p(v), _f32p(ks), _f32p(vs), _i32p(sl),
+                                             float(scale), _f64p(out), B, H, G, d, Nmax, _dtype_code(q),
+                                             int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_decode_attention_fp8 rejected its arguments")
+    return out
 
 
 def qkv_project(x, w_q, w_k, w_v, nthreads: int = 0):

@@ -26,6 +26,8 @@
  *    section "MQA 的推导" gives the shared-K/V (G = 1) form.
  *  - CSDN interview post on GQA, section 03: the key/value pair is repeated
  *    n_rep times, n_rep being the number of query heads sharing it.
+ *  - GQA paper, section 4: quantization of keys and values (the FP8 cache
+ *    functions; format and scale granularity are readings, stated there).
  *  - CSDN blog, section "MQA 的推导", and 2kiu.com explainer, section 3.2:
  *    the per-head Q and per-group K/V projections (oracle_qkv_project).
  *  - GQA paper, section 4: speculative sampling scores several proposed
@@ -212,6 +214,122 @@ int oracle_kv_append(const void *k_new, const void *v_new, void *k_cache, void *
         seq_lens[b] = L + 1;
     }
     return skipped;
+}
+
+/*
+ * FP8 KV cache.  The GQA paper, section 4 (related work), names quantization
+ * of keys and values as the lever complementary to GQA.  The cache then holds
+ * OCP FP8 E4M3 codes ("e4m3fn": 1 sign bit, 4 exponent bits with bias 7, 3
+ * mantissa bits; no infinities, S.1111.111 is NaN, the largest finite value
+ * 448) and one fp32 scale per KV head for K and one for V: the stored value
+ * of an element is code_value * scale[g].
+ */
+static double e4m3_value(uint8_t c) {
+    int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);                 /* subnormal: m/8 * 2^(1-7) */
+    else
+        v = ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* Round to nearest, ties to even, onto the E4M3 grid; finite values beyond
+ * 448 saturate to +-448, NaN gives 0x7F.  A plain scan of the 127
+ * non-negative finite codes (their values increase with the code). */
+static uint8_t e4m3_encode(float r) {
+    if (isnan(r)) return 0x7F;
+    uint8_t sign = signbit(r) ? 0x80 : 0x00;
+    double a = fabs((double)r);
+    if (a >= 448.0) return sign | 0x7E;
+    uint8_t best = 0;
+    double best_err = a;
+    for (int c = 1; c <= 0x7E; ++c) {
+        double err = fabs(e4m3_value((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+            best = (uint8_t)c;
+            best_err = err;
+        }
+    }
+    return sign | best;
+}
+
+void oracle_e4m3_decode_array(const uint8_t *c, double *out, long n) {
+    for (long i = 0; i < n; ++i) out[i] = e4m3_value(c[i]);
+}
+
+void oracle_e4m3_encode_array(const float *r, uint8_t *out, long n) {
+    for (long i = 0; i < n; ++i) out[i] = e4m3_encode(r[i]);
+}
+
+/*
+ * kv_append onto an FP8 cache: code = e4m3(x / scale[g]) with the division
+ * in fp32 (IEEE, round to nearest) from the stored new row x, then the same
+ * placement and length rule as oracle_kv_append.  Returns rows skipped.
+ */
+int oracle_kv_append_fp8(const void *k_new, const void *v_new, uint8_t *k_cache, uint8_t *v_cache,
+                         const float *k_scale, const float *v_scale, int32_t *seq_lens, int B, int G, int d,
+                         int Nmax, int dtype) {
+    int skipped = 0;
+    for (int b = 0; b < B; ++b) {
+        int32_t L = seq_lens[b];
+        if (L < 0 || L >= Nmax) { ++skipped; continue; }
+        for (int g = 0; g < G; ++g) {
+            size_t src = ((size_t)b * G + g) * d;
+            size_t dst = (((size_t)b * G + g) * Nmax + (size_t)L) * d;
+            for (int i = 0; i < d; ++i) {
+                float kx = (float)load_value(k_new, src + i, dtype);
+                float vx = (float)load_value(v_new, src + i, dtype);
+                k_cache[dst + i] = e4m3_encode(kx / k_scale[g]);
+                v_cache[dst + i] = e4m3_encode(vx / v_scale[g]);
+            }
+        }
+        seq_lens[b] += 1;
+    }
+    return skipped;
+}
+
+/*
+ * Decode attention over an FP8 cache: the definition of
+ * oracle_decode_attention with K[b,g,n,i] = e4m3_value(k8) * k_scale[g] and
+ * V likewise (exact in fp64).  q and out as there.
+ */
+int oracle_decode_attention_fp8(const void *q, const uint8_t *k8, const uint8_t *v8, const float *k_scale,
+                                const float *v_scale, const int32_t *seq_lens, double scale, double *out, int B,
+                                int H, int G, int d, int Nmax, int dtype, int nthreads) {
+    if (B <= 0 || H <= 0 || G <= 0 || d <= 0 || Nmax <= 0 || H % G != 0) return -1;
+    int n_rep = H / G, fail = 0;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : fail)
+#endif
+    for (long bh = 0; bh < (long)B * H; ++bh) {
+        int b = (int)(bh / H), h = (int)(bh % H), g = h / n_rep;
+        int L = clamp_len(seq_lens[b], Nmax);
+        double *o = out + (size_t)bh * d;
+        for (int i = 0; i < d; ++i) o[i] = 0.0;
+        if (L == 0) continue;
+        double *w = (double *)malloc((size_t)L * sizeof(double));
+        if (!w) { fail |= 1; continue; }
+        size_t kv = ((size_t)b * G + g) * Nmax * d;
+        double wmax = -INFINITY;
+        for (int n = 0; n < L; ++n) {
+            double qk = 0.0;
+            for (int i = 0; i < d; ++i)
+                qk += load_value(q, (size_t)bh * d + i, dtype) * (e4m3_value(k8[kv + (size_t)n * d + i]) * k_scale[g]);
+            w[n] = scale * qk;
+            if (w[n] > wmax) wmax = w[n];
+        }
+        double z = 0.0;
+        for (int n = 0; n < L; ++n) { w[n] = exp(w[n] - wmax); z += w[n]; }
+        for (int n = 0; n < L; ++n) w[n] = w[n] / z;
+        for (int n = 0; n < L; ++n)
+            for (int i = 0; i < d; ++i)
+                o[i] += w[n] * (e4m3_value(v8[kv + (size_t)n * d + i]) * v_scale[g]);
+        free(w);
+    }
+    return fail ? -1 : 0;
 }
 
 /*

@@ -38,6 +38,10 @@ PIN_BATTERY = [
     pins.test_projection_of_mean_pooled_weights_is_the_group_mean,
     pins.test_projection_matches_the_blog_einsums,
     pins.test_projection_brute_force,
+    pins.test_e4m3_decode_table_matches_torch,
+    pins.test_e4m3_encode_is_nearest_even_and_saturates,
+    pins.test_fp8_attention_is_attention_on_the_dequantized_cache,
+    pins.test_fp8_append_quantizes_and_places_the_row,
 ]
 
 # (name, text in the oracle source, replacement)
@@ -55,6 +59,12 @@ MUTANTS = [
     ("several tokens: every token reads token 0's query", "head_weights(q, k, (size_t)bth * d,",
      "head_weights(q, k, ((size_t)b * T * H + h) * d,"),
     ("several tokens: K used in place of V", "o[i] += w[n] * load_value(v, kvo", "o[i] += w[n] * load_value(k, kvo"),
+    ("e4m3: exponent bias 8", "v = ldexp(1.0 + m / 8.0, e - 7);", "v = ldexp(1.0 + m / 8.0, e - 8);"),
+    ("e4m3: ties away from zero", "(err == best_err && (c & 1) == 0 && (best & 1) == 1)", "(err == best_err && c > best)"),
+    ("fp8 append ignores the scale", "k_cache[dst + i] = e4m3_encode(kx / k_scale[g]);",
+     "k_cache[dst + i] = e4m3_encode(kx);"),
+    ("fp8 attention drops the V scale", "(e4m3_value(v8[kv + (size_t)n * d + i]) * v_scale[g])",
+     "(e4m3_value(v8[kv + (size_t)n * d + i]))"),
     ("projection reads the weight transposed", "load_value(p, ((size_t)h * A + a) * d + j, dtype)",
      "load_value(p, ((size_t)h * d + j) * A + a, dtype)"),
     ("K projected with the query weights", "project_heads(x, pk, k,", "project_heads(x, pq, k,"),

@@ -418,3 +418,69 @@ def test_projection_brute_force():
                 for j in range(d):
                     ref = mpmath.fsum(mpmath.mpf(float(x[b, a])) * mpmath.mpf(float(w[h, a, j])) for a in range(A))
                     assert abs(out[b, h, j] - float(ref)) < 1e-13 * (1 + abs(float(ref)))
+
+
+# ------------------------------------------------------- FP8 (E4M3) cache
+def test_e4m3_decode_table_matches_torch():
+    """All 256 codes against torch's float8_e4m3fn (an independent
+    implementation of the OCP format), plus the format's landmarks."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ours = oracle.e4m3_decode(codes)
+    ref = codes.view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan) and nan.sum() == 2          # 0x7F and 0xFF
+    np.testing.assert_array_equal(ours[~nan], ref[~nan])
+    assert ours[0x38] == 1.0 and ours[0x7E] == 448.0 and ours[0x01] == 2.0 ** -9 and ours[0x08] == 2.0 ** -6
+
+
+def test_e4m3_encode_is_nearest_even_and_saturates():
+    g = torch.Generator().manual_seed(50)
+    x = torch.cat([torch.randn(20000, generator=g) * 30, torch.randn(20000, generator=g) * 0.01,
+                   torch.tensor([0.0, -0.0, 1.0625, 1.1875, 2.0 ** -10, 3 * 2.0 ** -10, 464.0, -464.0, 447.9])])
+    ok = x.abs() <= 464.0                          # torch's cast overflows to NaN beyond, ours saturates
+    ours = oracle.e4m3_encode(x)
+    np.testing.assert_array_equal(ours[ok].numpy(), x[ok].to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+    big = torch.tensor([465.0, 1e6, float("inf"), -500.0, -float("inf")])
+    assert oracle.e4m3_encode(big).tolist() == [0x7E, 0x7E, 0x7E, 0xFE, 0xFE]
+    assert oracle.e4m3_encode(torch.tensor([float("nan")])).tolist() == [0x7F]
+
+
+def _fp8_case(B, H, G, d, N, lens, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, H, d, generator=g)
+    k8 = oracle.e4m3_encode(torch.randn(B, G, N, d, generator=g) * 16)
+    v8 = oracle.e4m3_encode(torch.randn(B, G, N, d, generator=g) * 16)
+    return q, k8, v8, torch.tensor(lens, dtype=torch.int32)
+
+
+def test_fp8_attention_is_attention_on_the_dequantized_cache():
+    """With power-of-two scales the dequantized cache is exact in fp32, so the
+    FP8 oracle must equal the plain oracle run on it."""
+    B, H, G, d, N = 3, 8, 2, 16, 40
+    q, k8, v8, sl = _fp8_case(B, H, G, d, N, [40, 1, 23], 51)
+    ks = torch.tensor([0.25, 2.0])
+    vs = torch.tensor([0.5, 0.125])
+    out = oracle.decode_attention_fp8(q, k8, v8, ks, vs, sl, 0.3)
+    kf = torch.from_numpy(oracle.e4m3_decode(k8)).float() * ks.view(1, G, 1, 1)
+    vf = torch.from_numpy(oracle.e4m3_decode(v8)).float() * vs.view(1, G, 1, 1)
+    ref = oracle.decode_attention(q, kf, vf, sl, 0.3)
+    np.testing.assert_allclose(out, ref, rtol=1e-13, atol=1e-14)
+
+
+def test_fp8_append_quantizes_and_places_the_row():
+    B, G, d, N = 3, 2, 8, 6
+    g = torch.Generator().manual_seed(52)
+    kn = torch.randn(B, G, d, generator=g).to(torch.bfloat16)
+    vn = torch.randn(B, G, d, generator=g).to(torch.bfloat16)
+    kc = torch.zeros(B, G, N, d, dtype=torch.uint8)
+    vc = torch.zeros(B, G, N, d, dtype=torch.uint8)
+    ks, vs = torch.tensor([0.01, 0.02]), torch.tensor([0.03, 0.05])  # no overflow (torch NaNs it)
+    sl = torch.tensor([0, 5, 6], dtype=torch.int32)
+    k2, v2, sl2, skipped = oracle.kv_append_fp8(kn, vn, kc, vc, ks, vs, sl)
+    assert skipped == 1 and sl2.tolist() == [1, 6, 6]
+    for b, L in ((0, 0), (1, 5)):
+        for gg in range(G):
+            want_k = (kn[b, gg].float() / ks[gg]).to(torch.float8_e4m3fn).view(torch.uint8)
+            want_v = (vn[b, gg].float() / vs[gg]).to(torch.float8_e4m3fn).view(torch.uint8)
+            assert torch.equal(k2[b, gg, L], want_k) and torch.equal(v2[b, gg, L], want_v)
+    assert torch.count_nonzero(k2[2]) == 0 and torch.count_nonzero(k2[0, :, 1:]) == 0
