@@ -393,6 +393,60 @@ def time_multi(w: workloads.Workload, device, iters: int, warm: int, l2_bytes: i
     return row
 
 
+def time_fp8(w: workloads.Workload, device, iters: int, l2_bytes: int, mem_budget: int):
+    """Table row of a decode workload over an FP8 E4M3 cache: device time per
+    gqa_decode_attention_fp8_ws call and per kv_append_fp8 call (CUDA-graph
+    replays over rotating cache copies, together >= 3 x L2), GB/s of the
+    algorithmic bytes (one byte per cached K/V element, bf16 q and out)."""
+    import grouped_query_decode_kv_b300 as gqa
+    cache = cost.kv_cache_bytes(w.B, w.G, w.Nmax, w.d, 1)
+    copies = max(2, min(64, math.ceil(3 * l2_bytes / max(cache, 1)), max(1, mem_budget // max(cache, 1))))
+    g = torch.Generator(device=device).manual_seed(3000 + w.index)
+    k = [torch.randint(0, 0x7E, (w.B, w.G, w.Nmax, w.d), generator=g, device=device, dtype=torch.uint8)
+         for _ in range(copies)]
+    v = [torch.randint(0, 0x7E, (w.B, w.G, w.Nmax, w.d), generator=g, device=device, dtype=torch.uint8)
+         for _ in range(copies)]
+    q = torch.randn(w.B, w.H, w.d, generator=g, device=device).bfloat16()
+    out = torch.empty_like(q)
+    ks = torch.full((w.G,), 1 / 64, device=device)
+    vs = torch.full((w.G,), 1 / 64, device=device)
+    kn = torch.randn(w.B, w.G, w.d, generator=g, device=device).bfloat16()
+    vn = torch.randn(w.B, w.G, w.d, generator=g, device=device).bfloat16()
+    lens = workloads.make_seq_lens(w)
+    full = lens.to(device)
+    pre = torch.clamp(lens.to(torch.int64) - 1, min=0).to(torch.int32)
+    rows = pre.unsqueeze(0).repeat(iters, 1).to(device).contiguous()
+    need = gqa.gqa_decode_workspace_bytes_fp8(w.B, w.H, w.G, w.d, w.Nmax)
+    ws = torch.zeros(max(need, 1), dtype=torch.uint8, device=device)
+
+    def attn():
+        for i in range(iters):
+            c = i % copies
+            gqa.gqa_decode_attention_fp8_ws(q, k[c], v[c], ks, vs, full, w.scale, out, ws)
+        return iters
+
+    def app():
+        for i in range(iters):
+            c = i % copies
+            gqa.kv_append_fp8(kn, vn, k[c], v[c], ks, vs, rows[i])
+        return iters
+
+    def reset():
+        rows.copy_(pre.unsqueeze(0).expand_as(rows))
+
+    us = _graph_time(attn)
+    us_app = _graph_time(app, reset=reset)
+    err = gqa.gqa_get_device_error()
+    nbytes = 2 * w.G * int(lens.sum()) * w.d + 2 * w.B * w.H * w.d * 2
+    peak, _ = hbm_peak()
+    row = {"B": w.B, "H": w.H, "G": w.G, "d": w.d, "Nmax": w.Nmax, "cache": "fp8 e4m3", "us": round(us, 2),
+           "bytes": nbytes, "gbs": round(nbytes / us / 1e3, 1), "frac_measured": round(nbytes / us / 1e3 / peak, 3),
+           "kv_append_fp8_us": round(us_app, 2), "copies": copies, "device_error": err}
+    del k, v, ws
+    torch.cuda.empty_cache()
+    return row
+
+
 def time_projection(name: str, device, iters: int, l2_bytes: int, mem_budget: int):
     """Table row of a Q/K/V projection layer: device time per
     gqa_qkv_project_ws call from CUDA-graph replays over rotating weight
@@ -638,6 +692,7 @@ def run_ours(args, world, rank, local):
     table = None
     table_multi = None
     table_proj = None
+    table_fp8 = None
     ceiling = None
     del st
     torch.cuda.empty_cache()
@@ -649,6 +704,9 @@ def run_ours(args, world, rank, local):
         table_multi = {}
         for name in workloads.multi_names():
             table_multi[name] = time_multi(workloads.workload(name), device, args.table_iters, 5, l2, mem_budget)
+        table_fp8 = {}
+        for name in ("mha", "gqa8", "mqa"):
+            table_fp8[name] = time_fp8(workloads.workload(name), device, args.table_iters, l2, mem_budget)
         table_proj = {}
         for name in sorted(workloads.PROJECTIONS):
             table_proj[name] = time_projection(name, device, args.table_iters, l2, mem_budget)
@@ -717,6 +775,7 @@ def run_ours(args, world, rank, local):
         "table": table,
         "table_multi_token": table_multi,
         "table_qkv_projection": table_proj,
+        "table_fp8_cache": table_fp8,
     }
     print(json.dumps(line), flush=True)
     return 0

@@ -17,6 +17,9 @@ Entry points (see ``include/gqa.h`` for the full contract):
   gqa_decode_step_ws(..., workspace)             append + attention in one launch
   gqa_decode_attention_multi(q[B,T,H,d], ..., out[B,T,H,d])   T query tokens per sequence
   gqa_decode_attention_multi_ex(..., split_tokens, workspace)
+  gqa_decode_attention_fp8(q, k_cache_u8, v_cache_u8, k_scale, v_scale, seq_lens, scale, out)
+  gqa_decode_attention_fp8_ws(..., workspace), gqa_decode_workspace_bytes_fp8(B, H, G, d, Nmax)
+  kv_append_fp8(k_new, v_new, k_cache_u8, v_cache_u8, k_scale, v_scale, seq_lens)
   gqa_qkv_project(x, w_q, w_k, w_v, q, k_new, v_new)   Q/K/V projections of the token
   gqa_qkv_project_ws(..., workspace), gqa_qkv_project_workspace_bytes(B, A, H, G, d)
   kv_append(k_new, v_new, k_cache, v_cache, seq_lens)
@@ -44,6 +47,7 @@ __all__ = [
     "gqa_decode_step", "gqa_decode_step_ws",
     "gqa_decode_attention_multi", "gqa_decode_attention_multi_ex",
     "gqa_qkv_project", "gqa_qkv_project_ws", "gqa_qkv_project_workspace_bytes",
+    "gqa_decode_attention_fp8", "gqa_decode_attention_fp8_ws", "gqa_decode_workspace_bytes_fp8", "kv_append_fp8",
     "DEVERR_ATTN_LEN", "DEVERR_APPEND_LEN", "DEVERR_TIMEOUT", "EXPORTED_SYMBOLS",
 ]
 
@@ -59,6 +63,7 @@ EXPORTED_SYMBOLS = (
     "gqa_decode_attention_noalloc", "gqa_decode_step", "gqa_decode_step_ws",
     "gqa_decode_attention_multi", "gqa_decode_attention_multi_ex",
     "gqa_qkv_project", "gqa_qkv_project_ws", "gqa_qkv_project_workspace_bytes",
+    "gqa_decode_attention_fp8", "gqa_decode_attention_fp8_ws", "gqa_decode_workspace_bytes_fp8", "kv_append_fp8",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -116,6 +121,15 @@ def load_library():
         lib.gqa_qkv_project_ws.restype = ci
         lib.gqa_qkv_project_workspace_bytes.argtypes = [ci] * 5
         lib.gqa_qkv_project_workspace_bytes.restype = sz
+        fp8 = [vp, vp, vp, vp, vp, vp, cf, vp, ci, ci, ci, ci, ci]
+        lib.gqa_decode_attention_fp8.argtypes = fp8 + [vp]
+        lib.gqa_decode_attention_fp8.restype = ci
+        lib.gqa_decode_attention_fp8_ws.argtypes = fp8 + [vp, sz, vp]
+        lib.gqa_decode_attention_fp8_ws.restype = ci
+        lib.gqa_decode_workspace_bytes_fp8.argtypes = [ci] * 5
+        lib.gqa_decode_workspace_bytes_fp8.restype = sz
+        lib.kv_append_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, vp]
+        lib.kv_append_fp8.restype = ci
         lib.kv_append.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, vp]
         lib.kv_append.restype = ci
         lib.mha_to_gqa_meanpool.argtypes = [vp, vp, ci, ci, ci, ci, ci, vp]
@@ -314,6 +328,65 @@ def gqa_decode_step_ws(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out, 
            lib.gqa_decode_step_ws(*_step_args(q, k_new, v_new, k_cache, v_cache, seq_lens, scale, out), wp, wn,
                                   _stream(q, stream)))
     return out
+
+
+def _fp8_args(q, k_cache, v_cache, k_scale, v_scale, seq_lens, scale, out):
+    B, H, d = q.shape
+    if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8 or k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache must be uint8 E4M3 codes [B, G, Nmax, d]")
+    Bk, G, Nmax, dk = k_cache.shape
+    if Bk != B or dk != d or tuple(out.shape) != (B, H, d):
+        raise ValueError("q, out [B,H,d] and the caches [B,G,Nmax,d] disagree")
+    if q.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
+        raise ValueError("q and out must be bf16")
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        if t.dtype != torch.float32 or tuple(t.shape) != (G,):
+            raise ValueError(f"{n} must be fp32 [G]")
+    if seq_lens.dtype != torch.int32 or tuple(seq_lens.shape) != (B,):
+        raise ValueError("seq_lens must be int32 [B]")
+    return [_dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _dev(k_scale, "k_scale"),
+            _dev(v_scale, "v_scale"), _dev(seq_lens, "seq_lens"), float(scale), _dev(out, "out"), B, H, G, d, Nmax]
+
+
+def gqa_decode_workspace_bytes_fp8(B, H, G, d, Nmax) -> int:
+    return int(load_library().gqa_decode_workspace_bytes_fp8(B, H, G, d, Nmax))
+
+
+def gqa_decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, seq_lens, scale, out, stream=None):
+    """Decode attention over an FP8 E4M3 cache (uint8 codes [B,G,Nmax,d],
+    per-KV-head fp32 scales [G]); q and out bf16 [B,H,d]."""
+    lib = load_library()
+    _check("gqa_decode_attention_fp8",
+           lib.gqa_decode_attention_fp8(*_fp8_args(q, k_cache, v_cache, k_scale, v_scale, seq_lens, scale, out),
+                                        _stream(q, stream)))
+    return out
+
+
+def gqa_decode_attention_fp8_ws(q, k_cache, v_cache, k_scale, v_scale, seq_lens, scale, out, workspace,
+                                stream=None):
+    """As gqa_decode_attention_fp8 with a caller-owned workspace of
+    gqa_decode_workspace_bytes_fp8(...) bytes."""
+    lib = load_library()
+    wp, wn = _ws(workspace)
+    _check("gqa_decode_attention_fp8_ws",
+           lib.gqa_decode_attention_fp8_ws(*_fp8_args(q, k_cache, v_cache, k_scale, v_scale, seq_lens, scale, out),
+                                           wp, wn, _stream(q, stream)))
+    return out
+
+
+def kv_append_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale, seq_lens, stream=None):
+    """Quantizes k_new / v_new [B,G,d] (bf16) to E4M3 with the per-head
+    scales into row seq_lens[b] of the uint8 caches, then seq_lens += 1."""
+    lib = load_library()
+    if k_cache.dtype != torch.uint8 or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache must be uint8 [B, G, Nmax, d]")
+    B, G, Nmax, d = k_cache.shape
+    if tuple(k_new.shape) != (B, G, d) or tuple(v_new.shape) != (B, G, d) or k_new.dtype != torch.bfloat16:
+        raise ValueError("k_new and v_new must be bf16 [B, G, d]")
+    _check("kv_append_fp8", lib.kv_append_fp8(_dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(k_cache, "k_cache"),
+                                              _dev(v_cache, "v_cache"), _dev(k_scale, "k_scale"),
+                                              _dev(v_scale, "v_scale"), _dev(seq_lens, "seq_lens"), B, G, d, Nmax,
+                                              _stream(k_cache, stream)))
 
 
 def _proj_args(x, w_q, w_k, w_v, q, k_new, v_new):

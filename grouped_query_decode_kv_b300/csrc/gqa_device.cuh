@@ -194,6 +194,32 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// An OCP FP8 E4M3 cache element (the raw code): 1 sign, 4 exponent bits
+// (bias 7), 3 mantissa bits, no infinities, S.1111.111 = NaN, max 448.
+struct e4m3_t {
+  uint8_t bits;
+};
+
+// Two E4M3 codes (low byte = first element) to fp32, exactly: the hardware
+// conversion to an f16 pair (every E4M3 value is an f16 value), then f16 to
+// f32.
+__device__ __forceinline__ void e4m3x2_to_float(uint32_t pair16, float &lo, float &hi) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)pair16));
+  uint16_t a, b;
+  asm("mov.b32 {%0, %1}, %2;" : "=h"(a), "=h"(b) : "r"(h2));
+  asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"(a));
+  asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"(b));
+}
+
+// fp32 pair to two E4M3 codes (low byte = lo): round to nearest even,
+// finite values beyond 448 saturate to +-448.
+__device__ __forceinline__ uint32_t float2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);

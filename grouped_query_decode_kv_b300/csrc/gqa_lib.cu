@@ -34,6 +34,9 @@ using MmaD64x4 = MmaCfg<64, 2, 2, 128, 2>;
 
 template <typename T, int D, int NH>
 using SimtFor = SimtCfg<T, D, NH, (32768 / (2 * D * (int)sizeof(T))), 3>;
+// FP8 E4M3 cache, bf16 q and out: 128 positions (32 KB of K and V) per stage
+template <int NH>
+using SimtFp8 = SimtCfg<e4m3_t, 128, NH, 128, 3, __nv_bfloat16>;
 
 struct KernelChoice {
   const void *func;
@@ -112,6 +115,13 @@ using TcD128x64 = TcCfg<64, 3, 1>;
 
 template <bool M>
 KernelChoice choose_kernel(gqa_dtype_t dt, int d, int n_rep) {
+  if constexpr (!M) {
+    if (dt == GQA_FP8_E4M3) {  // d = 128 (checked by the caller)
+      if (n_rep == 1) return make_choice<SimtFp8<1>, kSimt, M>();
+      if (n_rep == 2) return make_choice<SimtFp8<2>, kSimt, M>();
+      return make_choice<SimtFp8<4>, kSimt, M>();
+    }
+  }
   if (dt == GQA_BF16) {
     if (d == 128) {
       if (n_rep == 1) return make_choice<SimtFor<__nv_bfloat16, 128, 1>, kSimt, M>();
@@ -288,12 +298,15 @@ bool encode_cache_map(CUtensorMap *map, const void *base, gqa_dtype_t dt, int d,
                       int box_elems) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const size_t elt = dt == GQA_BF16 ? 2 : 4;
+  const size_t elt = dt == GQA_FP8_E4M3 ? 1 : (dt == GQA_BF16 ? 2 : 4);
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Nmax, (cuuint64_t)BG};
   cuuint64_t strides[2] = {(cuuint64_t)(d * elt), (cuuint64_t)((size_t)Nmax * d * elt)};
   cuuint32_t box[3] = {(cuuint32_t)box_elems, (cuuint32_t)block_n, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, dt == GQA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+  const CUtensorMapDataType ty = dt == GQA_FP8_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : dt == GQA_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  CUresult r = fn(map, ty, 3,
                   const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -349,7 +362,8 @@ struct StepAppend {
 // plan was made for tokens * H query rows.
 int run_attention(const void *q, const void *k, const void *v, const int32_t *sl, float scale, void *out, int B,
                   int H, int G, int d, int Nmax, gqa_dtype_t dt, const Plan &pl, void *ws, cudaStream_t st,
-                  const StepAppend &app = StepAppend(), int tokens = 1) {
+                  const StepAppend &app = StepAppend(), int tokens = 1, const float *k_scale = nullptr,
+                  const float *v_scale = nullptr) {
   CUtensorMap mk, mv;
   if (!encode_cache_map(&mk, k, dt, d, Nmax, B * G, pl.k.block_n, pl.k.box_elems) ||
       !encode_cache_map(&mv, v, dt, d, Nmax, B * G, pl.k.block_n, pl.k.box_elems))
@@ -376,7 +390,7 @@ int run_attention(const void *q, const void *k, const void *v, const int32_t *sl
   p.k_cache = app.k_cache;
   p.v_cache = app.v_cache;
   p.seq_lens_w = app.seq_lens;
-  p.row_chunks = d * (dt == GQA_BF16 ? 2 : 4) / 16;
+  p.row_chunks = d * (dt == GQA_FP8_E4M3 ? 1 : (dt == GQA_BF16 ? 2 : 4)) / 16;
   p.done_cnt = split ? reinterpret_cast<unsigned *>(w + step_counter_offset(pl, d)) : nullptr;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.B = B;
@@ -389,6 +403,8 @@ int run_attention(const void *q, const void *k, const void *v, const int32_t *sl
   p.tokens = tokens;
   p.heads_q = H;
   p.rep_kv = H / G;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
   if (pl.k.launch(dim3(pl.P), mk, mv, p, st) != cudaSuccess) {
     cudaGetLastError();
     return GQA_ERR_CUDA;
@@ -788,6 +804,69 @@ int gqa_qkv_project(const void *x, const void *w_q, const void *w_k, const void 
   int rc = run_projection(x, w_q, w_k, w_v, q, k_new, v_new, B, A, H, G, d, ws, stream);
   if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && rc == GQA_OK) rc = GQA_ERR_CUDA;
   return rc;
+}
+
+namespace {
+int check_fp8_args(const void *q, const void *k, const void *v, const float *ks, const float *vs, const int32_t *sl,
+                   const void *out, int B, int H, int G, int d, int Nmax) {
+  if (!ks || !vs) return GQA_ERR_INVALID_ARG;
+  if (int rc = check_attention_args(q, k, v, sl, out, B, H, G, d, Nmax, GQA_BF16)) return rc;
+  if (d != 128) return GQA_ERR_UNSUPPORTED;
+  return GQA_OK;
+}
+}  // namespace
+
+size_t gqa_decode_workspace_bytes_fp8(int B, int H, int G, int d, int Nmax) {
+  if (B <= 0 || H <= 0 || G <= 0 || Nmax <= 0 || H % G != 0 || d != 128) return 0;
+  return workspace_for(make_plan(B, H, G, d, Nmax, GQA_FP8_E4M3, 0), B, H, d);
+}
+
+int gqa_decode_attention_fp8_ws(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
+                                const float *v_scale, const int32_t *seq_lens, float scale, void *out, int B, int H,
+                                int G, int d, int Nmax, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (int rc = check_fp8_args(q, k_cache, v_cache, k_scale, v_scale, seq_lens, out, B, H, G, d, Nmax)) return rc;
+  const Plan pl = make_plan(B, H, G, d, Nmax, GQA_FP8_E4M3, 0);
+  if (!plan_fits(pl, B, G)) return GQA_ERR_UNSUPPORTED;
+  const size_t need = workspace_for(pl, B, H, d);
+  if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+    return GQA_ERR_INVALID_ARG;
+  return run_attention(q, k_cache, v_cache, seq_lens, scale, out, B, H, G, d, Nmax, GQA_FP8_E4M3, pl, workspace,
+                       stream, StepAppend(), 1, k_scale, v_scale);
+}
+
+int gqa_decode_attention_fp8(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
+                             const float *v_scale, const int32_t *seq_lens, float scale, void *out, int B, int H,
+                             int G, int d, int Nmax, cudaStream_t stream) {
+  if (int rc = check_fp8_args(q, k_cache, v_cache, k_scale, v_scale, seq_lens, out, B, H, G, d, Nmax)) return rc;
+  const Plan pl = make_plan(B, H, G, d, Nmax, GQA_FP8_E4M3, 0);
+  if (!plan_fits(pl, B, G)) return GQA_ERR_UNSUPPORTED;
+  const size_t need = workspace_for(pl, B, H, d);
+  void *ws = nullptr;
+  if (need > 0 && cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GQA_ERR_NO_MEMORY;
+  }
+  int rc = run_attention(q, k_cache, v_cache, seq_lens, scale, out, B, H, G, d, Nmax, GQA_FP8_E4M3, pl, ws, stream,
+                         StepAppend(), 1, k_scale, v_scale);
+  if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && rc == GQA_OK) rc = GQA_ERR_CUDA;
+  return rc;
+}
+
+int kv_append_fp8(const void *k_new, const void *v_new, void *k_cache, void *v_cache, const float *k_scale,
+                  const float *v_scale, int32_t *seq_lens, int B, int G, int d, int Nmax, cudaStream_t stream) {
+  if (!k_new || !v_new || !k_cache || !v_cache || !k_scale || !v_scale || !seq_lens) return GQA_ERR_INVALID_ARG;
+  if (B <= 0 || G <= 0 || d <= 0 || Nmax <= 0) return GQA_ERR_INVALID_ARG;
+  if (d % 16 != 0) return GQA_ERR_UNSUPPORTED;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return GQA_ERR_INVALID_ARG;
+  if (launch_pdl(gqa_kv_append_fp8_kernel, dim3(B), dim3(256), 0, stream,
+                 reinterpret_cast<const __nv_bfloat16 *>(k_new), reinterpret_cast<const __nv_bfloat16 *>(v_new),
+                 reinterpret_cast<uint8_t *>(k_cache), reinterpret_cast<uint8_t *>(v_cache), k_scale, v_scale,
+                 seq_lens, G, Nmax, d) != cudaSuccess) {
+    cudaGetLastError();
+    return GQA_ERR_CUDA;
+  }
+  return GQA_OK;
 }
 
 int kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache, int32_t *seq_lens, int B, int G,

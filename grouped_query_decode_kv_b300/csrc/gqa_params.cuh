@@ -44,6 +44,8 @@ struct SplitParams {
   int tokens;
   int heads_q;              // query heads of one token
   int rep_kv;               // query heads of one token per KV head
+  // FP8 (E4M3) cache: per-KV-head scales [G] of K and V (null otherwise)
+  const float *k_scale, *v_scale;
 };
 
 // Row (of D elements) of q and out that holds query row v of batch row b.

@@ -21,9 +21,13 @@
 
 namespace gqa {
 
-template <typename T, int D_, int NH_, int BLOCK_N_, int STAGES_>
+// T: cache element type; TQ: q and out element type (T unless the cache is
+// FP8 E4M3, whose q and out are bf16).
+template <typename T, int D_, int NH_, int BLOCK_N_, int STAGES_, typename TQ = T>
 struct SimtCfg {
   using Elem = T;
+  using QElem = TQ;
+  static constexpr bool FP8 = sizeof(T) == 1;
   static constexpr int D = D_;
   static constexpr int NH = NH_;  // query heads per CTA
   static constexpr int ELT = sizeof(T);
@@ -62,14 +66,41 @@ __device__ __forceinline__ void widen_chunk<__nv_bfloat16>(const uint4 &c, float
 }
 
 template <>
+__device__ __forceinline__ void widen_chunk<e4m3_t>(const uint4 &c, float *f) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    e4m3x2_to_float(w[i] & 0xffffu, f[4 * i], f[4 * i + 1]);
+    e4m3x2_to_float(w[i] >> 16, f[4 * i + 2], f[4 * i + 3]);
+  }
+}
+
+// N consecutive elements of type T (N * sizeof(T) a multiple of 16 bytes,
+// 16-byte aligned) to fp32, and back.
+template <typename T, int N>
+__device__ __forceinline__ void load_elems(const T *src, float *f) {
+  constexpr int PER = 16 / (int)sizeof(T);
+#pragma unroll
+  for (int c = 0; c < N / PER; ++c) widen_chunk<T>(__ldg(reinterpret_cast<const uint4 *>(src) + c), f + c * PER);
+}
+
+template <typename T>
+__device__ __forceinline__ void store_chunk(T *dst, const float *f);
+
+template <typename T, int N>
+__device__ __forceinline__ void store_elems(T *dst, const float *f) {
+  constexpr int PER = 16 / (int)sizeof(T);
+#pragma unroll
+  for (int c = 0; c < N / PER; ++c) store_chunk<T>(dst + c * PER, f + c * PER);
+}
+
+template <>
 __device__ __forceinline__ void widen_chunk<float>(const uint4 &c, float *f) {
   f[0] = __uint_as_float(c.x); f[1] = __uint_as_float(c.y);
   f[2] = __uint_as_float(c.z); f[3] = __uint_as_float(c.w);
 }
 
 // Round EPC fp32 values to T and store them as one 16-byte chunk.
-template <typename T>
-__device__ __forceinline__ void store_chunk(T *dst, const float *f);
 
 template <>
 __device__ __forceinline__ void store_chunk<__nv_bfloat16>(__nv_bfloat16 *dst, const float *f) {
@@ -97,6 +128,7 @@ __global__ void __launch_bounds__(C::THREADS)
     gqa_split_simt_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                           const SplitParams p) {
   using T = typename C::Elem;
+  using TQ = typename C::QElem;
   using Pipe = typename C::Pipe;
   constexpr int D = C::D, NH = C::NH, EPC = C::EPC, EPL = C::EPL, NBOX = C::NBOX;
   extern __shared__ uint8_t smem_raw[];
@@ -134,7 +166,7 @@ __global__ void __launch_bounds__(C::THREADS)
   }
   griddep_wait();  // lengths and cache rows written by earlier kernels are visible
   if (warp == 0) {
-    const CtaRange r = warp_plan_range(sp, lane, p.out, (size_t)p.H * D * sizeof(T));
+    const CtaRange r = warp_plan_range(sp, lane, p.out, (size_t)p.H * D * sizeof(TQ));
     if (lane == 0) *range_smem = r;
   }
   __syncthreads();
@@ -158,6 +190,10 @@ __global__ void __launch_bounds__(C::THREADS)
     const int h_first = g * p.n_rep + hc * NH;
     const int nh = min(NH, p.n_rep - hc * NH);
     const int L = attn_len(p.seq_lens, b, p.Nmax, p.append);
+    // FP8 cache: K's per-head scale joins the logit scale, V's multiplies the
+    // unit's result
+    const float sl2 = C::FP8 ? p.scale_log2 * __ldg(p.k_scale + g) : p.scale_log2;
+    const float vscale = C::FP8 ? __ldg(p.v_scale + g) : 1.f;
 
     // this lane's slice of q: element e of box bx is d = bx*BOX_ELEMS + j*EPC + e
     float qf[NH][EPL];
@@ -167,12 +203,9 @@ __global__ void __launch_bounds__(C::THREADS)
     for (int h = 0; h < NH; ++h) {
       const int hh = h_first + (h < nh ? h : 0);
       lim[h] = L - query_lag<MULTI>(p, hh);
-      const T *qrow = reinterpret_cast<const T *>(p.q) + query_row<MULTI>(p, b, hh) * D;
+      const TQ *qrow = reinterpret_cast<const TQ *>(p.q) + query_row<MULTI>(p, b, hh) * D;
 #pragma unroll
-      for (int bx = 0; bx < NBOX; ++bx) {
-        const uint4 c = __ldg(reinterpret_cast<const uint4 *>(qrow + bx * C::BOX_ELEMS + j * EPC));
-        widen_chunk<T>(c, &qf[h][bx * EPC]);
-      }
+      for (int bx = 0; bx < NBOX; ++bx) load_elems<TQ, EPC>(qrow + bx * C::BOX_ELEMS + j * EPC, &qf[h][bx * EPC]);
     }
 
     float acc[NH][EPL], m_run[NH], l_run[NH];
@@ -212,7 +245,7 @@ __global__ void __launch_bounds__(C::THREADS)
           dot += __shfl_xor_sync(0xffffffffu, dot, 1);
           dot += __shfl_xor_sync(0xffffffffu, dot, 2);
           dot += __shfl_xor_sync(0xffffffffu, dot, 4);
-          x[h] = dot * p.scale_log2;
+          x[h] = dot * sl2;
         }
         if (valid) {
           const bool lagged = tok >= L_all;  // only with several tokens
@@ -315,18 +348,23 @@ __global__ void __launch_bounds__(C::THREADS)
         const size_t bh = query_row<MULTI>(p, b, h_first + h);
         if (whole) {
           // a row with no visible position (several tokens only) is 0
-          const float inv = (!MULTI || l_run[h] > 0.f) ? 1.f / l_run[h] : 0.f;
-          T *orow = reinterpret_cast<T *>(p.out) + bh * D;
+          float inv = (!MULTI || l_run[h] > 0.f) ? 1.f / l_run[h] : 0.f;
+          if (C::FP8) inv *= vscale;
+          TQ *orow = reinterpret_cast<TQ *>(p.out) + bh * D;
 #pragma unroll
           for (int bx = 0; bx < NBOX; ++bx) {
             float f[EPC];
 #pragma unroll
             for (int e = 0; e < EPC; ++e) f[e] = acc[h][bx * EPC + e] * inv;
-            store_chunk<T>(orow + bx * C::BOX_ELEMS + j * EPC, f);
+            store_elems<TQ, EPC>(orow + bx * C::BOX_ELEMS + j * EPC, f);
           }
         } else {
           const size_t ps = (size_t)slot * p.heads_per_cta + h;
           float *prow = p.o_part + ps * D;
+          if (C::FP8) {
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[h][e] *= vscale;
+          }
 #pragma unroll
           for (int bx = 0; bx < NBOX; ++bx)
 #pragma unroll
@@ -341,7 +379,7 @@ __global__ void __launch_bounds__(C::THREADS)
     const bool whole = seg.t0 == 0 && seg.t1 == seg.tiles;
     if (threadIdx.x == 0) record_unit(p, seg, whole, partial_slot(seg_index), range, b);
     if (!whole && p.unit_cnt)
-      finish_split_unit<T, D, MULTI>(p, seg, range, b, h_first, nh, threadIdx.x, C::CONSUMER_WARPS * 32, um,
+      finish_split_unit<TQ, D, MULTI>(p, seg, range, b, h_first, nh, threadIdx.x, C::CONSUMER_WARPS * 32, um,
                               [] { consumer_bar_sync(C::CONSUMER_WARPS * 32); });
     consumer_bar_sync(C::CONSUMER_WARPS * 32);  // scratch free for the next unit
   }

@@ -41,7 +41,8 @@ extern "C" {
 
 typedef enum {
     GQA_F32 = 0,  /* IEEE binary32 */
-    GQA_BF16 = 1  /* bfloat16, fp32 accumulation inside the kernels */
+    GQA_BF16 = 1, /* bfloat16, fp32 accumulation inside the kernels */
+    GQA_FP8_E4M3 = 2 /* OCP FP8 E4M3 codes: the cache of the *_fp8 entry points only */
 } gqa_dtype_t;
 
 typedef enum {
@@ -229,6 +230,42 @@ int gqa_decode_attention_multi_ex(const void *q, const void *k_cache, const void
                                   int B, int T, int H, int G, int d, int Nmax, gqa_dtype_t dtype,
                                   int split_tokens, void *workspace, size_t workspace_bytes,
                                   cudaStream_t stream);
+
+/*
+ * FP8 KV cache (GQA paper, section 4: quantizing keys and values is the
+ * lever that complements GQA; it halves the bytes a decode step reads
+ * again).  The caches hold OCP FP8 E4M3 codes (1 sign bit, 4 exponent bits
+ * with bias 7, 3 mantissa bits; no infinities; S.1111.111 is NaN; largest
+ * finite 448), one byte per element, in the [B, G, Nmax, d] layout, with one
+ * fp32 scale per KV head for K and one for V: element value = code * scale.
+ *
+ * kv_append_fp8 — kv_append onto such a cache: code = E4M3(x / scale[g]),
+ * the division in fp32 (IEEE, round to nearest) and the conversion rounding
+ * to nearest even, finite values beyond 448 saturating to +-448; then
+ * seq_lens[b] += 1.  k_new, v_new [B, G, d] bf16; k_scale, v_scale [G] fp32,
+ * device memory.  Rows with L_b < 0 or >= Nmax are left alone
+ * (GQA_DEVERR_APPEND_LEN).  The codes are bit-exact to that definition.
+ *
+ * gqa_decode_attention_fp8[_ws] — gqa_decode_attention over such a cache:
+ * K[b,g,n,:] = code * k_scale[g], V likewise; q and out [B, H, d] bf16,
+ * fp32 accumulation.  d = 128.  Workspace as for gqa_decode_attention_ws,
+ * of gqa_decode_workspace_bytes_fp8 bytes.  The kernel takes up to four
+ * query heads of a group per pass over the group's K/V rows: groups of
+ * more than four heads re-read them once per four heads.
+ */
+int kv_append_fp8(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                  const float *k_scale, const float *v_scale, int32_t *seq_lens,
+                  int B, int G, int d, int Nmax, cudaStream_t stream);
+size_t gqa_decode_workspace_bytes_fp8(int B, int H, int G, int d, int Nmax);
+int gqa_decode_attention_fp8(const void *q, const void *k_cache, const void *v_cache,
+                             const float *k_scale, const float *v_scale, const int32_t *seq_lens,
+                             float scale, void *out, int B, int H, int G, int d, int Nmax,
+                             cudaStream_t stream);
+int gqa_decode_attention_fp8_ws(const void *q, const void *k_cache, const void *v_cache,
+                                const float *k_scale, const float *v_scale,
+                                const int32_t *seq_lens, float scale, void *out,
+                                int B, int H, int G, int d, int Nmax, void *workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * gqa_qkv_project — the Q, K and V projections of the decode token, the step

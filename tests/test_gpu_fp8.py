@@ -1,0 +1,121 @@
+"""Parity of the FP8 (E4M3) cache path with the fp64 oracle, through the C
+ABI: kv_append_fp8 bit for bit, gqa_decode_attention_fp8 within
+|gpu - oracle| <= 1e-2 + 1e-2*|oracle| (the dequantized cache is exact; the
+kernel's error is fp32 accumulation and the bf16 rounding of out)."""
+import numpy as np
+import pytest
+import torch
+
+import grouped_query_decode_kv_b300 as gqa
+import oracle
+import workloads
+
+from test_gpu_parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    torch.cuda.set_device(0)
+    gqa.load_library()
+    gqa.gqa_get_device_error()
+    yield
+
+
+def _w(name, B, H, G, N, index, lens=None):
+    return workloads.Workload(name, B, H, G, 128, N, "bf16", lens or ("fixed", N), index)
+
+
+def run_fp8(x, scale, use_ws=False):
+    dev = torch.device("cuda")
+    t = {k: v.to(dev) for k, v in x.items()}
+    out = torch.full_like(t["q"], float("nan"))
+    if use_ws:
+        B, H, d = t["q"].shape
+        G, N = t["k_cache"].shape[1], t["k_cache"].shape[2]
+        need = gqa.gqa_decode_workspace_bytes_fp8(B, H, G, d, N)
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        gqa.gqa_decode_attention_fp8_ws(t["q"], t["k_cache"], t["v_cache"], t["k_scale"], t["v_scale"],
+                                        t["seq_lens"], scale, out, ws)
+    else:
+        gqa.gqa_decode_attention_fp8(t["q"], t["k_cache"], t["v_cache"], t["k_scale"], t["v_scale"], t["seq_lens"],
+                                     scale, out)
+    torch.cuda.synchronize()
+    return out
+
+
+def check_fp8(w, seq_lens=None, expect_err=0):
+    x = workloads.make_fp8_cache(w, seq_lens)
+    ref = oracle.decode_attention_fp8(x["q"], x["k_cache"], x["v_cache"], x["k_scale"], x["v_scale"], x["seq_lens"],
+                                      w.scale)
+    got = run_fp8(x, w.scale).double().cpu().numpy()
+    assert_parity(got, ref, f"{w.name} fp8")
+    assert gqa.gqa_get_device_error() == expect_err
+    return got
+
+
+@pytest.mark.parametrize("H,G", [(8, 8), (8, 4), (12, 4), (16, 4), (16, 2), (32, 1)])
+def test_fp8_attention_small(H, G):
+    lens = torch.tensor([700, 1, 129, 64, 383], dtype=torch.int32)
+    check_fp8(_w("fp8_small", 5, H, G, 700, 10000 + H + G), lens)
+
+
+def test_fp8_attention_empty_row_is_flagged_and_zero():
+    lens = torch.tensor([0, 200, 37], dtype=torch.int32)
+    got = check_fp8(_w("fp8_empty", 3, 8, 4, 256, 10100), lens, expect_err=gqa.DEVERR_ATTN_LEN)
+    assert np.all(got[0] == 0)
+
+
+@pytest.mark.parametrize("H,G", [(8, 8), (64, 8)])
+def test_fp8_attention_more_than_64_sequences(H, G):
+    B, N = 70, 300
+    lens = torch.randint(1, N + 1, (B,), generator=torch.Generator().manual_seed(10200)).to(torch.int32)
+    check_fp8(_w("fp8_many", B, H, G, N, 10200 + H), lens)
+
+
+@pytest.mark.parametrize("name", ["mha", "gqa8"])
+def test_fp8_attention_full_size(name):
+    w = workloads.workload(name)
+    check_fp8(_w(f"fp8_{name}", w.B, w.H, w.G, w.Nmax, 10300 + w.index, w.lens))
+
+
+def test_fp8_workspace_variant_matches_bitwise():
+    w = _w("fp8_ws", 4, 32, 32, 2048, 10400, ("uniform", 1, 2048))
+    x = workloads.make_fp8_cache(w)
+    assert torch.equal(run_fp8(x, w.scale), run_fp8(x, w.scale, use_ws=True))
+
+
+def test_fp8_append_is_bit_exact():
+    w = _w("fp8_app", 5, 8, 4, 64, 10500)
+    x = workloads.make_fp8_cache(w, torch.tensor([0, 63, 64, 10, -1], dtype=torch.int32))
+    kc2, vc2, sl2, skipped = oracle.kv_append_fp8(x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["k_scale"],
+                                                  x["v_scale"], x["seq_lens"])
+    dev = torch.device("cuda")
+    t = {k: v.to(dev) for k, v in x.items()}
+    gqa.kv_append_fp8(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["k_scale"], t["v_scale"], t["seq_lens"])
+    torch.cuda.synchronize()
+    assert torch.equal(t["k_cache"].cpu(), kc2) and torch.equal(t["v_cache"].cpu(), vc2)
+    assert torch.equal(t["seq_lens"].cpu(), sl2) and skipped == 2
+    assert gqa.gqa_get_device_error() == gqa.DEVERR_APPEND_LEN
+
+
+def test_fp8_append_then_attend():
+    """An FP8 decode step: append the new token, then attend over the grown
+    cache; matches the oracle's append and attention."""
+    w = _w("fp8_step", 4, 16, 4, 512, 10600, ("uniform", 1, 511))
+    x = workloads.make_fp8_cache(w)
+    kc2, vc2, sl2, _ = oracle.kv_append_fp8(x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["k_scale"],
+                                            x["v_scale"], x["seq_lens"])
+    ref = oracle.decode_attention_fp8(x["q"], kc2, vc2, x["k_scale"], x["v_scale"], sl2, w.scale)
+    dev = torch.device("cuda")
+    t = {k: v.to(dev) for k, v in x.items()}
+    gqa.kv_append_fp8(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["k_scale"], t["v_scale"], t["seq_lens"])
+    out = torch.empty_like(t["q"])
+    gqa.gqa_decode_attention_fp8(t["q"], t["k_cache"], t["v_cache"], t["k_scale"], t["v_scale"], t["seq_lens"],
+                                 w.scale, out)
+    torch.cuda.synchronize()
+    assert_parity(out.double().cpu().numpy(), ref, "fp8 step")
+    assert gqa.gqa_get_device_error() == 0

@@ -35,7 +35,7 @@ from typing import Dict, Optional, Tuple
 import torch
 
 __all__ = ["Workload", "WORKLOADS", "workload", "make_inputs", "sweep_names", "multi_names", "make_qkv_inputs",
-           "PROJECTIONS"]
+           "PROJECTIONS", "make_fp8_cache"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -182,3 +182,34 @@ def make_qkv_inputs(B: int, A: int, H: int, G: int, d: int, seed: int,
     wk = torch.randn(G, A, d, generator=g) * s
     wv = torch.randn(G, A, d, generator=g) * s
     return {"x": x.to(dtype), "w_q": wq.to(dtype), "w_k": wk.to(dtype), "w_v": wv.to(dtype)}
+
+
+def make_fp8_cache(w: Workload, seq_lens: Optional[torch.Tensor] = None) -> Dict[str, torch.Tensor]:
+    """An FP8 E4M3 cache for workload `w`: raw codes drawn uniformly over the
+    254 finite codes (no value arithmetic: the bytes themselves are random),
+    per-KV-head scales 2^-7 * (1 + u), u ~ U[0,1), q ~ N(0,1) bf16 [B,H,d], and
+    new rows k_new / v_new ~ N(0,1) bf16.  Rows at positions >= L_b hold the
+    NaN code 0x7F.  Draws from manual_seed(3000 + index) in the order q, K
+    codes, V codes, k_scale, v_scale, k_new, v_new."""
+    g = torch.Generator().manual_seed(3000 + w.index)
+    q = torch.randn(w.B, w.H, w.d, generator=g).to(torch.bfloat16)
+    def codes():
+        c = torch.randint(0, 254, (w.B, w.G, w.Nmax, w.d), generator=g, dtype=torch.int32)
+        c = c + (c >= 0x7F).to(torch.int32)      # skip 0x7F (NaN); 0xFF is out of the drawn range
+        return c.to(torch.uint8)
+    k = codes()
+    v = codes()
+    k_scale = (1.0 + torch.rand(w.G, generator=g)) / 128
+    v_scale = (1.0 + torch.rand(w.G, generator=g)) / 128
+    k_new = torch.randn(w.B, w.G, w.d, generator=g).to(torch.bfloat16)
+    v_new = torch.randn(w.B, w.G, w.d, generator=g).to(torch.bfloat16)
+    if seq_lens is None:
+        seq_lens = make_seq_lens(w)
+    seq_lens = seq_lens.to(torch.int32).contiguous()
+    for b in range(w.B):
+        L = int(seq_lens[b])
+        if 0 <= L < w.Nmax:
+            k[b, :, L:] = 0x7F
+            v[b, :, L:] = 0x7F
+    return {"q": q, "k_cache": k, "v_cache": v, "k_scale": k_scale.float(), "v_scale": v_scale.float(),
+            "k_new": k_new, "v_new": v_new, "seq_lens": seq_lens}
