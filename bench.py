@@ -705,7 +705,7 @@ def run_ours(args, world, rank, local):
         for name in workloads.multi_names():
             table_multi[name] = time_multi(workloads.workload(name), device, args.table_iters, 5, l2, mem_budget)
         table_fp8 = {}
-        for name in ("mha", "gqa8", "mqa"):
+        for name in ("mha", "gqa8", "mqa", "sweep_g8"):
             table_fp8[name] = time_fp8(workloads.workload(name), device, args.table_iters, l2, mem_budget)
         table_proj = {}
         for name in sorted(workloads.PROJECTIONS):

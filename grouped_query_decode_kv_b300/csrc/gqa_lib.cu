@@ -99,6 +99,8 @@ KernelChoice make_choice() {
   c.heads = C::HEADS;
   if constexpr (F == kSimt)
     c.box_elems = C::BOX_ELEMS;
+  else if constexpr (F == kTc)
+    c.box_elems = C::FP8 ? 128 : 64;
   else
     c.box_elems = 64;
   c.launch = &launch_split<C, F, MULTI>;
@@ -112,11 +114,20 @@ constexpr int kTcMinNrep = 8;
 using TcD128x16 = TcCfg<16, 3, 2>;
 using TcD128x32 = TcCfg<32, 3, 2>;
 using TcD128x64 = TcCfg<64, 3, 1>;
+// FP8 cache: 2 stages of 32 KB codes plus two 64 KB bf16 staging tiles
+using TcFp8x16 = TcCfg<16, 2, 2, true>;
+using TcFp8x32 = TcCfg<32, 2, 2, true>;
+using TcFp8x64 = TcCfg<64, 2, 1, true>;
 
 template <bool M>
 KernelChoice choose_kernel(gqa_dtype_t dt, int d, int n_rep) {
   if constexpr (!M) {
     if (dt == GQA_FP8_E4M3) {  // d = 128 (checked by the caller)
+      if (n_rep >= kTcMinNrep) {
+        if (n_rep <= 16) return make_choice<TcFp8x16, kTc, M>();
+        if (n_rep <= 32) return make_choice<TcFp8x32, kTc, M>();
+        return make_choice<TcFp8x64, kTc, M>();
+      }
       if (n_rep == 1) return make_choice<SimtFp8<1>, kSimt, M>();
       if (n_rep == 2) return make_choice<SimtFp8<2>, kSimt, M>();
       return make_choice<SimtFp8<4>, kSimt, M>();
@@ -412,7 +423,7 @@ int run_attention(const void *q, const void *k, const void *v, const int32_t *sl
   if (split && !merge_in_kernel) {
     const dim3 blocks(ceil_div((long long)B * p.H, 4));
     cudaError_t e;
-    if (dt == GQA_BF16)
+    if (dt == GQA_BF16 || dt == GQA_FP8_E4M3)  // out is bf16 for an FP8 cache too
       e = d == 128 ? launch_pdl(gqa_combine_kernel<__nv_bfloat16, 128>, blocks, dim3(128), 0, st, p)
                    : launch_pdl(gqa_combine_kernel<__nv_bfloat16, 64>, blocks, dim3(128), 0, st, p);
     else

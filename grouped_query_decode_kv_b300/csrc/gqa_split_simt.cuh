@@ -117,11 +117,6 @@ __device__ __forceinline__ void store_chunk<float>(float *dst, const float *f) {
   *reinterpret_cast<float4 *>(dst) = make_float4(f[0], f[1], f[2], f[3]);
 }
 
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-  return v;
-}
 
 template <class C, bool MULTI>
 __global__ void __launch_bounds__(C::THREADS)

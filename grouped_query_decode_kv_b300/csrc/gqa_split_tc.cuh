@@ -44,8 +44,11 @@
 
 namespace gqa {
 
-template <int NR_, int STAGES_, int PB_>
+// FP8_: the cache holds E4M3 codes; four more warps convert each landed
+// tile to bf16 in a double-buffered staging area that the MMAs read.
+template <int NR_, int STAGES_, int PB_, bool FP8_ = false>
 struct TcCfg {
+  static constexpr bool FP8 = FP8_;
   static constexpr int D = 128;
   static constexpr int BLOCK_N = 128;  // positions per tile: M of S^T, K of P.V
   static constexpr int STAGES = STAGES_;
@@ -56,8 +59,14 @@ struct TcCfg {
   static constexpr int UNIT_COST = 2;  // stream-K charge per unit, in tiles (gqa_schedule.cuh)
   static_assert(NR == 16 || NR == 32 || NR == 64, "heads per unit");
   static_assert(PB == 1 || PB == 2, "P^T buffers");
-  using Pipe = KVPipe<2, BLOCK_N, STAGES, 1>;  // one "empty" arrival per tile: the MMA commit
-  static constexpr int THREADS = 6 * 32;
+  // one "empty" arrival per tile: the MMA commit (FP8: the 4 converter warps)
+  using Pipe = KVPipe<FP8 ? 1 : 2, BLOCK_N, STAGES, FP8 ? 4 : 1>;
+  static constexpr int THREADS = (FP8 ? 10 : 6) * 32;
+  static constexpr int KV_BOX = BLOCK_N * 128;  // one 128-byte-wide box of a bf16 K or V tile
+  // FP8: staging [2] x (K tile | V tile) in bf16, two boxes each (d 0-63, 64-127)
+  static constexpr int STG_OFF = Pipe::PIPE_BYTES;
+  static constexpr int STG_TILE = 2 * KV_BOX;
+  static constexpr int STG_BYTES = FP8 ? 2 * 2 * STG_TILE : 0;
   static constexpr int SOFT = 128;             // softmax threads
   // TMEM columns: S^T buffers [0, 2*NR), O^T buffers [2*NR, 4*NR)
   static constexpr int TM_S = 0;
@@ -67,7 +76,7 @@ struct TcCfg {
   // Q: two 128-byte-wide boxes (d 0-63, 64-127) of NR rows per buffer; two
   // buffers where shared memory allows, so that the next unit's Q lands
   // while the current one is still in use
-  static constexpr int Q_OFF = Pipe::PIPE_BYTES;
+  static constexpr int Q_OFF = STG_OFF + STG_BYTES;
   static constexpr int Q_BOX = NR * 128;
   static constexpr int Q_BYTES = 2 * Q_BOX;
   // P^T buffers, K-major like Q: one row of 128 positions per head, as two
@@ -75,8 +84,8 @@ struct TcCfg {
   static constexpr int P_BOX = NR * 128;
   static constexpr int P_BYTES = 2 * P_BOX;
   // pipe full[STAGES], empty[STAGES]; then s_full[2], s_free[2], p_full[2],
-  // pv_done[2], o_free[2], q_full[2], mma_done
-  static constexpr int NBAR = 2 * STAGES + 13;
+  // pv_done[2], o_free[2], q_full[2], mma_done; FP8: conv_full[2], stg_free[2]
+  static constexpr int NBAR = 2 * STAGES + 13 + (FP8 ? 4 : 0);
   static constexpr int RANGE_BYTES = ((int)sizeof(CtaRange) + 15) / 16 * 16;
   static constexpr int TAIL_BYTES = 4 * NQ * 4 + 3 * NQ * 4 + NBAR * 8 + 16 + RANGE_BYTES + (int)sizeof(UnitMerge);
   static constexpr int QB = 1024 + Q_OFF + 2 * Q_BYTES + PB * P_BYTES + TAIL_BYTES <= 227 * 1024 ? 2 : 1;
@@ -104,6 +113,8 @@ struct TcBars {
   __device__ __forceinline__ uint32_t o_free(int i) const { return b0 + 64 + 8 * i; }
   __device__ __forceinline__ uint32_t q_full(int i) const { return b0 + 80 + 8 * i; }
   __device__ __forceinline__ uint32_t mma_done() const { return b0 + 96; }
+  __device__ __forceinline__ uint32_t conv_full(int i) const { return b0 + 104 + 8 * i; }
+  __device__ __forceinline__ uint32_t stg_free(int i) const { return b0 + 120 + 8 * i; }
 };
 
 // All lanes of a warp wait; a wait that timed out in any lane counts as
@@ -232,6 +243,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     mbar_init(bars.q_full(0), 4);  // one arrival per softmax warp
     mbar_init(bars.q_full(1), 4);
     mbar_init(bars.mma_done(), 1);
+    if (C::FP8) {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(bars.conv_full(i), 4);  // one arrival per converter warp
+        mbar_init(bars.stg_free(i), 1);   // the MMA commit after the tile's P.V
+      }
+    }
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -248,7 +265,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     SchedParams spx = sp;
     spx.spec = 1;
     const CtaRange r0 = warp_plan_range<true>(spx, lane, nullptr, 0);
-    if (lane == 0 && r0.begin < r0.end) prefetch_first_tiles(spx, r0, &tmK, &tmV, 64, 2, p.G, p.head_chunks, ST);
+    if (lane == 0 && r0.begin < r0.end) prefetch_first_tiles(spx, r0, &tmK, &tmV, C::FP8 ? 128 : 64, C::FP8 ? 1 : 2, p.G, p.head_chunks, ST);
   }
   griddep_wait();  // lengths, q and cache rows written by earlier kernels are visible
   if (warp == 0) {
@@ -265,7 +282,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   if (range.begin < range.end) {
     if (warp == 0) {
       // ------------------------------------------------------------ producer
-      produce_range(pipe, sp, range, &tmK, &tmV, 64, p.G, p.head_chunks, p, lane);
+      produce_range(pipe, sp, range, &tmK, &tmV, C::FP8 ? 128 : 64, p.G, p.head_chunks, p, lane);
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
       if (lane == 0) {
@@ -307,14 +324,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             // unit u's Q is in buffer u % QB, its (u / QB)-th use
             const int qb = ws.unit % C::QB;
             const uint32_t qpar = (ws.unit / C::QB) & 1;
-            if ((ws.i != 0 || mbar_test(bars.q_full(qb), qpar)) && mbar_test(pipe.full(st), (tg / ST) & 1) &&
+            const bool k_ready = C::FP8 ? mbar_test(bars.conv_full(tg & 1), (tg >> 1) & 1)
+                                        : mbar_test(pipe.full(st), (tg / ST) & 1);
+            if ((ws.i != 0 || mbar_test(bars.q_full(qb), qpar)) && k_ready &&
                 (tg < 2 || mbar_test(bars.s_free(tg & 1), ((tg >> 1) - 1) & 1))) {
               tc::fence_after();
-              const uint32_t kt = pipe.k_tile(st);
+              const uint32_t kt = C::FP8 ? pipe.base + C::STG_OFF + (tg & 1) * 2 * C::STG_TILE : pipe.k_tile(st);
               const uint32_t qt = qbase + qb * C::Q_BYTES;
 #pragma unroll
               for (int ks = 0; ks < D / 16; ++ks) {
-                const uint64_t a = tc::smem_desc_sw128(kt + (ks >> 2) * Pipe::BOX_BYTES + (ks & 3) * 32, 16, 1024);
+                const uint64_t a = tc::smem_desc_sw128(kt + (ks >> 2) * C::KV_BOX + (ks & 3) * 32, 16, 1024);
                 const uint64_t b = tc::smem_desc_sw128(qt + (ks >> 2) * C::Q_BOX + (ks & 3) * 32, 16, 1024);
                 tc::mma_ss(tmem + C::TM_S + (tg & 1) * NR, a, b, IDESC_S, ks > 0);
               }
@@ -329,15 +348,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (mbar_test(bars.p_full(pb), use & 1) &&
                 (wp.i != 0 || wp.unit < 2 || mbar_test(bars.o_free(ob), ((wp.unit >> 1) - 1) & 1))) {
               tc::fence_after();
-              const uint32_t vt = pipe.v_tile(tg % ST);
+              const uint32_t vt =
+                  C::FP8 ? pipe.base + C::STG_OFF + (tg & 1) * 2 * C::STG_TILE + C::STG_TILE : pipe.v_tile(tg % ST);
 #pragma unroll
               for (int ks = 0; ks < BN / 16; ++ks) {
-                const uint64_t a = tc::smem_desc_sw128(vt + ks * 2048, Pipe::BOX_BYTES, 1024);
+                const uint64_t a = tc::smem_desc_sw128(vt + ks * 2048, C::KV_BOX, 1024);
                 const uint64_t b =
                     tc::smem_desc_sw128(pbase + pb * C::P_BYTES + (ks >> 2) * C::P_BOX + (ks & 3) * 32, 16, 1024);
                 tc::mma_ss(tmem + C::TM_O + ob * NR, a, b, IDESC_PV, wp.i > 0 || ks > 0);
               }
-              tc::commit(pipe.empty(tg % ST));
+              // the tile's K and V are no longer read: free its ring stage
+              // (FP8: its staging buffer; the converters free the stage)
+              tc::commit(C::FP8 ? bars.stg_free(tg & 1) : pipe.empty(tg % ST));
               tc::commit(bars.pv_done(pb));
               wp.advance(sp);
               progressed = true;
@@ -353,7 +375,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (wp.tg < ws.tg)
               mbar_try_wait_hint(bars.p_full(wp.tg % C::PB), (wp.tg / C::PB) & 1, 1000);
             else if (ws.has)
-              mbar_try_wait_hint(pipe.full(ws.tg % ST), (ws.tg / ST) & 1, 1000);
+              mbar_try_wait_hint(C::FP8 ? bars.conv_full(ws.tg & 1) : pipe.full(ws.tg % ST),
+                                 C::FP8 ? (ws.tg >> 1) & 1 : (ws.tg / ST) & 1, 1000);
             else
               __nanosleep(32);
             const unsigned long long now = global_timer_ns();
@@ -370,7 +393,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         mbar_wait(bars.mma_done(), 0);
       }
       __syncwarp();
-    } else {
+    } else if (warp < 6) {
       // ------------------------------------------------------------ softmax
       const int sub = warp & 3;       // TMEM lane quarter of this warp
       const int R = 32 * sub + lane;  // TMEM lane: tile position (S^T) / output dim (O^T)
@@ -440,6 +463,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int L = attn_len(p.seq_lens, b, p.Nmax, p.append);
         const int ob = unit & 1;
         const int ntl = seg.t1 - seg.t0;
+        // FP8 cache: K's per-head scale joins the logit scale, V's the result
+        const int g_unit = seg.uib / p.head_chunks;
+        const float sl2 = C::FP8 ? p.scale_log2 * __ldg(p.k_scale + g_unit) : p.scale_log2;
+        const float vscale = C::FP8 ? __ldg(p.v_scale + g_unit) : 1.f;
         float lp[NR];
 #pragma unroll
         for (int h = 0; h < NR; ++h) lp[h] = 0.f;
@@ -480,7 +507,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
               for (int c = 0; c < (NR < 32 ? NR : 32); ++c) {
                 const int h = c0 + c;
-                x[h] = (valid && h < nh) ? __uint_as_float(r[c]) * p.scale_log2 : -INFINITY;
+                x[h] = (valid && h < nh) ? __uint_as_float(r[c]) * sl2 : -INFINITY;
               }
             }
             if (MULTI && edge) {
@@ -564,7 +591,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               asm volatile("st.shared.u16 [%0], %1;" ::"r"(col + h * 128 + ((chunk ^ (h & 7)) << 4)), "h"(pb16[h])
                            : "memory");
           }
-          if (!valid && !dead && mbar_wait(pipe.full(st), (tg / ST) & 1)) {
+          if (!C::FP8 && !valid && !dead && mbar_wait(pipe.full(st), (tg / ST) & 1)) {
             // position past L: its V row may hold anything (NaN included) and
             // 0 * NaN = NaN inside the MMA, so clear it (after it landed)
             const uint32_t a = pipe.v_tile(st) + R * 128;
@@ -634,7 +661,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               tk += wrap ? 1 : 0;
             }
             if (h < nh) {
-              const float o = __uint_as_float(r[c]);
+              const float o = __uint_as_float(r[c]) * vscale;
               if (whole)
                 reinterpret_cast<__nv_bfloat16 *>(p.out)[orow * D + R] =
                     __float2bfloat16_rn((!MULTI || fin[h] > 0.f) ? o / fin[h] : 0.f);
@@ -654,6 +681,67 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         soft_bar();  // fin[] is reused by the next unit's reductions
         seg = nseg;
         have = next;
+      }
+    } else if constexpr (C::FP8) {
+      // ------------------------------------------------------------ FP8 converters
+      // Thread R converts position R of every tile: its K and V rows of 128
+      // E4M3 codes (one 128-byte swizzled row as TMA landed it) become two
+      // 128-byte swizzled rows of bf16 in the tile's staging buffer; rows at
+      // or past L become zeros (their codes may be NaN, and 0 * NaN = NaN in
+      // the P.V MMA).
+      const int R = 32 * (warp - 6) + lane;
+      SegmentCursor cur;
+      cur.init(sp, range);
+      Segment seg;
+      bool dead = false;
+      int tg = 0;
+      while (cur.next(sp, seg)) {
+        const int L = attn_len(p.seq_lens, seg.b, p.Nmax, p.append);
+        for (int t = seg.t0; t < seg.t1; ++t, ++tg) {
+          const int st = tg % ST, cb = tg & 1;
+          if (!dead && !warp_wait(pipe.full(st), (tg / ST) & 1)) dead = true;
+          if (tg >= 2 && !dead && !warp_wait(bars.stg_free(cb), ((tg >> 1) - 1) & 1)) dead = true;
+          const bool valid = t * BN + R < L;
+          const uint32_t stg = pipe.base + C::STG_OFF + cb * 2 * C::STG_TILE;
+#pragma unroll
+          for (int kv = 0; kv < 2; ++kv) {
+            const uint32_t src = kv == 0 ? pipe.k_tile(st) : pipe.v_tile(st);
+            const uint32_t dst = stg + kv * C::STG_TILE;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {  // 16 codes -> 16 bf16 (two 16-byte chunks)
+              uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+              if (valid) {
+                const uint4 w = lds128(swz128(src, R, c));
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                uint32_t o[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  float f0, f1, f2, f3;
+                  e4m3x2_to_float(ww[i] & 0xffffu, f0, f1);
+                  e4m3x2_to_float(ww[i] >> 16, f2, f3);
+                  o[2 * i] = pack_bf16x2(f0, f1);
+                  o[2 * i + 1] = pack_bf16x2(f2, f3);
+                }
+                lo = make_uint4(o[0], o[1], o[2], o[3]);
+                hi = make_uint4(o[4], o[5], o[6], o[7]);
+              }
+              const uint32_t box = dst + (c >> 2) * C::KV_BOX;
+              const int k0 = 2 * (c & 3);
+              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(swz128(box, R, k0)), "r"(lo.x), "r"(lo.y),
+                           "r"(lo.z), "r"(lo.w)
+                           : "memory");
+              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(swz128(box, R, k0 + 1)), "r"(hi.x),
+                           "r"(hi.y), "r"(hi.z), "r"(hi.w)
+                           : "memory");
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(bars.conv_full(cb));
+            mbar_arrive(pipe.empty(st));
+          }
+        }
       }
     }
   }

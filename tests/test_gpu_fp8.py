@@ -57,7 +57,7 @@ def check_fp8(w, seq_lens=None, expect_err=0):
     return got
 
 
-@pytest.mark.parametrize("H,G", [(8, 8), (8, 4), (12, 4), (16, 4), (16, 2), (32, 1)])
+@pytest.mark.parametrize("H,G", [(8, 8), (8, 4), (12, 4), (16, 4), (16, 2), (32, 1), (64, 1), (128, 2)])
 def test_fp8_attention_small(H, G):
     lens = torch.tensor([700, 1, 129, 64, 383], dtype=torch.int32)
     check_fp8(_w("fp8_small", 5, H, G, 700, 10000 + H + G), lens)
