@@ -48,11 +48,11 @@ __all__ = [
     "gqa_decode_attention_multi", "gqa_decode_attention_multi_ex",
     "gqa_qkv_project", "gqa_qkv_project_ws", "gqa_qkv_project_workspace_bytes",
     "gqa_decode_attention_fp8", "gqa_decode_attention_fp8_ws", "gqa_decode_workspace_bytes_fp8", "kv_append_fp8",
-    "DEVERR_ATTN_LEN", "DEVERR_APPEND_LEN", "DEVERR_TIMEOUT", "EXPORTED_SYMBOLS",
+    "DEVERR_ATTN_LEN", "DEVERR_APPEND_LEN", "DEVERR_TIMEOUT", "DEVERR_RANGE", "EXPORTED_SYMBOLS",
 ]
 
 GQA_F32, GQA_BF16 = 0, 1
-DEVERR_ATTN_LEN, DEVERR_APPEND_LEN, DEVERR_TIMEOUT = 1, 2, 4
+DEVERR_ATTN_LEN, DEVERR_APPEND_LEN, DEVERR_TIMEOUT, DEVERR_RANGE = 1, 2, 4, 8
 ERR_SCRATCH_LIMIT = -5
 NOALLOC_SCRATCH_BYTES = 32 << 20  # GQA_NOALLOC_SCRATCH_BYTES in include/gqa.h
 

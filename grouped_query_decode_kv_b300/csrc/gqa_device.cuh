@@ -219,6 +219,26 @@ __device__ __forceinline__ void e4m3x2_to_float(uint32_t pair16, float &lo, floa
   asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"(b));
 }
 
+// Two E4M3 codes (low byte first) to an f16 pair (low half first), exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair16) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)pair16));
+  return h2;
+}
+
+// fp32 pair to an f16 pair (low half = lo), round to nearest even.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint16_t f16_bits(float x) {
+  uint16_t r;
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(r) : "f"(x));
+  return r;
+}
+
 // fp32 pair to two E4M3 codes (low byte = lo): round to nearest even,
 // finite values beyond 448 saturate to +-448.
 __device__ __forceinline__ uint32_t float2_to_e4m3x2(float lo, float hi) {

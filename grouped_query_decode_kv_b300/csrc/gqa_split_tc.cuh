@@ -45,7 +45,8 @@
 namespace gqa {
 
 // FP8_: the cache holds E4M3 codes; four more warps convert each landed
-// tile to bf16 in a double-buffered staging area that the MMAs read.
+// tile to f16 (exact) in a double-buffered staging area that the MMAs read,
+// and Q and P are f16 too (one operand type per MMA).
 template <int NR_, int STAGES_, int PB_, bool FP8_ = false>
 struct TcCfg {
   static constexpr bool FP8 = FP8_;
@@ -63,7 +64,7 @@ struct TcCfg {
   using Pipe = KVPipe<FP8 ? 1 : 2, BLOCK_N, STAGES, FP8 ? 4 : 1>;
   static constexpr int THREADS = (FP8 ? 10 : 6) * 32;
   static constexpr int KV_BOX = BLOCK_N * 128;  // one 128-byte-wide box of a bf16 K or V tile
-  // FP8: staging [2] x (K tile | V tile) in bf16, two boxes each (d 0-63, 64-127)
+  // FP8: staging [2] x (K tile | V tile) in f16, two boxes each (d 0-63, 64-127)
   static constexpr int STG_OFF = Pipe::PIPE_BYTES;
   static constexpr int STG_TILE = 2 * KV_BOX;
   static constexpr int STG_BYTES = FP8 ? 2 * 2 * STG_TILE : 0;
@@ -286,8 +287,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
       if (lane == 0) {
-        constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(BN, NR, false, false);
-        constexpr uint32_t IDESC_PV = tc::idesc_bf16_f32(D, NR, true, false);
+        // FP8 cache: all operands are f16 (exact for the E4M3 values)
+        constexpr uint32_t IDESC_S =
+            C::FP8 ? tc::idesc_f16_f32(BN, NR, false, false) : tc::idesc_bf16_f32(BN, NR, false, false);
+        constexpr uint32_t IDESC_PV =
+            C::FP8 ? tc::idesc_f16_f32(D, NR, true, false) : tc::idesc_bf16_f32(D, NR, true, false);
         // Two walks over the CTA's tiles: S^T of tile ts may start once its K
         // tile landed, its S buffer is free and (first tile of a unit) the
         // unit's Q is in place; P.V of tile tp once its P is written and
@@ -435,6 +439,31 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           cp_async_wait<1>();
         else
           cp_async_wait<0>();
+        if constexpr (C::FP8) {
+          // f16 operands: this thread's bf16 chunks become f16 in place
+          const int row = R >> 1, half = R & 1;
+          if (row < NR) {
+            const uint32_t dst = qbase + buf * C::Q_BYTES + half * C::Q_BOX + row * 128;
+            bool big = false;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint32_t a = dst + ((c ^ (row & 7)) << 4);
+              const uint4 v = lds128(a);
+              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+              uint32_t o[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float lo = bf16_lo(w[i]), hi = bf16_hi(w[i]);
+                big |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
+                o[i] = pack_f16x2(lo, hi);
+              }
+              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(o[0]), "r"(o[1]), "r"(o[2]),
+                           "r"(o[3])
+                           : "memory");
+            }
+            if (big) flag_error(GQA_DEVERR_RANGE);
+          }
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.q_full(buf));
@@ -578,7 +607,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           for (int h = 0; h < NR; ++h) {
             const float pv = h < nh ? tc::ex2(x[h] - m_s[h]) : 0.f;
             lp[h] += pv;
-            pb16[h] = __bfloat16_as_ushort(__float2bfloat16_rn(pv));
+            pb16[h] = C::FP8 ? f16_bits(pv) : __bfloat16_as_ushort(__float2bfloat16_rn(pv));
           }
           // the P buffer was last read by the P.V of tile tg - PB
           const int pb = tg % C::PB;
@@ -686,7 +715,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       // ------------------------------------------------------------ FP8 converters
       // Thread R converts position R of every tile: its K and V rows of 128
       // E4M3 codes (one 128-byte swizzled row as TMA landed it) become two
-      // 128-byte swizzled rows of bf16 in the tile's staging buffer; rows at
+      // 128-byte swizzled rows of f16 in the tile's staging buffer; rows at
       // or past L become zeros (their codes may be NaN, and 0 * NaN = NaN in
       // the P.V MMA).
       const int R = 32 * (warp - 6) + lane;
@@ -708,7 +737,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const uint32_t src = kv == 0 ? pipe.k_tile(st) : pipe.v_tile(st);
             const uint32_t dst = stg + kv * C::STG_TILE;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {  // 16 codes -> 16 bf16 (two 16-byte chunks)
+            for (int c = 0; c < 8; ++c) {  // 16 codes -> 16 f16 (two 16-byte chunks)
               uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
               if (valid) {
                 const uint4 w = lds128(swz128(src, R, c));
@@ -716,11 +745,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 uint32_t o[8];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                  float f0, f1, f2, f3;
-                  e4m3x2_to_float(ww[i] & 0xffffu, f0, f1);
-                  e4m3x2_to_float(ww[i] >> 16, f2, f3);
-                  o[2 * i] = pack_bf16x2(f0, f1);
-                  o[2 * i + 1] = pack_bf16x2(f2, f3);
+                  o[2 * i] = e4m3x2_to_f16x2(ww[i] & 0xffffu);
+                  o[2 * i + 1] = e4m3x2_to_f16x2(ww[i] >> 16);
                 }
                 lo = make_uint4(o[0], o[1], o[2], o[3]);
                 hi = make_uint4(o[4], o[5], o[6], o[7]);

@@ -60,6 +60,8 @@ typedef enum {
 #define GQA_DEVERR_ATTN_LEN 1   /* attention saw seq_lens[b] <= 0 or > Nmax */
 #define GQA_DEVERR_APPEND_LEN 2 /* kv_append saw seq_lens[b] < 0 or >= Nmax */
 #define GQA_DEVERR_TIMEOUT 4    /* a pipeline wait gave up after its time limit */
+#define GQA_DEVERR_RANGE 8      /* FP8 cache, groups of 8+ heads: a query value beyond the f16
+                                   range (|q| > 65504) of that path's tensor-core operands */
 
 /*
  * gqa_decode_attention — attention of one decode token per sequence.
