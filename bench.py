@@ -834,6 +834,9 @@ def main(argv=None):
     ap.add_argument("--no-table", action="store_true", help="skip the per-workload table")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--table-iters", type=int, default=200)
+    ap.add_argument("--table-only", choices=["proj", "fp8", "multi"], default=None,
+                    help="time only one group of table rows (projection layers, FP8 cache, several "
+                         "tokens) and print them as one JSON line; for profiling those kernels")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--prewarm", type=float, default=1.0, help="seconds of untimed steps before the warm-up")
     args = ap.parse_args(argv)
@@ -842,7 +845,31 @@ def main(argv=None):
     world, rank, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.table_only:
+        return run_table_only(args, local)
     return run_ours(args, world, rank, local)
+
+
+def run_table_only(args, local):
+    """One group of table rows on this GPU, printed as one JSON line (no
+    step timing, no baselines): the command the ncu summaries of the
+    projection and FP8 kernels are taken with."""
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    mem_budget = int(torch.cuda.mem_get_info(device)[0] * 0.5)
+    rows = {}
+    if args.table_only == "proj":
+        for name in sorted(workloads.PROJECTIONS):
+            rows[name] = time_projection(name, device, args.table_iters, l2, mem_budget)
+    elif args.table_only == "fp8":
+        for name in ("mha", "gqa8"):
+            rows[name] = time_fp8(workloads.workload(name), device, args.table_iters, l2, mem_budget)
+    else:
+        for name in workloads.multi_names():
+            rows[name] = time_multi(workloads.workload(name), device, args.table_iters, 5, l2, mem_budget)
+    print(json.dumps({"table_only": args.table_only, "rows": rows}), flush=True)
+    return 0
 
 
 if __name__ == "__main__":
