@@ -16,21 +16,24 @@
 // point of GQA: GQA paper, section 2.2), and the MMA work per tile is the
 // 2 x 128 x 128 x 2 x N flop, well under the tensor pipe's rate.
 //
-// Softmax: thread R of the four softmax warps owns TMEM lane R, which is
-// cached position R of the tile in S^T and output dimension R in O^T.  For
-// each head h it keeps the running max m[h] (replicated in every thread,
-// base-2 units) and its own partial sum l_R[h].  A tile first votes whether
-// any logit exceeds m[h] + 8; only then (always on a unit's first tile) the
-// tile's per-head maxima are reduced across the 128 threads and m moves,
-// with O^T rescaled in TMEM.  P = 2^(S - m) is written to shared memory as
+// Softmax: thread R of a group of four softmax warps owns TMEM lane R, which
+// is cached position R of the tile in S^T and output dimension R in O^T.
+// With 32 or 64 heads two such groups share the head columns (half each),
+// so that two warps per sub-partition hide each other's latencies.  For
+// each of its heads h a thread keeps its own partial sum l_R[h]; the running
+// max m[h] (base-2 units) is shared by the group through shared memory.  A
+// tile first votes whether any logit exceeds m[h] + 8; only then (always on
+// a unit's first tile) the tile's per-head maxima are reduced across the
+// group's 128 threads and m moves, with O^T rescaled in TMEM.  P = 2^(S - m) is written to shared memory as
 // bf16 (double-buffered where shared memory allows, so that the softmax of
 // tile t+1 need not wait for the P.V of tile t); the l_R[h] are summed
 // across threads once per unit.
 //
-// Warp roles (192 threads, one CTA per SM):
+// Warp roles (one CTA per SM):
 //   warp 0     TMA producer of the CTA's stream-K range (gqa_pipeline.cuh)
 //   warp 1     MMA issuer (one thread) and TMEM owner
-//   warps 2..5 softmax, Q loads, output
+//   warps 2..  softmax and output, in SG groups of four (group 0 also
+//              loads Q); FP8: then four converter warps
 // S^T is double-buffered in TMEM so that S of tile t+1 overlaps the softmax
 // of tile t; O^T is double-buffered across units.  Every mbarrier wait is
 // bounded (about one second), after which the CTA winds down and flags
@@ -47,7 +50,7 @@ namespace gqa {
 // FP8_: the cache holds E4M3 codes; four more warps convert each landed
 // tile to f16 (exact) in a double-buffered staging area that the MMAs read,
 // and Q and P are f16 too (one operand type per MMA).
-template <int NR_, int STAGES_, int PB_, bool FP8_ = false>
+template <int NR_, int STAGES_, int PB_, bool FP8_ = false, int SG_ = 1>
 struct TcCfg {
   static constexpr bool FP8 = FP8_;
   static constexpr int D = 128;
@@ -60,15 +63,21 @@ struct TcCfg {
   static constexpr int UNIT_COST = 2;  // stream-K charge per unit, in tiles (gqa_schedule.cuh)
   static_assert(NR == 16 || NR == 32 || NR == 64, "heads per unit");
   static_assert(PB == 1 || PB == 2, "P^T buffers");
+  // softmax groups of four warps; group j owns the head columns
+  // [j*HG, (j+1)*HG) of S^T, P^T and O^T
+  static constexpr int SG = SG_;
+  static constexpr int HG = NR / SG;
+  static_assert(SG == 1 || (SG == 2 && NR >= 32), "two softmax groups need 16+ heads each");
   // one "empty" arrival per tile: the MMA commit (FP8: the 4 converter warps)
   using Pipe = KVPipe<FP8 ? 1 : 2, BLOCK_N, STAGES, FP8 ? 4 : 1>;
-  static constexpr int THREADS = (FP8 ? 10 : 6) * 32;
+  static constexpr int CONV_WARP0 = 2 + 4 * SG;  // first FP8 converter warp
+  static constexpr int THREADS = (CONV_WARP0 + (FP8 ? 4 : 0)) * 32;
   static constexpr int KV_BOX = BLOCK_N * 128;  // one 128-byte-wide box of a bf16 K or V tile
   // FP8: staging [2] x (K tile | V tile) in f16, two boxes each (d 0-63, 64-127)
   static constexpr int STG_OFF = Pipe::PIPE_BYTES;
   static constexpr int STG_TILE = 2 * KV_BOX;
   static constexpr int STG_BYTES = FP8 ? 2 * 2 * STG_TILE : 0;
-  static constexpr int SOFT = 128;             // softmax threads
+  static constexpr int SOFT = 128;             // threads of one softmax group
   // TMEM columns: S^T buffers [0, 2*NR), O^T buffers [2*NR, 4*NR)
   static constexpr int TM_S = 0;
   static constexpr int TM_O = 2 * NR;
@@ -91,7 +100,7 @@ struct TcCfg {
   static constexpr int TAIL_BYTES = 4 * NQ * 4 + 3 * NQ * 4 + NBAR * 8 + 16 + RANGE_BYTES + (int)sizeof(UnitMerge);
   static constexpr int QB = 1024 + Q_OFF + 2 * Q_BYTES + PB * P_BYTES + TAIL_BYTES <= 227 * 1024 ? 2 : 1;
   static constexpr int P_OFF = Q_OFF + QB * Q_BYTES;
-  static constexpr int RED_OFF = P_OFF + PB * P_BYTES;  // [4][NQ] cross-warp reduction
+  static constexpr int RED_OFF = P_OFF + PB * P_BYTES;  // [SG][4][HG] cross-warp reduction
   static constexpr int FIN_OFF = RED_OFF + 4 * NQ * 4;   // [NQ] reduced value
   static constexpr int M_OFF = FIN_OFF + NQ * 4;         // [NQ] running max of the unit
   static constexpr int CORR_OFF = M_OFF + NQ * 4;        // [NQ] rescale factor of a tile
@@ -125,17 +134,18 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
-// Named barrier 2 over the 128 softmax threads; the second form ORs a flag.
-__device__ __forceinline__ void soft_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
-__device__ __forceinline__ bool soft_bar_or(bool v) {
+// Named barrier 2 + j over the 128 threads of softmax group j; the second
+// form ORs a flag.
+__device__ __forceinline__ void soft_bar(int grp) { asm volatile("bar.sync %0, 128;" ::"r"(2 + grp) : "memory"); }
+__device__ __forceinline__ bool soft_bar_or(int grp, bool v) {
   uint32_t res;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 2, 128, p;\n\t"
+      "bar.red.or.pred q, %2, 128, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(res)
-      : "r"((uint32_t)v)
+      : "r"((uint32_t)v), "r"(2 + grp)
       : "memory");
   return res != 0;
 }
@@ -175,20 +185,44 @@ __device__ __forceinline__ void warp_transpose_reduce(float (&v)[NR], int lane) 
   }
 }
 
-// Per-head reduction of v over the 128 softmax threads (v is clobbered);
-// afterwards every softmax thread can read the result of head h from fin[h].
+// Per-head reduction of v (group grp's HG heads) over the group's 128
+// threads (v is clobbered); afterwards every thread of the group can read
+// the result of its head h from fin[grp*HG + h].  `red` holds [SG][4][HG].
 template <class C, bool MAX>
-__device__ __forceinline__ void soft_reduce(float (&v)[C::NR], int sub, int lane, float *red, float *fin, int R) {
-  using TR = TransposeReduce<C::NR>;
-  warp_transpose_reduce<C::NR, MAX>(v, lane);
+__device__ __forceinline__ void soft_reduce(float (&v)[C::HG], int grp, int sub, int lane, float *red, float *fin,
+                                            int R) {
+  using TR = TransposeReduce<C::HG>;
+  constexpr int HG = C::HG;
+  warp_transpose_reduce<HG, MAX>(v, lane);
+  float *rg = red + grp * 4 * HG;
 #pragma unroll
-  for (int j = 0; j < TR::K; ++j) red[sub * C::NQ + j + TR::K * (lane >> TR::SHIFT)] = v[j];
-  soft_bar();
-  if (R < C::NR) {
-    const float a = red[R], b2 = red[C::NQ + R], c = red[2 * C::NQ + R], d = red[3 * C::NQ + R];
-    fin[R] = MAX ? fmaxf(fmaxf(a, b2), fmaxf(c, d)) : (a + b2) + (c + d);
+  for (int j = 0; j < TR::K; ++j) rg[sub * HG + j + TR::K * (lane >> TR::SHIFT)] = v[j];
+  soft_bar(grp);
+  if (R < HG) {
+    const float a = rg[R], b2 = rg[HG + R], c = rg[2 * HG + R], d = rg[3 * HG + R];
+    fin[grp * HG + R] = MAX ? fmaxf(fmaxf(a, b2), fmaxf(c, d)) : (a + b2) + (c + d);
   }
-  soft_bar();
+  soft_bar(grp);
+}
+
+// 4x4 transpose across the four lanes of each quad (lanes 4k..4k+3): lane j
+// of a quad holds v[i] = M[j][i] before and v[i] = M[i][j] after (two
+// butterfly stages, each swapping one pair of values with the partner lane).
+__device__ __forceinline__ void quad_transpose(float (&v)[4], int lane) {
+  const bool b0 = (lane & 1) != 0, b1 = (lane & 2) != 0;
+  float r;
+  r = __shfl_xor_sync(0xffffffffu, b0 ? v[0] : v[1], 1);
+  v[0] = b0 ? r : v[0];
+  v[1] = b0 ? v[1] : r;
+  r = __shfl_xor_sync(0xffffffffu, b0 ? v[2] : v[3], 1);
+  v[2] = b0 ? r : v[2];
+  v[3] = b0 ? v[3] : r;
+  r = __shfl_xor_sync(0xffffffffu, b1 ? v[0] : v[2], 2);
+  v[0] = b1 ? r : v[0];
+  v[2] = b1 ? v[2] : r;
+  r = __shfl_xor_sync(0xffffffffu, b1 ? v[1] : v[3], 2);
+  v[1] = b1 ? r : v[1];
+  v[3] = b1 ? v[3] : r;
 }
 
 // Floor of the running max (log2 units): far below any logit, finite so
@@ -202,7 +236,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     gqa_split_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const SplitParams p) {
   using Pipe = typename C::Pipe;
-  constexpr int D = C::D, BN = C::BLOCK_N, ST = C::STAGES, NQ = C::NQ, NR = C::NR;
+  constexpr int D = C::D, BN = C::BLOCK_N, ST = C::STAGES, NR = C::NR, HG = C::HG;
+  constexpr int HCH = HG < 32 ? HG : 32;  // TMEM columns per tcgen05.ld of the softmax
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -234,14 +269,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     pipe.init();
     for (int i = 0; i < 2; ++i) {
       mbar_init(bars.s_full(i), 1);
-      mbar_init(bars.s_free(i), 4);
-      mbar_init(bars.o_free(i), 4);
+      mbar_init(bars.s_free(i), 4 * C::SG);  // one arrival per softmax warp
+      mbar_init(bars.o_free(i), 4 * C::SG);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bars.p_full(i), 4);
+      mbar_init(bars.p_full(i), 4 * C::SG);
       mbar_init(bars.pv_done(i), 1);
     }
-    mbar_init(bars.q_full(0), 4);  // one arrival per softmax warp
+    mbar_init(bars.q_full(0), 4);  // one arrival per warp of softmax group 0
     mbar_init(bars.q_full(1), 4);
     mbar_init(bars.mma_done(), 1);
     if (C::FP8) {
@@ -397,10 +432,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         mbar_wait(bars.mma_done(), 0);
       }
       __syncwarp();
-    } else if (warp < 6) {
+    } else if (warp < C::CONV_WARP0) {
       // ------------------------------------------------------------ softmax
       const int sub = warp & 3;       // TMEM lane quarter of this warp
       const int R = 32 * sub + lane;  // TMEM lane: tile position (S^T) / output dim (O^T)
+      const int grp = C::SG == 1 ? 0 : (warp - 2) >> 2;  // softmax group: head columns [hg0, hg0 + HG)
+      const int hg0 = grp * HG;
       const uint32_t trow = tmem + ((uint32_t)(32 * sub) << 16);
       SegmentCursor cur;
       cur.init(sp, range);
@@ -468,7 +505,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.q_full(buf));
       };
-      if (have) {
+      // softmax group 0 alone loads Q
+      if (have && grp == 0) {
         issue_q(seg, 0);
         SegmentCursor la = cur;
         Segment s1;
@@ -478,8 +516,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       }
       // After a wait that timed out the thread is "dead": its later waits
       // return at once, but it keeps the same control flow, so the four
-      // softmax warps still meet at every named barrier and finish (the
-      // error word already holds GQA_DEVERR_TIMEOUT).
+      // warps of its softmax group still meet at every named barrier and
+      // finish (the error word already holds GQA_DEVERR_TIMEOUT).
       bool dead = false;
       auto wait = [&](uint32_t bar, uint32_t parity) {
         if (!dead && !warp_wait(bar, parity)) dead = true;
@@ -496,19 +534,19 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int g_unit = seg.uib / p.head_chunks;
         const float sl2 = C::FP8 ? p.scale_log2 * __ldg(p.k_scale + g_unit) : p.scale_log2;
         const float vscale = C::FP8 ? __ldg(p.v_scale + g_unit) : 1.f;
-        float lp[NR];
+        float lp[HG];
 #pragma unroll
-        for (int h = 0; h < NR; ++h) lp[h] = 0.f;
+        for (int h = 0; h < HG; ++h) lp[h] = 0.f;
         // The running max starts at a finite floor rather than -inf, so that
         // a row that has seen no visible position yet (a query token whose
         // whole view lies in later tiles) gets 2^(-inf - floor) = 0, not NaN.
-        if (R < NQ) m_s[R] = MULTI ? kNoMax : -INFINITY;
-        soft_bar();
+        if (R < HG) m_s[hg0 + R] = MULTI ? kNoMax : -INFINITY;
+        soft_bar(grp);
         // Row h of the unit is query token t(h) = (row0 + h) / rep_kv of its
         // run and sees positions n < L_all + t(h); positions below L_all are
         // visible to every row.
         const int L_all = L - (p.tokens - 1);
-        const int row0 = h_first % p.n_rep;
+        const int row0 = h_first % p.n_rep + hg0;  // the group's first row
         const int t_first = row0 / p.rep_kv, k_first = row0 % p.rep_kv;
         for (int i = 0; i < ntl; ++i) {
           const int tg = t + i, sb = tg & 1, st = tg % ST;
@@ -522,28 +560,26 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           // this position's logits (log2 units); -inf where the row may not
           // see it (past L, or a later token of the row's own run) and for
           // padding rows
-          float x[NR];
+          float x[HG];
           auto load_s = [&]() {
+            // every column chunk is asked for before the one wait
+            uint32_t r[HG];
 #pragma unroll
-            for (int c0 = 0; c0 < NR; c0 += (NR < 32 ? NR : 32)) {
-              uint32_t r[32];
-              if constexpr (NR >= 32) {
-                tc::ld_32x32b_x32(trow + C::TM_S + sb * NR + c0, r);
+            for (int c0 = 0; c0 < HG; c0 += HCH) {
+              if constexpr (HCH == 32) {
+                tc::ld_32x32b_x32(trow + C::TM_S + sb * NR + hg0 + c0, r + c0);
               } else {
-                tc::ld_32x32b_x16(trow + C::TM_S + sb * NR + c0, r);
-              }
-              tc::wait_ld();
-#pragma unroll
-              for (int c = 0; c < (NR < 32 ? NR : 32); ++c) {
-                const int h = c0 + c;
-                x[h] = (valid && h < nh) ? __uint_as_float(r[c]) * sl2 : -INFINITY;
+                tc::ld_32x32b_x16(trow + C::TM_S + sb * NR + hg0 + c0, r + c0);
               }
             }
+            tc::wait_ld();
+#pragma unroll
+            for (int h = 0; h < HG; ++h) x[h] = (valid && hg0 + h < nh) ? __uint_as_float(r[h]) * sl2 : -INFINITY;
             if (MULTI && edge) {
               // row h is token t(h) of its run: it sees positions < L_all + t(h)
               int tk = t_first, kk = k_first;
 #pragma unroll
-              for (int h = 0; h < NR; ++h) {
+              for (int h = 0; h < HG; ++h) {
                 if (pos >= L_all + tk) x[h] = -INFINITY;
                 const bool wrap = ++kk == p.rep_kv;
                 kk = wrap ? 0 : kk;
@@ -554,58 +590,71 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           load_s();
           bool need = false;
 #pragma unroll
-          for (int h = 0; h < NR; ++h) need |= x[h] > m_s[h] + 8.f;
-          if (soft_bar_or(need)) {
+          for (int h = 0; h < HG; ++h) need |= x[h] > m_s[hg0 + h] + 8.f;
+          if (soft_bar_or(grp, need)) {
             // move the running maxima to this tile's maxima where they grew by
             // more than 8 (always on a unit's first tile); x is reduced in
-            // place and read again from TMEM afterwards
-            soft_reduce<C, true>(x, sub, lane, red, fin, R);
+            // place, so a copy is kept where registers allow (bf16, up to 32
+            // heads) or x is read again from TMEM
+            constexpr bool KEEP = !C::FP8 && HG <= 32;
+            float xk[KEEP ? HG : 1];
+            if constexpr (KEEP) {
+#pragma unroll
+              for (int h = 0; h < HG; ++h) xk[h] = x[h];
+            }
+            soft_reduce<C, true>(x, grp, sub, lane, red, fin, R);
             bool moved_mine = false;
-            if (R < NR) {
-              const float tmax = fin[R], mo = m_s[R];
+            if (R < HG) {
+              const float tmax = fin[hg0 + R], mo = m_s[hg0 + R];
               float corr = 1.f;
               if (tmax > mo + 8.f) {
                 corr = merge_weight(mo, tmax);
-                m_s[R] = tmax;
+                m_s[hg0 + R] = tmax;
                 moved_mine = true;
               }
-              corr_s[R] = corr;
+              corr_s[hg0 + R] = corr;
             }
-            const bool moved = soft_bar_or(moved_mine);
+            const bool moved = soft_bar_or(grp, moved_mine);
 #pragma unroll
-            for (int h = 0; h < NR; ++h) lp[h] *= corr_s[h];
+            for (int h = 0; h < HG; ++h) lp[h] *= corr_s[hg0 + h];
             if (i > 0 && moved) {
               // O^T holds P.V of the unit's tiles so far: rescale it once the
               // last of them landed (the same decision in every thread)
               wait(bars.pv_done((tg - 1) % C::PB), ((tg - 1) / C::PB) & 1);
               tc::fence_after();
 #pragma unroll
-              for (int c0 = 0; c0 < NR; c0 += (NR < 32 ? NR : 32)) {
+              for (int c0 = 0; c0 < HG; c0 += HCH) {
+                const uint32_t ta = trow + C::TM_O + ob * NR + hg0 + c0;
                 uint32_t r[32];
-                if constexpr (NR >= 32) {
-                  tc::ld_32x32b_x32(trow + C::TM_O + ob * NR + c0, r);
+                if constexpr (HCH == 32) {
+                  tc::ld_32x32b_x32(ta, r);
                 } else {
-                  tc::ld_32x32b_x16(trow + C::TM_O + ob * NR + c0, r);
+                  tc::ld_32x32b_x16(ta, r);
                 }
                 tc::wait_ld();
 #pragma unroll
-                for (int c = 0; c < (NR < 32 ? NR : 32); ++c)
-                  r[c] = __float_as_uint(__uint_as_float(r[c]) * corr_s[c0 + c]);
-                if constexpr (NR >= 32) {
-                  tc::st_32x32b_x32(trow + C::TM_O + ob * NR + c0, r);
+                for (int c = 0; c < HCH; ++c)
+                  r[c] = __float_as_uint(__uint_as_float(r[c]) * corr_s[hg0 + c0 + c]);
+                if constexpr (HCH == 32) {
+                  tc::st_32x32b_x32(ta, r);
                 } else {
-                  tc::st_32x32b_x16(trow + C::TM_O + ob * NR + c0, r);
+                  tc::st_32x32b_x16(ta, r);
                 }
               }
               tc::wait_st();
             }
-            load_s();
+            if constexpr (KEEP) {
+#pragma unroll
+              for (int h = 0; h < HG; ++h) x[h] = xk[h];
+            } else {
+              load_s();
+            }
           }
           // column R of P^T (position R of every head row): 2^(x - m) as bf16
-          uint16_t pb16[NR];
+          uint16_t pb16[HG];
 #pragma unroll
-          for (int h = 0; h < NR; ++h) {
-            const float pv = h < nh ? tc::ex2(x[h] - m_s[h]) : 0.f;
+          for (int h = 0; h < HG; ++h) {
+            const float pv = hg0 + h < nh ? tc::ex2(x[h] - m_s[hg0 + h]) : 0.f;
             lp[h] += pv;
             pb16[h] = C::FP8 ? f16_bits(pv) : __bfloat16_as_ushort(__float2bfloat16_rn(pv));
           }
@@ -616,11 +665,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const uint32_t col = pbase + pb * C::P_BYTES + (R >> 6) * C::P_BOX + (R & 7) * 2;
             const int chunk = (R & 63) >> 3;
 #pragma unroll
-            for (int h = 0; h < NR; ++h)
-              asm volatile("st.shared.u16 [%0], %1;" ::"r"(col + h * 128 + ((chunk ^ (h & 7)) << 4)), "h"(pb16[h])
+            for (int h = 0; h < HG; ++h) {
+              const int hh = hg0 + h;
+              asm volatile("st.shared.u16 [%0], %1;" ::"r"(col + hh * 128 + ((chunk ^ (hh & 7)) << 4)), "h"(pb16[h])
                            : "memory");
+            }
           }
-          if (!C::FP8 && !valid && !dead && mbar_wait(pipe.full(st), (tg / ST) & 1)) {
+          if (!C::FP8 && grp == 0 && !valid && !dead && mbar_wait(pipe.full(st), (tg / ST) & 1)) {
             // position past L: its V row may hold anything (NaN included) and
             // 0 * NaN = NaN inside the MMA, so clear it (after it landed)
             const uint32_t a = pipe.v_tile(st) + R * 128;
@@ -643,7 +694,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // the S^T of every tile of this unit is done, so Q may take the next unit
         Segment nseg;
         const bool next = cur.next(sp, nseg);
-        if (next) {
+        if (next && grp == 0) {
           if constexpr (C::QB == 2) {
             // unit + 1's Q was issued a unit ago; unit + 2's goes to this
             // unit's buffer, whose S^T MMAs have all completed
@@ -658,56 +709,75 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
         }
         // ---- epilogue: l[h] summed over the 128 positions' partials
-        const float mR = R < NQ ? m_s[R] : 0.f;  // kNoMax when the row saw no position
-        soft_reduce<C, false>(lp, sub, lane, red, fin, R);
+        const float mR = R < HG ? m_s[hg0 + R] : 0.f;  // kNoMax when the row saw no position
+        soft_reduce<C, false>(lp, grp, sub, lane, red, fin, R);
         // O^T of this unit is final once the P.V of its last tile landed
         wait(bars.pv_done((t - 1) % C::PB), ((t - 1) / C::PB) & 1);
         tc::fence_after();
         const bool whole = seg.t0 == 0 && seg.t1 == seg.tiles;
         const int slot = partial_slot(unit);
-        // output row of column h: (b*tokens + t(h))*heads_q + g*rep_kv + k(h),
-        // stepping (t, k) through the unit's rows (query_row without divisions)
-        int tk = t_first, kk = k_first;
+        // Thread R holds output dimension R of every head; a 4x4 transpose
+        // within each quad of lanes gives lane j of a quad four consecutive
+        // dimensions d4..d4+3 of head (block + j), written as one vector.
         const size_t orow_b = MULTI ? (size_t)b * p.tokens * p.heads_q + (size_t)(h_first / p.n_rep) * p.rep_kv
                                     : (size_t)b * p.H + h_first;
+        const int d4 = 32 * sub + (lane & ~3);
+        uint32_t r[HG];
 #pragma unroll
-        for (int c0 = 0; c0 < NR; c0 += (NR < 32 ? NR : 32)) {
-          uint32_t r[32];
-          if constexpr (NR >= 32) {
-            tc::ld_32x32b_x32(trow + C::TM_O + ob * NR + c0, r);
+        for (int c0 = 0; c0 < HG; c0 += HCH) {
+          if constexpr (HCH == 32) {
+            tc::ld_32x32b_x32(trow + C::TM_O + ob * NR + hg0 + c0, r + c0);
           } else {
-            tc::ld_32x32b_x16(trow + C::TM_O + ob * NR + c0, r);
+            tc::ld_32x32b_x16(trow + C::TM_O + ob * NR + hg0 + c0, r + c0);
           }
-          tc::wait_ld();
+        }
+        tc::wait_ld();
 #pragma unroll
-          for (int c = 0; c < (NR < 32 ? NR : 32); ++c) {
-            const int h = c0 + c;
-            size_t orow = orow_b + h;
-            if constexpr (MULTI) {
-              orow = orow_b + (size_t)tk * p.heads_q + kk;
-              const bool wrap = ++kk == p.rep_kv;
-              kk = wrap ? 0 : kk;
-              tk += wrap ? 1 : 0;
-            }
+        for (int c0 = 0; c0 < HG; c0 += HCH) {
+#pragma unroll
+          for (int q = 0; q < HCH; q += 4) {
+            float v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[c0 + q + i]) * vscale;
+            quad_transpose(v, lane);
+            const int h = hg0 + c0 + q + (lane & 3);
             if (h < nh) {
-              const float o = __uint_as_float(r[c]) * vscale;
-              if (whole)
-                reinterpret_cast<__nv_bfloat16 *>(p.out)[orow * D + R] =
-                    __float2bfloat16_rn((!MULTI || fin[h] > 0.f) ? o / fin[h] : 0.f);
-              else
-                p.o_part[((size_t)slot * p.heads_per_cta + h) * D + R] = o;
+              if (whole) {
+                // output row of head h: (b*tokens + t)*heads_q + g*rep_kv + k
+                // for row h_first % n_rep + h = t*rep_kv + k of the group
+                size_t orow = orow_b + h;
+                if constexpr (MULTI) {
+                  const int row = h_first % p.n_rep + h;
+                  orow = orow_b + (size_t)(row / p.rep_kv) * p.heads_q + row % p.rep_kv;
+                }
+                const float f = fin[h];
+                const bool seen = !MULTI || f > 0.f;  // a row that saw no position is 0
+                uint2 pk;
+                pk.x = pack_bf16x2(seen ? v[0] / f : 0.f, seen ? v[1] / f : 0.f);
+                pk.y = pack_bf16x2(seen ? v[2] / f : 0.f, seen ? v[3] / f : 0.f);
+                *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * D + d4) = pk;
+              } else {
+                *reinterpret_cast<float4 *>(p.o_part + ((size_t)slot * p.heads_per_cta + h) * D + d4) =
+                    make_float4(v[0], v[1], v[2], v[3]);
+              }
             }
           }
         }
-        if (!whole && R < nh)
-          reinterpret_cast<float2 *>(p.ml_part)[(size_t)slot * p.heads_per_cta + R] = make_float2(mR, fin[R]);
-        if (R == 0) record_unit(p, seg, whole, slot, range, b);
-        if (!whole && p.unit_cnt)
-          finish_split_unit<__nv_bfloat16, D, MULTI>(p, seg, range, b, h_first, nh, R, C::SOFT, um, [] { soft_bar(); });
+        if (!whole && R < HG && hg0 + R < nh)
+          reinterpret_cast<float2 *>(p.ml_part)[(size_t)slot * p.heads_per_cta + hg0 + R] =
+              make_float2(mR, fin[hg0 + R]);
+        if (R == 0 && grp == 0) record_unit(p, seg, whole, slot, range, b);
+        // (the host gives units of this kernel to the merge kernel; the
+        // in-kernel merge needs all of the unit's heads in one group)
+        if constexpr (C::SG == 1) {
+          if (!whole && p.unit_cnt)
+            finish_split_unit<__nv_bfloat16, D, MULTI>(p, seg, range, b, h_first, nh, R, C::SOFT, um,
+                                                       [] { soft_bar(0); });
+        }
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.o_free(ob));
-        soft_bar();  // fin[] is reused by the next unit's reductions
+        soft_bar(grp);  // fin[] is reused by the next unit's reductions
         seg = nseg;
         have = next;
       }
@@ -718,7 +788,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       // 128-byte swizzled rows of f16 in the tile's staging buffer; rows at
       // or past L become zeros (their codes may be NaN, and 0 * NaN = NaN in
       // the P.V MMA).
-      const int R = 32 * (warp - 6) + lane;
+      const int R = 32 * (warp - C::CONV_WARP0) + lane;
       SegmentCursor cur;
       cur.init(sp, range);
       Segment seg;

@@ -95,9 +95,10 @@ __device__ __forceinline__ void commit(uint32_t mbar) {
 }
 
 // ---------------------------------------------------------------- TMEM <-> registers
-// 32 consecutive 32-bit columns of this thread's lane (shape 32x32b: the
-// warp reads its 32-lane quarter of TMEM).  Whole warp; wait before use.
-__device__ __forceinline__ void ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+// 32 consecutive 32-bit columns of this thread's lane into r[0..31] (shape
+// 32x32b: the warp reads its 32-lane quarter of TMEM).  Whole warp; wait
+// (wait_ld) before using r; several loads may share one wait.
+__device__ __forceinline__ void ld_32x32b_x32(uint32_t taddr, uint32_t *r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -109,7 +110,7 @@ __device__ __forceinline__ void ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])
       : "r"(taddr));
 }
 
-__device__ __forceinline__ void st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+__device__ __forceinline__ void st_32x32b_x32(uint32_t taddr, const uint32_t *r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
       "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
@@ -121,8 +122,8 @@ __device__ __forceinline__ void st_32x32b_x32(uint32_t taddr, const uint32_t (&r
       : "memory");
 }
 
-// The first 16 of r: 16 consecutive columns of this thread's lane.
-__device__ __forceinline__ void ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[32]) {
+// 16 consecutive columns of this thread's lane into r[0..15].
+__device__ __forceinline__ void ld_32x32b_x16(uint32_t taddr, uint32_t *r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -131,7 +132,7 @@ __device__ __forceinline__ void ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[32])
       : "r"(taddr));
 }
 
-__device__ __forceinline__ void st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[32]) {
+__device__ __forceinline__ void st_32x32b_x16(uint32_t taddr, const uint32_t *r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
       "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
