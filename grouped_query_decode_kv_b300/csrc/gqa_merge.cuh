@@ -146,50 +146,81 @@ __device__ __forceinline__ void record_unit(const SplitParams &p, const Segment 
 // One warp per (b, h): the merge of the unit that holds head h when the
 // split cut it (info.y >= 0).  Whole units and empty sequences were written
 // by the split kernel.  It waits for the split grid to finish before it
-// reads the workspace.
+// reads the workspace.  The loads are batched so that a merge costs a few
+// L2 round trips whatever the number of partials: the length and the unit's
+// record together, then the (m, l) of up to 32 partials (one per lane), then
+// the partial rows four at a time; the sums still run over k = 0, 1, ... in
+// order.
 template <typename T, int D>
 __global__ void __launch_bounds__(128) gqa_combine_kernel(const SplitParams p) {
   constexpr int PER_LANE = D / 32;
+  constexpr unsigned FULL = 0xffffffffu;
   griddep_wait();
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long bh = (long long)blockIdx.x * 4 + warp;
   if (bh >= (long long)p.B * p.H) return;
   const int b = (int)(bh / p.H), h = (int)(bh % p.H);
-  const int L = max(0, min(p.seq_lens[b], p.Nmax));
-  if (L == 0) return;
   const int g = h / p.n_rep, rr = h % p.n_rep;
   const int hc = rr / p.heads_per_cta, hl = rr % p.heads_per_cta;
+  // (an empty sequence has no record: it is read, not used)
+  const int Lraw = p.seq_lens[b];
   const int2 info = p.unit_info[((size_t)b * p.G + g) * p.head_chunks + hc];
-  if (info.y < 0) return;
+  if (max(0, min(Lraw, p.Nmax)) == 0 || info.y < 0) return;
   const int c_lo = info.x >> 1;
   const int n = info.y - c_lo + 1;  // number of partials
   const float2 *ml = reinterpret_cast<const float2 *>(p.ml_part);
   auto slot_of = [&](int k) { return k == 0 ? info.x : 2 * (c_lo + k); };
+  float2 mine = make_float2(-INFINITY, 0.f);  // (m, l) of partial `lane`
   float M = -INFINITY;
-  for (int k = lane; k < n; k += 32) M = fmaxf(M, ml[(size_t)slot_of(k) * p.heads_per_cta + hl].x);
+  for (int k = lane; k < n; k += 32) {
+    const float2 v = ml[(size_t)slot_of(k) * p.heads_per_cta + hl];
+    if (k == lane) mine = v;
+    M = fmaxf(M, v.x);
+  }
 #pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, off));
   float acc[PER_LANE];
 #pragma unroll
   for (int e = 0; e < PER_LANE; ++e) acc[e] = 0.f;
   float l = 0.f;
-  for (int k = 0; k < n; ++k) {
-    const size_t ps = (size_t)slot_of(k) * p.heads_per_cta + hl;
-    const float2 mls = ml[ps];
-    const float w = merge_weight(mls.x, M);
-    l += w * mls.y;
-    const float *op = p.o_part + ps * D + lane * PER_LANE;
-    if constexpr (PER_LANE == 4) {
-      const float4 v = *reinterpret_cast<const float4 *>(op);
-      acc[0] += w * v.x;
-      acc[1] += w * v.y;
-      acc[2] += w * v.z;
-      acc[3] += w * v.w;
-    } else {
-      const float2 v = *reinterpret_cast<const float2 *>(op);
-      acc[0] += w * v.x;
-      acc[1] += w * v.y;
+  for (int k0 = 0; k0 < n; k0 += 32) {
+    // weight and weighted sum of partial k0 + lane
+    const int kl = k0 + lane;
+    float2 v = mine;
+    if (k0 > 0) v = kl < n ? ml[(size_t)slot_of(kl) * p.heads_per_cta + hl] : make_float2(-INFINITY, 0.f);
+    const float w = kl < n ? merge_weight(v.x, M) : 0.f;
+    const float wl = w * v.y;
+    const int cnt = min(32, n - k0);
+    for (int j = 0; j < cnt; j += 4) {
+      float o[4][PER_LANE];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (j + u < cnt) {
+          const float *op = p.o_part + ((size_t)slot_of(k0 + j + u) * p.heads_per_cta + hl) * D + lane * PER_LANE;
+          if constexpr (PER_LANE == 4) {
+            const float4 t = *reinterpret_cast<const float4 *>(op);
+            o[u][0] = t.x;
+            o[u][1] = t.y;
+            o[u][2] = t.z;
+            o[u][3] = t.w;
+          } else {
+            const float2 t = *reinterpret_cast<const float2 *>(op);
+            o[u][0] = t.x;
+            o[u][1] = t.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float wu = __shfl_sync(FULL, w, (j + u) & 31);
+        const float lu = __shfl_sync(FULL, wl, (j + u) & 31);
+        if (j + u < cnt) {
+          l += lu;
+#pragma unroll
+          for (int e = 0; e < PER_LANE; ++e) acc[e] += wu * o[u][e];
+        }
+      }
     }
   }
   const float inv = l > 0.f ? 1.f / l : 0.f;
