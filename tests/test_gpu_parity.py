@@ -250,6 +250,18 @@ def test_forced_splits_on_the_tensor_core_kernel(H, G, split_tokens):
     check_case(w, lens, split_tokens)
 
 
+@pytest.mark.parametrize("H,G", [(8, 1), (64, 2), (4, 1), (8, 8), (2, 1)])
+def test_one_long_sequence_cut_over_the_whole_grid(H, G):
+    """One sequence of 25600 positions: with one or two (batch, KV head)
+    units the persistent grid cuts each unit into dozens to ~150 pieces, so
+    a merge joins more than 32 partials (the merge kernel's second pass over
+    them; tcgen05 for n_rep 8 and 32, warp MMA for 4, and the in-kernel
+    merge of the CUDA-core kernel for 1 and 2)."""
+    N = 25600
+    w = _small(H, G, 128, N, "bf16", [N], 7600 + H + G)
+    check_case(w, torch.tensor([N], dtype=torch.int32))
+
+
 @pytest.mark.parametrize("H,G", [(8, 8), (16, 4), (16, 2), (64, 1)])
 def test_more_than_64_sequences(H, G):
     """B > 64 takes the second pass of the schedule's length scan."""
