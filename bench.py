@@ -753,8 +753,9 @@ def run_ours(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu:
         gbs, units, spent, threads = oracle_sample(w, args.cpu_seconds)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"{units} of {w.B * w.G} (batch, KV-group) units of the {w.name} workload "
-                         f"({spent:.1f} s of fp64 CPU work)"}
+               "sample": f"{units} (batch, KV-group) units of the {w.name} workload, taken in batch-row order "
+                         f"over its {w.B * w.G} units ({units / (w.B * w.G):.1f} passes; {spent:.1f} s of fp64 "
+                         f"CPU work)"}
 
     if world > 1:
         import torch.distributed as dist
