@@ -622,8 +622,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               // last of them landed (the same decision in every thread)
               wait(bars.pv_done((tg - 1) % C::PB), ((tg - 1) / C::PB) & 1);
               tc::fence_after();
-#pragma unroll
-              for (int c0 = 0; c0 < HG; c0 += HCH) {
+#pragma unroll 1
+              for (int c0 = 0; c0 < HG; c0 += HCH) {  // rare: kept small
                 const uint32_t ta = trow + C::TM_O + ob * NR + hg0 + c0;
                 uint32_t r[32];
                 if constexpr (HCH == 32) {
@@ -722,23 +722,23 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const size_t orow_b = MULTI ? (size_t)b * p.tokens * p.heads_q + (size_t)(h_first / p.n_rep) * p.rep_kv
                                     : (size_t)b * p.H + h_first;
         const int d4 = 32 * sub + (lane & ~3);
-        uint32_t r[HG];
-#pragma unroll
+        // one column chunk at a time, the chunk loop not unrolled: this code
+        // runs once per unit, and with 64 columns its size (instruction
+        // fetch), not its loads, is what it costs
+#pragma unroll 1
         for (int c0 = 0; c0 < HG; c0 += HCH) {
+          uint32_t r[32];
           if constexpr (HCH == 32) {
-            tc::ld_32x32b_x32(trow + C::TM_O + ob * NR + hg0 + c0, r + c0);
+            tc::ld_32x32b_x32(trow + C::TM_O + ob * NR + hg0 + c0, r);
           } else {
-            tc::ld_32x32b_x16(trow + C::TM_O + ob * NR + hg0 + c0, r + c0);
+            tc::ld_32x32b_x16(trow + C::TM_O + ob * NR + hg0 + c0, r);
           }
-        }
-        tc::wait_ld();
-#pragma unroll
-        for (int c0 = 0; c0 < HG; c0 += HCH) {
+          tc::wait_ld();
 #pragma unroll
           for (int q = 0; q < HCH; q += 4) {
             float v[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[c0 + q + i]) * vscale;
+            for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[q + i]) * vscale;
             quad_transpose(v, lane);
             const int h = hg0 + c0 + q + (lane & 3);
             if (h < nh) {
