@@ -32,6 +32,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -80,12 +81,22 @@ STEP_KERNEL_SOURCES = ("gqa_device.cuh", "gqa_params.cuh", "gqa_schedule.cuh", "
                        "gqa_small_kernels.cuh")
 
 
+def code_of(text: str) -> str:
+    """A C++ source without its comments, trailing blanks and empty lines:
+    what the compiler sees (the sources hold no string that contains a
+    comment marker)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash() -> str:
-    """Hash of the decode-attention kernels' device sources."""
+    """Hash of the decode-attention kernels' device code (comments left out,
+    so that editing a comment does not part a profile from its kernel)."""
     h = hashlib.sha256()
     for fn in STEP_KERNEL_SOURCES:
-        with open(os.path.join(CSRC, fn), "rb") as f:
-            h.update(fn.encode() + f.read())
+        with open(os.path.join(CSRC, fn)) as f:
+            h.update(fn.encode() + code_of(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -18,16 +18,17 @@
 //
 // Softmax: thread R of a group of four softmax warps owns TMEM lane R, which
 // is cached position R of the tile in S^T and output dimension R in O^T.
-// With 32 or 64 heads two such groups share the head columns (half each),
-// so that two warps per sub-partition hide each other's latencies.  For
-// each of its heads h a thread keeps its own partial sum l_R[h]; the running
-// max m[h] (base-2 units) is shared by the group through shared memory.  A
-// tile first votes whether any logit exceeds m[h] + 8; only then (always on
-// a unit's first tile) the tile's per-head maxima are reduced across the
-// group's 128 threads and m moves, with O^T rescaled in TMEM.  P = 2^(S - m) is written to shared memory as
-// bf16 (double-buffered where shared memory allows, so that the softmax of
-// tile t+1 need not wait for the P.V of tile t); the l_R[h] are summed
-// across threads once per unit.
+// A configuration may give the head columns to two such groups (half each;
+// the host does so for the several-token kernel with 32 rows per unit), so
+// that two warps per sub-partition share the softmax.  For each of its heads
+// h a thread keeps its own partial sum l_R[h]; the running max m[h] (base-2
+// units) is shared by the group through shared memory.  A tile first votes
+// whether any logit exceeds m[h] + 8; only then (always on a unit's first
+// tile) the tile's per-head maxima are reduced across the group's 128
+// threads and m moves, with O^T rescaled in TMEM.  P = 2^(S - m) is written
+// to shared memory as bf16 (double-buffered where shared memory allows, so
+// that the softmax of tile t+1 need not wait for the P.V of tile t); the
+// l_R[h] are summed across threads once per unit.
 //
 // Warp roles (one CTA per SM):
 //   warp 0     TMA producer of the CTA's stream-K range (gqa_pipeline.cuh)

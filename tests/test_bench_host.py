@@ -86,3 +86,10 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_kernel_hash_ignores_comments_but_not_code():
+    src = "int a = 1;  // one\n/* block\n comment */\n\nint b = 2;\n"
+    assert bench.code_of(src) == "int a = 1;\nint b = 2;"
+    assert bench.code_of(src.replace("// one", "// changed")) == bench.code_of(src)
+    assert bench.code_of(src.replace("= 2", "= 3")) != bench.code_of(src)
