@@ -270,8 +270,12 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 bool plan_fits(const Plan &pl, int B, int G) { return B <= 65535 && pl.units < (1LL << 31); }
 
-// Workspace: partial outputs and (m, l) of two slots per CTA, and 8 bytes
-// of merge bookkeeping per unit.  A single CTA never splits a unit.
+// Workspace: a fixed 256-byte head that holds the fused step's arrival
+// word, then partial outputs and (m, l) of two slots per CTA, and 8 bytes of
+// merge bookkeeping per unit.  The head sits at the same offset for every
+// shape, so calls of other shapes (or attention-only calls) that share the
+// workspace never write over it.  A single CTA never splits a unit.
+constexpr size_t kWsHead = 256;
 size_t ws_opart_bytes(const Plan &pl, int d) { return align256((size_t)2 * pl.P * pl.heads * d * sizeof(float)); }
 size_t ws_ml_bytes(const Plan &pl) { return align256((size_t)2 * pl.P * pl.heads * 2 * sizeof(float)); }
 
@@ -285,16 +289,14 @@ unsigned next_epoch() {
 }
 
 size_t ws_book_bytes(const Plan &pl) { return align256((size_t)pl.units * sizeof(unsigned long long)); }
-size_t step_counter_offset(const Plan &pl, int d) { return ws_opart_bytes(pl, d) + ws_ml_bytes(pl) + ws_book_bytes(pl); }
 
-// ... plus one 32-bit counter of finished CTAs for a fused decode step, which
-// must be zero before the workspace's first gqa_decode_step_ws call (each
-// call leaves it at zero).
+// Every word in it is tagged with the epoch of the call that wrote it, so
+// the workspace needs no clearing, ever.
 size_t workspace_for(const Plan &pl, int B, int H, int d) {
   (void)B;
   (void)H;
   if (pl.P <= 1) return 0;
-  return ws_opart_bytes(pl, d) + ws_ml_bytes(pl) + ws_book_bytes(pl) + 256;
+  return kWsHead + ws_opart_bytes(pl, d) + ws_ml_bytes(pl) + ws_book_bytes(pl);
 }
 
 // ----------------------------------------------------------- TMA descriptors
@@ -395,11 +397,11 @@ int run_attention(const void *q, const void *k, const void *v, const int32_t *sl
   p.out = out;
   const bool split = pl.P > 1;
   char *w = reinterpret_cast<char *>(ws);
-  p.o_part = split ? reinterpret_cast<float *>(w) : nullptr;
-  p.ml_part = split ? reinterpret_cast<float *>(w + ws_opart_bytes(pl, d)) : nullptr;
+  p.o_part = split ? reinterpret_cast<float *>(w + kWsHead) : nullptr;
+  p.ml_part = split ? reinterpret_cast<float *>(w + kWsHead + ws_opart_bytes(pl, d)) : nullptr;
   // units of one or two heads merge inside the split kernel; larger ones in
   // the merge kernel, which spreads the (bigger) partials over every SM
-  void *book = split ? w + ws_opart_bytes(pl, d) + ws_ml_bytes(pl) : nullptr;
+  void *book = split ? w + kWsHead + ws_opart_bytes(pl, d) + ws_ml_bytes(pl) : nullptr;
   const bool merge_in_kernel = pl.k.family == kSimt;
   p.unit_cnt = merge_in_kernel ? reinterpret_cast<unsigned long long *>(book) : nullptr;
   p.unit_info = merge_in_kernel ? nullptr : reinterpret_cast<int2 *>(book);
@@ -411,7 +413,7 @@ int run_attention(const void *q, const void *k, const void *v, const int32_t *sl
   p.v_cache = app.v_cache;
   p.seq_lens_w = app.seq_lens;
   p.row_chunks = d * (dt == GQA_FP8_E4M3 ? 1 : (dt == GQA_BF16 ? 2 : 4)) / 16;
-  p.done_cnt = split ? reinterpret_cast<unsigned *>(w + step_counter_offset(pl, d)) : nullptr;
+  p.done_cnt = split ? reinterpret_cast<unsigned long long *>(w) : nullptr;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.B = B;
   p.H = tokens * H;
@@ -699,13 +701,6 @@ int decode_step(const void *q, const void *k_new, const void *v_new, void *k_cac
     if (need > 0 && cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
       cudaGetLastError();
       return GQA_ERR_NO_MEMORY;
-    }
-    if (need > 0 &&
-        cudaMemsetAsync(reinterpret_cast<char *>(ws) + step_counter_offset(pl, d), 0, sizeof(unsigned), stream) !=
-            cudaSuccess) {
-      cudaGetLastError();
-      cudaFreeAsync(ws, stream);
-      return GQA_ERR_CUDA;
     }
   } else if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))) {
     return GQA_ERR_INVALID_ARG;

@@ -104,23 +104,47 @@ __device__ __forceinline__ void finish_split_unit(const SplitParams &p, const Se
   }
 }
 
+// Counts one more finished CTA of a fused decode step on the 64-bit word
+// (call epoch << 32) | count and returns the new count.  A word that carries
+// another tag (left by another call, or memory never cleared) is first
+// replaced by (epoch << 32) | 0 with one compare-and-swap; that swap can only
+// succeed before any CTA of this call has counted, because every count is
+// added to a word that already holds this call's tag.  So a stale word never
+// takes part in the count.  The counts themselves are plain atomic adds: a
+// compare-and-swap loop per arrival retries O(P) times under the grid's
+// contention.  Returns 0 (never a valid count) when the tag could not be
+// installed within a bounded number of tries.
+__device__ __forceinline__ unsigned arrive_step(unsigned long long *cnt, unsigned epoch) {
+  const unsigned long long tagged = (unsigned long long)epoch << 32;
+  unsigned long long cur = __ldcg(cnt);
+  for (int tries = 0; (unsigned)(cur >> 32) != epoch; ++tries) {
+    if (tries == 64) {
+      flag_error(GQA_DEVERR_TIMEOUT);
+      return 0u;
+    }
+    const unsigned long long seen = atomicCAS(cnt, cur, tagged);
+    cur = seen == cur ? tagged : seen;
+  }
+  return (unsigned)(atomicAdd(cnt, 1ull) + 1ull);
+}
+
 // End of a fused decode step, called by all `nthr` threads of a CTA after all
-// of the CTA's work (every CTA comes, busy or idle).  The last CTA of the
-// grid to get here advances seq_lens[b] to L_b + 1 for every row that took
-// the append, and puts the counter back to zero for the next call.  No CTA
-// reads the lengths after its own arrival, so the update cannot be seen half
-// way through the call.  A plain atomic add (no retry loop): all CTAs of the
-// grid arrive within a few microseconds of each other.  `flag` is a shared
-// word that broadcasts thread 0's finding.
+// of the CTA's work (every CTA comes, busy or idle, also after a timed-out
+// wait).  The last CTA of the grid to get here advances seq_lens[b] to
+// L_b + 1 for every row that took the append, and puts the count back to
+// zero under the same tag (so that a graph replay of the call, which keeps
+// its epoch, starts from zero too).  No CTA reads the lengths after its own
+// arrival, so the update cannot be seen half way through the call.  `flag`
+// is a shared word that broadcasts thread 0's finding.
 __device__ __forceinline__ void finish_step(const SplitParams &p, int tid, int nthr, volatile int *flag) {
   if (tid == 0) {
     bool last = true;
     if (p.done_cnt) {
       __threadfence();
-      last = atomicAdd(p.done_cnt, 1u) == gridDim.x - 1;
+      last = arrive_step(p.done_cnt, p.epoch) == gridDim.x;
       if (last) {
         __threadfence();
-        atomicExch(p.done_cnt, 0u);
+        atomicExch(p.done_cnt, (unsigned long long)p.epoch << 32);
       }
     }
     *flag = last;

@@ -27,7 +27,7 @@ struct SplitParams {
   void *k_cache, *v_cache;  // [B*G, Nmax, D]
   int32_t *seq_lens_w;      // the same array as seq_lens
   int row_chunks;           // 16-byte chunks per cache row (D * element size / 16)
-  unsigned *done_cnt;       // CTAs finished, zero between calls; null with one CTA
+  unsigned long long *done_cnt;  // (call epoch << 32) | CTAs finished; null with one CTA
   float scale_log2;         // scale * log2(e): softmax is evaluated with exp2
   int B, H, G, Nmax;
   int n_rep;                // H / G

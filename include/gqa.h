@@ -150,11 +150,13 @@ int gqa_decode_attention_ex(const void *q, const void *k_cache, const void *v_ca
  * that is <= 0 or > Nmax), exactly as the two separate calls would do.
  * gqa_decode_step takes its workspace from the stream-ordered allocator;
  * gqa_decode_step_ws from the caller: gqa_decode_workspace_bytes bytes,
- * 256-byte aligned, ZERO-FILLED once before its first gqa_decode_step_ws
- * call (the blocks count their arrivals in it; every call leaves the count
- * at zero, so later calls need no clearing unless a call failed with a
- * device error).  The same workspace also serves gqa_decode_attention_ws.
- * Calls sharing one workspace must not overlap on the device.
+ * 256-byte aligned, with any contents (it is never cleared).  The blocks
+ * count their arrivals on a word at the start of the workspace that carries
+ * the call's own tag; a word left by another call, of any shape or kind, or
+ * never written, is re-tagged before the first count, so it cannot make a
+ * block believe it is the last.  The same workspace also serves
+ * gqa_decode_attention_ws and calls of other shapes (each needing at most
+ * its size).  Calls sharing one workspace must not overlap on the device.
  */
 int gqa_decode_step(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                     int32_t *seq_lens, float scale, void *out, int B, int H, int G, int d, int Nmax,

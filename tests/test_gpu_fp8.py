@@ -76,8 +76,12 @@ def test_fp8_attention_more_than_64_sequences(H, G):
     check_fp8(_w("fp8_many", B, H, G, N, 10200 + H), lens)
 
 
-@pytest.mark.parametrize("name", ["mha", "gqa8"])
+@pytest.mark.parametrize("name", ["mha", "gqa8", "mqa", "sweep_g8", "sweep_g1"])
 def test_fp8_attention_full_size(name):
+    """The FP8 workloads the benchmark times, at full size, and the G=1 sweep
+    point: the CUDA-core FP8 kernel on MHA, the tcgen05 FP8 kernel with 16
+    head columns on GQA-8 and the G=8 sweep point (8 heads per group), 32 on
+    MQA and 64 on the G=1 sweep point."""
     w = workloads.workload(name)
     check_fp8(_w(f"fp8_{name}", w.B, w.H, w.G, w.Nmax, 10300 + w.index, w.lens))
 

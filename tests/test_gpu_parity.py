@@ -403,3 +403,39 @@ def test_decode_step_matches_oracle(name):
         assert torch.equal(sl.cpu(), slc)
         assert_parity(out.double().cpu().numpy(), ref, f"{name} step {step}")
     assert gqa.gqa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("H,G", [(32, 32), (64, 8), (32, 4)])
+def test_step_workspace_shared_across_shapes_and_never_cleared(H, G):
+    """One workspace, filled with 0xFF bytes (never zeroed), serves fused
+    steps of two batch sizes with attention-only calls of another shape in
+    between: every step must equal kv_append + gqa_decode_attention on
+    copies, lengths included (a stale arrival count would advance seq_lens
+    early or never)."""
+    dev = torch.device("cuda")
+    d, N = 128, 900
+    need = max(gqa.gqa_decode_workspace_bytes(B, H, G, d, N, torch.bfloat16) for B in (3, 9, 16))
+    ws = torch.full((max(need, 1),), 0xFF, dtype=torch.uint8, device=dev)
+    gqa.gqa_get_device_error()
+    for i, B in enumerate([9, 3, 9, 16, 3]):
+        w = workloads.Workload("ws", B, H, G, d, N, "bf16", ("uniform", 1, N - 2), 7700 + 10 * i + H + G)
+        x = workloads.make_inputs(w)
+        q, kn, vn = x["q"].to(dev), x["k_new"].to(dev), x["v_new"].to(dev)
+        k1, v1, sl1 = x["k_cache"].to(dev), x["v_cache"].to(dev), x["seq_lens"].to(dev)
+        k2, v2, sl2 = k1.clone(), v1.clone(), sl1.clone()
+        out1, out2 = torch.full_like(q, float("nan")), torch.full_like(q, float("nan"))
+        gqa.kv_append(kn, vn, k1, v1, sl1)
+        gqa.gqa_decode_attention(q, k1, v1, sl1, w.scale, out1)
+        gqa.gqa_decode_step_ws(q, kn, vn, k2, v2, sl2, w.scale, out2, ws)
+        # an attention-only call of another shape writes its partials all
+        # over the shared workspace before the next step
+        wo = workloads.Workload("ws2", 16, H, G, d, N, "bf16", ("fixed", N), 7790 + i)
+        xo = workloads.make_inputs(wo, poison=False)
+        oo = torch.empty(16, H, d, dtype=torch.bfloat16, device=dev)
+        gqa.gqa_decode_attention_ws(xo["q"].to(dev), xo["k_cache"].to(dev), xo["v_cache"].to(dev),
+                                    xo["seq_lens"].to(dev), wo.scale, oo, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(sl1, sl2), f"call {i}: lengths differ"
+        assert torch.equal(k1.view(torch.uint8), k2.view(torch.uint8))
+        np.testing.assert_array_equal(out1.double().cpu().numpy(), out2.double().cpu().numpy())
+    assert gqa.gqa_get_device_error() == 0

@@ -118,3 +118,89 @@ def test_charge_moves_real_tiles_away_from_ranges_with_many_units():
     many = [t for t, n in per_cta if n >= 4]
     one = [t for t, n in per_cta if n == 1]
     assert many and one and max(many) < min(one)
+
+
+# ---------------------------------------------------------------- step counter
+MASK64 = (1 << 64) - 1
+
+
+def _arrive_step(word, epoch):
+    """One CTA's arrival on the fused step's counter word (gqa_merge.cuh,
+    arrive_step), as a generator that yields before every access to the
+    shared word so that a scheduler can interleave the CTAs at will.
+    `word` is a one-element list (the word in L2); returns the count."""
+    tagged = epoch << 32
+    yield
+    cur = word[0]                      # __ldcg
+    tries = 0
+    while (cur >> 32) != epoch:
+        assert tries < 64
+        tries += 1
+        yield
+        seen = word[0]                 # atomicCAS(cnt, cur, tagged)
+        if seen == cur:
+            word[0] = tagged
+        cur = tagged if seen == cur else seen
+    yield
+    old = word[0]                      # atomicAdd(cnt, 1)
+    word[0] = (old + 1) & MASK64
+    return (old + 1) & 0xFFFFFFFF
+
+
+def _run_step_arrivals(word, epoch, P, rng):
+    """All P CTAs of one call arrive in a random interleaving; the one that
+    counts P resets the word to (epoch << 32) | 0 (finish_step).  Returns
+    the order of arrival (by the atomic add) and the CTAs elected last."""
+    gens = {c: _arrive_step(word, epoch) for c in range(P)}
+    for g in gens.values():
+        next(g)
+    order, elected = [], []
+    while gens:
+        c = rng.choice(list(gens))
+        try:
+            next(gens[c])
+        except StopIteration as stop:
+            del gens[c]
+            order.append(c)
+            if stop.value == P:
+                elected.append(c)
+                word[0] = epoch << 32
+    return order, elected
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_step_counter_stale_words_never_elect_a_wrong_last_cta(seed):
+    """Whatever the counter word holds before a call (uncleared memory, a
+    count left by a call of another shape or by a call that stopped half way,
+    another call's tag), exactly one CTA is elected, and it is the last of
+    the grid to count; the word is then ready for the next call (or a graph
+    replay of this one, with the same tag)."""
+    rng = random.Random(seed)
+    for _ in range(400):
+        P = rng.choice([1, 2, 3, 7, 148, 296])
+        epoch = rng.randint(1, 2 ** 32 - 1)
+        stale_tag = rng.choice([0, rng.randint(1, 2 ** 32 - 1), 0xFFFFFFFF])
+        if stale_tag == epoch:
+            stale_tag ^= 1
+        leftover = rng.choice([0, 1, P - 1, P, P + 5, rng.randint(0, 2 ** 32 - 1)])
+        word = [rng.choice([(stale_tag << 32) | leftover, rng.getrandbits(64)])]
+        if (word[0] >> 32) == epoch:
+            word[0] ^= 1 << 32
+        for replay in range(2):  # the call, then a replay with the same tag
+            order, elected = _run_step_arrivals(word, epoch, P, rng)
+            assert sorted(order) == list(range(P))
+            assert elected == [order[-1]], (P, hex(word[0]), elected, order[-1])
+            assert word[0] == epoch << 32
+
+
+def test_step_counter_fixed_offset_is_the_plain_count_without_a_tag():
+    """The mistake the tag guards against, on the model: a plain 32-bit count
+    that a call of another shape left at k > 0 elects a CTA that is not the
+    last (the count reaches P after P - k arrivals)."""
+    P, k = 8, 3
+    word = k
+    counts = []
+    for _ in range(P):
+        word += 1
+        counts.append(word)
+    assert counts.index(P) == P - k - 1 != P - 1
