@@ -90,10 +90,13 @@ struct TcCfg {
   static constexpr int Q_OFF = STG_OFF + STG_BYTES;
   static constexpr int Q_BOX = NR * 128;
   static constexpr int Q_BYTES = 2 * Q_BOX;
-  // P^T buffers, K-major like Q: one row of 128 positions per head, as two
-  // 128-byte-wide boxes (positions 0-63, 64-127), 128-byte swizzled
-  static constexpr int P_BOX = NR * 128;
-  static constexpr int P_BYTES = 2 * P_BOX;
+  // P^T buffers, MN-major: one row of NR heads (2*NR bytes) per position,
+  // stored with the swizzle of the row's width, so that the thread that owns
+  // a position writes its heads with 16-byte stores
+  static constexpr int P_ROW = 2 * NR;
+  static constexpr int P_BYTES = BLOCK_N * P_ROW;
+  static constexpr int P_SWZ_SHIFT = NR == 64 ? 0 : (NR == 32 ? 1 : 2);
+  static constexpr int P_SWZ_MASK = NR == 64 ? 7 : (NR == 32 ? 3 : 1);
   // pipe full[STAGES], empty[STAGES]; then s_full[2], s_free[2], p_full[2],
   // pv_done[2], o_free[2], q_full[2], mma_done; FP8: conv_full[2], stg_free[2]
   static constexpr int NBAR = 2 * STAGES + 13 + (FP8 ? 4 : 0);
@@ -327,7 +330,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         constexpr uint32_t IDESC_S =
             C::FP8 ? tc::idesc_f16_f32(BN, NR, false, false) : tc::idesc_bf16_f32(BN, NR, false, false);
         constexpr uint32_t IDESC_PV =
-            C::FP8 ? tc::idesc_f16_f32(D, NR, true, false) : tc::idesc_bf16_f32(D, NR, true, false);
+            C::FP8 ? tc::idesc_f16_f32(D, NR, true, true) : tc::idesc_bf16_f32(D, NR, true, true);
         // Two walks over the CTA's tiles: S^T of tile ts may start once its K
         // tile landed, its S buffer is free and (first tile of a unit) the
         // unit's Q is in place; P.V of tile tp once its P is written and
@@ -393,8 +396,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
               for (int ks = 0; ks < BN / 16; ++ks) {
                 const uint64_t a = tc::smem_desc_sw128(vt + ks * 2048, C::KV_BOX, 1024);
-                const uint64_t b =
-                    tc::smem_desc_sw128(pbase + pb * C::P_BYTES + (ks >> 2) * C::P_BOX + (ks & 3) * 32, 16, 1024);
+                const uint64_t b = tc::smem_desc_mn_rows(pbase + pb * C::P_BYTES + ks * 16 * C::P_ROW, C::P_ROW);
                 tc::mma_ss(tmem + C::TM_O + ob * NR, a, b, IDESC_PV, wp.i > 0 || ks > 0);
               }
               // the tile's K and V are no longer read: free its ring stage
@@ -541,7 +543,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // The running max starts at a finite floor rather than -inf, so that
         // a row that has seen no visible position yet (a query token whose
         // whole view lies in later tiles) gets 2^(-inf - floor) = 0, not NaN.
-        if (R < HG) m_s[hg0 + R] = MULTI ? kNoMax : -INFINITY;
+        // Padding rows (zero queries, so zero logits) are computed like real
+        // ones and never written out.
+        if (R < HG) m_s[hg0 + R] = kNoMax;
         soft_bar(grp);
         // Row h of the unit is query token t(h) = (row0 + h) / rep_kv of its
         // run and sees positions n < L_all + t(h); positions below L_all are
@@ -549,6 +553,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int L_all = L - (p.tokens - 1);
         const int row0 = h_first % p.n_rep + hg0;  // the group's first row
         const int t_first = row0 / p.rep_kv, k_first = row0 % p.rep_kv;
+        const float4 *m4 = reinterpret_cast<const float4 *>(m_s + hg0);
         for (int i = 0; i < ntl; ++i) {
           const int tg = t + i, sb = tg & 1, st = tg % ST;
           const bool valid = (seg.t0 + i) * BN + R < L;
@@ -556,15 +561,27 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           // several tokens; before it every position is visible to every row
           const bool edge = (seg.t0 + i + 1) * BN > L_all;
           const int pos = (seg.t0 + i) * BN + R;
-          wait(bars.s_full(sb), (tg >> 1) & 1);
-          tc::fence_after();
-          // this position's logits (log2 units); -inf where the row may not
-          // see it (past L, or a later token of the row's own run) and for
-          // padding rows
-          float x[HG];
-          auto load_s = [&]() {
-            // every column chunk is asked for before the one wait
-            uint32_t r[HG];
+          // -inf where the row may not see this position: past L (the cache
+          // row may hold NaN), or a later token of the row's own run
+          auto mask = [&](float(&v)[HG]) {
+            if (__any_sync(0xffffffffu, !valid)) {
+#pragma unroll
+              for (int h = 0; h < HG; ++h) v[h] = valid ? v[h] : -INFINITY;
+            }
+            if (MULTI && edge) {
+              int tk = t_first, kk = k_first;
+#pragma unroll
+              for (int h = 0; h < HG; ++h) {
+                if (pos >= L_all + tk) v[h] = -INFINITY;
+                const bool wrap = ++kk == p.rep_kv;
+                kk = wrap ? 0 : kk;
+                tk += wrap ? 1 : 0;
+              }
+            }
+          };
+          // this position's raw logits S of the group's heads (every column
+          // chunk asked for before the one wait)
+          auto load_s = [&](uint32_t(&r)[HG]) {
 #pragma unroll
             for (int c0 = 0; c0 < HG; c0 += HCH) {
               if constexpr (HCH == 32) {
@@ -574,36 +591,42 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               }
             }
             tc::wait_ld();
-#pragma unroll
-            for (int h = 0; h < HG; ++h) x[h] = (valid && hg0 + h < nh) ? __uint_as_float(r[h]) * sl2 : -INFINITY;
-            if (MULTI && edge) {
-              // row h is token t(h) of its run: it sees positions < L_all + t(h)
-              int tk = t_first, kk = k_first;
-#pragma unroll
-              for (int h = 0; h < HG; ++h) {
-                if (pos >= L_all + tk) x[h] = -INFINITY;
-                const bool wrap = ++kk == p.rep_kv;
-                kk = wrap ? 0 : kk;
-                tk += wrap ? 1 : 0;
-              }
-            }
           };
-          load_s();
-          bool need = false;
+          // y = S * scale_log2 - m, masked
+          auto compute_y = [&](float(&y)[HG]) {
+            uint32_t r[HG];
+            load_s(r);
 #pragma unroll
-          for (int h = 0; h < HG; ++h) need |= x[h] > m_s[hg0 + h] + 8.f;
-          if (soft_bar_or(grp, need)) {
-            // move the running maxima to this tile's maxima where they grew by
-            // more than 8 (always on a unit's first tile); x is reduced in
-            // place, so a copy is kept where registers allow (bf16, up to 32
-            // heads) or x is read again from TMEM
-            constexpr bool KEEP = !C::FP8 && HG <= 32;
-            float xk[KEEP ? HG : 1];
-            if constexpr (KEEP) {
-#pragma unroll
-              for (int h = 0; h < HG; ++h) xk[h] = x[h];
+            for (int h4 = 0; h4 < HG; h4 += 4) {
+              const float4 mm = m4[h4 >> 2];
+              y[h4 + 0] = fmaf(__uint_as_float(r[h4 + 0]), sl2, -mm.x);
+              y[h4 + 1] = fmaf(__uint_as_float(r[h4 + 1]), sl2, -mm.y);
+              y[h4 + 2] = fmaf(__uint_as_float(r[h4 + 2]), sl2, -mm.z);
+              y[h4 + 3] = fmaf(__uint_as_float(r[h4 + 3]), sl2, -mm.w);
             }
-            soft_reduce<C, true>(x, grp, sub, lane, red, fin, R);
+            mask(y);
+          };
+          wait(bars.s_full(sb), (tg >> 1) & 1);
+          tc::fence_after();
+          float y[HG];
+          compute_y(y);
+          float ymax = y[0];
+#pragma unroll
+          for (int h = 1; h < HG; ++h) ymax = fmaxf(ymax, y[h]);
+          // Lazy running max: it moves only where a logit beats it by more
+          // than 8 (log2 units), and always on a unit's first tile.
+          if (soft_bar_or(grp, i == 0 || ymax > 8.f)) {
+            {
+              float x[HG];
+              {
+                uint32_t r[HG];
+                load_s(r);
+#pragma unroll
+                for (int h = 0; h < HG; ++h) x[h] = __uint_as_float(r[h]) * sl2;
+              }
+              mask(x);
+              soft_reduce<C, true>(x, grp, sub, lane, red, fin, R);
+            }
             bool moved_mine = false;
             if (R < HG) {
               const float tmax = fin[hg0 + R], mo = m_s[hg0 + R];
@@ -618,6 +641,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const bool moved = soft_bar_or(grp, moved_mine);
 #pragma unroll
             for (int h = 0; h < HG; ++h) lp[h] *= corr_s[hg0 + h];
+            compute_y(y);  // against the moved maxima
             if (i > 0 && moved) {
               // O^T holds P.V of the unit's tiles so far: rescale it once the
               // last of them landed (the same decision in every thread)
@@ -644,31 +668,27 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               }
               tc::wait_st();
             }
-            if constexpr (KEEP) {
-#pragma unroll
-              for (int h = 0; h < HG; ++h) x[h] = xk[h];
-            } else {
-              load_s();
-            }
           }
-          // column R of P^T (position R of every head row): 2^(x - m) as bf16
-          uint16_t pb16[HG];
+          // row R of P^T (position R; the group's heads): 2^y, packed in pairs
+          uint32_t pk[HG / 2];
 #pragma unroll
-          for (int h = 0; h < HG; ++h) {
-            const float pv = hg0 + h < nh ? tc::ex2(x[h] - m_s[hg0 + h]) : 0.f;
-            lp[h] += pv;
-            pb16[h] = C::FP8 ? f16_bits(pv) : __bfloat16_as_ushort(__float2bfloat16_rn(pv));
+          for (int h = 0; h < HG; h += 2) {
+            const float p0 = tc::ex2(y[h]), p1 = tc::ex2(y[h + 1]);
+            lp[h] += p0;
+            lp[h + 1] += p1;
+            pk[h >> 1] = C::FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
           }
           // the P buffer was last read by the P.V of tile tg - PB
           const int pb = tg % C::PB;
           if (tg >= C::PB) wait(bars.pv_done(pb), ((tg / C::PB) - 1) & 1);
           {
-            const uint32_t col = pbase + pb * C::P_BYTES + (R >> 6) * C::P_BOX + (R & 7) * 2;
-            const int chunk = (R & 63) >> 3;
+            const uint32_t row = pbase + pb * C::P_BYTES + R * C::P_ROW;
+            const int swz = (R >> C::P_SWZ_SHIFT) & C::P_SWZ_MASK;
 #pragma unroll
-            for (int h = 0; h < HG; ++h) {
-              const int hh = hg0 + h;
-              asm volatile("st.shared.u16 [%0], %1;" ::"r"(col + hh * 128 + ((chunk ^ (hh & 7)) << 4)), "h"(pb16[h])
+            for (int c = 0; c < HG / 8; ++c) {
+              const int chunk = (hg0 >> 3) + c;
+              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(row + ((chunk ^ swz) << 4)),
+                           "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
                            : "memory");
             }
           }

@@ -48,6 +48,22 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// The same for an MN-major operand whose rows (one per K index) are
+// `row_bytes` = 128, 64 or 32 bytes wide, stored with the swizzle of that
+// width (swizzle mode 2, 4 or 6 in bits 61..63): 16-byte chunk c of row r
+// sits at chunk c ^ ((r >> s) & m) with (s, m) = (0, 7), (1, 3), (2, 1).  The
+// whole M/N extent fits in one row, so LBO is unused; SBO = 8 rows.
+__device__ __forceinline__ uint64_t smem_desc_mn_rows(uint32_t saddr, uint32_t row_bytes) {
+  const uint64_t mode = row_bytes == 128 ? 2 : (row_bytes == 64 ? 4 : 6);
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(((8 * row_bytes) >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= mode << 61;
+  return d;
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B and an fp32
 // accumulator: D format bits 4..5 = 1 (f32), A format bits 7..9 = 1 (bf16),
 // B format bits 10..12 = 1 (bf16), A major bit 15, B major bit 16
