@@ -138,6 +138,8 @@ def load_library():
         lib.gqa_get_device_error.restype = ci
         lib.gqa_status_string.argtypes = [ci]
         lib.gqa_status_string.restype = ctypes.c_char_p
+        lib.gqa_stream_read.argtypes = [vp, sz, ci, vp, vp]
+        lib.gqa_stream_read.restype = ci
         _lib = lib
         return lib
 
@@ -462,6 +464,19 @@ def mha_to_gqa_meanpool(w, w_out, stream=None):
     _check("mha_to_gqa_meanpool", lib.mha_to_gqa_meanpool(_dev(w, "w"), _dev(w_out, "w_out"), H, G, d, D,
                                                           _dtype_code(w), _stream(w, stream)))
     return w_out
+
+
+def gqa_stream_read(buf, mode, sink, stream=None):
+    """Reads every byte of the device tensor `buf` once and XORs its 32-bit
+    words into the int32 device tensor `sink` (one element, set by the
+    caller): the read-only streaming probe of the roofline.  mode 0: 16-byte
+    loads; mode 1: bulk copies of 32 KB chunks into shared memory."""
+    lib = load_library()
+    if sink.dtype != torch.int32 or sink.numel() < 1:
+        raise ValueError("sink must be an int32 tensor of at least one element")
+    nbytes = buf.numel() * buf.element_size()
+    _check("gqa_stream_read", lib.gqa_stream_read(_dev(buf, "buf"), nbytes, mode, _dev(sink, "sink"),
+                                                  _stream(buf, stream)))
 
 
 def gqa_get_device_error(stream=None, device=None) -> int:

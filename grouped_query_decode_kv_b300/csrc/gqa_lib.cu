@@ -13,6 +13,7 @@
 #include "gqa.h"
 #include "gqa_device.cuh"
 #include "gqa_params.cuh"
+#include "gqa_probe.cuh"
 #include "gqa_proj_tc.cuh"
 #include "gqa_small_kernels.cuh"
 #include "gqa_split_mma.cuh"
@@ -47,7 +48,9 @@ struct KernelChoice {
   int block_n;
   int heads;
   int box_elems;
-  cudaError_t (*launch)(dim3, const CUtensorMap &, const CUtensorMap &, const SplitParams &, cudaStream_t);
+  bool fp8;
+  cudaError_t (*launch)(dim3, int, const CUtensorMap &, const CUtensorMap &, const SplitParams &, cudaStream_t);
+  int (*clusters)(int);  // max_clusters of the kernel
 };
 
 // Launch with programmatic stream serialisation: the kernel may start while
@@ -83,10 +86,55 @@ auto split_kernel_ptr() {
     return &gqa_split_simt_kernel<C, MULTI>;
 }
 
+// The same in thread-block clusters of `cluster` CTAs along x.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, int cluster,
+                               cudaStream_t st, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cluster > 1 ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <class C, int F, bool MULTI>
-cudaError_t launch_split(dim3 grid, const CUtensorMap &k, const CUtensorMap &v, const SplitParams &p,
+cudaError_t launch_split(dim3 grid, int cluster, const CUtensorMap &k, const CUtensorMap &v, const SplitParams &p,
                          cudaStream_t st) {
-  return launch_pdl(split_kernel_ptr<C, F, MULTI>(), grid, dim3(C::THREADS), C::SMEM_BYTES, st, k, v, p);
+  return launch_pdl_cluster(split_kernel_ptr<C, F, MULTI>(), grid, dim3(C::THREADS), C::SMEM_BYTES, cluster, st, k,
+                            v, p);
+}
+
+// Clusters of `cluster` CTAs of this kernel that can be resident at once (0
+// when the query fails).
+template <class C, int F, bool MULTI>
+int max_clusters(int cluster) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cluster * 64);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, split_kernel_ptr<C, F, MULTI>(), &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 template <class C, int F, bool MULTI>
@@ -104,7 +152,12 @@ KernelChoice make_choice() {
     c.box_elems = C::FP8 ? 128 : 64;
   else
     c.box_elems = 64;
+  if constexpr (F == kTc)
+    c.fp8 = C::FP8;
+  else
+    c.fp8 = false;
   c.launch = &launch_split<C, F, MULTI>;
+  c.clusters = &max_clusters<C, F, MULTI>;
   return c;
 }
 
@@ -178,6 +231,7 @@ struct Plan {
   int head_chunks;  // HC
   int P;            // CTAs of the split kernel
   long long units;  // B * G * HC
+  int cluster = 0;  // CTAs per thread-block cluster (0: no clusters)
 };
 
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
@@ -263,6 +317,22 @@ Plan make_plan(int B, int H, int G, int d, int Nmax, gqa_dtype_t dt, int split_t
   }
   P = std::max<long long>(1, std::min<long long>(P, std::min<long long>(tiles_full, 1 << 20)));
   pl.P = (int)P;
+  // tcgen05 kernel with room for k = 2..8 CTAs per unit of a full batch:
+  // launch in clusters of k, so that with equal lengths a unit's pieces meet
+  // in one cluster and merge through distributed shared memory (no
+  // workspace round trip, no merge kernel).  The grid keeps whole clusters
+  // and no more of them than can be resident at once.
+  if (split_tokens == 0 && pl.k.family == kTc && !pl.k.fp8 && pl.units > 0) {
+    const long long k = P / pl.units;
+    if (k >= 2 && k <= 4) {
+      const int resident = pl.k.clusters((int)k);
+      const long long nclu = std::min<long long>(P / k, resident);
+      if (nclu >= pl.units) {
+        pl.cluster = (int)k;
+        pl.P = (int)(nclu * k);
+      }
+    }
+  }
   return pl;
 }
 
@@ -399,13 +469,17 @@ int run_attention(const void *q, const void *k, const void *v, const int32_t *sl
   char *w = reinterpret_cast<char *>(ws);
   p.o_part = split ? reinterpret_cast<float *>(w + kWsHead) : nullptr;
   p.ml_part = split ? reinterpret_cast<float *>(w + kWsHead + ws_opart_bytes(pl, d)) : nullptr;
-  // units of one or two heads merge inside the split kernel; larger ones in
-  // the merge kernel, which spreads the (bigger) partials over every SM
+  // units cut between CTAs merge inside the split kernel for the CUDA-core
+  // kernel (the unit's last CTA) and for a cluster launch of the tcgen05
+  // kernel (every CTA of the unit's cluster, after a cluster barrier); the
+  // rest in the merge kernel, which spreads the (bigger) partials of
+  // many-head units over every SM
   void *book = split ? w + kWsHead + ws_opart_bytes(pl, d) + ws_ml_bytes(pl) : nullptr;
-  const bool merge_in_kernel = pl.k.family == kSimt;
-  p.unit_cnt = merge_in_kernel ? reinterpret_cast<unsigned long long *>(book) : nullptr;
+  const bool merge_in_kernel = pl.k.family == kSimt || pl.cluster > 1;
+  p.unit_cnt = pl.k.family == kSimt ? reinterpret_cast<unsigned long long *>(book) : nullptr;
   p.unit_info = merge_in_kernel ? nullptr : reinterpret_cast<int2 *>(book);
   p.epoch = next_epoch();
+  p.cluster_k = pl.cluster;
   p.append = app.k_new != nullptr;
   p.k_new = app.k_new;
   p.v_new = app.v_new;
@@ -427,7 +501,7 @@ int run_attention(const void *q, const void *k, const void *v, const int32_t *sl
   p.rep_kv = H / G;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
-  if (pl.k.launch(dim3(pl.P), mk, mv, p, st) != cudaSuccess) {
+  if (pl.k.launch(dim3(pl.P), pl.cluster, mk, mv, p, st) != cudaSuccess) {
     cudaGetLastError();
     return GQA_ERR_CUDA;
   }
@@ -635,6 +709,42 @@ int run_projection(const void *x, const void *wq, const void *wk, const void *wv
 using namespace gqa;
 
 extern "C" {
+
+int gqa_stream_read(const void *buf, size_t bytes, int mode, uint32_t *sink, cudaStream_t stream) {
+  if (!buf || !sink || !aligned16(buf) || bytes == 0) return GQA_ERR_INVALID_ARG;
+  const int sms = device_sm_count();
+  cudaError_t e;
+  if (mode == 0) {
+    if (bytes % 16) return GQA_ERR_INVALID_ARG;
+    gqa_read_ldg_kernel<<<sms * 4, kProbeLdgThreads, 0, stream>>>(reinterpret_cast<const uint4 *>(buf), bytes / 16,
+                                                                   sink);
+    e = cudaGetLastError();
+  } else if (mode == 1) {
+    if (bytes % kProbeChunk) return GQA_ERR_INVALID_ARG;
+    static std::once_flag once[kMaxDevices];
+    const int dev = current_device();
+    if (dev < 0) return GQA_ERR_CUDA;
+    bool ok = true;
+    std::call_once(once[dev], [&] {
+      ok = cudaFuncSetAttribute(gqa_read_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kProbeBulkSmem) ==
+           cudaSuccess;
+    });
+    if (!ok) {
+      cudaGetLastError();
+      return GQA_ERR_CUDA;
+    }
+    gqa_read_bulk_kernel<<<sms, kProbeBulkThreads, kProbeBulkSmem, stream>>>(reinterpret_cast<const uint8_t *>(buf),
+                                                                              bytes / kProbeChunk, sink);
+    e = cudaGetLastError();
+  } else {
+    return GQA_ERR_INVALID_ARG;
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GQA_ERR_CUDA;
+  }
+  return GQA_OK;
+}
 
 size_t gqa_decode_workspace_bytes_ex(int B, int H, int G, int d, int Nmax, gqa_dtype_t dtype, int split_tokens) {
   if (B <= 0 || H <= 0 || G <= 0 || Nmax <= 0 || H % G != 0 || (d != 64 && d != 128)) return 0;

@@ -19,6 +19,9 @@ struct SplitParams {
   unsigned long long *unit_cnt;  // [B*G*HC] in-kernel merge: (call epoch << 32) | CTAs of the unit done
   int2 *unit_info;          // [B*G*HC] merge kernel: (first slot, last CTA) of a split unit, or -1
   unsigned epoch;           // nonzero, different for every call
+  // tcgen05 kernel launched in thread-block clusters of cluster_k CTAs (0 or
+  // 1: no clusters); see the cluster-aligned plan in gqa_schedule.cuh
+  int cluster_k;
   // Fused decode step (append != 0): the new token's K/V rows k_new/v_new
   // [B*G, D] go to cache row L_b of every (b, g) before attention over
   // L_b + 1 positions; the last CTA to finish then sets seq_lens[b] = L_b + 1.

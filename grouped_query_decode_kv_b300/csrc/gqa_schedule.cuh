@@ -50,6 +50,7 @@ struct SchedParams {
   int block_n;      // positions per tile
   int append;       // fused decode step: the call appends one token first
   int unit_cost;    // extra virtual tiles charged per unit (see below)
+  int cluster_k = 0;  // CTAs per thread-block cluster of the launch (0: no clusters)
   // speculative plan (before griddepcontrol.wait): lengths are read with
   // L1-bypassing loads, so that no stale copy stays in the non-coherent cache
   // for the real plan to hit
@@ -105,6 +106,8 @@ struct CtaRange {
   int P;            // CTAs that take part (<= gridDim.x); the rest have empty ranges
   int cost;         // virtual tiles charged per non-empty unit
   int tiles_b;      // tiles of each unit of row b
+  int cl;           // cluster plan, and this CTA's cluster has a unit: every CTA of
+                    // the cluster works on a piece of that unit only (see below)
 };
 
 // Virtual tiles of one unit of a row with `tiles` real tiles.
@@ -173,18 +176,62 @@ __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int la
     rows += __shfl_xor_sync(0xffffffffu, rows, off);
   }
   const bool uniform = rows > 0 && tmin == tmax;
+  CtaRange r;
+  r.b = 0;
+  r.pre_b = 0;
+  r.tiles_b = 0;
+  r.cl = 0;
+  if (s.cluster_k > 1) {
+    // Launched in clusters of k CTAs (the host made the grid hold k CTAs per
+    // unit of a full batch): cluster j takes the j-th non-empty unit whole,
+    // its CTA of rank q the tiles [floor(q*tiles/k), floor((q+1)*tiles/k)) of
+    // it (possibly none), so that a unit's partials meet in one cluster.  No
+    // charge.  A CTA with an empty piece still takes part in its cluster's
+    // merge; r.b, r.pre_b and r.tiles_b then still name the unit.
+    const int k = s.cluster_k;
+    const long long u = c / k;
+    const int q = c % k;
+    r.T = T;
+    r.P = rows * s.units_per_b * k;
+    r.cost = 0;
+    r.begin = r.end = T;
+    if (u >= (long long)rows * s.units_per_b) return r;  // a cluster with no unit: idle
+    r.cl = 1;
+    const int nr = (int)(u / s.units_per_b), uib = (int)(u % s.units_per_b);
+    long long acc = 0;
+    int seen = 0;  // non-empty rows before this chunk
+    for (int base = 0; base < s.B; base += 32) {
+      const int b = base + lane;
+      const int tu = base == 0 ? keep0 : base == 32 ? keep1 : (b < s.B ? row_tiles(s, b) : 0);
+      const long long t = (long long)tu * s.units_per_b;
+      const long long incl = warp_incl_scan(t, lane);
+      const int ne = (b < s.B && tu > 0) ? 1 : 0;
+      const unsigned nem = __ballot_sync(0xffffffffu, ne);
+      const int rank = seen + __popc(nem & ((1u << lane) - 1u));  // non-empty rows before row b
+      const unsigned hit = __ballot_sync(0xffffffffu, ne && rank == nr);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        r.b = base + src;
+        r.pre_b = acc + __shfl_sync(0xffffffffu, incl - t, src);
+        r.tiles_b = __shfl_sync(0xffffffffu, tu, src);
+        const long long u0 = r.pre_b + (long long)uib * r.tiles_b;
+        r.begin = u0 + (long long)q * r.tiles_b / k;
+        r.end = u0 + (long long)(q + 1) * r.tiles_b / k;
+        return r;
+      }
+      seen += __popc(nem);
+      acc += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    return r;
+  }
   if (uniform) P = aligned_cta_count((long long)rows * s.units_per_b, P);
   const int cost = uniform ? 0 : s.unit_cost;
   T += (long long)cost * rows * s.units_per_b;
-  CtaRange r;
   r.T = T;
   r.P = P;
   r.cost = cost;
   r.begin = c < P ? cta_start(c, T, P) : T;
   r.end = c < P ? cta_start(c + 1, T, P) : T;
-  r.b = 0;
-  r.pre_b = 0;
-  r.tiles_b = 0;
   if (r.begin >= r.end) return r;
   long long acc = 0;
   for (int base = 0; base < s.B; base += 32) {

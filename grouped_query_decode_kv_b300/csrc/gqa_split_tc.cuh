@@ -100,8 +100,8 @@ struct TcCfg {
   // pipe full[STAGES], empty[STAGES]; then s_full[2], s_free[2], p_full[2],
   // pv_done[2], o_free[2], q_full[2], mma_done; FP8: conv_full[2], stg_free[2]
   static constexpr int NBAR = 2 * STAGES + 13 + (FP8 ? 4 : 0);
-  static constexpr int RANGE_BYTES = ((int)sizeof(CtaRange) + 15) / 16 * 16;
-  static constexpr int TAIL_BYTES = 4 * NQ * 4 + 3 * NQ * 4 + NBAR * 8 + 16 + RANGE_BYTES + (int)sizeof(UnitMerge);
+  static constexpr int RANGE_BYTES = ((int)sizeof(CtaRange) + 7) / 8 * 8;
+  static constexpr int TAIL_BYTES = 4 * NQ * 4 + 3 * NQ * 4 + NBAR * 8 + 8 + RANGE_BYTES + (int)sizeof(UnitMerge);
   static constexpr int QB = 1024 + Q_OFF + 2 * Q_BYTES + PB * P_BYTES + TAIL_BYTES <= 227 * 1024 ? 2 : 1;
   static constexpr int P_OFF = Q_OFF + QB * Q_BYTES;
   static constexpr int RED_OFF = P_OFF + PB * P_BYTES;  // [SG][4][HG] cross-warp reduction
@@ -110,7 +110,7 @@ struct TcCfg {
   static constexpr int CORR_OFF = M_OFF + NQ * 4;        // [NQ] rescale factor of a tile
   static constexpr int BAR_OFF = CORR_OFF + NQ * 4;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBAR * 8;
-  static constexpr int RANGE_OFF = TMEM_SLOT_OFF + 16;
+  static constexpr int RANGE_OFF = TMEM_SLOT_OFF + 8;  // 8-byte aligned (barriers before it)
   static constexpr int MERGE_OFF = RANGE_OFF + RANGE_BYTES;
   static constexpr int SMEM_BYTES = 1024 + MERGE_OFF + (int)sizeof(UnitMerge);
   // more than half of an SM's shared memory: one CTA per SM, so the TMEM
@@ -229,6 +229,77 @@ __device__ __forceinline__ void quad_transpose(float (&v)[4], int lane) {
   v[3] = b1 ? v[3] : r;
 }
 
+// Merge of the unit whose k pieces the k CTAs of this cluster (ranks 0..k-1,
+// CTAs c0 .. c0+k-1) left in workspace slots 2*(c0+j) (none for an empty
+// piece): this CTA writes heads [r*hpr, min(nh, (r+1)*hpr)), hpr =
+// ceil(nh / k), r its rank,
+//   out = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j,  M = max_j m_j,
+// over the non-empty pieces j = 0 .. k-1 in order.  A thread takes 16
+// dimensions of one head and issues all of its loads before it uses any.
+template <class C, bool MULTI>
+__device__ __forceinline__ void merge_cluster_unit(const SplitParams &p, const CtaRange &range, int tid, int nthr) {
+  constexpr int D = C::D, KMAX = 4, SEG = 16;  // at most 4 CTAs per cluster (host)
+  const int k = p.cluster_k;
+  const int r = (int)cluster_rank();
+  const int c0 = (int)blockIdx.x - r;
+  // the unit, from the range (a CTA with an empty piece has no segment)
+  const int tiles = range.tiles_b;
+  const int uib = (int)((range.begin - range.pre_b) / tiles);
+  const int b = range.b, g = uib / p.head_chunks, hc = uib % p.head_chunks;
+  const int h_first = g * p.n_rep + hc * p.heads_per_cta;
+  const int nh = min(p.heads_per_cta, p.n_rep - hc * p.heads_per_cta);
+  const int hpr = (nh + k - 1) / k;
+  const int h_lo = r * hpr, h_hi = min(nh, h_lo + hpr);
+  const float2 *ml = reinterpret_cast<const float2 *>(p.ml_part);
+  for (int it = tid; it < (h_hi - h_lo) * (D / SEG); it += nthr) {
+    const int h = h_lo + it / (D / SEG), d0 = (it % (D / SEG)) * SEG;
+    float2 mlj[KMAX];
+    float4 oj[KMAX][SEG / 4];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (j < k && (long long)(j + 1) * tiles / k > (long long)j * tiles / k) {
+        const size_t ps = (size_t)2 * (c0 + j) * p.heads_per_cta + h;
+        mlj[j] = __ldcg(ml + ps);
+        const float4 *o = reinterpret_cast<const float4 *>(p.o_part + ps * D + d0);
+#pragma unroll
+        for (int q = 0; q < SEG / 4; ++q) oj[j][q] = __ldcg(o + q);
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (!(j < k && (long long)(j + 1) * tiles / k > (long long)j * tiles / k)) mlj[j] = make_float2(-INFINITY, 0.f);
+      if (j < k) M = fmaxf(M, mlj[j].x);
+    }
+    float L = 0.f, a[SEG];
+#pragma unroll
+    for (int e = 0; e < SEG; ++e) a[e] = 0.f;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (j < k && mlj[j].x != -INFINITY) {
+        const float w = merge_weight(mlj[j].x, M);
+        L += w * mlj[j].y;
+#pragma unroll
+        for (int q = 0; q < SEG / 4; ++q) {
+          a[4 * q + 0] += w * oj[j][q].x;
+          a[4 * q + 1] += w * oj[j][q].y;
+          a[4 * q + 2] += w * oj[j][q].z;
+          a[4 * q + 3] += w * oj[j][q].w;
+        }
+      }
+    }
+    const float inv = (!MULTI || L > 0.f) ? 1.f / L : 0.f;  // 0: a query row that sees no position
+    uint4 pk[2];
+    uint32_t *pw = reinterpret_cast<uint32_t *>(pk);
+#pragma unroll
+    for (int e = 0; e < SEG / 2; ++e) pw[e] = pack_bf16x2(a[2 * e] * inv, a[2 * e + 1] * inv);
+    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) +
+                                           query_row<MULTI>(p, b, h_first + h) * D + d0);
+    dst[0] = pk[0];
+    dst[1] = pk[1];
+  }
+}
+
 // Floor of the running max (log2 units): far below any logit, finite so
 // that 2^(x - floor) is 0 for x = -inf.  A partial left with it (a row with
 // no visible position in its segment) gets weight 0 in the merge unless every
@@ -268,6 +339,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   sp.block_n = BN;
   sp.append = p.append;
   sp.unit_cost = C::UNIT_COST;
+  sp.cluster_k = p.cluster_k;
 
   if (threadIdx.x == 0) {
     pipe.init();
@@ -735,19 +807,42 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // O^T of this unit is final once the P.V of its last tile landed
         wait(bars.pv_done((t - 1) % C::PB), ((t - 1) / C::PB) & 1);
         tc::fence_after();
-        const bool whole = seg.t0 == 0 && seg.t1 == seg.tiles;
+        // cluster plan: the cluster merges the partials of its one unit after
+        // the barrier at the end (at most one segment per CTA, always a
+        // partial, even when the piece is the whole unit)
+        const bool clm = !C::FP8 && range.cl;
+        const bool whole = !clm && seg.t0 == 0 && seg.t1 == seg.tiles;
         const int slot = partial_slot(unit);
-        // Thread R holds output dimension R of every head; a 4x4 transpose
-        // within each quad of lanes gives lane j of a quad four consecutive
-        // dimensions d4..d4+3 of head (block + j), written as one vector.
         const size_t orow_b = MULTI ? (size_t)b * p.tokens * p.heads_q + (size_t)(h_first / p.n_rep) * p.rep_kv
                                     : (size_t)b * p.H + h_first;
         const int d4 = 32 * sub + (lane & ~3);
-        // one column chunk at a time, the chunk loop not unrolled: this code
-        // runs once per unit, and with 64 columns its size (instruction
-        // fetch), not its loads, is what it costs
+        if (!whole) {
+          // a cut unit's partial: thread R writes dimension R of every head
+          // (consecutive lanes, consecutive words: each warp store is one
+          // 128-byte line, and no transpose is needed)
+          float *orow = p.o_part + (size_t)slot * p.heads_per_cta * D + R;
 #pragma unroll 1
-        for (int c0 = 0; c0 < HG; c0 += HCH) {
+          for (int c0 = 0; c0 < HG; c0 += HCH) {
+            uint32_t r[32];
+            if constexpr (HCH == 32) {
+              tc::ld_32x32b_x32(trow + C::TM_O + ob * NR + hg0 + c0, r);
+            } else {
+              tc::ld_32x32b_x16(trow + C::TM_O + ob * NR + hg0 + c0, r);
+            }
+            tc::wait_ld();
+#pragma unroll
+            for (int c = 0; c < HCH; ++c)
+              if (hg0 + c0 + c < nh) orow[(size_t)(hg0 + c0 + c) * D] = __uint_as_float(r[c]) * vscale;
+          }
+        }
+        // a whole unit goes to out: thread R holds output dimension R of
+        // every head; a 4x4 transpose within each quad of lanes gives lane j
+        // of a quad four consecutive dimensions d4..d4+3 of head (block + j),
+        // written as one 8-byte vector.  One column chunk at a time, the chunk
+        // loop not unrolled: this code runs once per unit, and with 64
+        // columns its size (instruction fetch), not its loads, is what it costs
+#pragma unroll 1
+        for (int c0 = 0; c0 < (whole ? HG : 0); c0 += HCH) {
           uint32_t r[32];
           if constexpr (HCH == 32) {
             tc::ld_32x32b_x32(trow + C::TM_O + ob * NR + hg0 + c0, r);
@@ -777,9 +872,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 pk.x = pack_bf16x2(seen ? v[0] / f : 0.f, seen ? v[1] / f : 0.f);
                 pk.y = pack_bf16x2(seen ? v[2] / f : 0.f, seen ? v[3] / f : 0.f);
                 *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * D + d4) = pk;
-              } else {
-                *reinterpret_cast<float4 *>(p.o_part + ((size_t)slot * p.heads_per_cta + h) * D + d4) =
-                    make_float4(v[0], v[1], v[2], v[3]);
               }
             }
           }
@@ -787,14 +879,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (!whole && R < HG && hg0 + R < nh)
           reinterpret_cast<float2 *>(p.ml_part)[(size_t)slot * p.heads_per_cta + hg0 + R] =
               make_float2(mR, fin[hg0 + R]);
+        // merge kernel (no cluster launch): where the unit's partials are
         if (R == 0 && grp == 0) record_unit(p, seg, whole, slot, range, b);
-        // (the host gives units of this kernel to the merge kernel; the
-        // in-kernel merge needs all of the unit's heads in one group)
-        if constexpr (C::SG == 1) {
-          if (!whole && p.unit_cnt)
-            finish_split_unit<__nv_bfloat16, D, MULTI>(p, seg, range, b, h_first, nh, R, C::SOFT, um,
-                                                       [] { soft_bar(0); });
-        }
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.o_free(ob));
@@ -861,6 +947,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
       }
     }
+  }
+  // ---- cluster plan: the k CTAs of the cluster wrote the partials of the k
+  // pieces of the same unit to their workspace slots (a CTA with an empty
+  // piece wrote none); after the barrier (cluster-scope release / acquire,
+  // which orders those global writes) the CTA of rank r merges the heads
+  // [r*ceil(nh/k), ...) from all of them.  No second launch and no second
+  // barrier: nothing is read from the peers' shared memory.  The plan is the
+  // same in every CTA, so either every CTA of a cluster comes here or none
+  // does.
+  if (!C::FP8 && range.cl) {
+    cluster_sync_all();
+    if (warp >= 2 && warp < C::CONV_WARP0) merge_cluster_unit<C, MULTI>(p, range, threadIdx.x - 64, C::SG * C::SOFT);
   }
   // ---- teardown: every tcgen05 operation has completed (the MMA thread
   // waited for its last commit); free the tensor memory

@@ -340,6 +340,22 @@ int mha_to_gqa_meanpool(const void *w, void *w_out, int H, int G, int d, int D,
                         gqa_dtype_t dtype, cudaStream_t stream);
 
 /*
+ * gqa_stream_read — a measurement utility with no counterpart in the pages:
+ * the read-only streaming ceiling that the decode kernels' HBM rates are
+ * judged against (a decode call reads its K/V bytes once and writes almost
+ * nothing, so a copy, which writes every byte too, is the wrong bound).
+ * Reads `bytes` bytes at `buf` (DEVICE memory, 16-byte aligned) once and
+ * XORs all its 32-bit words into *sink (DEVICE word, which the caller sets
+ * beforehand; the result is a checksum).
+ *   mode 0: 16-byte loads from every thread (bytes % 16 == 0);
+ *   mode 1: bulk asynchronous copies of 32 KB chunks into shared memory, as
+ *           the K/V pipeline streams (bytes % 32768 == 0).
+ * Asynchronous on `stream`; a bad argument returns GQA_ERR_INVALID_ARG with
+ * nothing enqueued.
+ */
+int gqa_stream_read(const void *buf, size_t bytes, int mode, uint32_t *sink, cudaStream_t stream);
+
+/*
  * Reads the current device's error word into *host_err and clears it.  This
  * call synchronises `stream` (it copies the word to the host on it).
  */

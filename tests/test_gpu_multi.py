@@ -128,3 +128,12 @@ def test_empty_rows_and_tokens_that_see_nothing_are_zero():
 @pytest.mark.parametrize("name", workloads.multi_names())
 def test_multi_token_full_size(name):
     check_multi(workloads.workload(name))
+
+
+@pytest.mark.parametrize("B,H,G,T", [(40, 8, 1, 4), (32, 16, 1, 4), (64, 4, 1, 8)])
+def test_multi_token_cluster_plan(B, H, G, T):
+    """Several tokens per sequence on shapes that run the tcgen05 kernel in
+    thread-block clusters (37..74 units), with ragged lengths that leave some
+    tokens with nothing to see and some pieces of a unit empty."""
+    w = workloads.Workload("multi_clu", B, H, G, 128, 400, "bf16", ("uniform", 1, 400), 8600 + B + H + T, tokens=T)
+    check_multi(w)

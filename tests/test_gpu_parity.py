@@ -439,3 +439,50 @@ def test_step_workspace_shared_across_shapes_and_never_cleared(H, G):
         assert torch.equal(k1.view(torch.uint8), k2.view(torch.uint8))
         np.testing.assert_array_equal(out1.double().cpu().numpy(), out2.double().cpu().numpy())
     assert gqa.gqa_get_device_error() == 0
+
+
+# ------------------------------------------------------------ cluster plan
+# Groups of 8+ heads (tcgen05 kernel) with 37..74 (batch, KV head) units run
+# in thread-block clusters of k = 2..4 CTAs, one unit per cluster, merged
+# inside the cluster.  These shapes reach that plan with ragged and short
+# lengths: pieces with no tile (a unit of fewer than k tiles), empty rows.
+@pytest.mark.parametrize("B,H,G,lens", [
+    (40, 32, 1, ("uniform", 0, 300)),     # 40 units, k = 3; many units of < 3 tiles
+    (20, 64, 2, ("uniform", 1, 1000)),    # 40 units of 32 heads
+    (64, 32, 1, ("uniform", 1, 2048)),    # the MQA shape with lengths from 1
+    (32, 64, 1, ("fixed", 200)),          # k = 4, every unit 2 tiles: two empty pieces each
+    (37, 16, 1, ("uniform", 100, 700)),   # k = 4, 16 heads
+])
+def test_cluster_plan_shapes(B, H, G, lens):
+    w = workloads.Workload("clu", B, H, G, 128, max(lens[1:]) if lens[0] == "uniform" else lens[1], "bf16", lens,
+                           8800 + B + H + G)
+    x = workloads.make_inputs(w)
+    ref = oracle.decode_attention(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], w.scale)
+    got = gpu_attention(x, w.scale)
+    assert_parity(got, ref, f"cluster plan B={B} H={H} G={G}")
+    err = gqa.gqa_get_device_error()
+    assert err in (0, gqa.DEVERR_ATTN_LEN)  # L = 0 rows are flagged
+
+
+@pytest.mark.parametrize("B,H,G", [(40, 32, 1), (32, 64, 1)])
+def test_cluster_plan_decode_step(B, H, G):
+    """Fused append + attention under the cluster plan, against the separate
+    calls (bit for bit) and the oracle."""
+    dev = torch.device("cuda")
+    N = 700
+    w = workloads.Workload("clu_step", B, H, G, 128, N, "bf16", ("uniform", 0, N - 1), 8900 + B + H)
+    x = workloads.make_inputs(w)
+    q, kn, vn = x["q"].to(dev), x["k_new"].to(dev), x["v_new"].to(dev)
+    k1, v1, sl1 = x["k_cache"].to(dev), x["v_cache"].to(dev), x["seq_lens"].to(dev)
+    k2, v2, sl2 = k1.clone(), v1.clone(), sl1.clone()
+    out1, out2 = torch.full_like(q, float("nan")), torch.full_like(q, float("nan"))
+    gqa.kv_append(kn, vn, k1, v1, sl1)
+    gqa.gqa_decode_attention(q, k1, v1, sl1, w.scale, out1)
+    gqa.gqa_decode_step(q, kn, vn, k2, v2, sl2, w.scale, out2)
+    torch.cuda.synchronize()
+    assert torch.equal(sl1, sl2)
+    np.testing.assert_array_equal(out1.double().cpu().numpy(), out2.double().cpu().numpy())
+    k_ref, v_ref, sl_ref, _ = oracle.kv_append(x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_lens"])
+    ref = oracle.decode_attention(x["q"], k_ref, v_ref, sl_ref, w.scale)
+    assert_parity(out2.double().cpu().numpy(), ref, f"cluster step B={B} H={H} G={G}")
+    gqa.gqa_get_device_error()
