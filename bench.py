@@ -280,11 +280,14 @@ def run_steps(st: DecodeState, first: int, count: int, ev=None):
             ev[i - first][1].record()
 
 
-def _graph_time(fn_seq, reset=None, reps: int = 3) -> float:
+def _graph_stats(fn_seq, reset=None, reps: int = 21) -> dict:
     """Device time per call (µs) of a sequence of library calls captured into
-    one CUDA graph: the graph is replayed `reps` times, each replay bracketed
-    by CUDA events, and the best replay is divided by the number of calls.
-    `reset` (outside the timed replay) restores state between replays."""
+    one CUDA graph (back to back, so the host's per-call cost is out): the
+    graph is replayed `reps` times after one untimed replay, each replay
+    bracketed by CUDA events; every replay gives the mean time of its calls,
+    and the median with the 10th and 90th percentiles of those replay means
+    is returned ({"us", "p10", "p90", "calls"}).  `reset` (outside the timed
+    replays) restores state between replays."""
     g = torch.cuda.CUDAGraph()
     side = torch.cuda.Stream()
     if reset:
@@ -298,8 +301,8 @@ def _graph_time(fn_seq, reset=None, reps: int = 3) -> float:
         reset()
     with torch.cuda.graph(g):
         n = fn_seq()
-    best = float("inf")
-    for _ in range(reps + 1):
+    per_call = []
+    for i in range(reps + 1):
         if reset:
             reset()
         torch.cuda.synchronize()
@@ -308,9 +311,16 @@ def _graph_time(fn_seq, reset=None, reps: int = 3) -> float:
         g.replay()
         b.record()
         torch.cuda.synchronize()
-        best = min(best, a.elapsed_time(b) * 1e3 / n)
+        if i > 0:
+            per_call.append(a.elapsed_time(b) * 1e3 / n)
     del g
-    return best
+    per_call.sort()
+    q = lambda f: per_call[min(len(per_call) - 1, int(f * len(per_call)))]
+    return {"us": statistics.median(per_call), "p10": q(0.1), "p90": q(0.9), "calls": n * reps}
+
+
+def _graph_time(fn_seq, reset=None) -> float:
+    return _graph_stats(fn_seq, reset)["us"]
 
 
 def time_attention_only(w: workloads.Workload, device, iters: int, warm: int, l2_bytes: int, mem_budget: int):
@@ -344,7 +354,8 @@ def time_attention_only(w: workloads.Workload, device, iters: int, warm: int, l2
     for i in range(warm):
         c = i % copies
         gqa.gqa_decode_attention_ws(st.q[c], st.k[c], st.v[c], full, w.scale, st.out[c], ws)
-    us = _graph_time(attn_seq)
+    stats = _graph_stats(attn_seq)
+    us = stats["us"]
     us_append = _graph_time(append_seq, reset=st.reset_lengths)
     us_step = _graph_time(step_seq, reset=st.reset_lengths)
     err = gqa.gqa_get_device_error()
@@ -353,7 +364,8 @@ def time_attention_only(w: workloads.Workload, device, iters: int, warm: int, l2
     peak, _ = hbm_peak()
     row = {
         "B": w.B, "H": w.H, "G": w.G, "d": w.d, "Nmax": w.Nmax, "dtype": w.dtype, "sum_L": int(sum(lens_full)),
-        "us": round(us, 2), "bytes": abytes, "gbs": round(abytes / us / 1e3, 1),
+        "us": round(us, 2), "us_p10": round(stats["p10"], 2), "us_p90": round(stats["p90"], 2),
+        "calls_timed": stats["calls"], "bytes": abytes, "gbs": round(abytes / us / 1e3, 1),
         "frac_measured": round(abytes / us / 1e3 / peak, 3),
         "frac_8tbs": round(abytes / us / 1e3 / NOMINAL_HBM_GBS, 3),
         "tflops": round(cost.decode_attention_flops(lens_full, w.H, w.d) / us / 1e6, 1),
@@ -504,32 +516,43 @@ def time_projection(name: str, device, iters: int, l2_bytes: int, mem_budget: in
     return row
 
 
-def read_ceiling(device) -> float:
-    """Read-only streaming ceiling (library reduction over 4 GiB), GB/s."""
-    x = torch.ones(2 ** 31, dtype=torch.bfloat16, device=device)
-    for _ in range(3):
-        x.sum()
-    ts = []
-    for _ in range(10):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        x.sum()
-        b.record()
-        torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b) * 1e-3)
+def read_ceiling(device) -> dict:
+    """Read-only streaming ceiling of this GPU: the library's probe reads a
+    4 GiB buffer once (16-byte loads, and bulk copies into shared memory as
+    the K/V pipeline does), best of 10 timed passes each after 3 warm-up
+    passes, in GB/s; `gbs` is the larger of the two."""
+    import grouped_query_decode_kv_b300 as gqa
+    nbytes = 1 << 32
+    x = torch.ones(nbytes // 2, dtype=torch.bfloat16, device=device)
+    sink = torch.zeros(1, dtype=torch.int32, device=device)
+    out = {}
+    for mode, name in ((0, "loads"), (1, "bulk_copies")):
+        for _ in range(3):
+            gqa.gqa_stream_read(x, mode, sink)
+        ts = []
+        for _ in range(10):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            gqa.gqa_stream_read(x, mode, sink)
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e-3)
+        out[name] = round(nbytes / min(ts) / 1e9, 1)
     del x
     torch.cuda.empty_cache()
-    return 2 ** 32 / min(ts) / 1e9
+    out["gbs"] = max(out["loads"], out["bulk_copies"])
+    return out
 
 
 # ----------------------------------------------------------------- CPU oracle
-def oracle_sample(w: workloads.Workload, budget_s: float, max_units: int = 1 << 30, _cache={}):
+def oracle_sample(w: workloads.Workload, budget_s: float, max_units: int = 1 << 30, _cache={}, threads: int = 0):
     """Times the fp64 CPU oracle on a bounded sample of the workload: whole
     (batch, KV group) units, batch rows in order, as many as fit in about
-    `budget_s` seconds (at least one).  Returns (GB/s of algorithmic bytes,
-    units done, seconds, threads)."""
+    `budget_s` seconds (at least one), on `threads` host threads (0: every
+    core in this process's affinity mask).  Returns (GB/s of algorithmic
+    bytes, units done, seconds, threads)."""
     import oracle
-    threads = len(os.sched_getaffinity(0))
+    threads = threads or len(os.sched_getaffinity(0))
     lens = workloads.make_seq_lens(w).tolist()
     key = w.name
     if key not in _cache:
@@ -562,6 +585,31 @@ def oracle_sample(w: workloads.Workload, budget_s: float, max_units: int = 1 << 
         done_bytes += cost.decode_attention_bytes([L], groups * w.n_rep, groups, w.d, w.elt)
         b += 1
     return done_bytes / spent / 1e9, done_units, spent, threads
+
+
+ORACLE_TABLE = ["tiny", "mha", "gqa8", "mqa", "long", "sweep_g1", "sweep_g8", "sweep_g64"]
+ORACLE_ONE_THREAD = ["tiny", "mha", "gqa8"]
+
+
+def oracle_table(budget_s: float) -> dict:
+    """The fp64 oracle per decode workload on a bounded sample of each (about
+    `budget_s` seconds), on every host core and, for the three smaller
+    workloads, on one thread: GB/s of algorithmic bytes and the µs one whole
+    call would take at that rate."""
+    out = {}
+    for name in ORACLE_TABLE:
+        w = workloads.workload(name)
+        lens = workloads.make_seq_lens(w).tolist()
+        call_bytes = cost.decode_attention_bytes(lens, w.H, w.G, w.d, w.elt)
+        row = {}
+        for label, thr in (("all_cores", 0), ("one_thread", 1)):
+            if label == "one_thread" and name not in ORACLE_ONE_THREAD:
+                continue
+            gbs, units, spent, used = oracle_sample(w, budget_s, threads=thr)
+            row[label] = {"gbs": round(gbs, 4), "us_per_call": round(call_bytes / gbs / 1e3, 1), "threads": used,
+                          "units_sampled": units, "seconds": round(spent, 2)}
+        out[name] = row
+    return out
 
 
 # ----------------------------------------------------------------- arms
@@ -746,10 +794,11 @@ def run_ours(args, world, rank, local):
     del st
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_table:
-        ceiling = round(read_ceiling(device), 1)
+        ceiling = read_ceiling(device)
         table = {}
         for name in TABLE_WORKLOADS:
             table[name] = time_attention_only(workloads.workload(name), device, args.table_iters, 5, l2, mem_budget)
+            table[name]["frac_read_ceiling"] = round(table[name]["gbs"] / ceiling["gbs"], 3)
         table_multi = {}
         for name in workloads.multi_names():
             table_multi[name] = time_multi(workloads.workload(name), device, args.table_iters, 5, l2, mem_budget)
@@ -761,7 +810,9 @@ def run_ours(args, world, rank, local):
             table_proj[name] = time_projection(name, device, args.table_iters, l2, mem_budget)
 
     cpu = None
+    cpu_table = None
     if rank == 0 and world == 1 and not args.no_cpu:
+        cpu_table = oracle_table(args.cpu_table_seconds)
         gbs, units, spent, threads = oracle_sample(w, args.cpu_seconds)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"{units} (batch, KV-group) units of the {w.name} workload, taken in batch-row order "
@@ -817,12 +868,14 @@ def run_ours(args, world, rank, local):
             "traffic": traffic,
         },
         "cpu_baseline": cpu,
+        "cpu_baseline_table": cpu_table,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "us_per_step": round(e_secs / e_steps * 1e6, 2), "host_issue_us_per_step": round(host_issue_us, 2)},
         "gpu_launches": launches_per_step(w) * steps,
         "clocks": clocks,
         "device_error": dev_err,
-        "read_ceiling_gbs": ceiling,
+        "read_ceiling_gbs": ceiling["gbs"] if ceiling else None,
+        "read_ceiling": ceiling,
         "table": table,
         "table_multi_token": table_multi,
         "table_qkv_projection": table_proj,
@@ -862,6 +915,8 @@ def main(argv=None):
                     help="time only one group of table rows (projection layers, FP8 cache, several "
                          "tokens) and print them as one JSON line; for profiling those kernels")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-table-seconds", type=float, default=2.0,
+                    help="seconds of oracle work per workload (and thread count) in cpu_baseline_table")
     ap.add_argument("--prewarm", type=float, default=1.0, help="seconds of untimed steps before the warm-up")
     args = ap.parse_args(argv)
     if args.warmup < 3:

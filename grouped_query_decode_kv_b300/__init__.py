@@ -64,6 +64,7 @@ EXPORTED_SYMBOLS = (
     "gqa_decode_attention_multi", "gqa_decode_attention_multi_ex",
     "gqa_qkv_project", "gqa_qkv_project_ws", "gqa_qkv_project_workspace_bytes",
     "gqa_decode_attention_fp8", "gqa_decode_attention_fp8_ws", "gqa_decode_workspace_bytes_fp8", "kv_append_fp8",
+    "gqa_stream_read", "gqa_set_workspace_allocator",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -140,6 +141,8 @@ def load_library():
         lib.gqa_status_string.restype = ctypes.c_char_p
         lib.gqa_stream_read.argtypes = [vp, sz, ci, vp, vp]
         lib.gqa_stream_read.restype = ci
+        lib.gqa_set_workspace_allocator.argtypes = [vp, vp, vp]
+        lib.gqa_set_workspace_allocator.restype = ci
         _lib = lib
         return lib
 

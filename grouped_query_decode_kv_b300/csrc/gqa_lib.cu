@@ -369,6 +369,37 @@ size_t workspace_for(const Plan &pl, int B, int H, int d) {
   return kWsHead + ws_opart_bytes(pl, d) + ws_ml_bytes(pl) + ws_book_bytes(pl);
 }
 
+// ----------------------------------------------------------- workspace allocator
+// The workspace of the calls that get their own (gqa_decode_attention,
+// gqa_decode_step, ...) comes from the stream-ordered allocator unless the
+// caller installed its own with gqa_set_workspace_allocator.
+std::atomic<gqa_alloc_fn> g_alloc{nullptr};
+std::atomic<gqa_free_fn> g_free{nullptr};
+std::atomic<void *> g_alloc_ctx{nullptr};
+
+bool ws_alloc(void **ptr, size_t bytes, cudaStream_t st) {
+  *ptr = nullptr;
+  if (const gqa_alloc_fn fn = g_alloc.load()) return fn(g_alloc_ctx.load(), ptr, bytes, st) == 0 && *ptr;
+  if (cudaMallocAsync(ptr, bytes, st) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return true;
+}
+
+// True when the release was accepted (enqueued).
+bool ws_free(void *ptr, cudaStream_t st) {
+  if (const gqa_free_fn fn = g_free.load()) {
+    fn(g_alloc_ctx.load(), ptr, st);
+    return true;
+  }
+  if (cudaFreeAsync(ptr, st) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return true;
+}
+
 // ----------------------------------------------------------- TMA descriptors
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static std::once_flag once;
@@ -710,6 +741,14 @@ using namespace gqa;
 
 extern "C" {
 
+int gqa_set_workspace_allocator(gqa_alloc_fn alloc, gqa_free_fn free_fn, void *ctx) {
+  if ((alloc == nullptr) != (free_fn == nullptr)) return GQA_ERR_INVALID_ARG;
+  g_alloc_ctx.store(ctx);
+  g_free.store(free_fn);
+  g_alloc.store(alloc);
+  return GQA_OK;
+}
+
 int gqa_stream_read(const void *buf, size_t bytes, int mode, uint32_t *sink, cudaStream_t stream) {
   if (!buf || !sink || !aligned16(buf) || bytes == 0) return GQA_ERR_INVALID_ARG;
   const int sms = device_sm_count();
@@ -785,13 +824,10 @@ int gqa_decode_attention(const void *q, const void *k_cache, const void *v_cache
   const size_t need = workspace_for(pl, B, H, d);
   void *ws = nullptr;
   if (need > 0) {
-    if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
-      cudaGetLastError();
-      return GQA_ERR_NO_MEMORY;
-    }
+    if (!ws_alloc(&ws, need, stream)) return GQA_ERR_NO_MEMORY;
   }
   int rc = run_attention(q, k_cache, v_cache, seq_lens, scale, out, B, H, G, d, Nmax, dtype, pl, ws, stream);
-  if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && rc == GQA_OK) rc = GQA_ERR_CUDA;
+  if (ws && !ws_free(ws, stream) && rc == GQA_OK) rc = GQA_ERR_CUDA;
   return rc;
 }
 
@@ -808,10 +844,7 @@ int decode_step(const void *q, const void *k_new, const void *v_new, void *k_cac
   void *ws = workspace;
   if (allocate) {
     ws = nullptr;
-    if (need > 0 && cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
-      cudaGetLastError();
-      return GQA_ERR_NO_MEMORY;
-    }
+    if (need > 0 && !ws_alloc(&ws, need, stream)) return GQA_ERR_NO_MEMORY;
   } else if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))) {
     return GQA_ERR_INVALID_ARG;
   }
@@ -822,7 +855,7 @@ int decode_step(const void *q, const void *k_new, const void *v_new, void *k_cac
   app.v_cache = v_cache;
   app.seq_lens = seq_lens;
   int rc = run_attention(q, k_cache, v_cache, seq_lens, scale, out, B, H, G, d, Nmax, dtype, pl, ws, stream, app);
-  if (allocate && ws && cudaFreeAsync(ws, stream) != cudaSuccess && rc == GQA_OK) rc = GQA_ERR_CUDA;
+  if (allocate && ws && !ws_free(ws, stream) && rc == GQA_OK) rc = GQA_ERR_CUDA;
   return rc;
 }
 }  // namespace
@@ -891,13 +924,10 @@ int gqa_decode_attention_multi(const void *q, const void *k_cache, const void *v
   if (!plan_fits(pl, B, G)) return GQA_ERR_UNSUPPORTED;
   const size_t need = workspace_for(pl, B, T * H, d);
   void *ws = nullptr;
-  if (need > 0 && cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
-    cudaGetLastError();
-    return GQA_ERR_NO_MEMORY;
-  }
+  if (need > 0 && !ws_alloc(&ws, need, stream)) return GQA_ERR_NO_MEMORY;
   int rc = run_attention(q, k_cache, v_cache, seq_lens, scale, out, B, H, G, d, Nmax, dtype, pl, ws, stream,
                          StepAppend(), T);
-  if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && rc == GQA_OK) rc = GQA_ERR_CUDA;
+  if (ws && !ws_free(ws, stream) && rc == GQA_OK) rc = GQA_ERR_CUDA;
   return rc;
 }
 
@@ -922,12 +952,9 @@ int gqa_qkv_project(const void *x, const void *w_q, const void *w_k, const void 
   if (int rc = check_proj_args(x, w_q, w_k, w_v, q, k_new, v_new, B, A, H, G, d, dtype)) return rc;
   const size_t need = proj_workspace(make_proj_plan(B, A, H, G, d));
   void *ws = nullptr;
-  if (need > 0 && cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
-    cudaGetLastError();
-    return GQA_ERR_NO_MEMORY;
-  }
+  if (need > 0 && !ws_alloc(&ws, need, stream)) return GQA_ERR_NO_MEMORY;
   int rc = run_projection(x, w_q, w_k, w_v, q, k_new, v_new, B, A, H, G, d, ws, stream);
-  if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && rc == GQA_OK) rc = GQA_ERR_CUDA;
+  if (ws && !ws_free(ws, stream) && rc == GQA_OK) rc = GQA_ERR_CUDA;
   return rc;
 }
 
@@ -967,13 +994,10 @@ int gqa_decode_attention_fp8(const void *q, const void *k_cache, const void *v_c
   if (!plan_fits(pl, B, G)) return GQA_ERR_UNSUPPORTED;
   const size_t need = workspace_for(pl, B, H, d);
   void *ws = nullptr;
-  if (need > 0 && cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
-    cudaGetLastError();
-    return GQA_ERR_NO_MEMORY;
-  }
+  if (need > 0 && !ws_alloc(&ws, need, stream)) return GQA_ERR_NO_MEMORY;
   int rc = run_attention(q, k_cache, v_cache, seq_lens, scale, out, B, H, G, d, Nmax, GQA_FP8_E4M3, pl, ws, stream,
                          StepAppend(), 1, k_scale, v_scale);
-  if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && rc == GQA_OK) rc = GQA_ERR_CUDA;
+  if (ws && !ws_free(ws, stream) && rc == GQA_OK) rc = GQA_ERR_CUDA;
   return rc;
 }
 

@@ -78,7 +78,10 @@ __device__ __forceinline__ int row_tiles(const SchedParams &s, int b) {
 }
 
 __device__ __forceinline__ long long cta_start(long long c, long long T, long long P) {
-  return T >= P ? (c * T) / P : (c < T ? c : T);
+  if (T < P) return c < T ? c : T;
+  const long long ct = c * T;
+  // 32-bit division whenever the product allows (the common case)
+  return ct < 0x7fffffffLL ? (long long)((int)ct / (int)P) : ct / P;
 }
 
 // The CTA whose range holds global tile t (0 <= t < T).
@@ -88,11 +91,29 @@ __device__ __forceinline__ int cta_of_tile(long long t, long long T, long long P
 }
 
 __device__ __forceinline__ long long warp_incl_scan(long long v, int lane) {
+  if (__all_sync(0xffffffffu, v < (1LL << 26))) {  // the 32-bit scan suffices
+    int x = (int)v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += o;
+    }
+    return x;
+  }
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const long long o = __shfl_up_sync(0xffffffffu, v, off);
     if (lane >= off) v += o;
   }
+  return v;
+}
+
+// Sum of v >= 0 over the warp: one reduction instruction while every lane's
+// value is small enough for its 32-bit form, else a 64-bit butterfly.
+__device__ __forceinline__ long long warp_sum(long long v) {
+  if (__all_sync(0xffffffffu, v < (1LL << 26))) return (long long)__reduce_add_sync(0xffffffffu, (unsigned)v);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
   return v;
 }
 
@@ -109,6 +130,10 @@ struct CtaRange {
   int cl;           // cluster plan, and this CTA's cluster has a unit: every CTA of
                     // the cluster works on a piece of that unit only (see below)
 };
+
+// First tile of piece q of a unit of `tiles` tiles cut into k pieces
+// (cluster plan): floor(q * tiles / k), in 32 bits (q, k <= 8, tiles < 2^27).
+__device__ __forceinline__ int piece_start(int q, int tiles, int k) { return q * tiles / k; }
 
 // Virtual tiles of one unit of a row with `tiles` real tiles.
 __device__ __forceinline__ long long unit_span(int tiles, int cost) { return tiles > 0 ? tiles + cost : 0; }
@@ -139,15 +164,16 @@ __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int la
   for (int base = 0; base < s.B; base += 32) {
     const int b = base + lane;
     long long t = 0;
+    int tu = 0;
     bool zero_mine = false;
     if (b < s.B) {
       const int Lstored = (SPECULATIVE || s.spec) ? *(volatile const int32_t *)(s.seq_lens + b) : __ldg(s.seq_lens + b);
       const bool appends = s.append && append_ok(Lstored, s.Nmax);
       const int Lraw = appends ? Lstored + 1 : Lstored;
       const int L = clamp_len(Lraw, s.Nmax);
-      t = (long long)((L + s.block_n - 1) / s.block_n) * s.units_per_b;
+      tu = (L + s.block_n - 1) / s.block_n;
+      t = (long long)tu * s.units_per_b;
       const bool mine = (b % gridDim.x) == c;
-      const int tu = (L + s.block_n - 1) / s.block_n;
       if (tu > 0) {
         tmin = min(tmin, tu);
         tmax = max(tmax, tu);
@@ -164,17 +190,14 @@ __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int la
       uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(out) + (size_t)(base + src) * row_bytes);
       for (size_t i = lane; i < row_bytes / 16; i += 32) o[i] = make_uint4(0, 0, 0, 0);
     }
-    if (base == 0) keep0 = (int)(t / s.units_per_b);
-    if (base == 32) keep1 = (int)(t / s.units_per_b);
-    const long long incl = warp_incl_scan(t, lane);
-    T += __shfl_sync(0xffffffffu, incl, 31);
+    if (base == 0) keep0 = tu;
+    if (base == 32) keep1 = tu;
+    T += warp_sum(t);
   }
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    tmin = min(tmin, __shfl_xor_sync(0xffffffffu, tmin, off));
-    tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
-    rows += __shfl_xor_sync(0xffffffffu, rows, off);
-  }
+  // warp-wide reductions, one instruction each (all values are >= 0)
+  tmin = (int)__reduce_min_sync(0xffffffffu, (unsigned)tmin);
+  tmax = (int)__reduce_max_sync(0xffffffffu, (unsigned)tmax);
+  rows = (int)__reduce_add_sync(0xffffffffu, (unsigned)rows);
   const bool uniform = rows > 0 && tmin == tmax;
   CtaRange r;
   r.b = 0;
@@ -189,15 +212,15 @@ __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int la
     // charge.  A CTA with an empty piece still takes part in its cluster's
     // merge; r.b, r.pre_b and r.tiles_b then still name the unit.
     const int k = s.cluster_k;
-    const long long u = c / k;
-    const int q = c % k;
+    const int u = c / k;
+    const int q = c - u * k;
     r.T = T;
     r.P = rows * s.units_per_b * k;
     r.cost = 0;
     r.begin = r.end = T;
-    if (u >= (long long)rows * s.units_per_b) return r;  // a cluster with no unit: idle
+    if ((long long)u >= (long long)rows * s.units_per_b) return r;  // a cluster with no unit: idle
     r.cl = 1;
-    const int nr = (int)(u / s.units_per_b), uib = (int)(u % s.units_per_b);
+    const int nr = u / s.units_per_b, uib = u - nr * s.units_per_b;
     long long acc = 0;
     int seen = 0;  // non-empty rows before this chunk
     for (int base = 0; base < s.B; base += 32) {
@@ -215,8 +238,8 @@ __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int la
         r.pre_b = acc + __shfl_sync(0xffffffffu, incl - t, src);
         r.tiles_b = __shfl_sync(0xffffffffu, tu, src);
         const long long u0 = r.pre_b + (long long)uib * r.tiles_b;
-        r.begin = u0 + (long long)q * r.tiles_b / k;
-        r.end = u0 + (long long)(q + 1) * r.tiles_b / k;
+        r.begin = u0 + piece_start(q, r.tiles_b, k);
+        r.end = u0 + piece_start(q + 1, r.tiles_b, k);
         return r;
       }
       seen += __popc(nem);
@@ -287,8 +310,16 @@ struct SegmentCursor {
         span = unit_span(tiles_b, cost);
       }
       const long long off = pos - pre_b;
-      const int uib = (int)(off / span);
-      const int v0 = (int)(off % span);
+      // (32-bit division whenever the values allow: a 64-bit one is a long
+      // software sequence, and this runs on every warp's start-up path)
+      int uib, v0;
+      if (off < 0x7fffffffLL && span < 0x7fffffffLL) {
+        uib = (int)off / (int)span;
+        v0 = (int)off - uib * (int)span;
+      } else {
+        uib = (int)(off / span);
+        v0 = (int)(off % span);
+      }
       const long long left = end - pos;
       const int v1 = left < span - v0 ? v0 + (int)left : (int)span;
       pos += v1 - v0;

@@ -209,6 +209,29 @@ __device__ __forceinline__ void soft_reduce(float (&v)[C::HG], int grp, int sub,
   soft_bar(grp);
 }
 
+// Per-head maximum of v (group grp's HG heads) over the group's 128 threads:
+// one warp-wide redux per head (every lane gets its warp's maximum), lane 0
+// of each warp stores its warp's HG maxima, and thread R < HG combines the
+// four warps'; afterwards every thread of the group can read the maximum of
+// its head h from fin[grp*HG + h].  Exact (a maximum does not depend on the
+// order); NaN inputs are ignored as by fmaxf.
+template <class C>
+__device__ __forceinline__ void soft_reduce_max(float (&v)[C::HG], int grp, int sub, int lane, float *red, float *fin,
+                                                int R) {
+  constexpr int HG = C::HG;
+#pragma unroll
+  for (int h = 0; h < HG; ++h) asm volatile("redux.sync.max.f32 %0, %0, 0xffffffff;" : "+f"(v[h]));
+  float *rg = red + grp * 4 * HG;
+  if (lane == 0) {
+#pragma unroll
+    for (int h = 0; h < HG; h += 4)
+      *reinterpret_cast<float4 *>(rg + sub * HG + h) = make_float4(v[h], v[h + 1], v[h + 2], v[h + 3]);
+  }
+  soft_bar(grp);
+  if (R < HG) fin[grp * HG + R] = fmaxf(fmaxf(rg[R], rg[HG + R]), fmaxf(rg[2 * HG + R], rg[3 * HG + R]));
+  soft_bar(grp);
+}
+
 // 4x4 transpose across the four lanes of each quad (lanes 4k..4k+3): lane j
 // of a quad holds v[i] = M[j][i] before and v[i] = M[i][j] after (two
 // butterfly stages, each swapping one pair of values with the partner lane).
@@ -242,9 +265,14 @@ __device__ __forceinline__ void merge_cluster_unit(const SplitParams &p, const C
   const int k = p.cluster_k;
   const int r = (int)cluster_rank();
   const int c0 = (int)blockIdx.x - r;
-  // the unit, from the range (a CTA with an empty piece has no segment)
+  // the unit, from the range (a CTA with an empty piece has no segment);
+  // piece j is empty when it starts where piece j + 1 does
   const int tiles = range.tiles_b;
-  const int uib = (int)((range.begin - range.pre_b) / tiles);
+  const long long uoff = range.begin - range.pre_b;
+  const int uib = uoff < 0x7fffffffLL ? (int)uoff / tiles : (int)(uoff / tiles);
+  bool has[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) has[j] = j < k && piece_start(j + 1, tiles, k) > piece_start(j, tiles, k);
   const int b = range.b, g = uib / p.head_chunks, hc = uib % p.head_chunks;
   const int h_first = g * p.n_rep + hc * p.heads_per_cta;
   const int nh = min(p.heads_per_cta, p.n_rep - hc * p.heads_per_cta);
@@ -257,7 +285,7 @@ __device__ __forceinline__ void merge_cluster_unit(const SplitParams &p, const C
     float4 oj[KMAX][SEG / 4];
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
-      if (j < k && (long long)(j + 1) * tiles / k > (long long)j * tiles / k) {
+      if (has[j]) {
         const size_t ps = (size_t)2 * (c0 + j) * p.heads_per_cta + h;
         mlj[j] = __ldcg(ml + ps);
         const float4 *o = reinterpret_cast<const float4 *>(p.o_part + ps * D + d0);
@@ -268,15 +296,15 @@ __device__ __forceinline__ void merge_cluster_unit(const SplitParams &p, const C
     float M = -INFINITY;
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
-      if (!(j < k && (long long)(j + 1) * tiles / k > (long long)j * tiles / k)) mlj[j] = make_float2(-INFINITY, 0.f);
-      if (j < k) M = fmaxf(M, mlj[j].x);
+      if (!has[j]) mlj[j] = make_float2(-INFINITY, 0.f);
+      M = fmaxf(M, mlj[j].x);
     }
     float L = 0.f, a[SEG];
 #pragma unroll
     for (int e = 0; e < SEG; ++e) a[e] = 0.f;
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
-      if (j < k && mlj[j].x != -INFINITY) {
+      if (has[j]) {
         const float w = merge_weight(mlj[j].x, M);
         L += w * mlj[j].y;
 #pragma unroll
@@ -378,6 +406,21 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     spx.spec = 1;
     const CtaRange r0 = warp_plan_range<true>(spx, lane, nullptr, 0);
     if (lane == 0 && r0.begin < r0.end) prefetch_first_tiles(spx, r0, &tmK, &tmV, C::FP8 ? 128 : 64, C::FP8 ? 1 : 2, p.G, p.head_chunks, ST);
+    if (!MULTI && r0.begin < r0.end) {
+      // and for the query rows of the first unit (a hint too: the copy
+      // after the wait still reads global memory)
+      SegmentCursor c0;
+      c0.init(spx, r0);
+      Segment s0;
+      if (c0.next(spx, s0)) {
+        const int g = s0.uib / p.head_chunks, hc = s0.uib % p.head_chunks;
+        const int hf = g * p.n_rep + hc * p.heads_per_cta;
+        const int nh = min(p.heads_per_cta, p.n_rep - hc * p.heads_per_cta);
+        const char *qb = reinterpret_cast<const char *>(p.q) + ((size_t)s0.b * p.H + hf) * D * 2;
+        for (int ln = lane; ln < nh * D * 2 / 128; ln += 32)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(qb + (size_t)ln * 128));
+      }
+    }
   }
   griddep_wait();  // lengths, q and cache rows written by earlier kernels are visible
   if (warp == 0) {
@@ -697,7 +740,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 for (int h = 0; h < HG; ++h) x[h] = __uint_as_float(r[h]) * sl2;
               }
               mask(x);
-              soft_reduce<C, true>(x, grp, sub, lane, red, fin, R);
+              soft_reduce_max<C>(x, grp, sub, lane, red, fin, R);
             }
             bool moved_mine = false;
             if (R < HG) {
@@ -711,8 +754,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               corr_s[hg0 + R] = corr;
             }
             const bool moved = soft_bar_or(grp, moved_mine);
+            if (i > 0) {  // (on a unit's first tile the sums are still 0)
 #pragma unroll
-            for (int h = 0; h < HG; ++h) lp[h] *= corr_s[hg0 + h];
+              for (int h = 0; h < HG; ++h) lp[h] *= corr_s[hg0 + h];
+            }
             compute_y(y);  // against the moved maxima
             if (i > 0 && moved) {
               // O^T holds P.V of the unit's tiles so far: rescale it once the

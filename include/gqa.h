@@ -340,6 +340,28 @@ int mha_to_gqa_meanpool(const void *w, void *w_out, int H, int G, int d, int D,
                         gqa_dtype_t dtype, cudaStream_t stream);
 
 /*
+ * gqa_set_workspace_allocator — where the calls that get their own workspace
+ * (gqa_decode_attention, gqa_decode_step, gqa_decode_attention_multi,
+ * gqa_decode_attention_fp8, gqa_qkv_project) take it from.  An integration
+ * hook with no counterpart in the pages: by default each such call takes its
+ * split scratch from the stream-ordered allocator (cudaMallocAsync, released
+ * with cudaFreeAsync after its kernels are enqueued); a serving engine that
+ * manages device memory itself installs its pool here.
+ *   alloc(ctx, &ptr, bytes, stream): returns 0 and a device pointer (256-byte
+ *     aligned) valid for work ordered after it on `stream`; anything else is
+ *     a failure, and the call then returns GQA_ERR_NO_MEMORY with nothing
+ *     enqueued.
+ *   free_fn(ctx, ptr, stream): releases ptr once the work enqueued on `stream`
+ *     so far has finished (stream-ordered, as cudaFreeAsync).
+ * Both NULL restores the default; exactly one NULL is GQA_ERR_INVALID_ARG.
+ * Process-wide: set it while no call is running on another thread.  The
+ * _ws / _ex calls, which take the caller's workspace, never use it.
+ */
+typedef int (*gqa_alloc_fn)(void *ctx, void **ptr, size_t bytes, cudaStream_t stream);
+typedef void (*gqa_free_fn)(void *ctx, void *ptr, cudaStream_t stream);
+int gqa_set_workspace_allocator(gqa_alloc_fn alloc, gqa_free_fn free_fn, void *ctx);
+
+/*
  * gqa_stream_read — a measurement utility with no counterpart in the pages:
  * the read-only streaming ceiling that the decode kernels' HBM rates are
  * judged against (a decode call reads its K/V bytes once and writes almost

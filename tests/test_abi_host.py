@@ -167,3 +167,47 @@ def test_projection_workspace(lib):
     assert lib.gqa_qkv_project_workspace_bytes(4, 100, 8, 2, 128) == 0   # A % 64 != 0
     args = (FAKE,) * 7 + (4, 256, 8, 2, 128, 1)
     assert lib.gqa_qkv_project_ws(*args, None, 0, None) == -1
+
+
+ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t,
+                            ctypes.c_void_p)
+FREE_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p)
+
+
+def test_workspace_allocation_failure_returns_no_memory(lib):
+    """A workspace allocator that fails (installed through the hook) makes
+    every allocating call return GQA_ERR_NO_MEMORY before anything is
+    enqueued: the freer is never called and no launch is attempted (fake
+    pointers would fail any launch with another status)."""
+    asked, freed = [], []
+
+    @ALLOC_FN
+    def failing(ctx, ptr, nbytes, stream):
+        asked.append(int(nbytes))
+        return 1
+
+    @FREE_FN
+    def free_(ctx, ptr, stream):
+        freed.append(ptr)
+
+    assert lib.gqa_set_workspace_allocator(ctypes.cast(failing, ctypes.c_void_p),
+                                           ctypes.cast(free_, ctypes.c_void_p), None) == 0
+    try:
+        B, H, G, d, N = 2, 8, 2, 128, 4096
+        assert _attn(lib, B=B, H=H, G=G, d=d, N=N) == -4
+        assert asked[-1] == lib.gqa_decode_workspace_bytes(B, H, G, d, N, 1)
+        assert lib.gqa_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, FAKE, B, H, G, d, N, 1, None) == -4
+        assert lib.gqa_decode_attention_multi(FAKE, FAKE, FAKE, FAKE, 0.1, FAKE, B, 4, H, G, d, N, 1, None) == -4
+        assert lib.gqa_qkv_project(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 8, 2, 128, 1, None) == -4
+        assert len(asked) == 4 and all(n > 0 for n in asked)
+        assert freed == []
+    finally:
+        assert lib.gqa_set_workspace_allocator(None, None, None) == 0
+
+
+def test_workspace_allocator_hook_rejects_half_a_pair(lib):
+    @ALLOC_FN
+    def a(ctx, ptr, nbytes, stream):
+        return 1
+    assert lib.gqa_set_workspace_allocator(ctypes.cast(a, ctypes.c_void_p), None, None) == -1
+    assert lib.gqa_set_workspace_allocator(None, None, None) == 0
