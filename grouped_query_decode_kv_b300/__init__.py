@@ -48,11 +48,11 @@ __all__ = [
     "gqa_decode_attention_multi", "gqa_decode_attention_multi_ex",
     "gqa_qkv_project", "gqa_qkv_project_ws", "gqa_qkv_project_workspace_bytes",
     "gqa_decode_attention_fp8", "gqa_decode_attention_fp8_ws", "gqa_decode_workspace_bytes_fp8", "kv_append_fp8",
-    "DEVERR_ATTN_LEN", "DEVERR_APPEND_LEN", "DEVERR_TIMEOUT", "DEVERR_RANGE", "EXPORTED_SYMBOLS",
+    "DEVERR_ATTN_LEN", "DEVERR_APPEND_LEN", "DEVERR_TIMEOUT", "DEVERR_RANGE", "DEVERR_BOUNDS", "EXPORTED_SYMBOLS",
 ]
 
 GQA_F32, GQA_BF16 = 0, 1
-DEVERR_ATTN_LEN, DEVERR_APPEND_LEN, DEVERR_TIMEOUT, DEVERR_RANGE = 1, 2, 4, 8
+DEVERR_ATTN_LEN, DEVERR_APPEND_LEN, DEVERR_TIMEOUT, DEVERR_RANGE, DEVERR_BOUNDS = 1, 2, 4, 8, 16
 ERR_SCRATCH_LIMIT = -5
 NOALLOC_SCRATCH_BYTES = 32 << 20  # GQA_NOALLOC_SCRATCH_BYTES in include/gqa.h
 
@@ -68,7 +68,9 @@ EXPORTED_SYMBOLS = (
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_HERE, "libgqa.so")
+# GQA_LIBRARY selects another build of the library (the checking build
+# libgqa_debug.so, say); by default the release build next to this file.
+_LIB_PATH = os.environ.get("GQA_LIBRARY") or os.path.join(_HERE, "libgqa.so")
 _lock = threading.Lock()
 _lib = None
 

@@ -23,6 +23,20 @@ constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;
 
 __device__ __forceinline__ void flag_error(int bits) { atomicOr(&g_device_error, bits); }
 
+// Bounds checks of the checking build (GQA_DEBUG): `if (in_bounds(i < n))`
+// guards a global access; a false condition sets GQA_DEVERR_BOUNDS and the
+// access is skipped (never a trap).  In the release build the condition is
+// not evaluated and the guard folds away.
+#ifdef GQA_DEBUG
+__device__ __forceinline__ bool in_bounds(bool ok) {
+  if (!ok) flag_error(GQA_DEVERR_BOUNDS);
+  return ok;
+}
+#define GQA_IN_BOUNDS(cond) ::gqa::in_bounds(cond)
+#else
+#define GQA_IN_BOUNDS(cond) true
+#endif
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -115,9 +115,24 @@ cudaError_t launch_split(dim3 grid, int cluster, const CUtensorMap &k, const CUt
 }
 
 // Clusters of `cluster` CTAs of this kernel that can be resident at once (0
-// when the query fails).
+// when the query fails); asked once per device and cluster size.
 template <class C, int F, bool MULTI>
 int max_clusters(int cluster) {
+  static std::mutex mu;
+  static int cache[64][9];  // [device][cluster], 0 = not asked yet, -1 = failed
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || cluster < 1 || cluster > 8) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev][cluster] != 0) return cache[dev][cluster] > 0 ? cache[dev][cluster] : 0;
+  if (cudaFuncSetAttribute(split_kernel_ptr<C, F, MULTI>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::SMEM_BYTES) != cudaSuccess) {
+    cudaGetLastError();
+    cache[dev][cluster] = -1;
+    return 0;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster * 64);
   cfg.blockDim = dim3(C::THREADS);
@@ -130,10 +145,12 @@ int max_clusters(int cluster) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, split_kernel_ptr<C, F, MULTI>(), &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, split_kernel_ptr<C, F, MULTI>(), &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
+    cache[dev][cluster] = -1;
     return 0;
   }
+  cache[dev][cluster] = n;
   return n;
 }
 
@@ -511,6 +528,7 @@ int run_attention(const void *q, const void *k, const void *v, const int32_t *sl
   p.unit_info = merge_in_kernel ? nullptr : reinterpret_cast<int2 *>(book);
   p.epoch = next_epoch();
   p.cluster_k = pl.cluster;
+  p.P = pl.P;
   p.append = app.k_new != nullptr;
   p.k_new = app.k_new;
   p.v_new = app.v_new;

@@ -96,6 +96,7 @@ __device__ __forceinline__ void finish_split_unit(const SplitParams &p, const Se
       a3 += w * o.w;
     }
     const float inv = (!MULTI || L > 0.f) ? 1.f / L : 0.f;  // 0: a query row that sees no position
+    if (!GQA_ROW_OK(p, query_row<MULTI>(p, b, h_first + h))) continue;
     T *dst = reinterpret_cast<T *>(p.out) + query_row<MULTI>(p, b, h_first + h) * D + d0;
     dst[0] = from_float<T>(a0 * inv);
     dst[1] = from_float<T>(a1 * inv);
@@ -193,6 +194,7 @@ __global__ void __launch_bounds__(128) gqa_combine_kernel(const SplitParams p) {
   if (max(0, min(Lraw, p.Nmax)) == 0 || info.y < 0) return;
   const int c_lo = info.x >> 1;
   const int n = info.y - c_lo + 1;  // number of partials
+  if (!GQA_IN_BOUNDS(info.x >= 0 && info.y < p.P && n >= 1) || !GQA_ROW_OK(p, query_row<true>(p, b, h))) return;
   const float2 *ml = reinterpret_cast<const float2 *>(p.ml_part);
   auto slot_of = [&](int k) { return k == 0 ? info.x : 2 * (c_lo + k); };
   float2 mine = make_float2(-INFINITY, 0.f);  // (m, l) of partial `lane`

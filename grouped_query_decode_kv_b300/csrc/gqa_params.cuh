@@ -22,6 +22,7 @@ struct SplitParams {
   // tcgen05 kernel launched in thread-block clusters of cluster_k CTAs (0 or
   // 1: no clusters); see the cluster-aligned plan in gqa_schedule.cuh
   int cluster_k;
+  int P;                    // CTAs of the split kernel (partial slots: 2P)
   // Fused decode step (append != 0): the new token's K/V rows k_new/v_new
   // [B*G, D] go to cache row L_b of every (b, g) before attention over
   // L_b + 1 positions; the last CTA to finish then sets seq_lens[b] = L_b + 1.
@@ -50,6 +51,14 @@ struct SplitParams {
   // FP8 (E4M3) cache: per-KV-head scales [G] of K and V (null otherwise)
   const float *k_scale, *v_scale;
 };
+
+// Checking build: a partial slot and head of the workspace, a row of q /
+// out, a cache row of K/V head bg.
+#define GQA_SLOT_OK(p, slot, h) \
+  GQA_IN_BOUNDS((slot) >= 0 && (slot) < 2 * (p).P && (h) >= 0 && (h) < (p).heads_per_cta)
+#define GQA_ROW_OK(p, row) GQA_IN_BOUNDS((size_t)(row) < (size_t)(p).B * (p).H)
+#define GQA_CACHE_OK(p, bg, n) \
+  GQA_IN_BOUNDS((bg) >= 0 && (bg) < (p).B * (p).G && (n) >= 0 && (n) < (p).Nmax)
 
 // Row (of D elements) of q and out that holds query row v of batch row b.
 // MULTI = false: the kernel was compiled for one token per sequence.

@@ -85,7 +85,7 @@ struct KVPipe {
 // before that load (after a fence.proxy.async for the TMA to see it).
 __device__ __forceinline__ void append_rows(const SplitParams &p, int b, int bg, int lane) {
   const int L = __ldg(p.seq_lens + b);
-  if (!append_ok(L, p.Nmax)) return;
+  if (!append_ok(L, p.Nmax) || !GQA_CACHE_OK(p, bg, L)) return;
   const uint4 *kn = reinterpret_cast<const uint4 *>(p.k_new) + (size_t)bg * p.row_chunks;
   const uint4 *vn = reinterpret_cast<const uint4 *>(p.v_new) + (size_t)bg * p.row_chunks;
   uint4 *kc = reinterpret_cast<uint4 *>(p.k_cache) + ((size_t)bg * p.Nmax + L) * p.row_chunks;

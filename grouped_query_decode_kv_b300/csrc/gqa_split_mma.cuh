@@ -381,12 +381,15 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
         pk.y = pack_bf16x2(a.z * inv, a.w * inv);
         pk.z = pack_bf16x2(c.x * inv, c.y * inv);
         pk.w = pack_bf16x2(c.z * inv, c.w * inv);
-        *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) +
-                                   query_row<MULTI>(p, b, h_first + hl) * D + d0) = pk;
+        if (GQA_ROW_OK(p, query_row<MULTI>(p, b, h_first + hl)))
+          *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) +
+                                     query_row<MULTI>(p, b, h_first + hl) * D + d0) = pk;
       } else {
         float *dst = p.o_part + ((size_t)slot * p.heads_per_cta + hl) * D + d0;
-        *reinterpret_cast<float4 *>(dst) = a;
-        *reinterpret_cast<float4 *>(dst + 4) = c;
+        if (GQA_SLOT_OK(p, slot, hl)) {
+          *reinterpret_cast<float4 *>(dst) = a;
+          *reinterpret_cast<float4 *>(dst + 4) = c;
+        }
       }
     }
     if (!whole)

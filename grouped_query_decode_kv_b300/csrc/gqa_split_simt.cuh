@@ -341,6 +341,7 @@ __global__ void __launch_bounds__(C::THREADS)
       for (int h = 0; h < NH; ++h) {
         if (h >= nh) break;
         const size_t bh = query_row<MULTI>(p, b, h_first + h);
+        if (!(whole ? GQA_ROW_OK(p, bh) : GQA_SLOT_OK(p, slot, h))) continue;
         if (whole) {
           // a row with no visible position (several tokens only) is 0
           float inv = (!MULTI || l_run[h] > 0.f) ? 1.f / l_run[h] : 0.f;

@@ -286,6 +286,7 @@ __device__ __forceinline__ void merge_cluster_unit(const SplitParams &p, const C
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
       if (has[j]) {
+        if (!GQA_SLOT_OK(p, 2 * (c0 + j), h)) continue;
         const size_t ps = (size_t)2 * (c0 + j) * p.heads_per_cta + h;
         mlj[j] = __ldcg(ml + ps);
         const float4 *o = reinterpret_cast<const float4 *>(p.o_part + ps * D + d0);
@@ -321,8 +322,9 @@ __device__ __forceinline__ void merge_cluster_unit(const SplitParams &p, const C
     uint32_t *pw = reinterpret_cast<uint32_t *>(pk);
 #pragma unroll
     for (int e = 0; e < SEG / 2; ++e) pw[e] = pack_bf16x2(a[2 * e] * inv, a[2 * e + 1] * inv);
-    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) +
-                                           query_row<MULTI>(p, b, h_first + h) * D + d0);
+    const size_t orow = query_row<MULTI>(p, b, h_first + h);
+    if (!GQA_ROW_OK(p, orow)) continue;
+    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * D + d0);
     dst[0] = pk[0];
     dst[1] = pk[1];
   }
@@ -577,10 +579,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         int h_first, nh;
         unit_heads(s, h_first, nh);
         const int row = R >> 1, half = R & 1;
-        if (row < NR) {
+        const size_t qrow = query_row<MULTI>(p, s.b, h_first + min(row, nh - 1));
+        if (row < NR && GQA_ROW_OK(p, qrow)) {
           const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(p.q) +
-                                                             query_row<MULTI>(p, s.b, h_first + min(row, nh - 1)) * D +
-                                                             half * 64);
+                                                             qrow * D + half * 64);
           const uint32_t dst = qbase + buf * C::Q_BYTES + half * C::Q_BOX + row * 128;
           const uint32_t bytes = row < nh ? 16u : 0u;
 #pragma unroll
@@ -867,7 +869,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           // 128-byte line, and no transpose is needed)
           float *orow = p.o_part + (size_t)slot * p.heads_per_cta * D + R;
 #pragma unroll 1
-          for (int c0 = 0; c0 < HG; c0 += HCH) {
+          for (int c0 = 0; c0 < (GQA_SLOT_OK(p, slot, nh - 1) ? HG : 0); c0 += HCH) {
             uint32_t r[32];
             if constexpr (HCH == 32) {
               tc::ld_32x32b_x32(trow + C::TM_O + ob * NR + hg0 + c0, r);
@@ -916,12 +918,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 uint2 pk;
                 pk.x = pack_bf16x2(seen ? v[0] / f : 0.f, seen ? v[1] / f : 0.f);
                 pk.y = pack_bf16x2(seen ? v[2] / f : 0.f, seen ? v[3] / f : 0.f);
-                *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * D + d4) = pk;
+                if (GQA_ROW_OK(p, orow))
+                  *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * D + d4) = pk;
               }
             }
           }
         }
-        if (!whole && R < HG && hg0 + R < nh)
+        if (!whole && R < HG && hg0 + R < nh && GQA_SLOT_OK(p, slot, hg0 + R))
           reinterpret_cast<float2 *>(p.ml_part)[(size_t)slot * p.heads_per_cta + hg0 + R] =
               make_float2(mR, fin[hg0 + R]);
         // merge kernel (no cluster launch): where the unit's partials are

@@ -62,6 +62,9 @@ typedef enum {
 #define GQA_DEVERR_TIMEOUT 4    /* a pipeline wait gave up after its time limit */
 #define GQA_DEVERR_RANGE 8      /* FP8 cache, groups of 8+ heads: a query value beyond the f16
                                    range (|q| > 65504) of that path's tensor-core operands */
+#define GQA_DEVERR_BOUNDS 16    /* only in the checking build (libgqa_debug.so, compiled with
+                                   GQA_DEBUG): an index outside its buffer was computed; the
+                                   access was skipped.  The release library never sets it. */
 
 /*
  * gqa_decode_attention — attention of one decode token per sequence.
