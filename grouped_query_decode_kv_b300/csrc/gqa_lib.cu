@@ -190,10 +190,11 @@ using TcD128x64 = TcCfg<64, 3, 1>;
 // GQA-8 with 4 tokens, B=16, Nmax=8192 ragged: 70.9 -> 64.7 us per call; for
 // one token the second group did not pay)
 using TcD128x32Multi = TcCfg<32, 3, 2, false, 2>;
-// FP8 cache: 2 stages of 32 KB codes plus two 64 KB bf16 staging tiles
-using TcFp8x16 = TcCfg<16, 2, 2, true>;
-using TcFp8x32 = TcCfg<32, 2, 2, true>;
-using TcFp8x64 = TcCfg<64, 2, 1, true>;
+// FP8 cache: stages of 32 KB of codes (K and V of 128 positions), two or
+// three 32 KB f16 V staging tiles (the f16 K tiles are in tensor memory)
+using TcFp8x16 = TcCfg<16, 3, 2, true, 1, 3>;
+using TcFp8x32 = TcCfg<32, 3, 2, true, 1, 3>;
+using TcFp8x64 = TcCfg<64, 3, 1, true>;
 
 template <bool M>
 KernelChoice choose_kernel(gqa_dtype_t dt, int d, int n_rep) {

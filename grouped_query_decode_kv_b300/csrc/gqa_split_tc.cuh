@@ -49,11 +49,15 @@
 namespace gqa {
 
 // FP8_: the cache holds E4M3 codes; four more warps convert each landed
-// tile to f16 (exact) in a double-buffered staging area that the MMAs read,
-// and Q and P are f16 too (one operand type per MMA).
-template <int NR_, int STAGES_, int PB_, bool FP8_ = false, int SG_ = 1>
+// tile to f16 (exact): the K tile into tensor memory, where the S^T MMA
+// reads it as its A operand, the V tile into a double-buffered shared-memory
+// staging area that the P.V MMA reads; Q and P are f16 too (one operand type
+// per MMA).
+template <int NR_, int STAGES_, int PB_, bool FP8_ = false, int SG_ = 1, int VSTG_ = 2>
 struct TcCfg {
   static constexpr bool FP8 = FP8_;
+  static constexpr int VSTG = VSTG_;  // FP8: f16 V staging buffers
+  static_assert(VSTG >= 2 && VSTG <= 3, "V staging buffers");
   static constexpr int D = 128;
   static constexpr int BLOCK_N = 128;  // positions per tile: M of S^T, K of P.V
   static constexpr int STAGES = STAGES_;
@@ -74,15 +78,19 @@ struct TcCfg {
   static constexpr int CONV_WARP0 = 2 + 4 * SG;  // first FP8 converter warp
   static constexpr int THREADS = (CONV_WARP0 + (FP8 ? 4 : 0)) * 32;
   static constexpr int KV_BOX = BLOCK_N * 128;  // one 128-byte-wide box of a bf16 K or V tile
-  // FP8: staging [2] x (K tile | V tile) in f16, two boxes each (d 0-63, 64-127)
+  // FP8: V staging [2] in f16, two boxes each (d 0-63, 64-127); the f16 K
+  // tiles live in tensor memory
   static constexpr int STG_OFF = Pipe::PIPE_BYTES;
   static constexpr int STG_TILE = 2 * KV_BOX;
-  static constexpr int STG_BYTES = FP8 ? 2 * 2 * STG_TILE : 0;
+  static constexpr int STG_BYTES = FP8 ? VSTG * STG_TILE : 0;
   static constexpr int SOFT = 128;             // threads of one softmax group
-  // TMEM columns: S^T buffers [0, 2*NR), O^T buffers [2*NR, 4*NR)
+  // TMEM columns: S^T buffers [0, 2*NR), O^T buffers [2*NR, 4*NR); FP8: two
+  // f16 K tiles [4*NR, 4*NR + 128) (lane = position, 64 columns of f16 pairs)
   static constexpr int TM_S = 0;
   static constexpr int TM_O = 2 * NR;
-  static constexpr int TM_COLS = 4 * NR < 32 ? 32 : 4 * NR;  // 64, 128 or 256: a power of two
+  static constexpr int TM_K = 4 * NR;
+  static constexpr int TM_USED = 4 * NR + (FP8 ? 128 : 0);
+  static constexpr int TM_COLS = TM_USED <= 32 ? 32 : TM_USED <= 64 ? 64 : TM_USED <= 128 ? 128 : TM_USED <= 256 ? 256 : 512;
   // shared memory
   // Q: two 128-byte-wide boxes (d 0-63, 64-127) of NR rows per buffer; two
   // buffers where shared memory allows, so that the next unit's Q lands
@@ -98,8 +106,8 @@ struct TcCfg {
   static constexpr int P_SWZ_SHIFT = NR == 64 ? 0 : (NR == 32 ? 1 : 2);
   static constexpr int P_SWZ_MASK = NR == 64 ? 7 : (NR == 32 ? 3 : 1);
   // pipe full[STAGES], empty[STAGES]; then s_full[2], s_free[2], p_full[2],
-  // pv_done[2], o_free[2], q_full[2], mma_done; FP8: conv_full[2], stg_free[2]
-  static constexpr int NBAR = 2 * STAGES + 13 + (FP8 ? 4 : 0);
+  // pv_done[2], o_free[2], q_full[2], mma_done; FP8: conv_full[2], stg_free[3]
+  static constexpr int NBAR = 2 * STAGES + 13 + (FP8 ? 5 : 0);
   static constexpr int RANGE_BYTES = ((int)sizeof(CtaRange) + 7) / 8 * 8;
   static constexpr int TAIL_BYTES = 4 * NQ * 4 + 3 * NQ * 4 + NBAR * 8 + 8 + RANGE_BYTES + (int)sizeof(UnitMerge);
   static constexpr int QB = 1024 + Q_OFF + 2 * Q_BYTES + PB * P_BYTES + TAIL_BYTES <= 227 * 1024 ? 2 : 1;
@@ -386,10 +394,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     mbar_init(bars.q_full(1), 4);
     mbar_init(bars.mma_done(), 1);
     if (C::FP8) {
-      for (int i = 0; i < 2; ++i) {
-        mbar_init(bars.conv_full(i), 4);  // one arrival per converter warp
-        mbar_init(bars.stg_free(i), 1);   // the MMA commit after the tile's P.V
-      }
+      for (int i = 0; i < 2; ++i) mbar_init(bars.conv_full(i), 4);  // one arrival per converter warp
+      for (int i = 0; i < C::VSTG; ++i) mbar_init(bars.stg_free(i), 1);  // the MMA commit after the tile's P.V
     }
     fence_barrier_init();
   }
@@ -489,13 +495,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if ((ws.i != 0 || mbar_test(bars.q_full(qb), qpar)) && k_ready &&
                 (tg < 2 || mbar_test(bars.s_free(tg & 1), ((tg >> 1) - 1) & 1))) {
               tc::fence_after();
-              const uint32_t kt = C::FP8 ? pipe.base + C::STG_OFF + (tg & 1) * 2 * C::STG_TILE : pipe.k_tile(st);
-              const uint32_t qt = qbase + qb * C::Q_BYTES;
+              // descriptors of the tile's first K step; the others are
+              // constant offsets from them (one add each)
+              const uint64_t b0 = tc::smem_desc_sw128(qbase + qb * C::Q_BYTES, 16, 1024);
+              const uint64_t a0 = C::FP8 ? 0 : tc::smem_desc_sw128(pipe.k_tile(st), 16, 1024);
+              const uint32_t dS = tmem + C::TM_S + (tg & 1) * NR;
 #pragma unroll
               for (int ks = 0; ks < D / 16; ++ks) {
-                const uint64_t a = tc::smem_desc_sw128(kt + (ks >> 2) * C::KV_BOX + (ks & 3) * 32, 16, 1024);
-                const uint64_t b = tc::smem_desc_sw128(qt + (ks >> 2) * C::Q_BOX + (ks & 3) * 32, 16, 1024);
-                tc::mma_ss(tmem + C::TM_S + (tg & 1) * NR, a, b, IDESC_S, ks > 0);
+                const uint64_t b = tc::desc_add(b0, (ks >> 2) * C::Q_BOX + (ks & 3) * 32);
+                if constexpr (C::FP8) {
+                  // A = the f16 K tile in tensor memory: 16 K elements = 8 columns
+                  tc::mma_ts(dS, tmem + C::TM_K + (tg & 1) * 64 + ks * 8, b, IDESC_S, ks > 0);
+                } else {
+                  tc::mma_ss(dS, tc::desc_add(a0, (ks >> 2) * C::KV_BOX + (ks & 3) * 32), b, IDESC_S, ks > 0);
+                }
               }
               tc::commit(bars.s_full(tg & 1));
               ws.advance(sp);
@@ -509,16 +522,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 (wp.i != 0 || wp.unit < 2 || mbar_test(bars.o_free(ob), ((wp.unit >> 1) - 1) & 1))) {
               tc::fence_after();
               const uint32_t vt =
-                  C::FP8 ? pipe.base + C::STG_OFF + (tg & 1) * 2 * C::STG_TILE + C::STG_TILE : pipe.v_tile(tg % ST);
+                  C::FP8 ? pipe.base + C::STG_OFF + (tg % C::VSTG) * C::STG_TILE : pipe.v_tile(tg % ST);
+              const uint64_t a0 = tc::smem_desc_sw128(vt, C::KV_BOX, 1024);
+              const uint64_t b0 = tc::smem_desc_mn_rows(pbase + pb * C::P_BYTES, C::P_ROW);
+              const uint32_t dO = tmem + C::TM_O + ob * NR;
 #pragma unroll
-              for (int ks = 0; ks < BN / 16; ++ks) {
-                const uint64_t a = tc::smem_desc_sw128(vt + ks * 2048, C::KV_BOX, 1024);
-                const uint64_t b = tc::smem_desc_mn_rows(pbase + pb * C::P_BYTES + ks * 16 * C::P_ROW, C::P_ROW);
-                tc::mma_ss(tmem + C::TM_O + ob * NR, a, b, IDESC_PV, wp.i > 0 || ks > 0);
-              }
+              for (int ks = 0; ks < BN / 16; ++ks)
+                tc::mma_ss(dO, tc::desc_add(a0, ks * 2048), tc::desc_add(b0, ks * 16 * C::P_ROW), IDESC_PV,
+                           wp.i > 0 || ks > 0);
               // the tile's K and V are no longer read: free its ring stage
               // (FP8: its staging buffer; the converters free the stage)
-              tc::commit(C::FP8 ? bars.stg_free(tg & 1) : pipe.empty(tg % ST));
+              tc::commit(C::FP8 ? bars.stg_free(tg % C::VSTG) : pipe.empty(tg % ST));
               tc::commit(bars.pv_done(pb));
               wp.advance(sp);
               progressed = true;
@@ -527,17 +541,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           if (progressed) {
             idle_since = 0;
           } else {
-            // Nothing ready: sleep on the barrier most likely to complete
-            // next (the P^T the P.V walk needs, else the K tile the S^T walk
-            // needs), so that the thread wakes the moment it does and leaves
-            // the issue slots to the softmax warp on this sub-partition.
-            if (wp.tg < ws.tg)
-              mbar_try_wait_hint(bars.p_full(wp.tg % C::PB), (wp.tg / C::PB) & 1, 1000);
-            else if (ws.has)
-              mbar_try_wait_hint(C::FP8 ? bars.conv_full(ws.tg & 1) : pipe.full(ws.tg % ST),
-                                 C::FP8 ? (ws.tg >> 1) & 1 : (ws.tg / ST) & 1, 1000);
-            else
-              __nanosleep(32);
+            // Nothing ready: a short sleep, then both walks test their
+            // barriers again, so that the thread leaves the issue slots to
+            // the warps on this sub-partition yet neither walk waits on the
+            // other (a sleep on the P^T barrier alone, in mbarrier.try_wait
+            // with a suspend hint, delayed the next tile's S^T until the
+            // softmax of the previous one was done)
+            __nanosleep(40);
             const unsigned long long now = global_timer_ns();
             if (idle_since == 0) {
               idle_since = now;
@@ -938,12 +948,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       }
     } else if constexpr (C::FP8) {
       // ------------------------------------------------------------ FP8 converters
-      // Thread R converts position R of every tile: its K and V rows of 128
-      // E4M3 codes (one 128-byte swizzled row as TMA landed it) become two
-      // 128-byte swizzled rows of f16 in the tile's staging buffer; rows at
-      // or past L become zeros (their codes may be NaN, and 0 * NaN = NaN in
-      // the P.V MMA).
-      const int R = 32 * (warp - C::CONV_WARP0) + lane;
+      // Thread R converts position R of every tile (R = the TMEM lane its
+      // warp may access): its K row of 128 E4M3 codes (one 128-byte swizzled
+      // row as TMA landed it) becomes 64 f16 pairs in TMEM lane R of the
+      // tile's K buffer, the A operand of S^T; its V row becomes two 128-byte
+      // swizzled rows of f16 in the tile's V staging buffer, zeros at or past
+      // L (the codes there may be NaN, and 0 * NaN = NaN in the P.V MMA; a
+      // NaN logit is masked by the softmax, so K rows need no clearing).
+      // K buffer tg & 1 is free once the S^T of tile tg - 2 has completed,
+      // V buffer tg % VSTG once the P.V of tile tg - VSTG has.
+      const int R = 32 * (warp & 3) + lane;
+      const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
       SegmentCursor cur;
       cur.init(sp, range);
       Segment seg;
@@ -954,44 +969,63 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         for (int t = seg.t0; t < seg.t1; ++t, ++tg) {
           const int st = tg % ST, cb = tg & 1;
           if (!dead && !warp_wait(pipe.full(st), (tg / ST) & 1)) dead = true;
-          if (tg >= 2 && !dead && !warp_wait(bars.stg_free(cb), ((tg >> 1) - 1) & 1)) dead = true;
-          const bool valid = t * BN + R < L;
-          const uint32_t stg = pipe.base + C::STG_OFF + cb * 2 * C::STG_TILE;
+          // the codes of this position go to registers first, so that the
+          // ring stage is released before the conversion (the producer's
+          // next copy into it then overlaps the conversion)
+          uint4 kw[8], vw[8];
 #pragma unroll
-          for (int kv = 0; kv < 2; ++kv) {
-            const uint32_t src = kv == 0 ? pipe.k_tile(st) : pipe.v_tile(st);
-            const uint32_t dst = stg + kv * C::STG_TILE;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {  // 16 codes -> 16 f16 (two 16-byte chunks)
-              uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-              if (valid) {
-                const uint4 w = lds128(swz128(src, R, c));
-                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-                uint32_t o[8];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  o[2 * i] = e4m3x2_to_f16x2(ww[i] & 0xffffu);
-                  o[2 * i + 1] = e4m3x2_to_f16x2(ww[i] >> 16);
-                }
-                lo = make_uint4(o[0], o[1], o[2], o[3]);
-                hi = make_uint4(o[4], o[5], o[6], o[7]);
-              }
-              const uint32_t box = dst + (c >> 2) * C::KV_BOX;
-              const int k0 = 2 * (c & 3);
-              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(swz128(box, R, k0)), "r"(lo.x), "r"(lo.y),
-                           "r"(lo.z), "r"(lo.w)
-                           : "memory");
-              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(swz128(box, R, k0 + 1)), "r"(hi.x),
-                           "r"(hi.y), "r"(hi.z), "r"(hi.w)
-                           : "memory");
-            }
+          for (int c = 0; c < 8; ++c) {
+            kw[c] = lds128(swz128(pipe.k_tile(st), R, c));
+            vw[c] = lds128(swz128(pipe.v_tile(st), R, c));
           }
-          fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(bars.conv_full(cb));
-            mbar_arrive(pipe.empty(st));
+          if (lane == 0) mbar_arrive(pipe.empty(st));
+          if (tg >= 2 && !dead && !warp_wait(bars.s_full(cb), ((tg >> 1) - 1) & 1)) dead = true;
+          {
+            uint32_t kr[64];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {  // 16 codes -> 8 f16 pairs
+              const uint32_t ww[4] = {kw[c].x, kw[c].y, kw[c].z, kw[c].w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                kr[8 * c + 2 * i] = e4m3x2_to_f16x2(ww[i] & 0xffffu);
+                kr[8 * c + 2 * i + 1] = e4m3x2_to_f16x2(ww[i] >> 16);
+              }
+            }
+            tc::st_32x32b_x64(tlane + C::TM_K + cb * 64, kr);
           }
+          const int vb = tg % C::VSTG;
+          if (tg >= C::VSTG && !dead && !warp_wait(bars.stg_free(vb), ((tg / C::VSTG) - 1) & 1)) dead = true;
+          const bool valid = t * BN + R < L;
+          const uint32_t dst = pipe.base + C::STG_OFF + vb * C::STG_TILE;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {  // 16 codes -> 16 f16 (two 16-byte chunks)
+            uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+            if (valid) {
+              const uint32_t ww[4] = {vw[c].x, vw[c].y, vw[c].z, vw[c].w};
+              uint32_t o[8];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                o[2 * i] = e4m3x2_to_f16x2(ww[i] & 0xffffu);
+                o[2 * i + 1] = e4m3x2_to_f16x2(ww[i] >> 16);
+              }
+              lo = make_uint4(o[0], o[1], o[2], o[3]);
+              hi = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+            const uint32_t box = dst + (c >> 2) * C::KV_BOX;
+            const int k0 = 2 * (c & 3);
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(swz128(box, R, k0)), "r"(lo.x), "r"(lo.y),
+                         "r"(lo.z), "r"(lo.w)
+                         : "memory");
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(swz128(box, R, k0 + 1)), "r"(hi.x),
+                         "r"(hi.y), "r"(hi.z), "r"(hi.w)
+                         : "memory");
+          }
+          tc::wait_st();
+          fence_proxy_async_smem();
+          tc::fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars.conv_full(cb));
         }
       }
     }
