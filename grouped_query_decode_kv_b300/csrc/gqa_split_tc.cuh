@@ -32,8 +32,9 @@
 //
 // Warp roles (one CTA per SM):
 //   warp 0     TMA producer of the CTA's stream-K range (gqa_pipeline.cuh)
-//   warp 1     MMA issuer (one thread) and TMEM owner
-//   warps 2..  softmax and output, in SG groups of four (group 0 also
+//   warp 1     S^T MMA issuer (one thread) and TMEM owner
+//   warp 2     P.V MMA issuer (one thread)
+//   warps 3..  softmax and output, in SG groups of four (group 0 also
 //              loads Q); FP8: then four converter warps
 // S^T is double-buffered in TMEM so that S of tile t+1 overlaps the softmax
 // of tile t; O^T is double-buffered across units.  Every mbarrier wait is
@@ -75,7 +76,8 @@ struct TcCfg {
   static_assert(SG == 1 || (SG == 2 && NR >= 32), "two softmax groups need 16+ heads each");
   // one "empty" arrival per tile: the MMA commit (FP8: the 4 converter warps)
   using Pipe = KVPipe<FP8 ? 1 : 2, BLOCK_N, STAGES, FP8 ? 4 : 1>;
-  static constexpr int CONV_WARP0 = 2 + 4 * SG;  // first FP8 converter warp
+  static constexpr int SOFT_WARP0 = 3;            // first softmax warp (after producer, two MMA issuers)
+  static constexpr int CONV_WARP0 = SOFT_WARP0 + 4 * SG;  // first FP8 converter warp
   static constexpr int THREADS = (CONV_WARP0 + (FP8 ? 4 : 0)) * 32;
   static constexpr int KV_BOX = BLOCK_N * 128;  // one 128-byte-wide box of a bf16 K or V tile
   // FP8: V staging [2] in f16, two boxes each (d 0-63, 64-127); the f16 K
@@ -392,7 +394,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     mbar_init(bars.q_full(0), 4);  // one arrival per warp of softmax group 0
     mbar_init(bars.q_full(1), 4);
-    mbar_init(bars.mma_done(), 1);
+    mbar_init(bars.mma_done(), 2);  // the commits of both MMA issuers
     if (C::FP8) {
       for (int i = 0; i < 2; ++i) mbar_init(bars.conv_full(i), 4);  // one arrival per converter warp
       for (int i = 0; i < C::VSTG; ++i) mbar_init(bars.stg_free(i), 1);  // the MMA commit after the tile's P.V
@@ -446,54 +448,39 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (warp == 0) {
       // ------------------------------------------------------------ producer
       produce_range(pipe, sp, range, &tmK, &tmV, C::FP8 ? 128 : 64, p.G, p.head_chunks, p, lane);
-    } else if (warp == 1) {
-      // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 2) {
+      // ------------------------------------------------------------ MMA issuers
+      // Two threads issue the MMAs, each walking the CTA's tiles on its own:
+      // lane 0 of warp 1 the S^T of every tile (once its K tile is ready, its
+      // S buffer free and, on a unit's first tile, the unit's Q in place),
+      // lane 0 of warp 2 the P.V (once its P^T is written and, on a unit's
+      // first tile, its O buffer free).  Issuing a tile's eight MMAs takes
+      // a few hundred nanoseconds; with one thread for both chains the S^T of
+      // the next tile waited behind the P.V of the previous one.  The chains
+      // meet only through the softmax (S -> P), and each commits its own
+      // MMAs to its barriers.
       if (lane == 0) {
         // FP8 cache: all operands are f16 (exact for the E4M3 values)
         constexpr uint32_t IDESC_S =
             C::FP8 ? tc::idesc_f16_f32(BN, NR, false, false) : tc::idesc_bf16_f32(BN, NR, false, false);
         constexpr uint32_t IDESC_PV =
             C::FP8 ? tc::idesc_f16_f32(D, NR, true, true) : tc::idesc_bf16_f32(D, NR, true, true);
-        // Two walks over the CTA's tiles: S^T of tile ts may start once its K
-        // tile landed, its S buffer is free and (first tile of a unit) the
-        // unit's Q is in place; P.V of tile tp once its P is written and
-        // (first tile of a unit) its O buffer is free.  The thread issues
-        // whichever is ready, so that a stage is released as soon as its P.V
-        // is done rather than after the next tile's load.
-        struct Walk {
-          SegmentCursor cur;
-          Segment seg;
-          bool has;
-          int unit, i, tg;
-          __device__ __forceinline__ void start(const SchedParams &s, const CtaRange &r) {
-            cur.init(s, r);
-            has = cur.next(s, seg);
-            unit = i = tg = 0;
-          }
-          __device__ __forceinline__ void advance(const SchedParams &s) {
-            ++tg;
-            if (++i == seg.t1 - seg.t0) {
-              i = 0;
-              ++unit;
-              has = cur.next(s, seg);
-            }
-          }
-        };
-        Walk ws, wp;
-        ws.start(sp, range);
-        wp.start(sp, range);
-        unsigned long long idle_since = 0;
-        while (wp.has) {
-          bool progressed = false;
-          if (ws.has && ws.tg < wp.tg + 2) {
-            const int tg = ws.tg, st = tg % ST;
-            // unit u's Q is in buffer u % QB, its (u / QB)-th use
-            const int qb = ws.unit % C::QB;
-            const uint32_t qpar = (ws.unit / C::QB) & 1;
-            const bool k_ready = C::FP8 ? mbar_test(bars.conv_full(tg & 1), (tg >> 1) & 1)
-                                        : mbar_test(pipe.full(st), (tg / ST) & 1);
-            if ((ws.i != 0 || mbar_test(bars.q_full(qb), qpar)) && k_ready &&
-                (tg < 2 || mbar_test(bars.s_free(tg & 1), ((tg >> 1) - 1) & 1))) {
+        SegmentCursor cur;
+        cur.init(sp, range);
+        Segment seg;
+        int tg = 0;
+        bool ok = true;
+        for (int unit = 0; ok && cur.next(sp, seg); ++unit) {
+          for (int i = 0; ok && i < seg.t1 - seg.t0; ++i, ++tg) {
+            if (warp == 1) {
+              const int st = tg % ST;
+              // unit u's Q is in buffer u % QB, its (u / QB)-th use
+              const int qb = unit % C::QB;
+              ok = (i != 0 || mbar_wait(bars.q_full(qb), (unit / C::QB) & 1)) &&
+                   (C::FP8 ? mbar_wait(bars.conv_full(tg & 1), (tg >> 1) & 1)
+                           : mbar_wait(pipe.full(st), (tg / ST) & 1)) &&
+                   (tg < 2 || mbar_wait(bars.s_free(tg & 1), ((tg >> 1) - 1) & 1));
+              if (!ok) break;
               tc::fence_after();
               // descriptors of the tile's first K step; the others are
               // constant offsets from them (one add each)
@@ -511,15 +498,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
               }
               tc::commit(bars.s_full(tg & 1));
-              ws.advance(sp);
-              progressed = true;
-            }
-          }
-          if (wp.tg < ws.tg) {
-            const int tg = wp.tg, ob = wp.unit & 1;
-            const int pb = tg % C::PB, use = tg / C::PB;
-            if (mbar_test(bars.p_full(pb), use & 1) &&
-                (wp.i != 0 || wp.unit < 2 || mbar_test(bars.o_free(ob), ((wp.unit >> 1) - 1) & 1))) {
+            } else {
+              const int ob = unit & 1, pb = tg % C::PB, use = tg / C::PB;
+              ok = mbar_wait(bars.p_full(pb), use & 1) &&
+                   (i != 0 || unit < 2 || mbar_wait(bars.o_free(ob), ((unit >> 1) - 1) & 1));
+              if (!ok) break;
               tc::fence_after();
               const uint32_t vt =
                   C::FP8 ? pipe.base + C::STG_OFF + (tg % C::VSTG) * C::STG_TILE : pipe.v_tile(tg % ST);
@@ -529,44 +512,25 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
               for (int ks = 0; ks < BN / 16; ++ks)
                 tc::mma_ss(dO, tc::desc_add(a0, ks * 2048), tc::desc_add(b0, ks * 16 * C::P_ROW), IDESC_PV,
-                           wp.i > 0 || ks > 0);
+                           i > 0 || ks > 0);
               // the tile's K and V are no longer read: free its ring stage
               // (FP8: its staging buffer; the converters free the stage)
               tc::commit(C::FP8 ? bars.stg_free(tg % C::VSTG) : pipe.empty(tg % ST));
               tc::commit(bars.pv_done(pb));
-              wp.advance(sp);
-              progressed = true;
-            }
-          }
-          if (progressed) {
-            idle_since = 0;
-          } else {
-            // Nothing ready: a short sleep, then both walks test their
-            // barriers again, so that the thread leaves the issue slots to
-            // the warps on this sub-partition yet neither walk waits on the
-            // other (a sleep on the P^T barrier alone, in mbarrier.try_wait
-            // with a suspend hint, delayed the next tile's S^T until the
-            // softmax of the previous one was done)
-            __nanosleep(40);
-            const unsigned long long now = global_timer_ns();
-            if (idle_since == 0) {
-              idle_since = now;
-            } else if (now - idle_since > kWaitLimitNs) {
-              flag_error(GQA_DEVERR_TIMEOUT);
-              break;
             }
           }
         }
-        // nothing of this thread's may still run when TMEM is freed
+        // nothing of either thread's may still run when TMEM is freed (the
+        // barrier counts both threads' commits)
         tc::commit(bars.mma_done());
         mbar_wait(bars.mma_done(), 0);
       }
       __syncwarp();
-    } else if (warp < C::CONV_WARP0) {
+    } else if (warp < C::CONV_WARP0) {  // (warp >= SOFT_WARP0)
       // ------------------------------------------------------------ softmax
       const int sub = warp & 3;       // TMEM lane quarter of this warp
       const int R = 32 * sub + lane;  // TMEM lane: tile position (S^T) / output dim (O^T)
-      const int grp = C::SG == 1 ? 0 : (warp - 2) >> 2;  // softmax group: head columns [hg0, hg0 + HG)
+      const int grp = C::SG == 1 ? 0 : (warp - C::SOFT_WARP0) >> 2;  // softmax group: head columns [hg0, hg0 + HG)
       const int hg0 = grp * HG;
       const uint32_t trow = tmem + ((uint32_t)(32 * sub) << 16);
       SegmentCursor cur;
@@ -1040,7 +1004,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   // does.
   if (!C::FP8 && range.cl) {
     cluster_sync_all();
-    if (warp >= 2 && warp < C::CONV_WARP0) merge_cluster_unit<C, MULTI>(p, range, threadIdx.x - 64, C::SG * C::SOFT);
+    if (warp >= C::SOFT_WARP0 && warp < C::CONV_WARP0)
+      merge_cluster_unit<C, MULTI>(p, range, threadIdx.x - 32 * C::SOFT_WARP0, C::SG * C::SOFT);
   }
   // ---- teardown: every tcgen05 operation has completed (the MMA thread
   // waited for its last commit); free the tensor memory
