@@ -48,7 +48,6 @@ struct KernelChoice {
   int block_n;
   int heads;
   int box_elems;
-  bool fp8;
   cudaError_t (*launch)(dim3, int, const CUtensorMap &, const CUtensorMap &, const SplitParams &, cudaStream_t);
   int (*clusters)(int);  // max_clusters of the kernel
 };
@@ -169,10 +168,6 @@ KernelChoice make_choice() {
     c.box_elems = C::FP8 ? 128 : 64;
   else
     c.box_elems = 64;
-  if constexpr (F == kTc)
-    c.fp8 = C::FP8;
-  else
-    c.fp8 = false;
   c.launch = &launch_split<C, F, MULTI>;
   c.clusters = &max_clusters<C, F, MULTI>;
   return c;
@@ -340,7 +335,7 @@ Plan make_plan(int B, int H, int G, int d, int Nmax, gqa_dtype_t dt, int split_t
   // in one cluster and merge through distributed shared memory (no
   // workspace round trip, no merge kernel).  The grid keeps whole clusters
   // and no more of them than can be resident at once.
-  if (split_tokens == 0 && pl.k.family == kTc && !pl.k.fp8 && pl.units > 0) {
+  if (split_tokens == 0 && pl.k.family == kTc && pl.units > 0) {
     const long long k = P / pl.units;
     if (k >= 2 && k <= 4) {
       const int resident = pl.k.clusters((int)k);
@@ -509,6 +504,7 @@ int run_attention(const void *q, const void *k, const void *v, const int32_t *sl
   if (!encode_cache_map(&mk, k, dt, d, Nmax, B * G, pl.k.block_n, pl.k.box_elems) ||
       !encode_cache_map(&mv, v, dt, d, Nmax, B * G, pl.k.block_n, pl.k.box_elems))
     return GQA_ERR_CUDA;
+
   if (int rc = ensure_smem_attr(pl.k)) return rc;
   SplitParams p;
   p.q = q;

@@ -831,7 +831,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // cluster plan: the cluster merges the partials of its one unit after
         // the barrier at the end (at most one segment per CTA, always a
         // partial, even when the piece is the whole unit)
-        const bool clm = !C::FP8 && range.cl;
+        const bool clm = range.cl;
         const bool whole = !clm && seg.t0 == 0 && seg.t1 == seg.tiles;
         const int slot = partial_slot(unit);
         const size_t orow_b = MULTI ? (size_t)b * p.tokens * p.heads_q + (size_t)(h_first / p.n_rep) * p.rep_kv
@@ -1002,7 +1002,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   // barrier: nothing is read from the peers' shared memory.  The plan is the
   // same in every CTA, so either every CTA of a cluster comes here or none
   // does.
-  if (!C::FP8 && range.cl) {
+  if (range.cl) {
     cluster_sync_all();
     if (warp >= C::SOFT_WARP0 && warp < C::CONV_WARP0)
       merge_cluster_unit<C, MULTI>(p, range, threadIdx.x - 32 * C::SOFT_WARP0, C::SG * C::SOFT);
