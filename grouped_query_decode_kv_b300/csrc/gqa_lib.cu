@@ -48,7 +48,8 @@ struct KernelChoice {
   int block_n;
   int heads;
   int box_elems;
-  cudaError_t (*launch)(dim3, int, const CUtensorMap &, const CUtensorMap &, const SplitParams &, cudaStream_t);
+  cudaError_t (*launch)(dim3, int, const CUtensorMap &, const CUtensorMap &, const CUtensorMap *,
+                        const SplitParams &, cudaStream_t);
   int (*clusters)(int);  // max_clusters of the kernel
 };
 
@@ -106,11 +107,17 @@ cudaError_t launch_pdl_cluster(void (*kernel)(Params...), dim3 grid, dim3 block,
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// tail[2]: the caches' maps with 16-position boxes (the tcgen05 kernel reads
+// the short last tile of a unit through them; the others take none).
 template <class C, int F, bool MULTI>
-cudaError_t launch_split(dim3 grid, int cluster, const CUtensorMap &k, const CUtensorMap &v, const SplitParams &p,
-                         cudaStream_t st) {
-  return launch_pdl_cluster(split_kernel_ptr<C, F, MULTI>(), grid, dim3(C::THREADS), C::SMEM_BYTES, cluster, st, k,
-                            v, p);
+cudaError_t launch_split(dim3 grid, int cluster, const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap *tail,
+                         const SplitParams &p, cudaStream_t st) {
+  if constexpr (F == kTc)
+    return launch_pdl_cluster(split_kernel_ptr<C, F, MULTI>(), grid, dim3(C::THREADS), C::SMEM_BYTES, cluster, st, k,
+                              v, tail[0], tail[1], p);
+  else
+    return launch_pdl_cluster(split_kernel_ptr<C, F, MULTI>(), grid, dim3(C::THREADS), C::SMEM_BYTES, cluster, st, k,
+                              v, p);
 }
 
 // Clusters of `cluster` CTAs of this kernel that can be resident at once (0
@@ -504,7 +511,10 @@ int run_attention(const void *q, const void *k, const void *v, const int32_t *sl
   if (!encode_cache_map(&mk, k, dt, d, Nmax, B * G, pl.k.block_n, pl.k.box_elems) ||
       !encode_cache_map(&mv, v, dt, d, Nmax, B * G, pl.k.block_n, pl.k.box_elems))
     return GQA_ERR_CUDA;
-
+  CUtensorMap tail[2];
+  if (pl.k.family == kTc && (!encode_cache_map(&tail[0], k, dt, d, Nmax, B * G, 16, pl.k.box_elems) ||
+                             !encode_cache_map(&tail[1], v, dt, d, Nmax, B * G, 16, pl.k.box_elems)))
+    return GQA_ERR_CUDA;
   if (int rc = ensure_smem_attr(pl.k)) return rc;
   SplitParams p;
   p.q = q;
@@ -547,7 +557,7 @@ int run_attention(const void *q, const void *k, const void *v, const int32_t *sl
   p.rep_kv = H / G;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
-  if (pl.k.launch(dim3(pl.P), pl.cluster, mk, mv, p, st) != cudaSuccess) {
+  if (pl.k.launch(dim3(pl.P), pl.cluster, mk, mv, tail, p, st) != cudaSuccess) {
     cudaGetLastError();
     return GQA_ERR_CUDA;
   }

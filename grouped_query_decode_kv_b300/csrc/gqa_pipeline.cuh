@@ -67,6 +67,29 @@ struct KVPipe {
     }
   }
 
+  // The last tile of a unit with only `rows` (< BLOCK_N) cached positions:
+  // ceil(rows / TAIL) boxes of TAIL positions from the short-box maps, so
+  // that the rest of the tile is not read from HBM.  The stage's other rows
+  // keep stale data: the consumers mask those positions (and clear their V
+  // rows), as they do for any position past L.  Returns false (nothing
+  // issued) when the whole box is as cheap.
+  template <int TAIL>
+  __device__ __forceinline__ bool load_tail(int r, const CUtensorMap *tmK, const CUtensorMap *tmV, int box_elems,
+                                            int bg, int n0, int rows, uint64_t pol) const {
+    const int n = (rows + TAIL - 1) / TAIL;
+    if (n * TAIL > BLOCK_N - 2 * TAIL) return false;
+    const int st = r % STAGES;
+    mbar_arrive_expect_tx(full(st), 2 * NBOX * n * TAIL * 128);
+    for (int j = 0; j < n; ++j) {
+#pragma unroll
+      for (int bx = 0; bx < NBOX; ++bx) {
+        tma_load_3d(k_tile(st) + bx * BOX_BYTES + j * TAIL * 128, tmK, bx * box_elems, n0 + j * TAIL, bg, full(st), pol);
+        tma_load_3d(v_tile(st) + bx * BOX_BYTES + j * TAIL * 128, tmV, bx * box_elems, n0 + j * TAIL, bg, full(st), pol);
+      }
+    }
+    return true;
+  }
+
   // Waits (bounded) for the last min(issued, STAGES) copies to land, so that
   // no copy is in flight when the block exits.
   __device__ __forceinline__ void drain(int issued) const {
@@ -108,10 +131,14 @@ __device__ __forceinline__ void fence_global_for_async_proxy() {
 // also writes the appended rows: the rows of units whose last tile falls in
 // the ring's first STAGES loads right before that load, all the others in one
 // batch once those first loads are in flight (their latency then overlaps).
+// tmK16 / tmV16 (or null): maps of the same caches with 16-position boxes,
+// for the last tile of each unit (see KVPipe::load_tail).
 template <class Pipe>
 __device__ __forceinline__ void produce_range(const Pipe &pipe, const SchedParams &s, const CtaRange &range,
                                               const CUtensorMap *tmK, const CUtensorMap *tmV, int box_elems, int G,
-                                              int HC, const SplitParams &p, int lane) {
+                                              int HC, const SplitParams &p, int lane,
+                                              const CUtensorMap *tmK16 = nullptr,
+                                              const CUtensorMap *tmV16 = nullptr) {
   const uint64_t pol = l2_policy_evict_first();
   SegmentCursor cur;
   cur.init(s, range);
@@ -141,7 +168,12 @@ __device__ __forceinline__ void produce_range(const Pipe &pipe, const SchedParam
       __syncwarp();
       if (lane == 0) {
         ok = pipe.acquire(r);
-        if (ok) pipe.load(r, tmK, tmV, box_elems, bg, t * Pipe::BLOCK_N, pol);
+        if (ok) {
+          const int rows =
+              tmK16 && t == seg.tiles - 1 ? attn_len(p.seq_lens, seg.b, p.Nmax, p.append) - t * Pipe::BLOCK_N : 0;
+          if (!(rows > 0 && pipe.template load_tail<16>(r, tmK16, tmV16, box_elems, bg, t * Pipe::BLOCK_N, rows, pol)))
+            pipe.load(r, tmK, tmV, box_elems, bg, t * Pipe::BLOCK_N, pol);
+        }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;

@@ -349,6 +349,7 @@ constexpr float kNoMax = -1e30f;
 template <class C, bool MULTI>
 __global__ void __launch_bounds__(C::THREADS, 1)
     gqa_split_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const __grid_constant__ CUtensorMap tmK16, const __grid_constant__ CUtensorMap tmV16,
                         const SplitParams p) {
   using Pipe = typename C::Pipe;
   constexpr int D = C::D, BN = C::BLOCK_N, ST = C::STAGES, NR = C::NR, HG = C::HG;
@@ -411,6 +412,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmK16);
+      tma_prefetch_desc(&tmV16);
     }
     SchedParams spx = sp;
     spx.spec = 1;
@@ -447,7 +450,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   if (range.begin < range.end) {
     if (warp == 0) {
       // ------------------------------------------------------------ producer
-      produce_range(pipe, sp, range, &tmK, &tmV, C::FP8 ? 128 : 64, p.G, p.head_chunks, p, lane);
+      // (a unit's last tile, when short, through the 16-position boxes)
+      produce_range(pipe, sp, range, &tmK, &tmV, C::FP8 ? 128 : 64, p.G, p.head_chunks, p, lane, &tmK16, &tmV16);
     } else if (warp == 1 || warp == 2) {
       // ------------------------------------------------------------ MMA issuers
       // Two threads issue the MMAs, each walking the CTA's tiles on its own:
