@@ -43,6 +43,24 @@ __device__ __forceinline__ unsigned arrive_unit(unsigned long long *cnt, unsigne
   return (unsigned)nv;
 }
 
+// The same count split in two halves, so that the arrival at the end of a
+// kernel is one atomic add.  tag_unit_counter runs early (before this CTA's
+// work on the unit): a word tagged by another call, or never written, is
+// replaced by (epoch << 32) | 0 with one compare-and-swap.  If the swap
+// fails another CTA of this call changed the word first, and while a call
+// runs only its own CTAs write the word (with this call's tag), so either
+// way the word carries the tag before any of this CTA's adds.
+__device__ __forceinline__ void tag_unit_counter(unsigned long long *cnt, unsigned epoch) {
+  const unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(cnt);
+  if ((unsigned)(old >> 32) != epoch) atomicCAS(cnt, old, (unsigned long long)epoch << 32);
+}
+
+// This CTA's arrival on a word tagged by tag_unit_counter; returns the count
+// including it.
+__device__ __forceinline__ unsigned add_unit_arrival(unsigned long long *cnt) {
+  return (unsigned)atomicAdd(cnt, 1ull) + 1u;
+}
+
 // Called by the `nthr` threads (tid 0..nthr-1) of the group that wrote this
 // CTA's partial of a split unit (heads [h_first, h_first + nh) of batch row
 // b), after those writes; `bar` synchronises the group.  When this CTA is the
@@ -79,12 +97,41 @@ __device__ __forceinline__ void finish_split_unit(const SplitParams &p, const Se
   for (int e = tid; e < nh * (D / 4); e += nthr) {
     const int h = e / (D / 4), d0 = (e % (D / 4)) * 4;
     float M = -INFINITY;
-    for (int k = 0; k < n; ++k) {
+    float L = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    if (n <= 4) {
+      // the usual case (a unit cut between two to four CTAs): every load of
+      // the merge in flight at once, then the same arithmetic in the same
+      // order as the general loops below
+      float2 mk[4];
+      float4 o[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (k < n) {
+          const size_t ps = (size_t)(k == 0 ? slot0 : 2 * (c_lo + k)) * hpc + h;
+          mk[k] = __ldcg(ml + ps);
+          o[k] = __ldcg(reinterpret_cast<const float4 *>(p.o_part + ps * D + d0));
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (k < n) M = fmaxf(M, mk[k].x);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (k < n) {
+          const float w = merge_weight(mk[k].x, M);
+          L += w * mk[k].y;
+          a0 += w * o[k].x;
+          a1 += w * o[k].y;
+          a2 += w * o[k].z;
+          a3 += w * o[k].w;
+        }
+      }
+    }
+    for (int k = 0; k < (n > 4 ? n : 0); ++k) {
       const int slot = k == 0 ? slot0 : 2 * (c_lo + k);
       M = fmaxf(M, __ldcg(ml + (size_t)slot * hpc + h).x);
     }
-    float L = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    for (int k = 0; k < n; ++k) {
+    for (int k = 0; k < (n > 4 ? n : 0); ++k) {
       const size_t ps = (size_t)(k == 0 ? slot0 : 2 * (c_lo + k)) * hpc + h;
       const float2 mk = __ldcg(ml + ps);
       const float w = merge_weight(mk.x, M);

@@ -114,6 +114,26 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     tma_prefetch_desc(&tmWq);
     tma_prefetch_desc(&tmWk);
     tma_prefetch_desc(&tmWv);
+    // The weights are parameters, not results of the previous kernel: ask L2
+    // for this CTA's first ring-full of weight tiles while that kernel ends
+    // (a hint only; the copies after the wait read global memory).
+    int item = (int)(begin / p.ktiles), t = (int)(begin % p.ktiles);
+    for (long long pos = begin; pos < end && pos < begin + ST; ++pos) {
+      int idx;
+      const int s = proj_output(p, item, idx);
+      const CUtensorMap *tm = s == 0 ? &tmWq : (s == 1 ? &tmWk : &tmWv);
+      if (p.d == 128) {
+        tma_prefetch_l2_3d(tm, 0, t * C::KT, idx);
+        tma_prefetch_l2_3d(tm, 64, t * C::KT, idx);
+      } else {
+        tma_prefetch_l2_3d(tm, 0, t * C::KT, 2 * idx);
+        tma_prefetch_l2_3d(tm, 0, t * C::KT, 2 * idx + 1);
+      }
+      if (++t == p.ktiles) {
+        t = 0;
+        ++item;
+      }
+    }
   }
   if (warp == 1) {
     tc::tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
@@ -130,17 +150,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (warp == 0) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {
+        const uint64_t pol = l2_policy_evict_first();
+        int item = (int)(begin / p.ktiles), t = (int)(begin % p.ktiles), idx;
+        int s = proj_output(p, item, idx);
+        const CUtensorMap *tm = s == 0 ? &tmWq : (s == 1 ? &tmWk : &tmWv);
         int r = 0;
         for (long long pos = begin; pos < end; ++pos, ++r) {
-          const int item = (int)(pos / p.ktiles), t = (int)(pos % p.ktiles);
-          int idx;
-          const int s = proj_output(p, item, idx);
-          const CUtensorMap *tm = s == 0 ? &tmWq : (s == 1 ? &tmWk : &tmWv);
           const int st = r % ST;
           if (r >= ST && !mbar_wait(empty(st), ((r / ST) - 1) & 1)) break;
           mbar_arrive_expect_tx(full(st), C::STAGE_BYTES);
           const uint32_t wt = base + st * C::STAGE_BYTES;
-          const uint64_t pol = l2_policy_evict_first();
           if (p.d == 128) {
             tma_load_3d(wt, tm, 0, t * C::KT, idx, full(st), pol);
             tma_load_3d(wt + C::W_BOX, tm, 64, t * C::KT, idx, full(st), pol);
@@ -151,6 +170,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
           for (int xb = 0; xb < C::KT / 64; ++xb)
             tma_load_2d(wt + C::W_TILE + xb * C::X_BOX, &tmX, t * C::KT + xb * 64, 0, full(st));
+          if (++t == p.ktiles) {
+            t = 0;
+            ++item;
+            s = proj_output(p, item, idx);
+            tm = s == 0 ? &tmWq : (s == 1 ? &tmWk : &tmWv);
+          }
         }
         // copies still in flight land before the CTA may end (bounded)
         for (int q = (r > ST ? r - ST : 0); q < r; ++q)
@@ -205,6 +230,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       bool dead = false;
       int seg = 0;
       long long pos = begin;
+      if (R == 0 && p.item_cnt) {
+        // only the range's first and last items can be cut: tag their
+        // counters now, off the path of the end-of-range arrival
+        const int i0 = (int)(begin / p.ktiles), i1 = (int)((end - 1) / p.ktiles);
+        const int t0 = (int)(begin - (long long)i0 * p.ktiles), e1 = (int)(end - (long long)i1 * p.ktiles);
+        if (t0 != 0 || (i0 == i1 && e1 != p.ktiles)) tag_unit_counter(p.item_cnt + i0, p.epoch);
+        if (i1 != i0 && e1 != p.ktiles) tag_unit_counter(p.item_cnt + i1, p.epoch);
+      }
       while (pos < end) {
         const int item = (int)(pos / p.ktiles), t0 = (int)(pos % p.ktiles);
         const int t1 = (int)min((long long)p.ktiles, t0 + (end - pos));
@@ -248,7 +281,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           const long long first = (long long)item * p.ktiles;
           const int c_lo = cta_of_tile(first, T, P), c_hi = cta_of_tile(first + p.ktiles - 1, T, P);
           if (R == 0) {
-            const bool last = arrive_unit(p.item_cnt + item, p.epoch) == (unsigned)(c_hi - c_lo + 1);
+            const bool last = add_unit_arrival(p.item_cnt + item) == (unsigned)(c_hi - c_lo + 1);
             if (last) {
               __threadfence();
               atomicExch(p.item_cnt + item, (unsigned long long)p.epoch << 32);
@@ -257,20 +290,29 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
           asm volatile("bar.sync 2, 128;" ::: "memory");
           if (*merge_flag) {
-            // 16 batch rows at a time, so that 16 independent L2 loads of a
-            // partial are in flight together; partials added in slot order
+            // 16 batch rows of up to four partials at a time, so that their
+            // 64 independent L2 loads are in flight together; the partials
+            // are still added in slot order
             const int slot0 = cta_start(c_lo, T, P) == first ? 2 * c_lo : 2 * c_lo + 1;
+            const int nparts = c_hi - c_lo + 1;
             for (int b0 = 0; b0 < p.B; b0 += 16) {
               float acc[16];
 #pragma unroll
               for (int n = 0; n < 16; ++n) acc[n] = 0.f;
-              for (int k = 0; k <= c_hi - c_lo; ++k) {
-                const float *src = p.part + ((size_t)(k == 0 ? slot0 : 2 * (c_lo + k)) * NB + b0) * 128 + R;
-                float v[16];
+              for (int k0 = 0; k0 < nparts; k0 += 4) {
+                float v[4][16];
 #pragma unroll
-                for (int n = 0; n < 16; ++n) v[n] = b0 + n < p.B ? __ldcg(src + (size_t)n * 128) : 0.f;
+                for (int kk = 0; kk < 4; ++kk) {
+                  const int k = k0 + kk;
+                  const float *src = p.part + ((size_t)(k == 0 ? slot0 : 2 * (c_lo + k)) * NB + b0) * 128 + R;
 #pragma unroll
-                for (int n = 0; n < 16; ++n) acc[n] += v[n];
+                  for (int n = 0; n < 16; ++n) v[kk][n] = k < nparts && b0 + n < p.B ? __ldcg(src + (size_t)n * 128) : 0.f;
+                }
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                  for (int n = 0; n < 16; ++n)
+                    if (k0 + kk < nparts) acc[n] += v[kk][n];
               }
 #pragma unroll
               for (int n = 0; n < 16; ++n)

@@ -154,8 +154,12 @@ __device__ __forceinline__ int aligned_cta_count(long long units, int P) {
 // (row b is owned by CTA b % P), writing `row_bytes` bytes per row of `out`.
 // SPECULATIVE: a plan from lengths that an earlier kernel may still be
 // changing, used only to pick tiles to prefetch into L2: no flags, no writes.
+// `seen` (or null): the stored lengths of rows lane and 32 + lane as read
+// (-1 past B), for spec_plan_holds.
 template <bool SPECULATIVE = false>
-__device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int lane, void *out, size_t row_bytes) {
+__device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int lane, void *out, size_t row_bytes,
+                                                    int2 *seen = nullptr) {
+  if (seen) *seen = make_int2(-1, -1);
   const int c = blockIdx.x;
   int P = gridDim.x;
   long long T = 0;                 // real tiles
@@ -168,6 +172,8 @@ __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int la
     bool zero_mine = false;
     if (b < s.B) {
       const int Lstored = (SPECULATIVE || s.spec) ? *(volatile const int32_t *)(s.seq_lens + b) : __ldg(s.seq_lens + b);
+      if (seen && base == 0) seen->x = Lstored;
+      if (seen && base == 32) seen->y = Lstored;
       const bool appends = s.append && append_ok(Lstored, s.Nmax);
       const int Lraw = appends ? Lstored + 1 : Lstored;
       const int L = clamp_len(Lraw, s.Nmax);
@@ -274,6 +280,27 @@ __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int la
     acc += __shfl_sync(0xffffffffu, incl, 31);
   }
   return r;
+}
+
+// After the wait for earlier kernels: whether the plan a speculative pass
+// made from the lengths `seen` (warp_plan_range<true>, before the wait) is
+// this call's plan.  It is when B <= 64 (the pass read every length once,
+// two rows per lane), every stored length still equals the one it read, and
+// no row needs what the speculative pass leaves out (a length flag, the zero
+// fill of an empty row).  The plan depends on nothing else, so the real
+// pass would return the same range.  Whole warp.
+__device__ __forceinline__ bool spec_plan_holds(const SchedParams &s, int lane, int2 seen) {
+  if (s.B > 64) return false;
+  const int b0 = lane, b1 = 32 + lane;
+  const int L0 = b0 < s.B ? __ldg(s.seq_lens + b0) : -1;
+  const int L1 = b1 < s.B ? __ldg(s.seq_lens + b1) : -1;
+  auto clean = [&](int L) {
+    const bool appends = s.append && append_ok(L, s.Nmax);
+    const int Lraw = appends ? L + 1 : L;
+    return Lraw > 0 && Lraw <= s.Nmax && (!s.append || appends);
+  };
+  const bool ok = L0 == seen.x && L1 == seen.y && (b0 >= s.B || clean(L0)) && (b1 >= s.B || clean(L1));
+  return __all_sync(0xffffffffu, ok);
 }
 
 // One segment: tiles [t0, t1) of unit (b, uib) where uib = g*HC + hc.

@@ -11,7 +11,8 @@
 //   O^T += V_tile^T . P^T   M = d = 128, N = heads, K = 128 positions
 //                           A = V tile as TMA landed it (MN-major: d runs
 //                           along the 128-byte rows), B = P^T written by the
-//                           softmax threads (K-major: one row per head)
+//                           softmax threads (MN-major: one row of N heads
+//                           per position, swizzled to the row's width)
 // Each K/V byte read from HBM serves every query head of the group (the
 // point of GQA: GQA paper, section 2.2), and the MMA work per tile is the
 // 2 x 128 x 128 x 2 x N flop, well under the tensor pipe's rate.
@@ -51,9 +52,9 @@ namespace gqa {
 
 // FP8_: the cache holds E4M3 codes; four more warps convert each landed
 // tile to f16 (exact): the K tile into tensor memory, where the S^T MMA
-// reads it as its A operand, the V tile into a double-buffered shared-memory
-// staging area that the P.V MMA reads; Q and P are f16 too (one operand type
-// per MMA).
+// reads it as its A operand, the V tile into one of VSTG shared-memory
+// staging buffers that the P.V MMA reads; Q and P are f16 too (one operand
+// type per MMA).
 template <int NR_, int STAGES_, int PB_, bool FP8_ = false, int SG_ = 1, int VSTG_ = 2>
 struct TcCfg {
   static constexpr bool FP8 = FP8_;
@@ -406,6 +407,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     tc::tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
     tc::tmem_relinquish();
   }
+  CtaRange r0;  // warp 0: the speculative plan, and the lengths it read
+  int2 spec_lens = make_int2(-1, -1);
   if (warp == 0) {
     // Ahead of the wait for earlier kernels: fetch the tensor maps and ask
     // L2 for the first tiles of a speculative plan (a hint only).
@@ -417,7 +420,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     SchedParams spx = sp;
     spx.spec = 1;
-    const CtaRange r0 = warp_plan_range<true>(spx, lane, nullptr, 0);
+    r0 = warp_plan_range<true>(spx, lane, nullptr, 0, &spec_lens);
     if (lane == 0 && r0.begin < r0.end) prefetch_first_tiles(spx, r0, &tmK, &tmV, C::FP8 ? 128 : 64, C::FP8 ? 1 : 2, p.G, p.head_chunks, ST);
     if (!MULTI && r0.begin < r0.end) {
       // and for the query rows of the first unit (a hint too: the copy
@@ -437,7 +440,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   }
   griddep_wait();  // lengths, q and cache rows written by earlier kernels are visible
   if (warp == 0) {
-    const CtaRange r = warp_plan_range(sp, lane, p.out, (size_t)p.H * D * sizeof(__nv_bfloat16));
+    const CtaRange r =
+        spec_plan_holds(sp, lane, spec_lens) ? r0 : warp_plan_range(sp, lane, p.out, (size_t)p.H * D * sizeof(__nv_bfloat16));
     if (lane == 0) *range_smem = r;
   }
   tc::fence_before();

@@ -204,3 +204,66 @@ def test_step_counter_fixed_offset_is_the_plain_count_without_a_tag():
         word += 1
         counts.append(word)
     assert counts.index(P) == P - k - 1 != P - 1
+
+
+# ------------------------------------------- split-item counter, two halves
+def _tag_then_arrive(word, epoch):
+    """One CTA of a cut projection item (gqa_proj_tc.cuh): tag_unit_counter
+    at the start of its range, add_unit_arrival at the end (gqa_merge.cuh),
+    yielding before every access to the word so that the CTAs' steps can be
+    interleaved at will.  Returns the count its add saw."""
+    yield
+    old = word[0]                      # volatile read
+    if (old >> 32) != epoch:
+        yield
+        if word[0] == old:             # atomicCAS(cnt, old, epoch << 32)
+            word[0] = epoch << 32
+    yield                              # ... the CTA's work on the item ...
+    yield
+    prev = word[0]                     # atomicAdd(cnt, 1)
+    word[0] = (prev + 1) & MASK64
+    return (prev + 1) & 0xFFFFFFFF
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_split_item_counter_tagged_early_elects_the_last_arrival(seed):
+    """The projection kernel tags a cut item's counter when a CTA starts and
+    counts its arrival with one add at the end.  Whatever the word held
+    before (uncleared memory, another call's tag and count), every add lands
+    on a word with this call's tag, exactly one CTA sees the full count and
+    it is the last to add; the merger's reset leaves the word ready for a
+    replay with the same tag."""
+    rng = random.Random(100 + seed)
+    for _ in range(600):
+        n = rng.choice([1, 2, 3, 4])
+        epoch = rng.randint(1, 2 ** 32 - 1)
+        word = [rng.choice([0, rng.getrandbits(64), (rng.randint(0, 2 ** 32 - 1) << 32) | rng.randint(0, 9)])]
+        if (word[0] >> 32) == epoch:
+            word[0] ^= 1 << 32
+        for replay in range(3):
+            gens = {c: _tag_then_arrive(word, epoch) for c in range(n)}
+            order, elected = [], []
+            while gens:
+                c = rng.choice(list(gens))
+                try:
+                    next(gens[c])
+                except StopIteration as stop:
+                    del gens[c]
+                    order.append(c)
+                    if stop.value == n:
+                        elected.append(c)
+                        word[0] = epoch << 32   # the merger's reset
+            assert elected == [order[-1]], (n, replay, elected, order)
+            assert word[0] == epoch << 32
+
+
+def test_split_item_counter_untagged_add_miscounts():
+    """Without the early tag, an add on a word another call left at (tag, k)
+    reaches n after n - k adds: the tag check is what the early half buys."""
+    n, k = 3, 1
+    word = (7 << 32) | k
+    counts = []
+    for _ in range(n):
+        word += 1
+        counts.append(word & 0xFFFFFFFF)
+    assert counts.index(n) == n - k - 1 != n - 1
