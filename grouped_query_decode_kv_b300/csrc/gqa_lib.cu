@@ -194,8 +194,8 @@ using TcD128x64 = TcCfg<64, 3, 1>;
 using TcD128x32Multi = TcCfg<32, 3, 2, false, 2>;
 // FP8 cache: stages of 32 KB of codes (K and V of 128 positions), two or
 // three 32 KB f16 V staging tiles (the f16 K tiles are in tensor memory)
-using TcFp8x16 = TcCfg<16, 3, 2, true, 1, 3>;
-using TcFp8x32 = TcCfg<32, 3, 2, true, 1, 3>;
+using TcFp8x16 = TcCfg<16, 6, 2, true, 1, 2, true>;
+using TcFp8x32 = TcCfg<32, 5, 2, true, 1, 2, true>;
 using TcFp8x64 = TcCfg<64, 3, 1, true>;
 
 template <bool M>

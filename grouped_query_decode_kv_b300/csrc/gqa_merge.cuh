@@ -97,41 +97,12 @@ __device__ __forceinline__ void finish_split_unit(const SplitParams &p, const Se
   for (int e = tid; e < nh * (D / 4); e += nthr) {
     const int h = e / (D / 4), d0 = (e % (D / 4)) * 4;
     float M = -INFINITY;
-    float L = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    if (n <= 4) {
-      // the usual case (a unit cut between two to four CTAs): every load of
-      // the merge in flight at once, then the same arithmetic in the same
-      // order as the general loops below
-      float2 mk[4];
-      float4 o[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        if (k < n) {
-          const size_t ps = (size_t)(k == 0 ? slot0 : 2 * (c_lo + k)) * hpc + h;
-          mk[k] = __ldcg(ml + ps);
-          o[k] = __ldcg(reinterpret_cast<const float4 *>(p.o_part + ps * D + d0));
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (k < n) M = fmaxf(M, mk[k].x);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        if (k < n) {
-          const float w = merge_weight(mk[k].x, M);
-          L += w * mk[k].y;
-          a0 += w * o[k].x;
-          a1 += w * o[k].y;
-          a2 += w * o[k].z;
-          a3 += w * o[k].w;
-        }
-      }
-    }
-    for (int k = 0; k < (n > 4 ? n : 0); ++k) {
+    for (int k = 0; k < n; ++k) {
       const int slot = k == 0 ? slot0 : 2 * (c_lo + k);
       M = fmaxf(M, __ldcg(ml + (size_t)slot * hpc + h).x);
     }
-    for (int k = 0; k < (n > 4 ? n : 0); ++k) {
+    float L = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    for (int k = 0; k < n; ++k) {
       const size_t ps = (size_t)(k == 0 ? slot0 : 2 * (c_lo + k)) * hpc + h;
       const float2 mk = __ldcg(ml + ps);
       const float w = merge_weight(mk.x, M);

@@ -89,8 +89,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   sp.unit_cost = C::UNIT_COST;
 
   if (threadIdx.x == 0) pipe.init();
-  CtaRange r0;  // warp 0: the speculative plan, and the lengths it read
-  int2 spec_lens = make_int2(-1, -1);
+  int2 spec_lens = make_int2(-1, -1);  // warp 0: the lengths the speculative plan read
   if (warp == 0) {
     // Ahead of the wait for earlier kernels: fetch the tensor maps and ask
     // L2 for the first tiles of a speculative plan (a hint only).
@@ -100,15 +99,18 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
     }
     SchedParams spx = sp;
     spx.spec = 1;
-    r0 = warp_plan_range<true>(spx, lane, nullptr, 0, &spec_lens);
+    const CtaRange r0 = warp_plan_range<true>(spx, lane, nullptr, 0, &spec_lens);
+    // kept in shared memory, not registers, across the wait
+    if (lane == 0) *range_smem = r0;
     if (lane == 0 && r0.begin < r0.end)
       prefetch_first_tiles(spx, r0, &tmK, &tmV, 64, Pipe::NBOX, p.G, p.head_chunks, Pipe::STAGES);
   }
   griddep_wait();  // lengths and cache rows written by earlier kernels are visible
   if (warp == 0) {
-    const CtaRange r =
-        spec_plan_holds(sp, lane, spec_lens) ? r0 : warp_plan_range(sp, lane, p.out, (size_t)p.H * D * sizeof(__nv_bfloat16));
-    if (lane == 0) *range_smem = r;
+    if (!spec_plan_holds(sp, lane, spec_lens)) {
+      const CtaRange r = warp_plan_range(sp, lane, p.out, (size_t)p.H * D * sizeof(__nv_bfloat16));
+      if (lane == 0) *range_smem = r;
+    }
   }
   __syncthreads();
   griddep_launch_dependents();

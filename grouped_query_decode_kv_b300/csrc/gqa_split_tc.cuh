@@ -55,9 +55,26 @@ namespace gqa {
 // reads it as its A operand, the V tile into one of VSTG shared-memory
 // staging buffers that the P.V MMA reads; Q and P are f16 too (one operand
 // type per MMA).
-template <int NR_, int STAGES_, int PB_, bool FP8_ = false, int SG_ = 1, int VSTG_ = 2>
+// F8N_ (with FP8_): no conversion at all.  Both MMAs are kind::f8f6f4 with
+// E4M3 operands and K = 32 per instruction, half the instructions of the f16
+// path: S^T reads the K tile as TMA landed it (K-major), P.V the V tile as
+// landed (MN-major: d runs along the 128-byte rows).  Q and P, which are not
+// E4M3 values, enter as two E4M3 terms each, a head's columns doubled:
+//   Q[h] = (Q_hi + Q_lo / 16) / qs_h   (qs_h a power of two per head that
+//                                        puts max |Q[h]| in [128, 256))
+//   P    =  P_hi + P_lo / 16           (P in f16 first; both terms E4M3)
+// so S^T and O^T have 2*NR columns, term 0 in [0, NR) and term 1 in
+// [NR, 2*NR), combined by one FMA per head after the MMA.  The two Q terms
+// hold every bf16 query exactly (4 + 4 significant bits) while qs_h keeps a
+// head's elements in the E4M3 normal range; the two P terms keep 8
+// significant bits (bf16 P in the bf16 path has 8), for p >= 2^-13 (smaller
+// probabilities, 2^-13 or less of the running maximum, are dropped).
+template <int NR_, int STAGES_, int PB_, bool FP8_ = false, int SG_ = 1, int VSTG_ = 2, bool F8N_ = false>
 struct TcCfg {
   static constexpr bool FP8 = FP8_;
+  static constexpr bool F8N = FP8_ && F8N_;          // native E4M3 MMAs, no converter warps
+  static constexpr bool CONV = FP8_ && !F8N_;        // converter warps (K to TMEM, V to f16 staging)
+  static constexpr int NM = F8N ? 2 * NR_ : NR_;     // N of both MMAs (two terms per head with F8N)
   static constexpr int VSTG = VSTG_;  // FP8: f16 V staging buffers
   static_assert(VSTG >= 2 && VSTG <= 3, "V staging buffers");
   static constexpr int D = 128;
@@ -75,35 +92,43 @@ struct TcCfg {
   static constexpr int SG = SG_;
   static constexpr int HG = NR / SG;
   static_assert(SG == 1 || (SG == 2 && NR >= 32), "two softmax groups need 16+ heads each");
+  static_assert(!F8N || (SG == 1 && NR <= 32), "native E4M3 path: one softmax group, up to 32 heads");
   // one "empty" arrival per tile: the MMA commit (FP8: the 4 converter warps)
-  using Pipe = KVPipe<FP8 ? 1 : 2, BLOCK_N, STAGES, FP8 ? 4 : 1>;
+  using Pipe = KVPipe<FP8 ? 1 : 2, BLOCK_N, STAGES, CONV ? 4 : 1>;
   static constexpr int SOFT_WARP0 = 3;            // first softmax warp (after producer, two MMA issuers)
   static constexpr int CONV_WARP0 = SOFT_WARP0 + 4 * SG;  // first FP8 converter warp
-  static constexpr int THREADS = (CONV_WARP0 + (FP8 ? 4 : 0)) * 32;
+  static constexpr int THREADS = (CONV_WARP0 + (CONV ? 4 : 0)) * 32;
   static constexpr int KV_BOX = BLOCK_N * 128;  // one 128-byte-wide box of a bf16 K or V tile
   // FP8: V staging [2] in f16, two boxes each (d 0-63, 64-127); the f16 K
   // tiles live in tensor memory
   static constexpr int STG_OFF = Pipe::PIPE_BYTES;
   static constexpr int STG_TILE = 2 * KV_BOX;
-  static constexpr int STG_BYTES = FP8 ? VSTG * STG_TILE : 0;
+  static constexpr int STG_BYTES = CONV ? VSTG * STG_TILE : 0;
   static constexpr int SOFT = 128;             // threads of one softmax group
-  // TMEM columns: S^T buffers [0, 2*NR), O^T buffers [2*NR, 4*NR); FP8: two
-  // f16 K tiles [4*NR, 4*NR + 128) (lane = position, 64 columns of f16 pairs)
+  // TMEM columns: S^T buffers [0, 2*NM), O^T buffers [2*NM, 4*NM); FP8 with
+  // converters: two f16 K tiles [4*NM, 4*NM + 128) (lane = position, 64
+  // columns of f16 pairs)
   static constexpr int TM_S = 0;
-  static constexpr int TM_O = 2 * NR;
-  static constexpr int TM_K = 4 * NR;
-  static constexpr int TM_USED = 4 * NR + (FP8 ? 128 : 0);
+  static constexpr int TM_O = 2 * NM;
+  static constexpr int TM_K = 4 * NM;
+  static constexpr int TM_USED = 4 * NM + (CONV ? 128 : 0);
   static constexpr int TM_COLS = TM_USED <= 32 ? 32 : TM_USED <= 64 ? 64 : TM_USED <= 128 ? 128 : TM_USED <= 256 ? 256 : 512;
   // shared memory
   // Q: two 128-byte-wide boxes (d 0-63, 64-127) of NR rows per buffer; two
   // buffers where shared memory allows, so that the next unit's Q lands
   // while the current one is still in use
+  // F8N: each buffer holds the E4M3 operand (NM rows of 128 codes: term 0
+  // of the NR heads, then term 1) and, after it, the bf16 rows as copied
+  // (two boxes, as above)
   static constexpr int Q_OFF = STG_OFF + STG_BYTES;
   static constexpr int Q_BOX = NR * 128;
-  static constexpr int Q_BYTES = 2 * Q_BOX;
-  // P^T buffers, MN-major: one row of NR heads (2*NR bytes) per position,
-  // stored with the swizzle of the row's width, so that the thread that owns
-  // a position writes its heads with 16-byte stores
+  static constexpr int Q_OP = F8N ? NM * 128 : 0;  // E4M3 operand bytes
+  static constexpr int Q_STG = Q_OP;               // offset of the bf16 rows in a buffer
+  static constexpr int Q_BYTES = Q_OP + 2 * Q_BOX;
+  // P^T buffers, MN-major: one row of NR heads (2*NR bytes: bf16 or f16, or
+  // with F8N the two E4M3 terms) per position, stored with the swizzle of the
+  // row's width, so that the thread that owns a position writes its heads
+  // with 16-byte stores
   static constexpr int P_ROW = 2 * NR;
   static constexpr int P_BYTES = BLOCK_N * P_ROW;
   static constexpr int P_SWZ_SHIFT = NR == 64 ? 0 : (NR == 32 ? 1 : 2);
@@ -112,14 +137,17 @@ struct TcCfg {
   // pv_done[2], o_free[2], q_full[2], mma_done; FP8: conv_full[2], stg_free[3]
   static constexpr int NBAR = 2 * STAGES + 13 + (FP8 ? 5 : 0);
   static constexpr int RANGE_BYTES = ((int)sizeof(CtaRange) + 7) / 8 * 8;
-  static constexpr int TAIL_BYTES = 4 * NQ * 4 + 3 * NQ * 4 + NBAR * 8 + 8 + RANGE_BYTES + (int)sizeof(UnitMerge);
+  static constexpr int QSC_BYTES = F8N ? 2 * NQ * 4 + NQ * 4 : 0;  // F8N: 1/qs per Q buffer, logit factor per head
+  static constexpr int TAIL_BYTES =
+      4 * NQ * 4 + 3 * NQ * 4 + QSC_BYTES + NBAR * 8 + 8 + RANGE_BYTES + (int)sizeof(UnitMerge);
   static constexpr int QB = 1024 + Q_OFF + 2 * Q_BYTES + PB * P_BYTES + TAIL_BYTES <= 227 * 1024 ? 2 : 1;
   static constexpr int P_OFF = Q_OFF + QB * Q_BYTES;
   static constexpr int RED_OFF = P_OFF + PB * P_BYTES;  // [SG][4][HG] cross-warp reduction
   static constexpr int FIN_OFF = RED_OFF + 4 * NQ * 4;   // [NQ] reduced value
   static constexpr int M_OFF = FIN_OFF + NQ * 4;         // [NQ] running max of the unit
   static constexpr int CORR_OFF = M_OFF + NQ * 4;        // [NQ] rescale factor of a tile
-  static constexpr int BAR_OFF = CORR_OFF + NQ * 4;
+  static constexpr int QSC_OFF = CORR_OFF + NQ * 4;      // F8N: [2][NQ] 1/qs_h, then [NQ] logit factor
+  static constexpr int BAR_OFF = QSC_OFF + QSC_BYTES;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBAR * 8;
   static constexpr int RANGE_OFF = TMEM_SLOT_OFF + 8;  // 8-byte aligned (barriers before it)
   static constexpr int MERGE_OFF = RANGE_OFF + RANGE_BYTES;
@@ -397,7 +425,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     mbar_init(bars.q_full(0), 4);  // one arrival per warp of softmax group 0
     mbar_init(bars.q_full(1), 4);
     mbar_init(bars.mma_done(), 2);  // the commits of both MMA issuers
-    if (C::FP8) {
+    if (C::CONV) {
       for (int i = 0; i < 2; ++i) mbar_init(bars.conv_full(i), 4);  // one arrival per converter warp
       for (int i = 0; i < C::VSTG; ++i) mbar_init(bars.stg_free(i), 1);  // the MMA commit after the tile's P.V
     }
@@ -407,8 +435,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     tc::tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
     tc::tmem_relinquish();
   }
-  CtaRange r0;  // warp 0: the speculative plan, and the lengths it read
-  int2 spec_lens = make_int2(-1, -1);
+  int2 spec_lens = make_int2(-1, -1);  // warp 0: the lengths the speculative plan read
   if (warp == 0) {
     // Ahead of the wait for earlier kernels: fetch the tensor maps and ask
     // L2 for the first tiles of a speculative plan (a hint only).
@@ -420,7 +447,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     SchedParams spx = sp;
     spx.spec = 1;
-    r0 = warp_plan_range<true>(spx, lane, nullptr, 0, &spec_lens);
+    const CtaRange r0 = warp_plan_range<true>(spx, lane, nullptr, 0, &spec_lens);
+    // kept in shared memory, not registers, across the wait
+    if (lane == 0) *range_smem = r0;
     if (lane == 0 && r0.begin < r0.end) prefetch_first_tiles(spx, r0, &tmK, &tmV, C::FP8 ? 128 : 64, C::FP8 ? 1 : 2, p.G, p.head_chunks, ST);
     if (!MULTI && r0.begin < r0.end) {
       // and for the query rows of the first unit (a hint too: the copy
@@ -440,9 +469,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   }
   griddep_wait();  // lengths, q and cache rows written by earlier kernels are visible
   if (warp == 0) {
-    const CtaRange r =
-        spec_plan_holds(sp, lane, spec_lens) ? r0 : warp_plan_range(sp, lane, p.out, (size_t)p.H * D * sizeof(__nv_bfloat16));
-    if (lane == 0) *range_smem = r;
+    if (!spec_plan_holds(sp, lane, spec_lens)) {
+      const CtaRange r = warp_plan_range(sp, lane, p.out, (size_t)p.H * D * sizeof(__nv_bfloat16));
+      if (lane == 0) *range_smem = r;
+    }
   }
   tc::fence_before();
   __syncthreads();
@@ -469,10 +499,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       // MMAs to its barriers.
       if (lane == 0) {
         // FP8 cache: all operands are f16 (exact for the E4M3 values)
-        constexpr uint32_t IDESC_S =
-            C::FP8 ? tc::idesc_f16_f32(BN, NR, false, false) : tc::idesc_bf16_f32(BN, NR, false, false);
-        constexpr uint32_t IDESC_PV =
-            C::FP8 ? tc::idesc_f16_f32(D, NR, true, true) : tc::idesc_bf16_f32(D, NR, true, true);
+        constexpr uint32_t IDESC_S = C::F8N   ? tc::idesc_e4m3_f32(BN, C::NM, false, false)
+                                     : C::FP8 ? tc::idesc_f16_f32(BN, NR, false, false)
+                                              : tc::idesc_bf16_f32(BN, NR, false, false);
+        constexpr uint32_t IDESC_PV = C::F8N   ? tc::idesc_e4m3_f32(D, C::NM, true, true)
+                                      : C::FP8 ? tc::idesc_f16_f32(D, NR, true, true)
+                                               : tc::idesc_bf16_f32(D, NR, true, true);
         SegmentCursor cur;
         cur.init(sp, range);
         Segment seg;
@@ -485,7 +517,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               // unit u's Q is in buffer u % QB, its (u / QB)-th use
               const int qb = unit % C::QB;
               ok = (i != 0 || mbar_wait(bars.q_full(qb), (unit / C::QB) & 1)) &&
-                   (C::FP8 ? mbar_wait(bars.conv_full(tg & 1), (tg >> 1) & 1)
+                   (C::CONV ? mbar_wait(bars.conv_full(tg & 1), (tg >> 1) & 1)
                            : mbar_wait(pipe.full(st), (tg / ST) & 1)) &&
                    (tg < 2 || mbar_wait(bars.s_free(tg & 1), ((tg >> 1) - 1) & 1));
               if (!ok) break;
@@ -493,12 +525,19 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               // descriptors of the tile's first K step; the others are
               // constant offsets from them (one add each)
               const uint64_t b0 = tc::smem_desc_sw128(qbase + qb * C::Q_BYTES, 16, 1024);
-              const uint64_t a0 = C::FP8 ? 0 : tc::smem_desc_sw128(pipe.k_tile(st), 16, 1024);
-              const uint32_t dS = tmem + C::TM_S + (tg & 1) * NR;
+              const uint64_t a0 = C::CONV ? 0 : tc::smem_desc_sw128(pipe.k_tile(st), 16, 1024);
+              const uint32_t dS = tmem + C::TM_S + (tg & 1) * C::NM;
+              if constexpr (C::F8N) {
+                // E4M3 K tile (one 128-byte row of codes per position) times
+                // the two-term E4M3 Q: 32 K elements (32 bytes) per step
 #pragma unroll
-              for (int ks = 0; ks < D / 16; ++ks) {
+                for (int ks = 0; ks < D / 32; ++ks)
+                  tc::mma_ss_f8(dS, tc::desc_add(a0, ks * 32), tc::desc_add(b0, ks * 32), IDESC_S, ks > 0);
+              }
+#pragma unroll
+              for (int ks = 0; ks < (C::F8N ? 0 : D / 16); ++ks) {
                 const uint64_t b = tc::desc_add(b0, (ks >> 2) * C::Q_BOX + (ks & 3) * 32);
-                if constexpr (C::FP8) {
+                if constexpr (C::CONV) {
                   // A = the f16 K tile in tensor memory: 16 K elements = 8 columns
                   tc::mma_ts(dS, tmem + C::TM_K + (tg & 1) * 64 + ks * 8, b, IDESC_S, ks > 0);
                 } else {
@@ -513,17 +552,27 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               if (!ok) break;
               tc::fence_after();
               const uint32_t vt =
-                  C::FP8 ? pipe.base + C::STG_OFF + (tg % C::VSTG) * C::STG_TILE : pipe.v_tile(tg % ST);
+                  C::CONV ? pipe.base + C::STG_OFF + (tg % C::VSTG) * C::STG_TILE : pipe.v_tile(tg % ST);
               const uint64_t a0 = tc::smem_desc_sw128(vt, C::KV_BOX, 1024);
               const uint64_t b0 = tc::smem_desc_mn_rows(pbase + pb * C::P_BYTES, C::P_ROW);
-              const uint32_t dO = tmem + C::TM_O + ob * NR;
+              const uint32_t dO = tmem + C::TM_O + ob * C::NM;
+              if constexpr (C::F8N) {
+                // E4M3 V tile, MN-major (128 d codes per position row): 32
+                // positions (32 rows of 128 bytes) per step
 #pragma unroll
-              for (int ks = 0; ks < BN / 16; ++ks)
-                tc::mma_ss(dO, tc::desc_add(a0, ks * 2048), tc::desc_add(b0, ks * 16 * C::P_ROW), IDESC_PV,
-                           i > 0 || ks > 0);
+                for (int ks = 0; ks < BN / 32; ++ks)
+                  tc::mma_ss_f8(dO, tc::desc_add(a0, ks * 4096), tc::desc_add(b0, ks * 32 * C::P_ROW), IDESC_PV,
+                                i > 0 || ks > 0);
+              } else {
+#pragma unroll
+                for (int ks = 0; ks < BN / 16; ++ks)
+                  tc::mma_ss(dO, tc::desc_add(a0, ks * 2048), tc::desc_add(b0, ks * 16 * C::P_ROW), IDESC_PV,
+                             i > 0 || ks > 0);
+              }
               // the tile's K and V are no longer read: free its ring stage
-              // (FP8: its staging buffer; the converters free the stage)
-              tc::commit(C::FP8 ? bars.stg_free(tg % C::VSTG) : pipe.empty(tg % ST));
+              // (FP8 with converters: its staging buffer; the converters free
+              // the stage)
+              tc::commit(C::CONV ? bars.stg_free(tg % C::VSTG) : pipe.empty(tg % ST));
               tc::commit(bars.pv_done(pb));
             }
           }
@@ -565,7 +614,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (row < NR && GQA_ROW_OK(p, qrow)) {
           const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(p.q) +
                                                              qrow * D + half * 64);
-          const uint32_t dst = qbase + buf * C::Q_BYTES + half * C::Q_BOX + row * 128;
+          const uint32_t dst = qbase + buf * C::Q_BYTES + C::Q_STG + half * C::Q_BOX + row * 128;
           const uint32_t bytes = row < nh ? 16u : 0u;
 #pragma unroll
           for (int c = 0; c < 8; ++c) cp_async_16(dst + ((c ^ (row & 7)) << 4), src + c, bytes);
@@ -578,7 +627,66 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           cp_async_wait<1>();
         else
           cp_async_wait<0>();
-        if constexpr (C::FP8) {
+        if constexpr (C::F8N) {
+          // (the rows were copied by other threads of the group: every copy
+          // of this buffer has landed once all of them passed their wait)
+          soft_bar(0);
+          // E4M3 operand: eight threads per row (R & 7 = part: d 16*part ..
+          // 16*part + 15, chunks 2*(part & 3) and + 1 of box part >> 2 of the
+          // copied bf16 row); the row's eight lanes agree on its scale qs (a
+          // power of two: max |Q[h]| * qs in [128, 256)), then each writes
+          // its 16 codes of term 0 (operand row h) and of term 1 (row NR + h)
+          const int part = R & 7;
+#pragma unroll
+          for (int it = 0; it < NR / 16; ++it) {
+            const int row = 16 * it + (R >> 3);
+            const uint32_t src = qbase + buf * C::Q_BYTES + C::Q_STG + (part >> 2) * C::Q_BOX + row * 128;
+            uint4 v[2];
+            float mx = 0.f;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const int c = 2 * (part & 3) + j;
+              v[j] = lds128(src + ((c ^ (row & 7)) << 4));
+              const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+            }
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            // qs = 2^(7 - floor(log2 mx)), from the exponent field (clamped
+            // to the normal range; 1 for an all-zero row)
+            const int e = (int)((__float_as_uint(mx) >> 23) & 0xffu) - 127;
+            const int f = mx > 0.f ? min(254, max(1, 127 + 7 - e)) : 127;
+            const float qs = __uint_as_float((uint32_t)f << 23);
+            if (part == 0) reinterpret_cast<float *>(smem + C::QSC_OFF)[buf * C::NQ + row] = 1.f / qs;
+            uint32_t t0[4], t1[4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+              for (int i = 0; i < 4; i += 2) {
+                const float x0 = bf16_lo(w[i]) * qs, x1 = bf16_hi(w[i]) * qs;
+                const float x2 = bf16_lo(w[i + 1]) * qs, x3 = bf16_hi(w[i + 1]) * qs;
+                const uint32_t a = float2_to_e4m3x2(x0, x1), b = float2_to_e4m3x2(x2, x3);
+                float a0, a1, b0, b1;
+                e4m3x2_to_float(a, a0, a1);
+                e4m3x2_to_float(b, b0, b1);
+                const uint32_t la = float2_to_e4m3x2((x0 - a0) * 16.f, (x1 - a1) * 16.f);
+                const uint32_t lb = float2_to_e4m3x2((x2 - b0) * 16.f, (x3 - b1) * 16.f);
+                t0[2 * j + i / 2] = a | (b << 16);
+                t1[2 * j + i / 2] = la | (lb << 16);
+              }
+            }
+            const uint32_t op = qbase + buf * C::Q_BYTES;
+            const int r0 = row, r1 = NR + row;
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(op + r0 * 128 + ((part ^ (r0 & 7)) << 4)),
+                         "r"(t0[0]), "r"(t0[1]), "r"(t0[2]), "r"(t0[3])
+                         : "memory");
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(op + r1 * 128 + ((part ^ (r1 & 7)) << 4)),
+                         "r"(t1[0]), "r"(t1[1]), "r"(t1[2]), "r"(t1[3])
+                         : "memory");
+          }
+        } else if constexpr (C::FP8) {
           // f16 operands: this thread's bf16 chunks become f16 in place
           const int row = R >> 1, half = R & 1;
           if (row < NR) {
@@ -645,6 +753,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // Padding rows (zero queries, so zero logits) are computed like real
         // ones and never written out.
         if (R < HG) m_s[hg0 + R] = kNoMax;
+        // F8N: head h's logit factor, the logit scale over the head's Q scale
+        // (this unit's Q buffer was completed by this group before the unit)
+        float *cf_s = reinterpret_cast<float *>(smem + C::QSC_OFF) + 2 * C::NQ;
+        if (C::F8N && R < HG)
+          cf_s[hg0 + R] = sl2 * reinterpret_cast<const float *>(smem + C::QSC_OFF)[(unit % C::QB) * C::NQ + hg0 + R];
         soft_bar(grp);
         // Row h of the unit is query token t(h) = (row0 + h) / rep_kv of its
         // run and sees positions n < L_all + t(h); positions below L_all are
@@ -679,29 +792,51 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
           };
           // this position's raw logits S of the group's heads (every column
-          // chunk asked for before the one wait)
-          auto load_s = [&](uint32_t(&r)[HG]) {
+          // chunk asked for before the one wait); F8N: the two Q terms'
+          // columns, combined (term 0 + term 1 / 16; the head's Q scale is in
+          // its logit factor)
+          auto load_s = [&](float(&x)[HG]) {
+            uint32_t r[HG];
 #pragma unroll
             for (int c0 = 0; c0 < HG; c0 += HCH) {
               if constexpr (HCH == 32) {
-                tc::ld_32x32b_x32(trow + C::TM_S + sb * NR + hg0 + c0, r + c0);
+                tc::ld_32x32b_x32(trow + C::TM_S + sb * C::NM + hg0 + c0, r + c0);
               } else {
-                tc::ld_32x32b_x16(trow + C::TM_S + sb * NR + hg0 + c0, r + c0);
+                tc::ld_32x32b_x16(trow + C::TM_S + sb * C::NM + hg0 + c0, r + c0);
               }
             }
-            tc::wait_ld();
+            if constexpr (C::F8N) {
+              uint32_t r1[HG];
+#pragma unroll
+              for (int c0 = 0; c0 < HG; c0 += HCH) {
+                if constexpr (HCH == 32) {
+                  tc::ld_32x32b_x32(trow + C::TM_S + sb * C::NM + NR + hg0 + c0, r1 + c0);
+                } else {
+                  tc::ld_32x32b_x16(trow + C::TM_S + sb * C::NM + NR + hg0 + c0, r1 + c0);
+                }
+              }
+              tc::wait_ld();
+#pragma unroll
+              for (int h = 0; h < HG; ++h) x[h] = fmaf(__uint_as_float(r1[h]), 0.0625f, __uint_as_float(r[h]));
+            } else {
+              tc::wait_ld();
+#pragma unroll
+              for (int h = 0; h < HG; ++h) x[h] = __uint_as_float(r[h]);
+            }
           };
-          // y = S * scale_log2 - m, masked
+          const float4 *cf4 = reinterpret_cast<const float4 *>(cf_s + hg0);
+          // y = S * scale_log2 - m (F8N: S * factor[h] - m), masked
           auto compute_y = [&](float(&y)[HG]) {
-            uint32_t r[HG];
-            load_s(r);
+            float x[HG];
+            load_s(x);
 #pragma unroll
             for (int h4 = 0; h4 < HG; h4 += 4) {
               const float4 mm = m4[h4 >> 2];
-              y[h4 + 0] = fmaf(__uint_as_float(r[h4 + 0]), sl2, -mm.x);
-              y[h4 + 1] = fmaf(__uint_as_float(r[h4 + 1]), sl2, -mm.y);
-              y[h4 + 2] = fmaf(__uint_as_float(r[h4 + 2]), sl2, -mm.z);
-              y[h4 + 3] = fmaf(__uint_as_float(r[h4 + 3]), sl2, -mm.w);
+              const float4 cf = C::F8N ? cf4[h4 >> 2] : make_float4(sl2, sl2, sl2, sl2);
+              y[h4 + 0] = fmaf(x[h4 + 0], cf.x, -mm.x);
+              y[h4 + 1] = fmaf(x[h4 + 1], cf.y, -mm.y);
+              y[h4 + 2] = fmaf(x[h4 + 2], cf.z, -mm.z);
+              y[h4 + 3] = fmaf(x[h4 + 3], cf.w, -mm.w);
             }
             mask(y);
           };
@@ -717,12 +852,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           if (soft_bar_or(grp, i == 0 || ymax > 8.f)) {
             {
               float x[HG];
-              {
-                uint32_t r[HG];
-                load_s(r);
+              load_s(x);
 #pragma unroll
-                for (int h = 0; h < HG; ++h) x[h] = __uint_as_float(r[h]) * sl2;
-              }
+              for (int h = 0; h < HG; ++h) x[h] *= C::F8N ? cf_s[hg0 + h] : sl2;
               mask(x);
               soft_reduce_max<C>(x, grp, sub, lane, red, fin, R);
             }
@@ -749,8 +881,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               wait(bars.pv_done((tg - 1) % C::PB), ((tg - 1) / C::PB) & 1);
               tc::fence_after();
 #pragma unroll 1
-              for (int c0 = 0; c0 < HG; c0 += HCH) {  // rare: kept small
-                const uint32_t ta = trow + C::TM_O + ob * NR + hg0 + c0;
+              for (int cc = 0; cc < (C::F8N ? 2 : 1) * HG; cc += HCH) {  // rare: kept small
+                // (F8N: the columns of both P terms of the group's heads)
+                const int c0 = cc % HG;
+                const uint32_t ta = trow + C::TM_O + ob * C::NM + (cc / HG) * NR + hg0 + c0;
                 uint32_t r[32];
                 if constexpr (HCH == 32) {
                   tc::ld_32x32b_x32(ta, r);
@@ -770,14 +904,32 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               tc::wait_st();
             }
           }
-          // row R of P^T (position R; the group's heads): 2^y, packed in pairs
+          // row R of P^T (position R; the group's heads): 2^y, packed in
+          // pairs; F8N: P in f16, then its two E4M3 terms P_hi = e4m3(P) and
+          // P_lo = e4m3(16 (P - P_hi)) (P <= 2^8 under the lazy max, so
+          // neither saturates), HG codes of each
           uint32_t pk[HG / 2];
 #pragma unroll
           for (int h = 0; h < HG; h += 2) {
             const float p0 = tc::ex2(y[h]), p1 = tc::ex2(y[h + 1]);
             lp[h] += p0;
             lp[h + 1] += p1;
-            pk[h >> 1] = C::FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+            if constexpr (C::F8N) {
+              const uint32_t ph = pack_f16x2(p0, p1);
+              const uint32_t c_hi = f16x2_to_e4m3x2(ph);
+              const uint32_t c_lo = f16x2_to_e4m3x2(hmul2_16(hsub2_u32(ph, e4m3x2_to_f16x2(c_hi))));
+              // hi codes fill the first HG/4 words, lo codes the next HG/4
+              const int w = h >> 2, sh = (h & 2) * 8;
+              if ((h & 2) == 0) {
+                pk[w] = c_hi;
+                pk[HG / 4 + w] = c_lo;
+              } else {
+                pk[w] |= c_hi << sh;
+                pk[HG / 4 + w] |= c_lo << sh;
+              }
+            } else {
+              pk[h >> 1] = C::FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+            }
           }
           // the P buffer was last read by the P.V of tile tg - PB
           const int pb = tg % C::PB;
@@ -787,21 +939,25 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const int swz = (R >> C::P_SWZ_SHIFT) & C::P_SWZ_MASK;
 #pragma unroll
             for (int c = 0; c < HG / 8; ++c) {
+              // F8N: chunks [0, HG/16) hold the hi codes, the next HG/16 the
+              // lo codes (the row is NR hi codes, then NR lo codes; HG = NR)
               const int chunk = (hg0 >> 3) + c;
               asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(row + ((chunk ^ swz) << 4)),
                            "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
                            : "memory");
             }
           }
-          if (!C::FP8 && grp == 0 && !valid && !dead && mbar_wait(pipe.full(st), (tg / ST) & 1)) {
+          if (!C::CONV && grp == 0 && !valid && !dead && mbar_wait(pipe.full(st), (tg / ST) & 1)) {
             // position past L: its V row may hold anything (NaN included) and
-            // 0 * NaN = NaN inside the MMA, so clear it (after it landed)
+            // 0 * NaN = NaN inside the MMA, so clear it (after it landed;
+            // bf16: two 128-byte boxes, E4M3: one)
             const uint32_t a = pipe.v_tile(st) + R * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
               asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(a + 16 * c), "r"(0u) : "memory");
-              asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(a + Pipe::BOX_BYTES + 16 * c), "r"(0u)
-                           : "memory");
+              if (!C::FP8)
+                asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(a + Pipe::BOX_BYTES + 16 * c), "r"(0u)
+                             : "memory");
             }
           }
           fence_proxy_async_smem();
@@ -845,6 +1001,31 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const size_t orow_b = MULTI ? (size_t)b * p.tokens * p.heads_q + (size_t)(h_first / p.n_rep) * p.rep_kv
                                     : (size_t)b * p.H + h_first;
         const int d4 = 32 * sub + (lane & ~3);
+        // columns [c0, c0 + HCH) of the group's heads of O^T (dimension R):
+        // F8N adds the P_lo term's columns / 16
+        auto load_o = [&](int c0, float(&o)[32]) {
+          uint32_t r[32];
+          if constexpr (HCH == 32) {
+            tc::ld_32x32b_x32(trow + C::TM_O + ob * C::NM + hg0 + c0, r);
+          } else {
+            tc::ld_32x32b_x16(trow + C::TM_O + ob * C::NM + hg0 + c0, r);
+          }
+          if constexpr (C::F8N) {
+            uint32_t r1[32];
+            if constexpr (HCH == 32) {
+              tc::ld_32x32b_x32(trow + C::TM_O + ob * C::NM + NR + hg0 + c0, r1);
+            } else {
+              tc::ld_32x32b_x16(trow + C::TM_O + ob * C::NM + NR + hg0 + c0, r1);
+            }
+            tc::wait_ld();
+#pragma unroll
+            for (int c = 0; c < HCH; ++c) o[c] = fmaf(__uint_as_float(r1[c]), 0.0625f, __uint_as_float(r[c]));
+          } else {
+            tc::wait_ld();
+#pragma unroll
+            for (int c = 0; c < HCH; ++c) o[c] = __uint_as_float(r[c]);
+          }
+        };
         if (!whole) {
           // a cut unit's partial: thread R writes dimension R of every head
           // (consecutive lanes, consecutive words: each warp store is one
@@ -852,16 +1033,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           float *orow = p.o_part + (size_t)slot * p.heads_per_cta * D + R;
 #pragma unroll 1
           for (int c0 = 0; c0 < (GQA_SLOT_OK(p, slot, nh - 1) ? HG : 0); c0 += HCH) {
-            uint32_t r[32];
-            if constexpr (HCH == 32) {
-              tc::ld_32x32b_x32(trow + C::TM_O + ob * NR + hg0 + c0, r);
-            } else {
-              tc::ld_32x32b_x16(trow + C::TM_O + ob * NR + hg0 + c0, r);
-            }
-            tc::wait_ld();
+            float o[32];
+            load_o(c0, o);
 #pragma unroll
             for (int c = 0; c < HCH; ++c)
-              if (hg0 + c0 + c < nh) orow[(size_t)(hg0 + c0 + c) * D] = __uint_as_float(r[c]) * vscale;
+              if (hg0 + c0 + c < nh) orow[(size_t)(hg0 + c0 + c) * D] = o[c] * vscale;
           }
         }
         // a whole unit goes to out: thread R holds output dimension R of
@@ -872,18 +1048,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // columns its size (instruction fetch), not its loads, is what it costs
 #pragma unroll 1
         for (int c0 = 0; c0 < (whole ? HG : 0); c0 += HCH) {
-          uint32_t r[32];
-          if constexpr (HCH == 32) {
-            tc::ld_32x32b_x32(trow + C::TM_O + ob * NR + hg0 + c0, r);
-          } else {
-            tc::ld_32x32b_x16(trow + C::TM_O + ob * NR + hg0 + c0, r);
-          }
-          tc::wait_ld();
+          float o[32];
+          load_o(c0, o);
 #pragma unroll
           for (int q = 0; q < HCH; q += 4) {
             float v[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[q + i]) * vscale;
+            for (int i = 0; i < 4; ++i) v[i] = o[q + i] * vscale;
             quad_transpose(v, lane);
             const int h = hg0 + c0 + q + (lane & 3);
             if (h < nh) {
@@ -918,7 +1089,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         seg = nseg;
         have = next;
       }
-    } else if constexpr (C::FP8) {
+    } else if constexpr (C::CONV) {
       // ------------------------------------------------------------ FP8 converters
       // Thread R converts position R of every tile (R = the TMEM lane its
       // warp may access): its K row of 128 E4M3 codes (one 128-byte swizzled

@@ -60,8 +60,9 @@ typedef enum {
 #define GQA_DEVERR_ATTN_LEN 1   /* attention saw seq_lens[b] <= 0 or > Nmax */
 #define GQA_DEVERR_APPEND_LEN 2 /* kv_append saw seq_lens[b] < 0 or >= Nmax */
 #define GQA_DEVERR_TIMEOUT 4    /* a pipeline wait gave up after its time limit */
-#define GQA_DEVERR_RANGE 8      /* FP8 cache, groups of 8+ heads: a query value beyond the f16
-                                   range (|q| > 65504) of that path's tensor-core operands */
+#define GQA_DEVERR_RANGE 8      /* FP8 cache, groups of 33+ heads: a query value beyond the f16
+                                   range (|q| > 65504) of that path's tensor-core operands
+                                   (groups of 8..32 heads take any finite query) */
 #define GQA_DEVERR_BOUNDS 16    /* only in the checking build (libgqa_debug.so, compiled with
                                    GQA_DEBUG): an index outside its buffer was computed; the
                                    access was skipped.  The release library never sets it. */

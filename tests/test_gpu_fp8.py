@@ -123,3 +123,21 @@ def test_fp8_append_then_attend():
     torch.cuda.synchronize()
     assert_parity(out.double().cpu().numpy(), ref, "fp8 step")
     assert gqa.gqa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("H,G", [(64, 8), (32, 1)])
+def test_fp8_native_e4m3_path_takes_queries_of_any_magnitude(H, G):
+    """Groups of 8..32 heads run both MMAs on E4M3 operands, the query as two
+    E4M3 terms under a per-head power-of-two scale: heads whose queries span
+    1e-3 .. 1e5 (the last beyond the f16 range) still match the oracle, and
+    no range flag is raised."""
+    w = _w("fp8_qmag", 3, H, G, 640, 10200 + H)
+    lens = torch.tensor([640, 131, 17], dtype=torch.int32)
+    x = workloads.make_fp8_cache(w, lens)
+    mag = torch.tensor([10.0 ** ((h % 9) - 3) for h in range(H)], dtype=torch.float64)
+    x["q"] = (x["q"].double() * mag[None, :, None]).to(x["q"].dtype)
+    ref = oracle.decode_attention_fp8(x["q"], x["k_cache"], x["v_cache"], x["k_scale"], x["v_scale"], x["seq_lens"],
+                                      w.scale)
+    got = run_fp8(x, w.scale).double().cpu().numpy()
+    assert_parity(got, ref, "fp8 query magnitudes")
+    assert gqa.gqa_get_device_error() == 0
