@@ -52,6 +52,7 @@ METRIC = "GQA decode attention µs/step and achieved HBM GB/s (fraction of B300 
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6400.0
 TABLE_WORKLOADS = ["tiny", "mha", "gqa8", "mqa", "long"] + workloads.sweep_names()
+FP8_TABLE = ("mha", "gqa8", "mqa", "sweep_g8")  # decode workloads also timed over an FP8 cache
 CSRC = os.path.join(ROOT, "grouped_query_decode_kv_b300", "csrc")
 PROFILES = os.path.join(ROOT, "profiles")
 
@@ -815,7 +816,7 @@ def run_ours(args, world, rank, local):
         for name in workloads.multi_names():
             table_multi[name] = time_multi(workloads.workload(name), device, args.table_iters, 5, l2, mem_budget)
         table_fp8 = {}
-        for name in ("mha", "gqa8", "mqa", "sweep_g8"):
+        for name in FP8_TABLE:
             table_fp8[name] = time_fp8(workloads.workload(name), device, args.table_iters, l2, mem_budget)
         table_proj = {}
         for name in sorted(workloads.PROJECTIONS):
@@ -984,7 +985,7 @@ def run_table_only(args, local):
         for name in sorted(workloads.PROJECTIONS):
             rows[name] = time_projection(name, device, args.table_iters, l2, mem_budget)
     elif args.table_only == "fp8":
-        for name in ("mha", "gqa8"):
+        for name in FP8_TABLE:
             rows[name] = time_fp8(workloads.workload(name), device, args.table_iters, l2, mem_budget)
     else:
         for name in workloads.multi_names():

@@ -337,11 +337,11 @@ Plan make_plan(int B, int H, int G, int d, int Nmax, gqa_dtype_t dt, int split_t
   }
   P = std::max<long long>(1, std::min<long long>(P, std::min<long long>(tiles_full, 1 << 20)));
   pl.P = (int)P;
-  // tcgen05 kernel with room for k = 2..8 CTAs per unit of a full batch:
-  // launch in clusters of k, so that with equal lengths a unit's pieces meet
-  // in one cluster and merge through distributed shared memory (no
-  // workspace round trip, no merge kernel).  The grid keeps whole clusters
-  // and no more of them than can be resident at once.
+  // tcgen05 kernel with room for k = 2..4 CTAs per unit of a full batch:
+  // launch in clusters of k, each cluster taking one unit whole, so that a
+  // unit's pieces meet in one cluster and are merged by it after a cluster
+  // barrier (through the workspace in L2; no merge kernel).  The grid keeps
+  // whole clusters and no more of them than can be resident at once.
   if (split_tokens == 0 && pl.k.family == kTc && pl.units > 0) {
     const long long k = P / pl.units;
     if (k >= 2 && k <= 4) {

@@ -84,7 +84,12 @@ struct TcCfg {
   static constexpr int NQ = NR;
   static constexpr int HEADS = NR;
   static constexpr int PB = PB_;       // P^T buffers
-  static constexpr int UNIT_COST = 2;  // stream-K charge per unit, in tiles (gqa_schedule.cuh)
+  // stream-K charge per unit, in tiles (gqa_schedule.cuh).  A unit's fixed
+  // cost takes about the same time on every path, so it is worth more of the
+  // native E4M3 path's shorter tiles (FP8 GQA-8 with charge 2, 4, 6, 8:
+  // 37.0, 33.0, 31.7, 32.4 us per call; bf16 GQA-8 with 2, 3, 4: 49.0,
+  // 49.4, 49.7 us)
+  static constexpr int UNIT_COST = F8N ? 6 : 2;
   static_assert(NR == 16 || NR == 32 || NR == 64, "heads per unit");
   static_assert(PB == 1 || PB == 2, "P^T buffers");
   // softmax groups of four warps; group j owns the head columns

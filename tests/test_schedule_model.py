@@ -104,7 +104,7 @@ def test_schedule_covers_every_tile_once_and_merges_consistently(seed):
         else:
             lens = [rng.randint(0, Nmax) for _ in range(B)]
         _check(lens, Nmax, rng.choice([64, 128]), rng.choice([1, 2, 4, 8, 16]), rng.choice([1, 7, 148, 296]),
-               rng.choice([0, 1, 2, 3]))
+               rng.choice([0, 1, 2, 3, 6, 8, 12]))
 
 
 def test_charge_moves_real_tiles_away_from_ranges_with_many_units():
