@@ -71,17 +71,20 @@ def main():
     check(out.double().cpu().numpy(), ref, "multi")
     assert not gqa.gqa_get_device_error() & gqa.DEVERR_BOUNDS
     print("multi ok", flush=True)
-    w = workloads.Workload("dbg_fp8", 3, 64, 8, 128, 600, "bf16", ("uniform", 1, 600), 13300)
-    x = workloads.make_fp8_cache(w)
-    ref = oracle.decode_attention_fp8(x["q"], x["k_cache"], x["v_cache"], x["k_scale"], x["v_scale"],
-                                      x["seq_lens"], w.scale)
-    t = {n: v.to(dev) for n, v in x.items()}
-    out = torch.empty_like(t["q"])
-    gqa.gqa_decode_attention_fp8(t["q"], t["k_cache"], t["v_cache"], t["k_scale"], t["v_scale"], t["seq_lens"],
-                                 w.scale, out)
-    torch.cuda.synchronize()
-    check(out.double().cpu().numpy(), ref, "fp8")
-    assert not gqa.gqa_get_device_error() & gqa.DEVERR_BOUNDS
+    # FP8 cache: 8 heads per group (native E4M3 kernel, 16 head slots) and
+    # 32 (native E4M3 kernel, 32 head slots)
+    for name, H, G, seed in (("dbg_fp8", 64, 8, 13300), ("dbg_fp8_32", 32, 1, 13310)):
+        w = workloads.Workload(name, 3, H, G, 128, 600, "bf16", ("uniform", 1, 600), seed)
+        x = workloads.make_fp8_cache(w)
+        ref = oracle.decode_attention_fp8(x["q"], x["k_cache"], x["v_cache"], x["k_scale"], x["v_scale"],
+                                          x["seq_lens"], w.scale)
+        t = {n: v.to(dev) for n, v in x.items()}
+        out = torch.empty_like(t["q"])
+        gqa.gqa_decode_attention_fp8(t["q"], t["k_cache"], t["v_cache"], t["k_scale"], t["v_scale"],
+                                     t["seq_lens"], w.scale, out)
+        torch.cuda.synchronize()
+        check(out.double().cpu().numpy(), ref, name)
+        assert not gqa.gqa_get_device_error() & gqa.DEVERR_BOUNDS
     print("fp8 ok", flush=True)
     w = workloads.Workload("dbg_noalloc", 4, 32, 4, 128, 800, "bf16", ("uniform", 1, 800), 13400)
     x = workloads.make_inputs(w)

@@ -63,9 +63,13 @@ def test_fp8_attention_small(H, G):
     check_fp8(_w("fp8_small", 5, H, G, 700, 10000 + H + G), lens)
 
 
-def test_fp8_attention_empty_row_is_flagged_and_zero():
+@pytest.mark.parametrize("H,G", [(8, 4), (64, 8), (32, 1)])
+def test_fp8_attention_empty_row_is_flagged_and_zero(H, G):
+    """An empty sequence is flagged and its output rows are zero, on the
+    CUDA-core kernel (2 heads per group) and on the native E4M3 tcgen05
+    kernel (8 and 32 heads per group)."""
     lens = torch.tensor([0, 200, 37], dtype=torch.int32)
-    got = check_fp8(_w("fp8_empty", 3, 8, 4, 256, 10100), lens, expect_err=gqa.DEVERR_ATTN_LEN)
+    got = check_fp8(_w("fp8_empty", 3, H, G, 256, 10100 + H), lens, expect_err=gqa.DEVERR_ATTN_LEN)
     assert np.all(got[0] == 0)
 
 
