@@ -36,7 +36,8 @@
 //   warp 1     S^T MMA issuer (one thread) and TMEM owner
 //   warp 2     P.V MMA issuer (one thread)
 //   warps 3..  softmax and output, in SG groups of four (group 0 also
-//              loads Q); FP8: then four converter warps
+//              loads Q); FP8 with 33-64 heads: then four converter warps
+//              (8-32 heads use E4M3 MMAs on the landed tiles, no converters)
 // S^T is double-buffered in TMEM so that S of tile t+1 overlaps the softmax
 // of tile t; O^T is double-buffered across units.  Every mbarrier wait is
 // bounded (about one second), after which the CTA winds down and flags
@@ -1191,8 +1192,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (warp >= C::SOFT_WARP0 && warp < C::CONV_WARP0)
       merge_cluster_unit<C, MULTI>(p, range, threadIdx.x - 32 * C::SOFT_WARP0, C::SG * C::SOFT);
   }
-  // ---- teardown: every tcgen05 operation has completed (the MMA thread
-  // waited for its last commit); free the tensor memory
+  // ---- teardown: every tcgen05 operation has completed (the MMA threads
+  // waited for their last commits); free the tensor memory
   tc::fence_before();
   __syncthreads();
   if (warp == 1) {
