@@ -259,10 +259,13 @@ __device__ __forceinline__ void soft_reduce(float (&v)[C::HG], int grp, int sub,
 // of each warp stores its warp's HG maxima, and thread R < HG combines the
 // four warps'; afterwards every thread of the group can read the maximum of
 // its head h from fin[grp*HG + h].  Exact (a maximum does not depend on the
-// order); NaN inputs are ignored as by fmaxf.
+// order); NaN inputs are ignored as by fmaxf.  With m_first (a unit's first
+// tile) thread R also sets the running max of its head, m_first[grp*HG + R],
+// to that maximum, or keeps `floor` when the maximum does not exceed it by
+// more than 8, before the same final barrier.
 template <class C>
 __device__ __forceinline__ void soft_reduce_max(float (&v)[C::HG], int grp, int sub, int lane, float *red, float *fin,
-                                                int R) {
+                                                int R, float *m_first = nullptr, float floor = 0.f) {
   constexpr int HG = C::HG;
 #pragma unroll
   for (int h = 0; h < HG; ++h) asm volatile("redux.sync.max.f32 %0, %0, 0xffffffff;" : "+f"(v[h]));
@@ -273,7 +276,11 @@ __device__ __forceinline__ void soft_reduce_max(float (&v)[C::HG], int grp, int 
       *reinterpret_cast<float4 *>(rg + sub * HG + h) = make_float4(v[h], v[h + 1], v[h + 2], v[h + 3]);
   }
   soft_bar(grp);
-  if (R < HG) fin[grp * HG + R] = fmaxf(fmaxf(rg[R], rg[HG + R]), fmaxf(rg[2 * HG + R], rg[3 * HG + R]));
+  if (R < HG) {
+    const float t = fmaxf(fmaxf(rg[R], rg[HG + R]), fmaxf(rg[2 * HG + R], rg[3 * HG + R]));
+    fin[grp * HG + R] = t;
+    if (m_first) m_first[grp * HG + R] = t > floor + 8.f ? t : floor;
+  }
   soft_bar(grp);
 }
 
@@ -849,13 +856,50 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           wait(bars.s_full(sb), (tg >> 1) & 1);
           tc::fence_after();
           float y[HG];
-          compute_y(y);
-          float ymax = y[0];
+          // Lazy running max: it starts at a unit's first tile's maximum and
+          // then moves only where a logit beats it by more than 8 (log2
+          // units).  On the first tile one read of S serves both the maximum
+          // and y, and there is neither a vote nor a rescale.  Measured, this
+          // pays on the bf16 groups of 32 heads (sweep G=2 26.5 -> 26.2 us,
+          // MQA 15.7 -> 15.2 us) but costs the 16-head and E4M3 kernels
+          // (their larger code slows the steady tile: FP8 GQA-8 32.0 -> 32.9
+          // us) and gains nothing with 64 heads, which keep the general path.
+          constexpr bool FIRST_FAST = !C::FP8 && HG == 32;
+          bool rare;
+          if constexpr (FIRST_FAST) {
+            if (i == 0) {
+              float x[HG];
+              load_s(x);
 #pragma unroll
-          for (int h = 1; h < HG; ++h) ymax = fmaxf(ymax, y[h]);
-          // Lazy running max: it moves only where a logit beats it by more
-          // than 8 (log2 units), and always on a unit's first tile.
-          if (soft_bar_or(grp, i == 0 || ymax > 8.f)) {
+              for (int h = 0; h < HG; ++h) x[h] *= sl2;
+              mask(x);
+#pragma unroll
+              for (int h = 0; h < HG; ++h) y[h] = x[h];
+              soft_reduce_max<C>(x, grp, sub, lane, red, fin, R, m_s, kNoMax);
+#pragma unroll
+              for (int h4 = 0; h4 < HG; h4 += 4) {
+                const float4 mm = m4[h4 >> 2];
+                y[h4 + 0] -= mm.x;
+                y[h4 + 1] -= mm.y;
+                y[h4 + 2] -= mm.z;
+                y[h4 + 3] -= mm.w;
+              }
+              rare = false;
+            } else {
+              compute_y(y);
+              float ymax = y[0];
+#pragma unroll
+              for (int h = 1; h < HG; ++h) ymax = fmaxf(ymax, y[h]);
+              rare = soft_bar_or(grp, ymax > 8.f);
+            }
+          } else {
+            compute_y(y);
+            float ymax = y[0];
+#pragma unroll
+            for (int h = 1; h < HG; ++h) ymax = fmaxf(ymax, y[h]);
+            rare = soft_bar_or(grp, i == 0 || ymax > 8.f);
+          }
+          if (rare) {
             {
               float x[HG];
               load_s(x);
