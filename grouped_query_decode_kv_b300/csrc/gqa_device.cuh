@@ -269,15 +269,15 @@ __device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h2) {
   return r;
 }
 
-// f16 pair arithmetic on 32-bit words: a - b, and 16 * a (exact).
+// f16 pair arithmetic on 32-bit words: a - b, and 32 * a (exact).
 __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
-__device__ __forceinline__ uint32_t hmul2_16(uint32_t a) {
+__device__ __forceinline__ uint32_t hmul2_32(uint32_t a) {
   uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(0x4c004c00u));
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(0x50005000u));
   return r;
 }
 

@@ -26,7 +26,8 @@
 // units) is shared by the group through shared memory.  A tile first votes
 // whether any logit exceeds m[h] + 8; only then (always on a unit's first
 // tile) the tile's per-head maxima are reduced across the group's 128
-// threads and m moves, with O^T rescaled in TMEM.  P = 2^(S - m) is written
+// threads and m moves (to the tile's maximum, or P_LIFT below it), with O^T
+// rescaled in TMEM.  P = 2^(S - m) is written
 // to shared memory as bf16 (double-buffered where shared memory allows, so
 // that the softmax of tile t+1 need not wait for the P.V of tile t); the
 // l_R[h] are summed across threads once per unit.
@@ -63,19 +64,25 @@ namespace gqa {
 // E4M3 values, enter as two E4M3 terms each, a head's columns doubled:
 //   Q[h] = (Q_hi + Q_lo / 16) / qs_h   (qs_h a power of two per head that
 //                                        puts max |Q[h]| in [128, 256))
-//   P    =  P_hi + P_lo / 16           (P in f16 first; both terms E4M3)
+//   P    =  P_hi + P_lo / 32           (P in f16 first; both terms E4M3)
 // so S^T and O^T have 2*NR columns, term 0 in [0, NR) and term 1 in
 // [NR, 2*NR), combined by one FMA per head after the MMA.  The two Q terms
 // hold every bf16 query exactly (4 + 4 significant bits) while qs_h keeps a
-// head's elements in the E4M3 normal range; the two P terms keep 8
-// significant bits (bf16 P in the bf16 path has 8), for p >= 2^-13 (smaller
-// probabilities, 2^-13 or less of the running maximum, are dropped).
+// head's elements in the E4M3 normal range.  P's range is set by where the
+// running max sits: when it moves, it moves to P_LIFT = 2 (log2 units) below
+// the tile's maximum, so the largest P is 2^2 and may grow to 2^8 before the
+// next move.  The two terms keep 8 significant bits (bf16 P in the bf16
+// path has 8) for P >= 2^-6 and reach down to P = 2^-15: a probability under
+// 2^-17 of the largest one is dropped.  (A larger lift reaches further but
+// leaves less room before the next move: measured, 6 made the rescales
+// frequent and the calls 10-30 % slower; 2 costs nothing measurable.)
 template <int NR_, int STAGES_, int PB_, bool FP8_ = false, int SG_ = 1, int VSTG_ = 2, bool F8N_ = false>
 struct TcCfg {
   static constexpr bool FP8 = FP8_;
   static constexpr bool F8N = FP8_ && F8N_;          // native E4M3 MMAs, no converter warps
   static constexpr bool CONV = FP8_ && !F8N_;        // converter warps (K to TMEM, V to f16 staging)
   static constexpr int NM = F8N ? 2 * NR_ : NR_;     // N of both MMAs (two terms per head with F8N)
+  static constexpr int P_LIFT = F8N ? 2 : 0;         // where a moved running max sits below the tile max
   static constexpr int VSTG = VSTG_;  // FP8: f16 V staging buffers
   static_assert(VSTG >= 2 && VSTG <= 3, "V staging buffers");
   static constexpr int D = 128;
@@ -913,8 +920,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               const float tmax = fin[hg0 + R], mo = m_s[hg0 + R];
               float corr = 1.f;
               if (tmax > mo + 8.f) {
-                corr = merge_weight(mo, tmax);
-                m_s[hg0 + R] = tmax;
+                const float mn = tmax - (float)C::P_LIFT;
+                corr = merge_weight(mo, mn);
+                m_s[hg0 + R] = mn;
                 moved_mine = true;
               }
               corr_s[hg0 + R] = corr;
@@ -956,8 +964,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
           // row R of P^T (position R; the group's heads): 2^y, packed in
           // pairs; F8N: P in f16, then its two E4M3 terms P_hi = e4m3(P) and
-          // P_lo = e4m3(16 (P - P_hi)) (P <= 2^8 under the lazy max, so
-          // neither saturates), HG codes of each
+          // P_lo = e4m3(32 (P - P_hi)) (P <= 2^8 under the lazy max, so
+          // |P - P_hi| <= 8 and neither saturates), HG codes of each
           uint32_t pk[HG / 2];
 #pragma unroll
           for (int h = 0; h < HG; h += 2) {
@@ -967,7 +975,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if constexpr (C::F8N) {
               const uint32_t ph = pack_f16x2(p0, p1);
               const uint32_t c_hi = f16x2_to_e4m3x2(ph);
-              const uint32_t c_lo = f16x2_to_e4m3x2(hmul2_16(hsub2_u32(ph, e4m3x2_to_f16x2(c_hi))));
+              const uint32_t c_lo = f16x2_to_e4m3x2(hmul2_32(hsub2_u32(ph, e4m3x2_to_f16x2(c_hi))));
               // hi codes fill the first HG/4 words, lo codes the next HG/4
               const int w = h >> 2, sh = (h & 2) * 8;
               if ((h & 2) == 0) {
@@ -1052,7 +1060,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                     : (size_t)b * p.H + h_first;
         const int d4 = 32 * sub + (lane & ~3);
         // columns [c0, c0 + HCH) of the group's heads of O^T (dimension R):
-        // F8N adds the P_lo term's columns / 16
+        // F8N adds the P_lo term's columns / 32
         auto load_o = [&](int c0, float(&o)[32]) {
           uint32_t r[32];
           if constexpr (HCH == 32) {
@@ -1069,7 +1077,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
             tc::wait_ld();
 #pragma unroll
-            for (int c = 0; c < HCH; ++c) o[c] = fmaf(__uint_as_float(r1[c]), 0.0625f, __uint_as_float(r[c]));
+            for (int c = 0; c < HCH; ++c) o[c] = fmaf(__uint_as_float(r1[c]), 0.03125f, __uint_as_float(r[c]));
           } else {
             tc::wait_ld();
 #pragma unroll

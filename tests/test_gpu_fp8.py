@@ -145,3 +145,35 @@ def test_fp8_native_e4m3_path_takes_queries_of_any_magnitude(H, G):
     got = run_fp8(x, w.scale).double().cpu().numpy()
     assert_parity(got, ref, "fp8 query magnitudes")
     assert gqa.gqa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("H,G", [(16, 2), (32, 1)])
+def test_fp8_native_path_keeps_a_long_tail_of_small_probabilities(H, G):
+    """In every sequence one dominant position (the first) and 2047 others
+    whose logits sit 15 (log2 units) below it: each tail probability is
+    2^-15 of the maximum, together ~6 % of the mass.  With 80 sequences a
+    CTA's piece of the split holds most of a sequence, dominant position
+    included, so its running maximum is the dominant logit.  The native E4M3
+    kernel sets a moved running maximum 2 below the tile's maximum, so its
+    two E4M3 terms of P reach down to 2^-17 of the largest probability and
+    the tail is kept.  V is -1 at the dominant position and +1 in the tail
+    (a tail of random V would average out): a P whose terms stop at 2^-14 of
+    the maximum moves the output from -0.881 to -0.941."""
+    N, B = 2048, 80
+    w = _w("fp8_tail", B, H, G, N, 10300 + H)
+    x = workloads.make_fp8_cache(w, torch.full((B,), N, dtype=torch.int32))
+    k, v = x["k_cache"], x["v_cache"]
+    k[:, :, 0, :] = 0x38        # E4M3 1.0 at the dominant position
+    k[:, :, 1:, :] = 0x30       # E4M3 0.5 everywhere else
+    v[:, :, 0, :] = 0xB8        # V = -1 at the dominant position, +1 in the tail:
+    v[:, :, 1:, :] = 0x38       # a dropped tail would move the output by ~0.06
+    x["k_scale"] = torch.full_like(x["k_scale"], 1.0 / 128)
+    x["v_scale"] = torch.ones_like(x["v_scale"])
+    # logit gap = scale * q * 128 * 0.5 / 128 per unit of q; 15 in log2 units
+    gap_q = 15.0 / (w.scale * 0.5 * 1.4426950408889634)
+    x["q"] = torch.full_like(x["q"], gap_q).to(torch.bfloat16)
+    ref = oracle.decode_attention_fp8(x["q"], x["k_cache"], x["v_cache"], x["k_scale"], x["v_scale"], x["seq_lens"],
+                                      w.scale)
+    got = run_fp8(x, w.scale).double().cpu().numpy()
+    assert_parity(got, ref, "fp8 long tail")
+    assert gqa.gqa_get_device_error() == 0
