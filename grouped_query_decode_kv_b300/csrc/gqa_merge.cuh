@@ -123,55 +123,76 @@ __device__ __forceinline__ void finish_split_unit(const SplitParams &p, const Se
   }
 }
 
+// Atomics of the fused step's counter word at GPU scope with acquire and
+// release semantics: the add (or the swap) that counts a CTA releases what the
+// CTA did before it (its threads' reads of the lengths, ordered by the
+// barrier ahead of the arrival) and acquires what the CTAs counted earlier
+// did, so the CTA that counts last may then write the lengths.
+__device__ __forceinline__ unsigned long long atom_add_acq_rel(unsigned long long *a, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(a), "l"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ unsigned long long atom_cas_acq_rel(unsigned long long *a, unsigned long long cmp,
+                                                               unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;" : "=l"(old) : "l"(a), "l"(cmp), "l"(v) : "memory");
+  return old;
+}
+
 // Counts one more finished CTA of a fused decode step on the 64-bit word
-// (call epoch << 32) | count and returns the new count.  A word that carries
-// another tag (left by another call, or memory never cleared) is first
-// replaced by (epoch << 32) | 0 with one compare-and-swap; that swap can only
-// succeed before any CTA of this call has counted, because every count is
-// added to a word that already holds this call's tag.  So a stale word never
-// takes part in the count.  The counts themselves are plain atomic adds: a
-// compare-and-swap loop per arrival retries O(P) times under the grid's
-// contention.  Returns 0 (never a valid count) when the tag could not be
-// installed within a bounded number of tries.
+// (call epoch << 32) | count and returns the new count, 1..P for the grid's
+// P CTAs.  Most CTAs count with one atomic add: the add returns the word as
+// it was, and if that carried this call's tag the add was the count.  An add
+// that found another tag (the previous call's, or memory never cleared) went
+// into a stale word; that CTA then installs (epoch << 32) | 1, counting
+// itself, with a compare-and-swap, or adds again once it sees that another
+// CTA installed the tag.  A stale word never takes part in the count: the
+// swap replaces it whole, and after it the word keeps this call's tag to the
+// end of the call.  Each failed swap follows a change of the word by another
+// CTA (at most one stale add each, then the tag), so a CTA retries at most P
+// times; past that bound it flags GQA_DEVERR_TIMEOUT and returns 0, never a
+// valid count.  The CTA counted last is the one that returns P.
 __device__ __forceinline__ unsigned arrive_step(unsigned long long *cnt, unsigned epoch) {
   const unsigned long long tagged = (unsigned long long)epoch << 32;
-  unsigned long long cur = __ldcg(cnt);
-  for (int tries = 0; (unsigned)(cur >> 32) != epoch; ++tries) {
-    if (tries == 64) {
+  unsigned long long old = atom_add_acq_rel(cnt, 1ull);
+  if ((unsigned)(old >> 32) == epoch) return (unsigned)old + 1u;
+  unsigned long long cur = old + 1ull;  // the word as this add left it
+  for (unsigned tries = 0;; ++tries) {
+    if ((unsigned)(cur >> 32) == epoch) return (unsigned)atom_add_acq_rel(cnt, 1ull) + 1u;
+    if (tries > gridDim.x) {
       flag_error(GQA_DEVERR_TIMEOUT);
       return 0u;
     }
-    const unsigned long long seen = atomicCAS(cnt, cur, tagged);
-    cur = seen == cur ? tagged : seen;
+    const unsigned long long seen = atom_cas_acq_rel(cnt, cur, tagged | 1ull);
+    if (seen == cur) return 1u;
+    cur = seen;
   }
-  return (unsigned)(atomicAdd(cnt, 1ull) + 1ull);
 }
 
 // End of a fused decode step, called by all `nthr` threads of a CTA after all
-// of the CTA's work (every CTA comes, busy or idle, also after a timed-out
-// wait).  The last CTA of the grid to get here advances seq_lens[b] to
-// L_b + 1 for every row that took the append, and puts the count back to
-// zero under the same tag (so that a graph replay of the call, which keeps
-// its epoch, starts from zero too).  No CTA reads the lengths after its own
-// arrival, so the update cannot be seen half way through the call.  `flag`
-// is a shared word that broadcasts thread 0's finding.
+// of the CTA's work and a barrier of the whole CTA (every CTA comes, busy or
+// idle, also after a timed-out wait).  The last CTA of the grid to count
+// advances seq_lens[b] to L_b + 1 for every row that took the append, and
+// puts the count back to zero under the same tag (so that a graph replay of
+// the call, which keeps its epoch, starts from zero too; a plain store, since
+// every CTA of the call has counted).  No CTA reads the lengths after its own
+// arrival, so the update cannot be seen half way through the call, and the
+// lengths the last CTA reads are those the whole call read.  `flag` is a
+// shared word that broadcasts thread 0's finding.
 __device__ __forceinline__ void finish_step(const SplitParams &p, int tid, int nthr, volatile int *flag) {
   if (tid == 0) {
     bool last = true;
     if (p.done_cnt) {
-      __threadfence();
       last = arrive_step(p.done_cnt, p.epoch) == gridDim.x;
-      if (last) {
-        __threadfence();
-        atomicExch(p.done_cnt, (unsigned long long)p.epoch << 32);
-      }
+      if (last) *reinterpret_cast<volatile unsigned long long *>(p.done_cnt) = (unsigned long long)p.epoch << 32;
     }
     *flag = last;
   }
   __syncthreads();
   if (!*flag) return;
   for (int b = tid; b < p.B; b += nthr) {
-    const int L = __ldcg(p.seq_lens_w + b);
+    const int L = __ldg(p.seq_lens + b);
     if (append_ok(L, p.Nmax)) p.seq_lens_w[b] = L + 1;
   }
 }

@@ -124,34 +124,41 @@ def test_charge_moves_real_tiles_away_from_ranges_with_many_units():
 MASK64 = (1 << 64) - 1
 
 
-def _arrive_step(word, epoch):
+def _arrive_step(word, epoch, P):
     """One CTA's arrival on the fused step's counter word (gqa_merge.cuh,
     arrive_step), as a generator that yields before every access to the
     shared word so that a scheduler can interleave the CTAs at will.
     `word` is a one-element list (the word in L2); returns the count."""
     tagged = epoch << 32
     yield
-    cur = word[0]                      # __ldcg
+    old = word[0]                      # atom_add_acq_rel(cnt, 1)
+    word[0] = (old + 1) & MASK64
+    if (old >> 32) == epoch:
+        return (old + 1) & 0xFFFFFFFF
+    cur = (old + 1) & MASK64
     tries = 0
-    while (cur >> 32) != epoch:
-        assert tries < 64
+    while True:
+        if (cur >> 32) == epoch:
+            yield
+            old = word[0]              # atom_add_acq_rel(cnt, 1)
+            word[0] = (old + 1) & MASK64
+            assert (old >> 32) == epoch
+            return (old + 1) & 0xFFFFFFFF
+        assert tries <= P              # the kernel flags a timeout past this bound
         tries += 1
         yield
-        seen = word[0]                 # atomicCAS(cnt, cur, tagged)
+        seen = word[0]                 # atom_cas_acq_rel(cnt, cur, tagged | 1)
         if seen == cur:
-            word[0] = tagged
-        cur = tagged if seen == cur else seen
-    yield
-    old = word[0]                      # atomicAdd(cnt, 1)
-    word[0] = (old + 1) & MASK64
-    return (old + 1) & 0xFFFFFFFF
+            word[0] = tagged | 1
+            return 1
+        cur = seen
 
 
 def _run_step_arrivals(word, epoch, P, rng):
     """All P CTAs of one call arrive in a random interleaving; the one that
     counts P resets the word to (epoch << 32) | 0 (finish_step).  Returns
     the order of arrival (by the atomic add) and the CTAs elected last."""
-    gens = {c: _arrive_step(word, epoch) for c in range(P)}
+    gens = {c: _arrive_step(word, epoch, P) for c in range(P)}
     for g in gens.values():
         next(g)
     order, elected = [], []
@@ -191,6 +198,43 @@ def test_step_counter_stale_words_never_elect_a_wrong_last_cta(seed):
             assert sorted(order) == list(range(P))
             assert elected == [order[-1]], (P, hex(word[0]), elected, order[-1])
             assert word[0] == epoch << 32
+
+
+@pytest.mark.parametrize("P", [2, 7, 148])
+def test_step_counter_retry_bound_holds_in_the_worst_interleaving(P):
+    """One CTA's swap fails after every other CTA's add into the stale word
+    and once more when another CTA installs the tag: it still counts within
+    the kernel's bound of P retries, and exactly the last CTA is elected."""
+    epoch = 77
+    word = [(5 << 32) | 3]
+    gens = {c: _arrive_step(word, epoch, P) for c in range(P)}
+    for g in gens.values():
+        next(g)
+    order, elected = [], []
+
+    def step(c):
+        try:
+            next(gens[c])
+        except StopIteration as stop:
+            del gens[c]
+            order.append(c)
+            if stop.value == P:
+                elected.append(c)
+                word[0] = epoch << 32
+
+    step(0)                            # CTA 0 adds into the stale word
+    for c in range(1, P):
+        step(c)                        # another stale add ...
+        step(0)                        # ... so CTA 0's swap fails
+    if P > 1:
+        step(P - 1)                    # the last CTA to add saw the word as it is: its swap installs the tag
+        assert word[0] == (epoch << 32) | 1
+        step(0)                        # CTA 0's swap fails on the tag, then it adds
+    while gens:
+        step(min(gens))
+    assert sorted(order) == list(range(P))
+    assert elected == [order[-1]]
+    assert word[0] == epoch << 32
 
 
 def test_step_counter_fixed_offset_is_the_plain_count_without_a_tag():
