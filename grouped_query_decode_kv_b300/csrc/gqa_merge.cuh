@@ -23,10 +23,11 @@
 namespace gqa {
 
 struct UnitMerge {
-  int last;   // this CTA merges the unit
-  int slot0;  // partial slot of the unit's first CTA
-  int c_lo;   // the unit's first CTA
-  int n;      // number of CTAs (partials) of the unit
+  int last;        // this CTA merges the unit
+  int slot0;       // partial slot of the unit's first CTA
+  int c_lo;        // the unit's first CTA
+  int n;           // number of CTAs (partials) of the unit
+  int reads_done;  // fused step: warps that have read the lengths for the last time
 };
 
 // Counts one more finished CTA of the unit and returns the new count.  The
@@ -192,6 +193,56 @@ __device__ __forceinline__ void finish_step(const SplitParams &p, int tid, int n
   __syncthreads();
   if (!*flag) return;
   for (int b = tid; b < p.B; b += nthr) {
+    const int L = __ldg(p.seq_lens + b);
+    if (append_ok(L, p.Nmax)) p.seq_lens_w[b] = L + 1;
+  }
+}
+
+// Fused step, early arrival (the CUDA-core kernel): the CTA counts on the
+// step word as soon as none of its threads will read the lengths again,
+// which is long before its work ends, so the count and the last CTA's update
+// of the lengths overlap the CTAs' remaining work instead of following it.
+// Each consumer warp signals once, after its last read (the start of its
+// last segment, or the end of its loop); the producer warp, whose reads end
+// with its last copy, waits for those signals and counts the CTA.
+
+// One consumer warp: every lane has done its last read of the lengths.
+__device__ __forceinline__ void signal_lengths_read(UnitMerge *um, int lane) {
+  __syncwarp();
+  if (lane == 0)
+    asm volatile("red.release.cta.shared::cta.add.u32 [%0], 1;" ::"r"(smem_u32(&um->reads_done)) : "memory");
+}
+
+// The producer warp, after its own last read: waits (bounded) for `n`
+// consumer warps' signals, then counts the CTA; the warp of the CTA counted
+// last advances the lengths.  After a timed-out wait it still counts, as
+// every CTA must, with GQA_DEVERR_TIMEOUT set.
+__device__ __forceinline__ void arrive_step_early(const SplitParams &p, UnitMerge *um, int n, int lane) {
+  int last = 0;
+  if (lane == 0) {
+    const uint32_t a = smem_u32(&um->reads_done);
+    auto seen = [&] {
+      uint32_t v;
+      asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+      return (int)v;
+    };
+    if (seen() < n) {
+      const unsigned long long t0 = global_timer_ns();
+      while (seen() < n) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          flag_error(GQA_DEVERR_TIMEOUT);
+          break;
+        }
+        __nanosleep(100);
+      }
+    }
+    last = p.done_cnt ? arrive_step(p.done_cnt, p.epoch) == gridDim.x : 1;
+    if (last && p.done_cnt)
+      *reinterpret_cast<volatile unsigned long long *>(p.done_cnt) = (unsigned long long)p.epoch << 32;
+  }
+  __syncwarp();
+  if (!__shfl_sync(0xffffffffu, last, 0)) return;
+  for (int b = lane; b < p.B; b += 32) {
     const int L = __ldg(p.seq_lens + b);
     if (append_ok(L, p.Nmax)) p.seq_lens_w[b] = L + 1;
   }

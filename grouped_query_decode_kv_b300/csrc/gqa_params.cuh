@@ -25,7 +25,8 @@ struct SplitParams {
   int P;                    // CTAs of the split kernel (partial slots: 2P)
   // Fused decode step (append != 0): the new token's K/V rows k_new/v_new
   // [B*G, D] go to cache row L_b of every (b, g) before attention over
-  // L_b + 1 positions; the last CTA to finish then sets seq_lens[b] = L_b + 1.
+  // L_b + 1 positions; the last CTA to stop reading the lengths then sets
+  // seq_lens[b] = L_b + 1.
   int append;
   const void *k_new, *v_new;
   void *k_cache, *v_cache;  // [B*G, Nmax, D]

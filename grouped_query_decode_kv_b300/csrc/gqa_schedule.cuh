@@ -331,6 +331,11 @@ struct SegmentCursor {
       if (pos >= end) return false;
       long long span = unit_span(tiles_b, cost);
       while (pos >= pre_b + span * s.units_per_b) {
+        // pos starts a row here, so a unit's charge comes first: with no
+        // more than that left in the range there is no real tile, and the
+        // next row's length is not read (after a CTA's last segment the
+        // cursor reads no length)
+        if (end - pos <= cost) return false;
         pre_b += span * s.units_per_b;
         ++b;
         tiles_b = row_tiles(s, b);

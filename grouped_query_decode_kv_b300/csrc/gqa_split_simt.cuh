@@ -169,12 +169,15 @@ __global__ void __launch_bounds__(C::THREADS)
       if (lane == 0) *range_smem = r;
     }
   }
+  if (threadIdx.x == 0) um->reads_done = 0;
   __syncthreads();
   griddep_launch_dependents();
   const CtaRange range = *range_smem;
-  if (range.begin < range.end && warp == C::CONSUMER_WARPS) {
-    produce_range(pipe, sp, range, &tmK, &tmV, C::BOX_ELEMS, p.G, p.head_chunks, p, lane);
+  if (warp == C::CONSUMER_WARPS) {
+    if (range.begin < range.end) produce_range(pipe, sp, range, &tmK, &tmV, C::BOX_ELEMS, p.G, p.head_chunks, p, lane);
+    if (p.append) arrive_step_early(p, um, C::CONSUMER_WARPS, lane);
   }
+  bool lens_read = !p.append || warp == C::CONSUMER_WARPS;  // this warp has signalled (or need not)
   if (range.begin < range.end && warp != C::CONSUMER_WARPS) {
 
   const int tg = lane >> 3, j = lane & 7;
@@ -190,6 +193,13 @@ __global__ void __launch_bounds__(C::THREADS)
     const int h_first = g * p.n_rep + hc * NH;
     const int nh = min(NH, p.n_rep - hc * NH);
     const int L = attn_len(p.seq_lens, b, p.Nmax, p.append);
+    if (!lens_read && cur.end - cur.pos <= cur.cost) {
+      // a fused step, and the CTA's last segment: the cursor now ends on a
+      // unit boundary (or the range's end) with at most a unit's charge
+      // left, so no real tile follows and it reads no more lengths
+      signal_lengths_read(um, lane);
+      lens_read = true;
+    }
     // FP8 cache: K's per-head scale joins the logit scale, V's multiplies the
     // unit's result
     const float sl2 = C::FP8 ? p.scale_log2 * __ldg(p.k_scale + g) : p.scale_log2;
@@ -385,10 +395,7 @@ __global__ void __launch_bounds__(C::THREADS)
     consumer_bar_sync(C::CONSUMER_WARPS * 32);  // scratch free for the next unit
   }
   }
-  if (p.append) {
-    __syncthreads();
-    finish_step(p, threadIdx.x, blockDim.x, &um->last);
-  }
+  if (!lens_read) signal_lengths_read(um, lane);  // empty range, or a timed-out wait ended the loop
 }
 
 }  // namespace gqa

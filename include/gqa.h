@@ -144,7 +144,7 @@ int gqa_decode_attention_ex(const void *q, const void *k_cache, const void *v_ca
  *   gqa_decode_attention(q, k_cache, v_cache, seq_lens, scale, out, ...);
  * on the same stream (bit for bit), without the second launch: the thread
  * block that loads the tile holding row L_b writes k_new/v_new there first,
- * and the last block to finish advances seq_lens.
+ * and the last block to stop reading seq_lens advances it.
  *
  *   q [B,H,d], k_new/v_new [B,G,d], k_cache/v_cache [B,G,Nmax,d] (updated),
  *   seq_lens [B] int32 DEVICE memory (read, then L_b + 1 where appended),

@@ -61,6 +61,75 @@ def segments(c, tiles, T, P, U, cost):
     return out
 
 
+def cursor_calls(c, tiles, T, P, U, cost):
+    """SegmentCursor::next as the device runs it, call by call, with its early
+    end (a row start with no more than a unit's charge left in the range
+    ends the walk before that row's length is read).  Returns, per call, the
+    segment (or None for the call that returns false), the cursor position
+    after the call and the lengths read during the call."""
+    if c >= P:
+        return [(None, 0, 0)]
+    pos, end = cta_start(c, T, P), cta_start(c + 1, T, P)
+    pre, b = 0, 0
+    if pos < end:  # the plan hands the cursor the row that holds its first tile
+        while pos >= pre + span(tiles[b], cost) * U:
+            pre += span(tiles[b], cost) * U
+            b += 1
+    tiles_b = tiles[b] if pos < end else 0
+    calls = []
+    while True:
+        reads, seg = 0, None
+        while True:
+            if pos >= end:
+                break
+            sp = span(tiles_b, cost)
+            stop = False
+            while pos >= pre + sp * U:
+                if end - pos <= cost:
+                    stop = True
+                    break
+                pre += sp * U
+                b += 1
+                tiles_b = tiles[b]
+                reads += 1
+                sp = span(tiles_b, cost)
+            if stop:
+                break
+            uib, v0 = divmod(pos - pre, sp)
+            v1 = min(v0 + (end - pos), sp)
+            pos += v1 - v0
+            if v1 <= cost:
+                continue
+            seg = dict(b=b, uib=uib, t0=max(v0 - cost, 0), t1=v1 - cost, tiles=tiles_b,
+                       unit_first=pre + uib * sp + cost)
+            break
+        calls.append((seg, end - pos, reads))
+        if seg is None:
+            return calls
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_cursor_last_segment_test_and_no_length_read_after_it(seed):
+    """The fused step's early arrival: a CTA's segment is its last exactly
+    when the range has no more than a unit's charge left after it; the early
+    end of the walk gives the same segments as the plain walk; and the call
+    that ends the walk reads no length."""
+    rng = random.Random(seed)
+    for _ in range(60):
+        B = rng.choice([1, 2, 5, 16, 40])
+        Nmax = rng.choice([128, 1000, 4096])
+        lens = [rng.choice([0, 1, 127, 128, 129, rng.randint(0, Nmax)]) for _ in range(B)]
+        U, P0 = rng.choice([1, 2, 8]), rng.choice([1, 3, 17, 148])
+        tiles, T, P, cost = plan(lens, Nmax, 128, U, P0, 2)
+        for c in range(P0):
+            calls = cursor_calls(c, tiles, T, P, U, cost)
+            segs = [sg for sg, _, _ in calls if sg is not None]
+            assert segs == segments(c, tiles, T, P, U, cost)
+            assert calls[-1][0] is None and calls[-1][2] == 0, "the closing call read a length"
+            for i, (sg, left, _) in enumerate(calls[:-1]):
+                assert (left <= cost) == (i == len(calls) - 2), (c, i, left, cost)
+
+
 def _check(lens, Nmax, BN, U, P0, unit_cost):
     tiles, T, P, cost = plan(lens, Nmax, BN, U, P0, unit_cost)
     owner, segs = {}, {}
