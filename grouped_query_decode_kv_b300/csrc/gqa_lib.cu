@@ -50,6 +50,11 @@ struct KernelChoice {
   int box_elems;
   cudaError_t (*launch)(dim3, int, const CUtensorMap &, const CUtensorMap &, const CUtensorMap *,
                         const SplitParams &, cudaStream_t);
+  // the fused decode step's instantiation, where it has its own (null: the
+  // kernel above serves the step too)
+  const void *func_step;
+  cudaError_t (*launch_step)(dim3, int, const CUtensorMap &, const CUtensorMap &, const CUtensorMap *,
+                             const SplitParams &, cudaStream_t);
   int (*clusters)(int);  // max_clusters of the kernel
 };
 
@@ -75,13 +80,14 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
 enum Family { kSimt = 0, kMma = 1, kTc = 2 };
 
 // MULTI: the instantiation for several query tokens per sequence; the
-// one-token kernels are compiled without any of that code.
-template <class C, int F, bool MULTI>
+// one-token kernels are compiled without any of that code.  STEP (tcgen05
+// only): the fused decode step's instantiation.
+template <class C, int F, bool MULTI, bool STEP = false>
 auto split_kernel_ptr() {
   if constexpr (F == kMma)
     return &gqa_split_mma_kernel<C, MULTI>;
   else if constexpr (F == kTc)
-    return &gqa_split_tc_kernel<C, MULTI>;
+    return &gqa_split_tc_kernel<C, MULTI, STEP>;
   else
     return &gqa_split_simt_kernel<C, MULTI>;
 }
@@ -109,12 +115,12 @@ cudaError_t launch_pdl_cluster(void (*kernel)(Params...), dim3 grid, dim3 block,
 
 // tail[2]: the caches' maps with 16-position boxes (the tcgen05 kernel reads
 // the short last tile of a unit through them; the others take none).
-template <class C, int F, bool MULTI>
+template <class C, int F, bool MULTI, bool STEP = false>
 cudaError_t launch_split(dim3 grid, int cluster, const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap *tail,
                          const SplitParams &p, cudaStream_t st) {
   if constexpr (F == kTc)
-    return launch_pdl_cluster(split_kernel_ptr<C, F, MULTI>(), grid, dim3(C::THREADS), C::SMEM_BYTES, cluster, st, k,
-                              v, tail[0], tail[1], p);
+    return launch_pdl_cluster(split_kernel_ptr<C, F, MULTI, STEP>(), grid, dim3(C::THREADS), C::SMEM_BYTES, cluster,
+                              st, k, v, tail[0], tail[1], p);
   else
     return launch_pdl_cluster(split_kernel_ptr<C, F, MULTI>(), grid, dim3(C::THREADS), C::SMEM_BYTES, cluster, st, k,
                               v, p);
@@ -176,6 +182,16 @@ KernelChoice make_choice() {
   else
     c.box_elems = 64;
   c.launch = &launch_split<C, F, MULTI>;
+  // the one-token bf16 tcgen05 kernels count a fused step's CTAs early (a
+  // separate instantiation, so that attention alone keeps its code)
+  c.func_step = nullptr;
+  c.launch_step = nullptr;
+  if constexpr (F == kTc && !MULTI) {
+    if constexpr (!C::FP8) {
+      c.func_step = reinterpret_cast<const void *>(split_kernel_ptr<C, F, MULTI, true>());
+      c.launch_step = &launch_split<C, F, MULTI, true>;
+    }
+  }
   c.clusters = &max_clusters<C, F, MULTI>;
   return c;
 }
@@ -470,8 +486,9 @@ int check_attention_args(const void *q, const void *k, const void *v, const int3
   return GQA_OK;
 }
 
-// Opts a split kernel in to its dynamic shared memory, once per device.
-int ensure_smem_attr(const KernelChoice &kc) {
+// Opts a split kernel (`func`, of the choice kc) in to its dynamic shared
+// memory, once per device.
+int ensure_smem_attr(const KernelChoice &kc, const void *func) {
   static std::mutex mu;
   static const void *done_func[256];
   static int done_dev[256];
@@ -479,15 +496,15 @@ int ensure_smem_attr(const KernelChoice &kc) {
   const int dev = current_device();
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < n; ++i)
-    if (done_func[i] == kc.func && done_dev[i] == dev) return GQA_OK;
-  if (cudaFuncSetAttribute(kc.func, cudaFuncAttributeMaxDynamicSharedMemorySize, kc.smem) != cudaSuccess ||
-      cudaFuncSetAttribute(kc.func, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+    if (done_func[i] == func && done_dev[i] == dev) return GQA_OK;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, kc.smem) != cudaSuccess ||
+      cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
           cudaSuccess) {
     cudaGetLastError();
     return GQA_ERR_CUDA;
   }
   if (n < 256 && dev >= 0) {
-    done_func[n] = kc.func;
+    done_func[n] = func;
     done_dev[n] = dev;
     ++n;
   }
@@ -515,7 +532,8 @@ int run_attention(const void *q, const void *k, const void *v, const int32_t *sl
   if (pl.k.family == kTc && (!encode_cache_map(&tail[0], k, dt, d, Nmax, B * G, 16, pl.k.box_elems) ||
                              !encode_cache_map(&tail[1], v, dt, d, Nmax, B * G, 16, pl.k.box_elems)))
     return GQA_ERR_CUDA;
-  if (int rc = ensure_smem_attr(pl.k)) return rc;
+  const bool own_step = app.k_new != nullptr && pl.k.launch_step != nullptr;
+  if (int rc = ensure_smem_attr(pl.k, own_step ? pl.k.func_step : pl.k.func)) return rc;
   SplitParams p;
   p.q = q;
   p.seq_lens = sl;
@@ -557,7 +575,8 @@ int run_attention(const void *q, const void *k, const void *v, const int32_t *sl
   p.rep_kv = H / G;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
-  if (pl.k.launch(dim3(pl.P), pl.cluster, mk, mv, tail, p, st) != cudaSuccess) {
+  const auto launch = own_step ? pl.k.launch_step : pl.k.launch;
+  if (launch(dim3(pl.P), pl.cluster, mk, mv, tail, p, st) != cudaSuccess) {
     cudaGetLastError();
     return GQA_ERR_CUDA;
   }

@@ -198,19 +198,24 @@ __device__ __forceinline__ void finish_step(const SplitParams &p, int tid, int n
   }
 }
 
-// Fused step, early arrival (the CUDA-core kernel): the CTA counts on the
-// step word as soon as none of its threads will read the lengths again,
-// which is long before its work ends, so the count and the last CTA's update
-// of the lengths overlap the CTAs' remaining work instead of following it.
-// Each consumer warp signals once, after its last read (the start of its
-// last segment, or the end of its loop); the producer warp, whose reads end
-// with its last copy, waits for those signals and counts the CTA.
+// Fused step, early arrival (the CUDA-core and tcgen05 kernels): the CTA
+// counts on the step word as soon as none of its threads will read the
+// lengths again, which is long before its work ends, so the count and the
+// last CTA's update of the lengths overlap the CTAs' remaining work instead
+// of following it.  Each warp (or lone thread) that walks the segments
+// signals once, after its last read (the start of its last segment, or the
+// end of its loop); the producer warp, whose reads end with its last copy,
+// waits for those signals and counts the CTA.
 
-// One consumer warp: every lane has done its last read of the lengths.
+// One thread that walks the segments alone: it has done its last read.
+__device__ __forceinline__ void signal_lengths_read_thread(UnitMerge *um) {
+  asm volatile("red.release.cta.shared::cta.add.u32 [%0], 1;" ::"r"(smem_u32(&um->reads_done)) : "memory");
+}
+
+// One warp: every lane has done its last read of the lengths.
 __device__ __forceinline__ void signal_lengths_read(UnitMerge *um, int lane) {
   __syncwarp();
-  if (lane == 0)
-    asm volatile("red.release.cta.shared::cta.add.u32 [%0], 1;" ::"r"(smem_u32(&um->reads_done)) : "memory");
+  if (lane == 0) signal_lengths_read_thread(um);
 }
 
 // The producer warp, after its own last read: waits (bounded) for `n`

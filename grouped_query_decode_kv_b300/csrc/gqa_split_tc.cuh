@@ -111,6 +111,9 @@ struct TcCfg {
   static constexpr int SOFT_WARP0 = 3;            // first softmax warp (after producer, two MMA issuers)
   static constexpr int CONV_WARP0 = SOFT_WARP0 + 4 * SG;  // first FP8 converter warp
   static constexpr int THREADS = (CONV_WARP0 + (CONV ? 4 : 0)) * 32;
+  // fused step: the signals the producer waits for before it counts the CTA
+  // (the two MMA issuer threads, the softmax warps, the converter warps)
+  static constexpr int LEN_READERS = 2 + 4 * SG + (CONV ? 4 : 0);
   static constexpr int KV_BOX = BLOCK_N * 128;  // one 128-byte-wide box of a bf16 K or V tile
   // FP8: V staging [2] in f16, two boxes each (d 0-63, 64-127); the f16 K
   // tiles live in tensor memory
@@ -395,7 +398,10 @@ __device__ __forceinline__ void merge_cluster_unit(const SplitParams &p, const C
 // partial of the row has it, and a row whose sum stays 0 is written as 0.
 constexpr float kNoMax = -1e30f;
 
-template <class C, bool MULTI>
+// STEP: the instantiation for the fused decode step, whose CTAs count on the
+// step word as soon as no thread will read the lengths again (the others,
+// compiled without that code, count after all of their work when asked to).
+template <class C, bool MULTI, bool STEP = false>
 __global__ void __launch_bounds__(C::THREADS, 1)
     gqa_split_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const __grid_constant__ CUtensorMap tmK16, const __grid_constant__ CUtensorMap tmV16,
@@ -494,6 +500,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (lane == 0) *range_smem = r;
     }
   }
+  if (STEP && threadIdx.x == 0) um->reads_done = 0;
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -530,7 +537,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         Segment seg;
         int tg = 0;
         bool ok = true;
+        bool lens_read = !STEP || !p.append;
         for (int unit = 0; ok && cur.next(sp, seg); ++unit) {
+          if (STEP && !lens_read && cur.end - cur.pos <= cur.cost) {  // the last segment: no more reads
+            signal_lengths_read_thread(um);
+            lens_read = true;
+          }
           for (int i = 0; ok && i < seg.t1 - seg.t0; ++i, ++tg) {
             if (warp == 1) {
               const int st = tg % ST;
@@ -597,6 +609,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
           }
         }
+        if (STEP && !lens_read) signal_lengths_read_thread(um);
         // nothing of either thread's may still run when TMEM is freed (the
         // barrier counts both threads' commits)
         tc::commit(bars.mma_done());
@@ -753,11 +766,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (!dead && !warp_wait(bar, parity)) dead = true;
       };
       int t = 0;
+      bool lens_read = !STEP || !p.append;
       for (int unit = 0; have; ++unit) {
         int h_first, nh;
         unit_heads(seg, h_first, nh);
         const int b = seg.b;
         const int L = attn_len(p.seq_lens, b, p.Nmax, p.append);
+        if (STEP && !lens_read && cur.end - cur.pos <= cur.cost) {
+          // the last unit: the cursor reads no more lengths (nor do the Q
+          // look-aheads, which stand at or past it)
+          signal_lengths_read(um, lane);
+          lens_read = true;
+        }
         const int ob = unit & 1;
         const int ntl = seg.t1 - seg.t0;
         // FP8 cache: K's per-head scale joins the logit scale, V's the result
@@ -1147,6 +1167,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         seg = nseg;
         have = next;
       }
+      if (STEP && !lens_read) signal_lengths_read(um, lane);
     } else if constexpr (C::CONV) {
       // ------------------------------------------------------------ FP8 converters
       // Thread R converts position R of every tile (R = the TMEM lane its
@@ -1165,8 +1186,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       Segment seg;
       bool dead = false;
       int tg = 0;
+      bool lens_read = !STEP || !p.append;
       while (cur.next(sp, seg)) {
         const int L = attn_len(p.seq_lens, seg.b, p.Nmax, p.append);
+        if (STEP && !lens_read && cur.end - cur.pos <= cur.cost) {
+          signal_lengths_read(um, lane);
+          lens_read = true;
+        }
         for (int t = seg.t0; t < seg.t1; ++t, ++tg) {
           const int st = tg % ST, cb = tg & 1;
           if (!dead && !warp_wait(pipe.full(st), (tg / ST) & 1)) dead = true;
@@ -1229,8 +1255,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           if (lane == 0) mbar_arrive(bars.conv_full(cb));
         }
       }
+      if (STEP && !lens_read) signal_lengths_read(um, lane);
     }
   }
+  // fused step: the producer, done with its copies, counts the CTA once every
+  // reader of the lengths has signalled (an empty range has none)
+  if (STEP && warp == 0 && p.append) arrive_step_early(p, um, range.begin < range.end ? C::LEN_READERS : 0, lane);
   // ---- cluster plan: the k CTAs of the cluster wrote the partials of the k
   // pieces of the same unit to their workspace slots (a CTA with an empty
   // piece wrote none); after the barrier (cluster-scope release / acquire,
@@ -1252,7 +1282,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     tc::fence_after();
     tc::tmem_dealloc(tmem, C::TM_COLS);
   }
-  if (p.append) finish_step(p, threadIdx.x, blockDim.x, &um->last);
+  if (!STEP && p.append) finish_step(p, threadIdx.x, blockDim.x, &um->last);
 }
 
 }  // namespace gqa
