@@ -81,7 +81,7 @@ enum Family { kSimt = 0, kMma = 1, kTc = 2 };
 
 // MULTI: the instantiation for several query tokens per sequence; the
 // one-token kernels are compiled without any of that code.  STEP (tcgen05
-// only): the fused decode step's instantiation.
+// and CUDA-core kernels): the fused decode step's instantiation.
 template <class C, int F, bool MULTI, bool STEP = false>
 auto split_kernel_ptr() {
   if constexpr (F == kMma)
@@ -89,7 +89,7 @@ auto split_kernel_ptr() {
   else if constexpr (F == kTc)
     return &gqa_split_tc_kernel<C, MULTI, STEP>;
   else
-    return &gqa_split_simt_kernel<C, MULTI>;
+    return &gqa_split_simt_kernel<C, MULTI, STEP>;
 }
 
 // The same in thread-block clusters of `cluster` CTAs along x.
@@ -122,8 +122,8 @@ cudaError_t launch_split(dim3 grid, int cluster, const CUtensorMap &k, const CUt
     return launch_pdl_cluster(split_kernel_ptr<C, F, MULTI, STEP>(), grid, dim3(C::THREADS), C::SMEM_BYTES, cluster,
                               st, k, v, tail[0], tail[1], p);
   else
-    return launch_pdl_cluster(split_kernel_ptr<C, F, MULTI>(), grid, dim3(C::THREADS), C::SMEM_BYTES, cluster, st, k,
-                              v, p);
+    return launch_pdl_cluster(split_kernel_ptr<C, F, MULTI, STEP>(), grid, dim3(C::THREADS), C::SMEM_BYTES, cluster,
+                              st, k, v, p);
 }
 
 // Clusters of `cluster` CTAs of this kernel that can be resident at once (0
@@ -182,11 +182,12 @@ KernelChoice make_choice() {
   else
     c.box_elems = 64;
   c.launch = &launch_split<C, F, MULTI>;
-  // the one-token bf16 tcgen05 kernels count a fused step's CTAs early (a
-  // separate instantiation, so that attention alone keeps its code)
+  // the one-token tcgen05 and CUDA-core kernels of the step's dtypes count a
+  // fused step's CTAs early (a separate instantiation, so that attention
+  // alone keeps its code)
   c.func_step = nullptr;
   c.launch_step = nullptr;
-  if constexpr (F == kTc && !MULTI) {
+  if constexpr (F != kMma && !MULTI) {
     if constexpr (!C::FP8) {
       c.func_step = reinterpret_cast<const void *>(split_kernel_ptr<C, F, MULTI, true>());
       c.launch_step = &launch_split<C, F, MULTI, true>;

@@ -118,7 +118,10 @@ __device__ __forceinline__ void store_chunk<float>(float *dst, const float *f) {
 }
 
 
-template <class C, bool MULTI>
+// STEP: the instantiation for the fused decode step, whose CTAs count on the
+// step word as soon as no thread will read the lengths again (the others,
+// compiled without that code, count after all of their work when asked to).
+template <class C, bool MULTI, bool STEP = false>
 __global__ void __launch_bounds__(C::THREADS)
     gqa_split_simt_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                           const SplitParams p) {
@@ -169,15 +172,15 @@ __global__ void __launch_bounds__(C::THREADS)
       if (lane == 0) *range_smem = r;
     }
   }
-  if (threadIdx.x == 0) um->reads_done = 0;
+  if (STEP && threadIdx.x == 0) um->reads_done = 0;
   __syncthreads();
   griddep_launch_dependents();
   const CtaRange range = *range_smem;
   if (warp == C::CONSUMER_WARPS) {
     if (range.begin < range.end) produce_range(pipe, sp, range, &tmK, &tmV, C::BOX_ELEMS, p.G, p.head_chunks, p, lane);
-    if (p.append) arrive_step_early(p, um, C::CONSUMER_WARPS, lane);
+    if (STEP && p.append) arrive_step_early(p, um, C::CONSUMER_WARPS, lane);
   }
-  bool lens_read = !p.append || warp == C::CONSUMER_WARPS;  // this warp has signalled (or need not)
+  bool lens_read = !STEP || !p.append || warp == C::CONSUMER_WARPS;  // this warp has signalled (or need not)
   if (range.begin < range.end && warp != C::CONSUMER_WARPS) {
 
   const int tg = lane >> 3, j = lane & 7;
@@ -193,7 +196,7 @@ __global__ void __launch_bounds__(C::THREADS)
     const int h_first = g * p.n_rep + hc * NH;
     const int nh = min(NH, p.n_rep - hc * NH);
     const int L = attn_len(p.seq_lens, b, p.Nmax, p.append);
-    if (!lens_read && cur.end - cur.pos <= cur.cost) {
+    if (STEP && !lens_read && cur.end - cur.pos <= cur.cost) {
       // a fused step, and the CTA's last segment: the cursor now ends on a
       // unit boundary (or the range's end) with at most a unit's charge
       // left, so no real tile follows and it reads no more lengths
@@ -395,7 +398,12 @@ __global__ void __launch_bounds__(C::THREADS)
     consumer_bar_sync(C::CONSUMER_WARPS * 32);  // scratch free for the next unit
   }
   }
-  if (!lens_read) signal_lengths_read(um, lane);  // empty range, or a timed-out wait ended the loop
+  if constexpr (STEP) {
+    if (!lens_read) signal_lengths_read(um, lane);  // empty range, or a timed-out wait ended the loop
+  } else if (p.append) {
+    __syncthreads();
+    finish_step(p, threadIdx.x, blockDim.x, &um->last);
+  }
 }
 
 }  // namespace gqa
