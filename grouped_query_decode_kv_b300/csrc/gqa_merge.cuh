@@ -171,9 +171,11 @@ __device__ __forceinline__ unsigned arrive_step(unsigned long long *cnt, unsigne
   }
 }
 
-// End of a fused decode step, called by all `nthr` threads of a CTA after all
-// of the CTA's work and a barrier of the whole CTA (every CTA comes, busy or
-// idle, also after a timed-out wait).  The last CTA of the grid to count
+// End of a fused decode step where a kernel counts after all of its work
+// (the warp-MMA kernel; the others' attention instantiations, should one be
+// asked to append), called by all `nthr` threads of a CTA after that work and
+// a barrier of the whole CTA (every CTA comes, busy or idle, also after a
+// timed-out wait).  The last CTA of the grid to count
 // advances seq_lens[b] to L_b + 1 for every row that took the append, and
 // puts the count back to zero under the same tag (so that a graph replay of
 // the call, which keeps its epoch, starts from zero too; a plain store, since
