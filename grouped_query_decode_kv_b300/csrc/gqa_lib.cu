@@ -80,12 +80,12 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
 enum Family { kSimt = 0, kMma = 1, kTc = 2 };
 
 // MULTI: the instantiation for several query tokens per sequence; the
-// one-token kernels are compiled without any of that code.  STEP (tcgen05
-// and CUDA-core kernels): the fused decode step's instantiation.
+// one-token kernels are compiled without any of that code.  STEP: the fused
+// decode step's instantiation.
 template <class C, int F, bool MULTI, bool STEP = false>
 auto split_kernel_ptr() {
   if constexpr (F == kMma)
-    return &gqa_split_mma_kernel<C, MULTI>;
+    return &gqa_split_mma_kernel<C, MULTI, STEP>;
   else if constexpr (F == kTc)
     return &gqa_split_tc_kernel<C, MULTI, STEP>;
   else
@@ -182,12 +182,11 @@ KernelChoice make_choice() {
   else
     c.box_elems = 64;
   c.launch = &launch_split<C, F, MULTI>;
-  // the one-token tcgen05 and CUDA-core kernels of the step's dtypes count a
-  // fused step's CTAs early (a separate instantiation, so that attention
-  // alone keeps its code)
+  // the one-token kernels of the step's dtypes count a fused step's CTAs
+  // early (a separate instantiation, so that attention alone keeps its code)
   c.func_step = nullptr;
   c.launch_step = nullptr;
-  if constexpr (F != kMma && !MULTI) {
+  if constexpr (!MULTI) {
     if constexpr (!C::FP8) {
       c.func_step = reinterpret_cast<const void *>(split_kernel_ptr<C, F, MULTI, true>());
       c.launch_step = &launch_split<C, F, MULTI, true>;

@@ -172,10 +172,10 @@ __device__ __forceinline__ unsigned arrive_step(unsigned long long *cnt, unsigne
 }
 
 // End of a fused decode step where a kernel counts after all of its work
-// (the warp-MMA kernel; the others' attention instantiations, should one be
-// asked to append), called by all `nthr` threads of a CTA after that work and
-// a barrier of the whole CTA (every CTA comes, busy or idle, also after a
-// timed-out wait).  The last CTA of the grid to count
+// (an attention instantiation, should one be asked to append: the host
+// launches the step instantiations, which count early), called by all `nthr`
+// threads of a CTA after that work and a barrier of the whole CTA (every CTA
+// comes, busy or idle, also after a timed-out wait).  The last CTA of the grid to count
 // advances seq_lens[b] to L_b + 1 for every row that took the append, and
 // puts the count back to zero under the same tag (so that a graph replay of
 // the call, which keeps its epoch, starts from zero too; a plain store, since
@@ -200,8 +200,8 @@ __device__ __forceinline__ void finish_step(const SplitParams &p, int tid, int n
   }
 }
 
-// Fused step, early arrival (the CUDA-core and tcgen05 kernels): the CTA
-// counts on the step word as soon as none of its threads will read the
+// Fused step, early arrival (the step instantiations of the split kernels):
+// the CTA counts on the step word as soon as none of its threads will read the
 // lengths again, which is long before its work ends, so the count and the
 // last CTA's update of the lengths overlap the CTAs' remaining work instead
 // of following it.  Each warp (or lone thread) that walks the segments

@@ -38,6 +38,7 @@ struct MmaCfg {
   static constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;
   static constexpr int HEADS = 16 * MFW * WH;  // query heads per CTA
   static constexpr int UNIT_COST = 2;          // stream-K charge per unit, in tiles (gqa_schedule.cuh)
+  static constexpr bool FP8 = false;           // bf16 caches only
   static constexpr int MIN_BLOCKS = MIN_BLOCKS_;  // resident CTAs per SM the register budget must allow
   using Pipe = KVPipe<D * 2 / 128, BLOCK_N_, STAGES_, CONSUMER_WARPS>;
   static constexpr int BLOCK_N = BLOCK_N_;
@@ -59,7 +60,10 @@ struct MmaCfg {
   static_assert(D == 64 || D == 128, "head dimension");
 };
 
-template <class C, bool MULTI>
+// STEP: the instantiation for the fused decode step, whose CTAs count on the
+// step word as soon as no thread will read the lengths again (the others,
+// compiled without that code, count after all of their work when asked to).
+template <class C, bool MULTI, bool STEP = false>
 __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
     gqa_split_mma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                          const SplitParams p) {
@@ -112,12 +116,15 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
       if (lane == 0) *range_smem = r;
     }
   }
+  if (STEP && threadIdx.x == 0) um->reads_done = 0;
   __syncthreads();
   griddep_launch_dependents();
   const CtaRange range = *range_smem;
-  if (range.begin < range.end && warp == C::CONSUMER_WARPS) {
-    produce_range(pipe, sp, range, &tmK, &tmV, 64, p.G, p.head_chunks, p, lane);
+  if (warp == C::CONSUMER_WARPS) {
+    if (range.begin < range.end) produce_range(pipe, sp, range, &tmK, &tmV, 64, p.G, p.head_chunks, p, lane);
+    if (STEP && p.append) arrive_step_early(p, um, C::CONSUMER_WARPS, lane);
   }
+  bool lens_read = !STEP || !p.append || warp == C::CONSUMER_WARPS;  // this warp has signalled (or need not)
   if (range.begin < range.end && warp != C::CONSUMER_WARPS) {
 
   const int wh = warp >> 2, wn = warp & 3;
@@ -133,6 +140,13 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
     const int h_first = g * p.n_rep + hc * C::HEADS;
     const int nh = min(C::HEADS, p.n_rep - hc * C::HEADS);
     const int L = attn_len(p.seq_lens, b, p.Nmax, p.append);
+    if (STEP && !lens_read && cur.end - cur.pos <= cur.cost) {
+      // a fused step, and the CTA's last segment: the cursor now ends on a
+      // unit boundary (or the range's end) with at most a unit's charge
+      // left, so no real tile follows and it reads no more lengths
+      signal_lengths_read(um, lane);
+      lens_read = true;
+    }
 
     // Q fragments (A operand, row-major 16x16 per k-step), kept in registers.
     uint32_t qa[MFW][KS][4];
@@ -407,7 +421,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
     consumer_bar_sync(NCONS);  // scratch free for the next unit
   }
   }
-  if (p.append) {
+  if constexpr (STEP) {
+    if (!lens_read) signal_lengths_read(um, lane);  // empty range, or a timed-out wait ended the loop
+  } else if (p.append) {
     __syncthreads();
     finish_step(p, threadIdx.x, blockDim.x, &um->last);
   }
