@@ -49,6 +49,7 @@ __all__ = [
     "gqa_qkv_project", "gqa_qkv_project_ws", "gqa_qkv_project_workspace_bytes",
     "gqa_decode_attention_fp8", "gqa_decode_attention_fp8_ws", "gqa_decode_workspace_bytes_fp8", "kv_append_fp8",
     "DEVERR_ATTN_LEN", "DEVERR_APPEND_LEN", "DEVERR_TIMEOUT", "DEVERR_RANGE", "DEVERR_BOUNDS", "EXPORTED_SYMBOLS",
+    "gqa_stream_read", "gqa_wait_timeout_selftest",
 ]
 
 GQA_F32, GQA_BF16 = 0, 1
@@ -64,7 +65,7 @@ EXPORTED_SYMBOLS = (
     "gqa_decode_attention_multi", "gqa_decode_attention_multi_ex",
     "gqa_qkv_project", "gqa_qkv_project_ws", "gqa_qkv_project_workspace_bytes",
     "gqa_decode_attention_fp8", "gqa_decode_attention_fp8_ws", "gqa_decode_workspace_bytes_fp8", "kv_append_fp8",
-    "gqa_stream_read", "gqa_set_workspace_allocator",
+    "gqa_stream_read", "gqa_set_workspace_allocator", "gqa_wait_timeout_selftest",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -143,6 +144,8 @@ def load_library():
         lib.gqa_status_string.restype = ctypes.c_char_p
         lib.gqa_stream_read.argtypes = [vp, sz, ci, vp, vp]
         lib.gqa_stream_read.restype = ci
+        lib.gqa_wait_timeout_selftest.argtypes = [ci, vp]
+        lib.gqa_wait_timeout_selftest.restype = ci
         lib.gqa_set_workspace_allocator.argtypes = [vp, vp, vp]
         lib.gqa_set_workspace_allocator.restype = ci
         _lib = lib
@@ -469,6 +472,16 @@ def mha_to_gqa_meanpool(w, w_out, stream=None):
     _check("mha_to_gqa_meanpool", lib.mha_to_gqa_meanpool(_dev(w, "w"), _dev(w_out, "w_out"), H, G, d, D,
                                                           _dtype_code(w), _stream(w, stream)))
     return w_out
+
+
+def gqa_wait_timeout_selftest(which, stream=None):
+    """Launches one warp whose bounded wait (which = 0: the single-thread
+    mbarrier wait, 1: the tcgen05 kernel's whole-warp wait, 2: a fused step's
+    wait for its warps' signals) runs out after about one second and sets
+    GQA_DEVERR_TIMEOUT; read it with gqa_get_device_error."""
+    lib = load_library()
+    st = torch.cuda.current_stream() if stream is None else stream
+    _check("gqa_wait_timeout_selftest", lib.gqa_wait_timeout_selftest(int(which), st.cuda_stream))
 
 
 def gqa_stream_read(buf, mode, sink, stream=None):

@@ -19,6 +19,7 @@
 #include "gqa_split_mma.cuh"
 #include "gqa_split_simt.cuh"
 #include "gqa_split_tc.cuh"
+#include "gqa_selftest.cuh"
 
 namespace gqa {
 namespace {
@@ -790,6 +791,13 @@ int gqa_set_workspace_allocator(gqa_alloc_fn alloc, gqa_free_fn free_fn, void *c
   g_alloc_ctx.store(ctx);
   g_free.store(free_fn);
   g_alloc.store(alloc);
+  return GQA_OK;
+}
+
+int gqa_wait_timeout_selftest(int which, cudaStream_t stream) {
+  if (which < 0 || which > 2) return GQA_ERR_INVALID_ARG;
+  gqa_wait_selftest_kernel<<<1, 32, 0, stream>>>(which);
+  if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
   return GQA_OK;
 }
 

@@ -382,6 +382,24 @@ int gqa_set_workspace_allocator(gqa_alloc_fn alloc, gqa_free_fn free_fn, void *c
 int gqa_stream_read(const void *buf, size_t bytes, int mode, uint32_t *sink, cudaStream_t stream);
 
 /*
+ * gqa_wait_timeout_selftest — a check of the error path, with no counterpart
+ * in the pages: launches one warp that waits, through the same time-bounded
+ * waits the split kernels use, on a condition that nothing will satisfy.
+ * The wait gives up after about one second, sets GQA_DEVERR_TIMEOUT in the
+ * error word and returns, and the kernel ends: no fault, no trap, and the
+ * context stays usable.  Read (and clear) the word with gqa_get_device_error.
+ *   which = 0: the single-thread mbarrier wait (TMA producers, CUDA-core and
+ *              warp-MMA consumers);
+ *           1: the whole-warp wait of the tcgen05 kernel's softmax and
+ *              converter warps;
+ *           2: a fused step's producer waiting for its warps' signals
+ *              before it counts its block.
+ * Asynchronous on `stream` (about one second of device time); `which`
+ * outside 0..2 returns GQA_ERR_INVALID_ARG with nothing enqueued.
+ */
+int gqa_wait_timeout_selftest(int which, cudaStream_t stream);
+
+/*
  * Reads the current device's error word into *host_err and clears it.  This
  * call synchronises `stream` (it copies the word to the host on it).
  */

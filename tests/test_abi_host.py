@@ -174,6 +174,12 @@ ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(ctypes
 FREE_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p)
 
 
+def test_wait_selftest_rejects_an_unknown_wait(lib):
+    """Checked before anything is enqueued, so it needs no GPU."""
+    for which in (-1, 3):
+        assert lib.gqa_wait_timeout_selftest(which, None) == -1
+
+
 def test_workspace_allocation_failure_returns_no_memory(lib):
     """A workspace allocator that fails (installed through the hook) makes
     every allocating call return GQA_ERR_NO_MEMORY before anything is
