@@ -441,6 +441,49 @@ def test_step_workspace_shared_across_shapes_and_never_cleared(H, G):
     assert gqa.gqa_get_device_error() == 0
 
 
+@pytest.mark.parametrize("H,G,d", [(32, 32, 128), (64, 8, 128), (8, 2, 64), (64, 1, 128)])
+def test_back_to_back_steps_see_each_others_lengths(H, G, d):
+    """Eight fused steps enqueued back to back on the same caches and lengths,
+    with no host synchronisation in between.  A step's kernel may start while
+    the previous one still runs and advances the lengths (its blocks count as
+    soon as they stop reading them), so the next kernel's speculative plan
+    can read half of that update; each step must still equal kv_append +
+    attention done as separate calls on copies, bit for bit, and the last
+    one the oracle."""
+    dev = torch.device("cuda")
+    B, N, K = 6, 700, 8
+    w = workloads.Workload("b2b", B, H, G, d, N, "bf16", ("uniform", 1, N - K - 1), 7900 + H + G + d)
+    x = workloads.make_inputs(w)  # cache rows past each length hold NaN
+    g = torch.Generator().manual_seed(7901 + H + G + d)
+    qs = [torch.randn(B, H, d, generator=g).to(torch.bfloat16) for _ in range(K)]
+    kns = [torch.randn(B, G, d, generator=g).to(torch.bfloat16) for _ in range(K)]
+    vns = [torch.randn(B, G, d, generator=g).to(torch.bfloat16) for _ in range(K)]
+    k1, v1, sl1 = x["k_cache"].to(dev), x["v_cache"].to(dev), x["seq_lens"].to(dev)
+    k2, v2, sl2 = k1.clone(), v1.clone(), sl1.clone()
+    ws = torch.zeros(max(gqa.gqa_decode_workspace_bytes(B, H, G, d, N, torch.bfloat16), 1), dtype=torch.uint8,
+                     device=dev)
+    out1 = [torch.full((B, H, d), float("nan"), dtype=torch.bfloat16, device=dev) for _ in range(K)]
+    out2 = [torch.full((B, H, d), float("nan"), dtype=torch.bfloat16, device=dev) for _ in range(K)]
+    qd, knd, vnd = [t.to(dev) for t in qs], [t.to(dev) for t in kns], [t.to(dev) for t in vns]
+    gqa.gqa_get_device_error()
+    torch.cuda.synchronize()
+    for i in range(K):
+        gqa.gqa_decode_step_ws(qd[i], knd[i], vnd[i], k2, v2, sl2, w.scale, out2[i], ws)
+    for i in range(K):
+        gqa.kv_append(knd[i], vnd[i], k1, v1, sl1)
+        gqa.gqa_decode_attention(qd[i], k1, v1, sl1, w.scale, out1[i])
+    torch.cuda.synchronize()
+    assert torch.equal(sl1, sl2)
+    assert torch.equal(sl2.cpu(), x["seq_lens"] + K)
+    assert torch.equal(k1.view(torch.uint8), k2.view(torch.uint8))
+    assert torch.equal(v1.view(torch.uint8), v2.view(torch.uint8))
+    for i in range(K):
+        np.testing.assert_array_equal(out1[i].double().cpu().numpy(), out2[i].double().cpu().numpy())
+    ref = oracle.decode_attention(qs[-1], k2.cpu(), v2.cpu(), sl2.cpu(), w.scale)
+    assert_parity(out2[-1].double().cpu().numpy(), ref, f"step {K} of {K}")
+    assert gqa.gqa_get_device_error() == 0
+
+
 # ------------------------------------------------------------ cluster plan
 # Groups of 8+ heads (tcgen05 kernel) with 37..74 (batch, KV head) units run
 # in thread-block clusters of k = 2..4 CTAs, one unit per cluster, merged
