@@ -35,6 +35,7 @@ struct SimtCfg {
   static constexpr int BOX_ELEMS = 128 / ELT;
   static constexpr int EPC = 16 / ELT;      // elements per 16-byte chunk
   static constexpr int EPL = NBOX * EPC;    // elements of a row held by one lane
+  static_assert(EPL % 2 == 0, "pairs of elements for the packed FMA");
   static constexpr int CONSUMER_WARPS = 4;
   static constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;
   static constexpr int HEADS = NH;
@@ -252,9 +253,21 @@ __global__ void __launch_bounds__(C::THREADS)
         float x[NH];
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
-          float dot = 0.f;
+          // bf16 / fp32: the packed two-lane fp32 FMA, even and odd elements
+          // in two partial sums (measured: sweep G=32 332.6 -> 315.6 us; the
+          // E4M3 instantiation measured 2 % slower with it and keeps one sum)
+          float dot;
+          if constexpr (C::FP8) {
+            dot = 0.f;
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) dot = fmaf(qf[h][e], kf[e], dot);
+            for (int e = 0; e < EPL; ++e) dot = fmaf(qf[h][e], kf[e], dot);
+          } else {
+            float2 d2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < EPL; e += 2)
+              d2 = __ffma2_rn(make_float2(qf[h][e], qf[h][e + 1]), make_float2(kf[e], kf[e + 1]), d2);
+            dot = d2.x + d2.y;
+          }
           dot += __shfl_xor_sync(0xffffffffu, dot, 1);
           dot += __shfl_xor_sync(0xffffffffu, dot, 2);
           dot += __shfl_xor_sync(0xffffffffu, dot, 4);
@@ -280,8 +293,19 @@ __global__ void __launch_bounds__(C::THREADS)
             }
             const float pw = exp2f(x[h] - m_run[h]);
             l_run[h] += pw;
+            if constexpr (C::FP8) {
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) acc[h][e] = fmaf(pw, vf[e], acc[h][e]);
+              for (int e = 0; e < EPL; ++e) acc[h][e] = fmaf(pw, vf[e], acc[h][e]);
+            } else {
+              // the same FMA per element, two elements per instruction
+              const float2 pw2 = make_float2(pw, pw);
+#pragma unroll
+              for (int e = 0; e < EPL; e += 2) {
+                const float2 a = __ffma2_rn(pw2, make_float2(vf[e], vf[e + 1]), make_float2(acc[h][e], acc[h][e + 1]));
+                acc[h][e] = a.x;
+                acc[h][e + 1] = a.y;
+              }
+            }
           }
         }
       }
