@@ -138,14 +138,13 @@ __device__ __forceinline__ int piece_start(int q, int tiles, int k) { return q *
 // Virtual tiles of one unit of a row with `tiles` real tiles.
 __device__ __forceinline__ long long unit_span(int tiles, int cost) { return tiles > 0 ? tiles + cost : 0; }
 
-// CTAs used for T tiles by a fused step when every non-empty unit holds the
-// same number of tiles and there are no more units than CTAs: k = floor(P /
-// units) CTAs per unit, each taking an equal piece of one unit, so that no
-// CTA works on two units (two epilogues, two partials, two appended rows).
-// Measured on B300 the step is faster so (long context 84.4 -> 82.9 us),
-// while attention alone is faster on all P CTAs (sweep G=4 46.0 -> 44.6 us,
-// long context 83.1 -> 82.4 us) and keeps the plain tile-level split, as do
-// more units than CTAs and units of unequal length.
+// CTAs used for T tiles when every non-empty unit holds the same number of
+// tiles and there are no more units than CTAs: k = floor(P / units) CTAs per
+// unit, each taking an equal piece of one unit, so that no CTA works on two
+// units (two epilogues, two partials).  Measured on B300 this beats the
+// plain split over all P CTAs even when it leaves some CTAs idle, because
+// the K/V stream stays saturated.  With more units than CTAs, or units of
+// unequal length, the plain tile-level split over all P CTAs is kept.
 __device__ __forceinline__ int aligned_cta_count(long long units, int P) {
   return (units > 0 && units <= P) ? (int)(units * (P / units)) : P;
 }
@@ -254,7 +253,7 @@ __device__ __forceinline__ CtaRange warp_plan_range(const SchedParams &s, int la
     }
     return r;
   }
-  if (uniform && s.append) P = aligned_cta_count((long long)rows * s.units_per_b, P);
+  if (uniform) P = aligned_cta_count((long long)rows * s.units_per_b, P);
   const int cost = uniform ? 0 : s.unit_cost;
   T += (long long)cost * rows * s.units_per_b;
   r.T = T;

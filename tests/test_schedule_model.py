@@ -8,7 +8,7 @@ rule for the first partial's slot names the slot that CTA wrote.
 The model follows the device code (gqa_schedule.cuh, gqa_merge.cuh): per-row
 tile counts, a per-unit charge of `cost` virtual tiles ahead of the unit's
 first real tile when lengths differ (0 when every non-empty row has the same
-tile count, where a fused step uses the aligned CTA count), contiguous ranges
+tile count, where the aligned CTA count applies), contiguous ranges
 start(c) = floor(c*T/P).  No GPU needed."""
 import random
 
@@ -27,12 +27,12 @@ def span(tiles, cost):
     return tiles + cost if tiles > 0 else 0
 
 
-def plan(lens, Nmax, BN, U, P0, unit_cost, step=False):
+def plan(lens, Nmax, BN, U, P0, unit_cost):
     tiles = [(max(0, min(L, Nmax)) + BN - 1) // BN for L in lens]
     nz = [t for t in tiles if t > 0]
     uniform = bool(nz) and min(nz) == max(nz)
     P = P0
-    if uniform and step and len(nz) * U <= P:  # the aligned CTA count of a fused step
+    if uniform and len(nz) * U <= P:
         P = len(nz) * U * (P // (len(nz) * U))
     cost = 0 if uniform else unit_cost
     return tiles, sum(span(t, cost) * U for t in tiles), P, cost
@@ -120,7 +120,7 @@ def test_cursor_last_segment_test_and_no_length_read_after_it(seed):
         Nmax = rng.choice([128, 1000, 4096])
         lens = [rng.choice([0, 1, 127, 128, 129, rng.randint(0, Nmax)]) for _ in range(B)]
         U, P0 = rng.choice([1, 2, 8]), rng.choice([1, 3, 17, 148])
-        tiles, T, P, cost = plan(lens, Nmax, 128, U, P0, 2, step=rng.random() < 0.5)
+        tiles, T, P, cost = plan(lens, Nmax, 128, U, P0, 2)
         for c in range(P0):
             calls = cursor_calls(c, tiles, T, P, U, cost)
             segs = [sg for sg, _, _ in calls if sg is not None]
@@ -130,8 +130,8 @@ def test_cursor_last_segment_test_and_no_length_read_after_it(seed):
                 assert (left <= cost) == (i == len(calls) - 2), (c, i, left, cost)
 
 
-def _check(lens, Nmax, BN, U, P0, unit_cost, step=False):
-    tiles, T, P, cost = plan(lens, Nmax, BN, U, P0, unit_cost, step)
+def _check(lens, Nmax, BN, U, P0, unit_cost):
+    tiles, T, P, cost = plan(lens, Nmax, BN, U, P0, unit_cost)
     owner, segs = {}, {}
     for c in range(P0):
         segs[c] = segments(c, tiles, T, P, U, cost)
@@ -173,7 +173,7 @@ def test_schedule_covers_every_tile_once_and_merges_consistently(seed):
         else:
             lens = [rng.randint(0, Nmax) for _ in range(B)]
         _check(lens, Nmax, rng.choice([64, 128]), rng.choice([1, 2, 4, 8, 16]), rng.choice([1, 7, 148, 296]),
-               rng.choice([0, 1, 2, 3, 6, 8, 12]), step=rng.random() < 0.5)
+               rng.choice([0, 1, 2, 3, 6, 8, 12]))
 
 
 def test_charge_moves_real_tiles_away_from_ranges_with_many_units():
