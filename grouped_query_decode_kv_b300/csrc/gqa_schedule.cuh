@@ -141,9 +141,12 @@ __device__ __forceinline__ long long unit_span(int tiles, int cost) { return til
 // CTAs used for T tiles when every non-empty unit holds the same number of
 // tiles and there are no more units than CTAs: k = floor(P / units) CTAs per
 // unit, each taking an equal piece of one unit, so that no CTA works on two
-// units (two epilogues, two partials).  Measured on B300 this beats the
-// plain split over all P CTAs even when it leaves some CTAs idle, because
-// the K/V stream stays saturated.  With more units than CTAs, or units of
+// units (two epilogues, two partials).  Measured on B300 against the plain
+// split over all P CTAs: clearly faster with two CTAs per SM, where the idle
+// CTAs leave no SM empty (MHA, 256 units on 296 CTAs: 78.8 against 81.4
+// us), and for fused steps; with one CTA per SM, where it leaves SMs idle,
+// attention alone is faster on the plain split (sweep G=4 44.6 against
+// 46.0 us), which is not used yet.  With more units than CTAs, or units of
 // unequal length, the plain tile-level split over all P CTAs is kept.
 __device__ __forceinline__ int aligned_cta_count(long long units, int P) {
   return (units > 0 && units <= P) ? (int)(units * (P / units)) : P;
